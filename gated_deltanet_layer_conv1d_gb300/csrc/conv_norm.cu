@@ -1,0 +1,218 @@
+// conv_norm.cu -- standalone conv + SiLU + L2 norm over many tokens, the conv-state
+// update that follows it, and the Z-gated RMSNorm (sm_103a).
+//
+// gdn_conv_kernel: one CTA per token; each thread takes 4 consecutive channels, so a
+//   warp covers 128 channels = one head at d = 128 and the per-head L2 norm of q and k
+//   is a shuffle reduction over the lanes of that head (layer_struct.rs,
+//   conv1d_l2norm_f32_strided_k / conv1d_prefill_k).  Inputs before a sequence's first
+//   token come from its conv state, which this kernel only reads.
+// gdn_conv_state_kernel: afterwards, each sequence's conv state becomes its last d_conv
+//   raw inputs (exact copies).  Running it as a second launch keeps every read of the
+//   old state ordered before the write of the new one.
+// gdn_gated_rmsnorm_kernel: one warp per (token, value head) (layer_struct.rs,
+//   gated_rms_norm_f32_k / gated_rms_norm_prefill_k).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kW = 4;
+constexpr int kConvThreads = 256;
+
+// Sequence of token t: the last s with cu[s] <= t (cu has n+1 entries).
+__device__ __forceinline__ int seq_of(const int32_t* cu, int n, int t) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const __grid_constant__ ConvParams p) {
+  using A = Act<T>;
+  const int t = blockIdx.x;
+  const int seq = seq_of(p.cu_seqlens, p.n, t);
+  const int t0 = p.cu_seqlens[seq], t1 = p.cu_seqlens[seq + 1];
+  const int pos = t - t0;
+  if (t0 < 0 || t < t0 || t >= t1 || t1 > p.total_tokens) {
+    if (threadIdx.x == 0) report(p.status, GDN_ERR_BAD_SEQLENS);
+    return;
+  }
+  const int slot = p.slots[seq];
+  if (slot < 0 || slot >= p.n_slots) {
+    if (threadIdx.x == 0) report(p.status, GDN_ERR_BAD_SLOT);
+    return;
+  }
+  const T* qkv = reinterpret_cast<const T*>(p.qkv);
+  const T* cs = reinterpret_cast<const T*>(p.conv_pool) + size_t(slot) * p.conv_dim * kW;
+  const int nq = p.conv_dim / 4;          // channel quads
+  const int qk_quads = 2 * p.Hk * D / 4;  // quads of q and k (normalised)
+  const int nq_pad = (nq + 31) & ~31;     // whole warps take part in the shuffles
+  constexpr int kHeadLanes = D / 4;       // lanes of one head
+
+  for (int qd = threadIdx.x; qd < nq_pad; qd += kConvThreads) {
+    const bool live = qd < nq;
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) {
+      const int c = qd * 4;
+      float4 win[kW];
+#pragma unroll
+      for (int j = 0; j < kW; ++j) {
+        const int sp = pos - (kW - 1) + j;  // sequence position of window entry j
+        if (sp >= 0) {
+          win[j] = A::load4(qkv + size_t(t0 + sp) * p.qkv_stride + c);
+        } else {
+          // entry kW + sp of the conv state of channels c .. c+3
+          win[j].x = A::to_f(cs[size_t(c + 0) * kW + kW + sp]);
+          win[j].y = A::to_f(cs[size_t(c + 1) * kW + kW + sp]);
+          win[j].z = A::to_f(cs[size_t(c + 2) * kW + kW + sp]);
+          win[j].w = A::to_f(cs[size_t(c + 3) * kW + kW + sp]);
+        }
+      }
+      const float4 w0 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 0) * kW);
+      const float4 w1 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 1) * kW);
+      const float4 w2 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 2) * kW);
+      const float4 w3 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 3) * kW);
+      y.x = silu_f(w0.x * win[0].x + w0.y * win[1].x + w0.z * win[2].x + w0.w * win[3].x);
+      y.y = silu_f(w1.x * win[0].y + w1.y * win[1].y + w1.z * win[2].y + w1.w * win[3].y);
+      y.z = silu_f(w2.x * win[0].z + w2.y * win[1].z + w2.z * win[2].z + w2.w * win[3].z);
+      y.w = silu_f(w3.x * win[0].w + w3.y * win[1].w + w3.z * win[2].w + w3.w * win[3].w);
+    }
+    // L2 norm of each q / k head over its D channels (kHeadLanes lanes).
+    float ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+#pragma unroll
+    for (int off = 1; off < kHeadLanes; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (live) {
+      if (qd < qk_quads) {
+        const bool is_q = qd < qk_quads / 2;
+        const float r = (is_q ? p.q_scale : 1.f) * rsqrtf(ss + p.l2_eps);
+        y.x *= r; y.y *= r; y.z *= r; y.w *= r;
+      }
+      const size_t o = size_t(t) * p.conv_dim + qd * 4;
+      if (p.out_bf16) Act<__nv_bfloat16>::store4(reinterpret_cast<__nv_bfloat16*>(p.out) + o, y);
+      else *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) = y;
+    }
+  }
+}
+
+// New conv state of each (sequence, channel): its last kW raw inputs.
+template <typename T>
+__global__ void gdn_conv_state_kernel(const __grid_constant__ ConvParams p) {
+  using A = Act<T>;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= p.n * p.conv_dim) return;
+  const int seq = idx / p.conv_dim, c = idx - seq * p.conv_dim;
+  const int t0 = p.cu_seqlens[seq], len = p.cu_seqlens[seq + 1] - t0;
+  const int slot = p.slots[seq];
+  if (len <= 0 || t0 < 0 || t0 + len > p.total_tokens || slot < 0 || slot >= p.n_slots) return;
+  T* cs = reinterpret_cast<T*>(p.conv_pool) + (size_t(slot) * p.conv_dim + c) * kW;
+  const float4 old = A::load4(cs);
+  const float o[kW] = {old.x, old.y, old.z, old.w};
+  const T* qkv = reinterpret_cast<const T*>(p.qkv);
+  float nw[kW];
+#pragma unroll
+  for (int j = 0; j < kW; ++j) {
+    const int sp = len - kW + j;  // sequence position of the new entry j
+    nw[j] = sp >= 0 ? A::to_f(qkv[size_t(t0 + sp) * p.qkv_stride + c]) : o[kW + sp];
+  }
+  A::store4(cs, make_float4(nw[0], nw[1], nw[2], nw[3]));
+}
+
+// Validates cu_seqlens once (device-side) for the conv launches.
+__global__ void gdn_seqlens_check_kernel(const int32_t* cu, int n, int total, int32_t* status) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int a = cu[i], b = cu[i + 1];
+    if (a < 0 || b < a || b > total || (i == 0 && a != 0) || (i == n - 1 && b != total))
+      report(status, GDN_ERR_BAD_SEQLENS);
+  }
+}
+
+template <typename T, int D>
+__global__ void gdn_gated_rmsnorm_kernel(const float* __restrict__ o, const T* __restrict__ z,
+                                         int64_t z_stride, const float* __restrict__ w,
+                                         float eps, int T_, int Hv, T* __restrict__ y) {
+  using A = Act<T>;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < T_ * Hv; r += warps) {
+    const int t = r / Hv, h = r - t * Hv;
+    const int j = lane * 4;
+    float4 ov = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (j < D) ov = *reinterpret_cast<const float4*>(o + size_t(r) * D + j);
+    const float ss = warp_sum(ov.x * ov.x + ov.y * ov.y + ov.z * ov.z + ov.w * ov.w);
+    if (j < D) {
+      const float inv = rsqrtf(ss / float(D) + eps);
+      const float4 w4 = *reinterpret_cast<const float4*>(w + j);
+      const float4 z4 = A::load4(z + size_t(t) * z_stride + h * D + j);
+      float4 yv;
+      yv.x = ov.x * inv * w4.x * silu_f(z4.x);
+      yv.y = ov.y * inv * w4.y * silu_f(z4.y);
+      yv.z = ov.z * inv * w4.z * silu_f(z4.z);
+      yv.w = ov.w * inv * w4.w * silu_f(z4.w);
+      A::store4(y + size_t(t) * Hv * D + h * D + j, yv);
+    }
+  }
+}
+
+template <typename T>
+cudaError_t conv_typed(const ConvParams& p, cudaStream_t stream) {
+  gdn_seqlens_check_kernel<<<1, 128, 0, stream>>>(p.cu_seqlens, p.n, p.total_tokens, p.status);
+  if (p.total_tokens > 0) {
+    if (p.D == 128) gdn_conv_kernel<T, 128><<<p.total_tokens, kConvThreads, 0, stream>>>(p);
+    else gdn_conv_kernel<T, 16><<<p.total_tokens, kConvThreads, 0, stream>>>(p);
+  }
+  const int total = p.n * p.conv_dim;
+  gdn_conv_state_kernel<T><<<(total + 255) / 256, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_conv_step(const ConvParams& p, int dtype, cudaStream_t stream) {
+  if (dtype == GDN_DTYPE_BF16) return conv_typed<__nv_bfloat16>(p, stream);
+  return conv_typed<float>(p, stream);
+}
+
+cudaError_t launch_conv_state_update(const ConvParams& p, int dtype, cudaStream_t stream) {
+  const int total = p.n * p.conv_dim;
+  if (dtype == GDN_DTYPE_BF16)
+    gdn_conv_state_kernel<__nv_bfloat16><<<(total + 255) / 256, 256, 0, stream>>>(p);
+  else
+    gdn_conv_state_kernel<float><<<(total + 255) / 256, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_seqlens_check(const int32_t* cu, int n, int total, int32_t* status,
+                                 cudaStream_t stream) {
+  gdn_seqlens_check_kernel<<<1, 128, 0, stream>>>(cu, n, total, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gated_rmsnorm(const float* o, const void* z, int64_t z_stride,
+                                 const float* w, float eps, int T, int Hv, int D, int dtype,
+                                 void* y, cudaStream_t stream) {
+  const int rows = T * Hv;
+  if (rows == 0) return cudaSuccess;
+  const int threads = 256, per_block = threads / 32;
+  int blocks = (rows + per_block - 1) / per_block;
+  const int cap = sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (dtype == GDN_DTYPE_BF16) {
+    auto zp = reinterpret_cast<const __nv_bfloat16*>(z);
+    auto yp = reinterpret_cast<__nv_bfloat16*>(y);
+    if (D == 128) gdn_gated_rmsnorm_kernel<__nv_bfloat16, 128><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
+    else gdn_gated_rmsnorm_kernel<__nv_bfloat16, 16><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
+  } else {
+    auto zp = reinterpret_cast<const float*>(z);
+    auto yp = reinterpret_cast<float*>(y);
+    if (D == 128) gdn_gated_rmsnorm_kernel<float, 128><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
+    else gdn_gated_rmsnorm_kernel<float, 16><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

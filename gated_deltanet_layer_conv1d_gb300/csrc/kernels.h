@@ -1,0 +1,99 @@
+// kernels.h -- host-side declarations of the GDN kernel launchers (internal to libgdn.so).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+constexpr int kMaxG = 4;  // value heads per key head a launch supports
+
+// Parameters of the fused decode / verify kernel (by value, in the constant bank).
+struct RecParams {
+  int32_t Hk, Hv, G, conv_dim, n, n_slots;
+  float q_scale, l2_eps, norm_eps;
+  const float* conv_w;
+  const float* A_log;
+  const float* dt_bias;
+  const float* norm_w;
+  const void* qkv;
+  int64_t qkv_stride;
+  const void* z;
+  int64_t z_stride;
+  const void* a;
+  const void* b;
+  int64_t ab_stride;
+  float* h_pool;           // decode: [n_slots][Hv][D][D]
+  const uint64_t* tables;  // verify: [16][128]
+  void* conv_pool;         // [n_slots][conv_dim][4]
+  const int32_t* slots;    // [n]
+  void* conv_inter;        // verify, nullable: [n][15][conv_dim][4]
+  void* y;
+  float* core_out;
+  int32_t* status;
+  int32_t n_items;         // n * Hk
+  uint8_t ks[GDN_MAX_SEQS];       // tokens of sequence i (original index)
+  uint8_t order[GDN_MAX_SEQS];    // sequence indices, most tokens first
+  uint16_t row_off[GDN_MAX_SEQS]; // first token row of sequence i
+};
+
+// Fused conv + L2 + gates + recurrence + gated norm, one launch for all sequences.
+cudaError_t launch_recurrent(const RecParams& p, int dtype, int D, bool verify,
+                             cudaStream_t stream);
+
+// Conv + SiLU + L2 norm over T tokens of n sequences -> f32 [T][conv_dim]
+// (or bf16 when out_bf16), then the conv-state update.
+struct ConvParams {
+  int32_t Hk, Hv, D, conv_dim, n, n_slots, total_tokens;
+  float q_scale, l2_eps;
+  const float* conv_w;
+  const void* qkv;
+  int64_t qkv_stride;
+  const int32_t* cu_seqlens;
+  void* conv_pool;
+  const int32_t* slots;
+  void* out;
+  int32_t out_bf16;
+  int32_t* status;
+};
+cudaError_t launch_conv_step(const ConvParams& p, int dtype, cudaStream_t stream);
+
+cudaError_t launch_gated_rmsnorm(const float* o, const void* z, int64_t z_stride,
+                                 const float* w, float eps, int T, int Hv, int D, int dtype,
+                                 void* y, cudaStream_t stream);
+
+// Chunked prefill.
+struct PrefillParams {
+  int32_t Hk, Hv, G, D, conv_dim, n, n_slots, total_tokens, max_seqlen, max_chunks;
+  float q_scale, l2_eps, norm_eps;
+  const float* conv_w;
+  const float* A_log;
+  const float* dt_bias;
+  const float* norm_w;
+  const void* qkv;
+  int64_t qkv_stride;
+  const void* z;
+  int64_t z_stride;
+  const void* a;
+  const void* b;
+  int64_t ab_stride;
+  const int32_t* cu_seqlens;
+  const uint64_t* h_ptrs;
+  void* conv_pool;
+  const int32_t* slots;
+  void* y;
+  float* core_out;
+  int32_t* status;
+  void* workspace;
+  size_t workspace_bytes;
+};
+size_t prefill_workspace_bytes(int Hk, int Hv, int D, int n, int total_tokens,
+                               int max_seqlen);
+cudaError_t launch_prefill(const PrefillParams& p, int dtype, cudaStream_t stream);
+
+int sm_count();
+
+}  // namespace gdn

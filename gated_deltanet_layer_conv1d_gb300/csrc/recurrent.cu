@@ -1,0 +1,618 @@
+// recurrent.cu -- token-sequential GDN mixer kernels (sm_103a): fused batched decode,
+// ragged batched verify, and the token-sequential prefill.
+//
+// gdn_recurrent_kernel runs, for every (sequence, key head) "item":
+//   conv + SiLU over the item's channels (q and k of the key head, v of its G value
+//   heads) for the sequence's tokens, the conv-state update, the L2 norms of q and k,
+//   the gates, then for each value head the token-sequential gated delta rule on its
+//   f32 state and the Z-gated RMSNorm of the outputs
+//   (layer_struct.rs: conv1d_l2norm_f32_strided_k, gdn_f32_strided_norm_k,
+//   gdn_f32_strided_norm_smem_k, gated_rms_norm_f32_strided_k for decode;
+//   gdn_wyn_table_k, gdn_f32_strided_norm_snap_k and gdn_verify_fused_conv_kn_batched_k
+//   for the batched verify, which writes every intermediate state through the WY
+//   pointer tables of transformer_layer.rs, VERIFY_WY_TABLE_SEQS).
+// Decode is verify with one token per sequence, its state addressed through the slot
+// pool instead of table 0 and no intermediates.
+//
+// Design (HBM-bound: the state tile is read once, and written once per token kept):
+//   * persistent grid, one CTA of 512 threads per SM; items are dealt to CTAs in a
+//     zig-zag over the item list (most tokens first), so ragged k balances;
+//   * one elected thread streams the 64 KiB state tile of each (item, value head) into
+//     a shared-memory ring with bulk async copies completing on mbarriers; the tile is
+//     moved to registers (32 floats per thread) and its stage refilled at once, so
+//     STAGES tiles are in flight while one is computed;
+//   * thread (warp w, lane l) owns rows rb*32 + (l/8) + 4m (m < 8) and columns
+//     cb*32 + (l%8)*4 .. +3 of the [d_k][d_v] tile (rb = w/4, cb = w%4): every
+//     shared-memory read is conflict-free and every 128-bit global store of a warp
+//     covers four whole 128-byte lines;
+//   * per token, the column sums u = S k and p = S q are reduced in registers, across
+//     the row-lanes with warp shuffles and across the row-block warps through shared
+//     memory (one barrier per token), then
+//       delta = beta (v - alpha u),  S <- alpha S + k delta^T,  o = alpha p + delta (k.q)
+//     which is S_t = alpha S (I - beta k k^T) + beta v k^T, o = S_t q regrouped;
+//   * the gated RMSNorm of a head's outputs runs one warp per token, with z staged in
+//     shared memory by the item prologue.
+//
+// gdn_prefill_seq_kernel is the same per-token update run over a whole sequence, one CTA
+// per (sequence, value head), in segments of 16 tokens (layer_struct.rs,
+// gdn_prefill_k: the sequential prefill recurrence).  It serves head sizes and dtypes
+// the tensor-core chunked prefill does not take.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kW = 4;  // conv width
+
+template <int D, int NT>
+struct RecMap {
+  static constexpr int CQ = (D / 4 < 8) ? D / 4 : 8;  // lanes across a row segment
+  static constexpr int RS = 32 / CQ;                  // rows per warp instruction
+  static constexpr int NW = NT / 32;
+  static constexpr int CB = D / (4 * CQ);             // column blocks
+  static constexpr int RB = NW / CB;                  // row blocks
+  static constexpr int M = D / (RB * RS);             // rows per thread
+  static_assert(CB * RB == NW, "warps must tile the columns");
+  static_assert(RB * RS * M == D, "threads must tile the rows");
+};
+
+// Thread coordinates inside a [D][D] tile.
+template <int D, int NT>
+struct Lane {
+  using Map = RecMap<D, NT>;
+  int warp, lane, rb, rs, col0, rowb;
+  __device__ __forceinline__ Lane(int tid) {
+    warp = tid >> 5;
+    lane = tid & 31;
+    const int cb = warp % Map::CB;
+    rb = warp / Map::CB;
+    const int cq = lane % Map::CQ;
+    rs = lane / Map::CQ;
+    col0 = cb * 4 * Map::CQ + cq * 4;
+    rowb = rb * (Map::RS * Map::M) + rs;  // row of m = 0; row m is rowb + RS*m
+  }
+  __device__ __forceinline__ int row(int m) const { return rowb + Map::RS * m; }
+};
+
+// One token of the gated delta rule on the register tile S (rows L.row(m), columns
+// L.col0..+3).  xq, xk: the normalised q, k of the token in shared memory; xv: its v;
+// red: this token's reduction buffer [2][RB][D] (alternate per token); orow: where the
+// (rb == 0, rs == 0) threads put o.  Contains one __syncthreads.
+template <int D, int NT>
+__device__ __forceinline__ void token_update(float4 (&S)[RecMap<D, NT>::M], const Lane<D, NT>& L,
+                                             const float* xq, const float* xk, const float* xv,
+                                             float al, float be, float kq, float* red,
+                                             float* orow) {
+  using Map = RecMap<D, NT>;
+  float kr[Map::M];
+  float4 u = make_float4(0.f, 0.f, 0.f, 0.f), pp = u;
+#pragma unroll
+  for (int m = 0; m < Map::M; ++m) {
+    const int i = L.row(m);
+    const float ki = xk[i], qi = xq[i];
+    kr[m] = ki;
+    u.x += S[m].x * ki; u.y += S[m].y * ki; u.z += S[m].z * ki; u.w += S[m].w * ki;
+    pp.x += S[m].x * qi; pp.y += S[m].y * qi; pp.z += S[m].z * qi; pp.w += S[m].w * qi;
+  }
+#pragma unroll
+  for (int off = Map::CQ; off < 32; off <<= 1) {
+    u.x += __shfl_xor_sync(0xffffffffu, u.x, off);
+    u.y += __shfl_xor_sync(0xffffffffu, u.y, off);
+    u.z += __shfl_xor_sync(0xffffffffu, u.z, off);
+    u.w += __shfl_xor_sync(0xffffffffu, u.w, off);
+    pp.x += __shfl_xor_sync(0xffffffffu, pp.x, off);
+    pp.y += __shfl_xor_sync(0xffffffffu, pp.y, off);
+    pp.z += __shfl_xor_sync(0xffffffffu, pp.z, off);
+    pp.w += __shfl_xor_sync(0xffffffffu, pp.w, off);
+  }
+  if (L.rs == 0) {
+    *reinterpret_cast<float4*>(red + L.rb * D + L.col0) = u;
+    *reinterpret_cast<float4*>(red + (Map::RB + L.rb) * D + L.col0) = pp;
+  }
+  __syncthreads();
+  float4 U = make_float4(0.f, 0.f, 0.f, 0.f), PP = U;
+#pragma unroll
+  for (int b = 0; b < Map::RB; ++b) {
+    const float4 a4 = *reinterpret_cast<const float4*>(red + b * D + L.col0);
+    const float4 p4 = *reinterpret_cast<const float4*>(red + (Map::RB + b) * D + L.col0);
+    U.x += a4.x; U.y += a4.y; U.z += a4.z; U.w += a4.w;
+    PP.x += p4.x; PP.y += p4.y; PP.z += p4.z; PP.w += p4.w;
+  }
+  const float4 v4 = *reinterpret_cast<const float4*>(xv + L.col0);
+  float4 dl;
+  dl.x = be * (v4.x - al * U.x);
+  dl.y = be * (v4.y - al * U.y);
+  dl.z = be * (v4.z - al * U.z);
+  dl.w = be * (v4.w - al * U.w);
+  if (L.rb == 0 && L.rs == 0) {
+    float4 o;
+    o.x = al * PP.x + dl.x * kq;
+    o.y = al * PP.y + dl.y * kq;
+    o.z = al * PP.z + dl.z * kq;
+    o.w = al * PP.w + dl.w * kq;
+    *reinterpret_cast<float4*>(orow + L.col0) = o;
+  }
+#pragma unroll
+  for (int m = 0; m < Map::M; ++m) {
+    S[m].x = al * S[m].x + kr[m] * dl.x;
+    S[m].y = al * S[m].y + kr[m] * dl.y;
+    S[m].z = al * S[m].z + kr[m] * dl.z;
+    S[m].w = al * S[m].w + kr[m] * dl.w;
+  }
+}
+
+template <int D, int NT>
+__device__ __forceinline__ void store_tile(float* dst, const float4 (&S)[RecMap<D, NT>::M],
+                                           const Lane<D, NT>& L) {
+#pragma unroll
+  for (int m = 0; m < RecMap<D, NT>::M; ++m)
+    *reinterpret_cast<float4*>(dst + L.row(m) * D + L.col0) = S[m];
+}
+
+// L2-normalises q and k of `k` tokens held in shared memory (q at x + t*stride, k right
+// after it) and records kq[t] = q.k; one warp per token.
+template <int D, int NW>
+__device__ __forceinline__ void l2norm_tokens(float* x, int stride, int k, float q_scale,
+                                              float eps, float* kq_s, int warp, int lane) {
+  for (int t = warp; t < k; t += NW) {
+    float* xq = x + t * stride;
+    float* xk = xq + D;
+    float sq = 0.f, sk = 0.f;
+    for (int i = lane; i < D; i += 32) {
+      sq += xq[i] * xq[i];
+      sk += xk[i] * xk[i];
+    }
+    sq = warp_sum(sq);
+    sk = warp_sum(sk);
+    const float rq = q_scale * rsqrtf(sq + eps);
+    const float rk = rsqrtf(sk + eps);
+    float kq = 0.f;
+    for (int i = lane; i < D; i += 32) {
+      const float qn = xq[i] * rq, kn = xk[i] * rk;
+      xq[i] = qn;
+      xk[i] = kn;
+      kq += qn * kn;
+    }
+    kq = warp_sum(kq);
+    if (lane == 0) kq_s[t] = kq;
+  }
+}
+
+// Gated RMSNorm of one value head's outputs for `k` tokens, one warp per token.
+// o: [k][D] f32 in shared memory; z: [k][zstride] f32 in shared memory (this head's
+// slice); y row r = row0 + t.
+template <typename T, int D, int NW>
+__device__ __forceinline__ void norm_tokens(const float* o, const float* z, int zstride, int k,
+                                            int row0, int h, const float* norm_w, float eps,
+                                            int Hv, T* y, float* core_out, int warp, int lane) {
+  using A = Act<T>;
+  for (int t = warp; t < k; t += NW) {
+    const int row = row0 + t;
+    const int j = lane * 4;
+    float4 ov = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (j < D) ov = *reinterpret_cast<const float4*>(o + t * D + j);
+    const float ss = warp_sum(ov.x * ov.x + ov.y * ov.y + ov.z * ov.z + ov.w * ov.w);
+    if (j < D) {
+      const float inv = rsqrtf(ss / float(D) + eps);
+      const float4 w4 = *reinterpret_cast<const float4*>(norm_w + j);
+      const float4 z4 = *reinterpret_cast<const float4*>(z + t * zstride + j);
+      float4 yv;
+      yv.x = ov.x * inv * w4.x * silu_f(z4.x);
+      yv.y = ov.y * inv * w4.y * silu_f(z4.y);
+      yv.z = ov.z * inv * w4.z * silu_f(z4.z);
+      yv.w = ov.w * inv * w4.w * silu_f(z4.w);
+      A::store4(y + size_t(row) * Hv * D + h * D + j, yv);
+      if (core_out) *reinterpret_cast<float4*>(core_out + (size_t(row) * Hv + h) * D + j) = ov;
+    }
+  }
+}
+
+// ======================================================================================
+// decode / verify
+// ======================================================================================
+template <int D, int NT, int KMAX, int STAGES>
+struct RecSmem {
+  using Map = RecMap<D, NT>;
+  static constexpr size_t kTile = size_t(D) * D * sizeof(float);
+  static constexpr size_t kStage = 0;
+  static constexpr size_t kRed = kStage + STAGES * kTile;                  // [2][2][RB][D]
+  static constexpr size_t kObuf = kRed + size_t(2) * 2 * Map::RB * D * 4;  // [KMAX][D]
+  static constexpr size_t kBar = kObuf + size_t(KMAX) * D * 4;             // [STAGES] u64
+  static constexpr size_t kGate = kBar + 8 * ((STAGES + 1) / 2 * 2);       // [KMAX][kMaxG][2]
+  static constexpr size_t kKq = kGate + size_t(KMAX) * kMaxG * 2 * 4;      // [KMAX]
+  static constexpr size_t kXs = kKq + ((size_t(KMAX) * 4 + 15) / 16) * 16;
+  // xs: [KMAX][(2 + 2G) D] = q | k | v of G heads | z of G heads, per token
+  static size_t bytes(int G) { return kXs + size_t(KMAX) * (2 + 2 * G) * D * 4; }
+};
+
+// The item this CTA owns in round r: a zig-zag over the item list.
+__device__ __forceinline__ int item_at(int cta, int r, int P) {
+  return r * P + ((r & 1) ? (P - 1 - cta) : cta);
+}
+
+struct Item {
+  int seq, kh, k, row0, slot;
+};
+
+// Decodes item j and checks everything the device must check before touching memory.
+// Returns 0 if the item can run, else the GDN_ERR_* code.
+template <bool VERIFY>
+__device__ __forceinline__ int item_decode(const RecParams& p, int j, Item& it) {
+  const int rank = j / p.Hk;
+  it.kh = j - rank * p.Hk;
+  it.seq = VERIFY ? int(p.order[rank]) : rank;
+  it.k = VERIFY ? int(p.ks[it.seq]) : 1;
+  it.row0 = VERIFY ? int(p.row_off[it.seq]) : it.seq;
+  it.slot = p.slots[it.seq];
+  if (it.slot < 0 || it.slot >= p.n_slots) return GDN_ERR_BAD_SLOT;
+  if (VERIFY) {
+    for (int t = 0; t < it.k; ++t) {
+      const uint64_t e = p.tables[t * GDN_VERIFY_WY_TABLE_SEQS + it.seq];
+      if (e == 0 || (e & 15u) != 0) return GDN_ERR_BAD_TABLE_ENTRY;
+    }
+  }
+  return 0;
+}
+
+// The state of value head h of an item: written after token t (t = k-1: final state).
+template <int D, bool VERIFY>
+__device__ __forceinline__ float* state_dst(const RecParams& p, const Item& it, int h, int t) {
+  if (VERIFY) {
+    const int table = (t == it.k - 1) ? 0 : t + 1;
+    const uint64_t e = p.tables[table * GDN_VERIFY_WY_TABLE_SEQS + it.seq];
+    return reinterpret_cast<float*>(e) + size_t(h) * D * D;
+  }
+  return p.h_pool + (size_t(it.slot) * p.Hv + h) * D * D;
+}
+
+// The state of value head h of an item as read at its start.
+template <int D, bool VERIFY>
+__device__ __forceinline__ const float* state_src(const RecParams& p, const Item& it, int h) {
+  if (VERIFY) {
+    const uint64_t e = p.tables[it.seq];  // table 0
+    return reinterpret_cast<const float*>(e) + size_t(h) * D * D;
+  }
+  return p.h_pool + (size_t(it.slot) * p.Hv + h) * D * D;
+}
+
+template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY>
+__global__ void __launch_bounds__(NT, 1)
+    gdn_recurrent_kernel(const __grid_constant__ RecParams p) {
+  using Map = RecMap<D, NT>;
+  using SL = RecSmem<D, NT, KMAX, STAGES>;
+  using A = Act<T>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  float* stage = reinterpret_cast<float*>(smem + SL::kStage);
+  float* red = reinterpret_cast<float*>(smem + SL::kRed);
+  float* obuf = reinterpret_cast<float*>(smem + SL::kObuf);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SL::kBar);
+  float* gate = reinterpret_cast<float*>(smem + SL::kGate);
+  float* kq_s = reinterpret_cast<float*>(smem + SL::kKq);
+  float* xs = reinterpret_cast<float*>(smem + SL::kXs);
+
+  const int tid = threadIdx.x;
+  const Lane<D, NT> L(tid);
+  const int G = p.G, Hk = p.Hk;
+  const int CH = (2 + G) * D;   // conv channels of one item
+  const int CHX = CH + G * D;   // plus the z channels
+  const int P = gridDim.x, cta = blockIdx.x;
+  const int rounds = (p.n_items + P - 1) / P;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // ---- producer cursor (thread 0 only): the next (round, value head) to load.  It walks
+  // the same item sequence as the consumer loop below and skips the same bad items.
+  int pr = 0, pg = 0;
+  int issued = 0;  // tiles the producer has started
+  Item pit;
+  bool pvalid = false;
+  auto prod_next = [&](const float** src) -> bool {
+    while (pr < rounds) {
+      if (!pvalid) {
+        const int j = item_at(cta, pr, P);
+        if (j < p.n_items && item_decode<VERIFY>(p, j, pit) == 0) {
+          pvalid = true;
+          pg = 0;
+        } else {
+          ++pr;
+          continue;
+        }
+      }
+      if (pg < G) {
+        *src = state_src<D, VERIFY>(p, pit, pit.kh * G + pg);
+        ++pg;
+        return true;
+      }
+      pvalid = false;
+      ++pr;
+    }
+    return false;
+  };
+  auto prod_issue = [&](int s) {
+    const float* src;
+    if (prod_next(&src)) {
+      ++issued;
+      mbar_arrive_expect_tx(&bar[s], uint32_t(SL::kTile));
+      constexpr uint32_t kPiece = SL::kTile >= 16384 ? 16384u : uint32_t(SL::kTile);
+#pragma unroll
+      for (uint32_t off = 0; off < SL::kTile; off += kPiece)
+        bulk_g2s(reinterpret_cast<unsigned char*>(stage) + s * SL::kTile + off,
+                 reinterpret_cast<const unsigned char*>(src) + off, kPiece, &bar[s]);
+    }
+  };
+  if (tid == 0)
+    for (int s = 0; s < STAGES; ++s) prod_issue(s);
+
+  int q = 0;  // tiles consumed by this CTA
+  for (int r = 0; r < rounds; ++r) {
+    const int j = item_at(cta, r, P);
+    if (j >= p.n_items) continue;
+    Item it;
+    const int bad = item_decode<VERIFY>(p, j, it);
+    if (bad) {
+      if (tid == 0) report(p.status, bad);
+      continue;
+    }
+    const int k = it.k;
+
+    // ---------------- item prologue: conv + SiLU (+ state update), z, gates, L2 norms
+    for (int lc = tid; lc < CHX; lc += NT) {
+      if (lc >= CH) {  // z channel: staged as f32
+        const int zc = lc - CH;
+        const T* zp = reinterpret_cast<const T*>(p.z) + size_t(it.row0) * p.z_stride +
+                      it.kh * G * D + zc;
+        for (int t = 0; t < k; ++t) xs[t * CHX + lc] = A::to_f(zp[size_t(t) * p.z_stride]);
+        continue;
+      }
+      int gc;
+      if (lc < D) gc = it.kh * D + lc;
+      else if (lc < 2 * D) gc = Hk * D + it.kh * D + (lc - D);
+      else gc = 2 * Hk * D + it.kh * G * D + (lc - 2 * D);
+      T* cs = reinterpret_cast<T*>(p.conv_pool) + (size_t(it.slot) * p.conv_dim + gc) * kW;
+      const float4 w4 = *reinterpret_cast<const float4*>(p.conv_w + size_t(gc) * kW);
+      float buf[kW + KMAX];
+      const float4 s4 = A::load4(cs);
+      buf[0] = s4.x; buf[1] = s4.y; buf[2] = s4.z; buf[3] = s4.w;
+      const T* xrow = reinterpret_cast<const T*>(p.qkv) + size_t(it.row0) * p.qkv_stride + gc;
+#pragma unroll
+      for (int t = 0; t < KMAX; ++t)
+        if (t < k) buf[kW + t] = A::to_f(xrow[size_t(t) * p.qkv_stride]);
+#pragma unroll
+      for (int t = 0; t < KMAX; ++t) {
+        if (t < k) {
+          // window of token t: the last kW raw inputs, buf[t+1 .. t+4]
+          const float acc = w4.x * buf[t + 1] + w4.y * buf[t + 2] + w4.z * buf[t + 3] +
+                            w4.w * buf[t + 4];
+          xs[t * CHX + lc] = silu_f(acc);
+          if (VERIFY && p.conv_inter && t < k - 1) {
+            T* ci = reinterpret_cast<T*>(p.conv_inter) +
+                    ((size_t(it.seq) * (GDN_VERIFY_WY_TABLES_PER_LAYER - 1) + t) * p.conv_dim + gc) * kW;
+            A::store4(ci, make_float4(buf[t + 1], buf[t + 2], buf[t + 3], buf[t + 4]));
+          }
+        }
+      }
+      float4 ns = s4;
+#pragma unroll
+      for (int t = 1; t <= KMAX; ++t)
+        if (t == k) ns = make_float4(buf[t], buf[t + 1], buf[t + 2], buf[t + 3]);
+      A::store4(cs, ns);  // exact copies of raw inputs
+    }
+    for (int idx = tid; idx < k * G; idx += NT) {
+      const int t = idx / G, g = idx - t * G;
+      const int h = it.kh * G + g;
+      const size_t ro = size_t(it.row0 + t) * p.ab_stride + h;
+      float al, be;
+      gates_f(A::to_f(reinterpret_cast<const T*>(p.a)[ro]),
+              A::to_f(reinterpret_cast<const T*>(p.b)[ro]), p.A_log[h], p.dt_bias[h], &al, &be);
+      gate[(t * kMaxG + g) * 2 + 0] = al;
+      gate[(t * kMaxG + g) * 2 + 1] = be;
+    }
+    __syncthreads();
+    l2norm_tokens<D, Map::NW>(xs, CHX, k, p.q_scale, p.l2_eps, kq_s, L.warp, L.lane);
+    __syncthreads();
+
+    // ---------------- value heads of the item
+    for (int g = 0; g < G; ++g) {
+      const int h = it.kh * G + g;
+      const int s = q % STAGES;
+      const uint32_t parity = uint32_t(q / STAGES) & 1u;
+      const bool ok = mbar_wait_bounded(&bar[s], parity);
+      float4 S[Map::M];
+      const float* tile = stage + size_t(s) * D * D;
+#pragma unroll
+      for (int m = 0; m < Map::M; ++m)
+        S[m] = *reinterpret_cast<const float4*>(tile + L.row(m) * D + L.col0);
+      if (__syncthreads_or(!ok)) {
+        if (tid == 0) {
+          report(p.status, GDN_ERR_TIMEOUT);
+          // Let this CTA's copies still in flight land before it exits (bounded).
+          for (int x = q; x < issued; ++x)
+            mbar_wait_bounded(&bar[x % STAGES], uint32_t(x / STAGES) & 1u, kWaitBudgetNs / 8);
+        }
+        return;
+      }
+      ++q;
+      if (tid == 0) {
+        fence_proxy_async_smem();
+        prod_issue(s);  // refill the stage just emptied
+      }
+      for (int t = 0; t < k; ++t) {
+        const float* xq = xs + t * CHX;
+        token_update<D, NT>(S, L, xq, xq + D, xq + (2 + g) * D, gate[(t * kMaxG + g) * 2 + 0],
+                            gate[(t * kMaxG + g) * 2 + 1], kq_s[t],
+                            red + (t & 1) * 2 * Map::RB * D, obuf + t * D);
+        if (VERIFY || t == k - 1) store_tile<D, NT>(state_dst<D, VERIFY>(p, it, h, t), S, L);
+      }
+      __syncthreads();  // obuf complete
+      norm_tokens<T, D, Map::NW>(obuf, xs + CH + g * D, CHX, k, it.row0, h, p.norm_w,
+                                 p.norm_eps, p.Hv, reinterpret_cast<T*>(p.y), p.core_out,
+                                 L.warp, L.lane);
+    }
+  }
+}
+
+template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY>
+cudaError_t launch_rec(const RecParams& p, cudaStream_t stream) {
+  using SL = RecSmem<D, NT, KMAX, STAGES>;
+  auto kern = gdn_recurrent_kernel<T, D, NT, KMAX, STAGES, VERIFY>;
+  const size_t smem = SL::bytes(p.G);
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  const int P = p.n_items < sm_count() ? p.n_items : sm_count();
+  kern<<<P, NT, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_rec_typed(const RecParams& p, int D, bool verify, cudaStream_t stream) {
+  if (D == 128) {
+    if (verify) return launch_rec<T, 128, 512, GDN_VERIFY_K_MAX, 2, true>(p, stream);
+    return launch_rec<T, 128, 512, 1, 3, false>(p, stream);
+  }
+  if (verify) return launch_rec<T, 16, 64, GDN_VERIFY_K_MAX, 2, true>(p, stream);
+  return launch_rec<T, 16, 64, 1, 3, false>(p, stream);
+}
+
+// ======================================================================================
+// token-sequential prefill: one CTA per (sequence, value head)
+// ======================================================================================
+constexpr int kSeg = 16;  // tokens per segment
+
+template <int D, int NT>
+struct SeqSmem {
+  using Map = RecMap<D, NT>;
+  static constexpr int kCHX = 4 * D;  // q | k | v | z of one value head
+  static constexpr size_t kRed = 0;
+  static constexpr size_t kObuf = kRed + size_t(2) * 2 * Map::RB * D * 4;
+  static constexpr size_t kGate = kObuf + size_t(kSeg) * D * 4;
+  static constexpr size_t kKq = kGate + kSeg * 2 * 4;
+  static constexpr size_t kXs = kKq + kSeg * 4;
+  static constexpr size_t kBytes = kXs + size_t(kSeg) * kCHX * 4;
+};
+
+template <typename T, int D, int NT>
+__global__ void __launch_bounds__(NT, 1)
+    gdn_prefill_seq_kernel(const __grid_constant__ PrefillParams p) {
+  using Map = RecMap<D, NT>;
+  using SL = SeqSmem<D, NT>;
+  using A = Act<T>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  float* red = reinterpret_cast<float*>(smem + SL::kRed);
+  float* obuf = reinterpret_cast<float*>(smem + SL::kObuf);
+  float* gate = reinterpret_cast<float*>(smem + SL::kGate);
+  float* kq_s = reinterpret_cast<float*>(smem + SL::kKq);
+  float* xs = reinterpret_cast<float*>(smem + SL::kXs);
+  constexpr int CHX = SL::kCHX;
+
+  const int tid = threadIdx.x;
+  const Lane<D, NT> L(tid);
+  const int seq = blockIdx.x / p.Hv, h = blockIdx.x % p.Hv;
+  const int kh = h / p.G;
+  const int t_begin = p.cu_seqlens[seq], t_end = p.cu_seqlens[seq + 1];
+  const int len = t_end - t_begin;
+  const int slot = p.slots[seq];
+  const uint64_t hp = p.h_ptrs[seq];
+  {
+    int bad = 0;
+    if (t_begin < 0 || len < 0 || t_end > p.total_tokens || len > p.max_seqlen)
+      bad = GDN_ERR_BAD_SEQLENS;
+    else if (slot < 0 || slot >= p.n_slots) bad = GDN_ERR_BAD_SLOT;
+    else if (hp == 0 || (hp & 15u) != 0) bad = GDN_ERR_BAD_TABLE_ENTRY;
+    if (bad) {
+      if (tid == 0) report(p.status, bad);
+      return;
+    }
+  }
+  float* Hg = reinterpret_cast<float*>(hp) + size_t(h) * D * D;
+  float4 S[Map::M];
+#pragma unroll
+  for (int m = 0; m < Map::M; ++m)
+    S[m] = *reinterpret_cast<const float4*>(Hg + L.row(m) * D + L.col0);
+  const T* cs = reinterpret_cast<const T*>(p.conv_pool) + size_t(slot) * p.conv_dim * kW;
+  const T* qkv = reinterpret_cast<const T*>(p.qkv);
+
+  for (int t0 = 0; t0 < len; t0 += kSeg) {
+    const int k = (len - t0) < kSeg ? (len - t0) : kSeg;
+    for (int lc = tid; lc < CHX; lc += NT) {
+      if (lc >= 3 * D) {  // z
+        const T* zp = reinterpret_cast<const T*>(p.z) + size_t(t_begin + t0) * p.z_stride +
+                      h * D + (lc - 3 * D);
+        for (int t = 0; t < k; ++t) xs[t * CHX + lc] = A::to_f(zp[size_t(t) * p.z_stride]);
+        continue;
+      }
+      int gc;
+      if (lc < D) gc = kh * D + lc;
+      else if (lc < 2 * D) gc = p.Hk * D + kh * D + (lc - D);
+      else gc = 2 * p.Hk * D + h * D + (lc - 2 * D);
+      const float4 w4 = *reinterpret_cast<const float4*>(p.conv_w + size_t(gc) * kW);
+      // raw input at sequence position pos: pos < 0 reads the conv state (entry kW + pos)
+      auto raw = [&](int pos) -> float {
+        return pos < 0 ? A::to_f(cs[size_t(gc) * kW + kW + pos])
+                       : A::to_f(qkv[size_t(t_begin + pos) * p.qkv_stride + gc]);
+      };
+      float w0 = raw(t0 - 3), w1 = raw(t0 - 2), w2 = raw(t0 - 1);
+      for (int t = 0; t < k; ++t) {
+        const float w3 = raw(t0 + t);
+        xs[t * CHX + lc] = silu_f(w4.x * w0 + w4.y * w1 + w4.z * w2 + w4.w * w3);
+        w0 = w1; w1 = w2; w2 = w3;
+      }
+    }
+    for (int t = tid; t < k; t += NT) {
+      const size_t ro = size_t(t_begin + t0 + t) * p.ab_stride + h;
+      float al, be;
+      gates_f(A::to_f(reinterpret_cast<const T*>(p.a)[ro]),
+              A::to_f(reinterpret_cast<const T*>(p.b)[ro]), p.A_log[h], p.dt_bias[h], &al, &be);
+      gate[2 * t] = al;
+      gate[2 * t + 1] = be;
+    }
+    __syncthreads();
+    l2norm_tokens<D, Map::NW>(xs, CHX, k, p.q_scale, p.l2_eps, kq_s, L.warp, L.lane);
+    __syncthreads();
+    for (int t = 0; t < k; ++t) {
+      const float* xq = xs + t * CHX;
+      token_update<D, NT>(S, L, xq, xq + D, xq + 2 * D, gate[2 * t], gate[2 * t + 1], kq_s[t],
+                          red + (t & 1) * 2 * Map::RB * D, obuf + t * D);
+    }
+    __syncthreads();
+    norm_tokens<T, D, Map::NW>(obuf, xs + 3 * D, CHX, k, t_begin + t0, h, p.norm_w, p.norm_eps,
+                               p.Hv, reinterpret_cast<T*>(p.y), p.core_out, L.warp, L.lane);
+    __syncthreads();  // xs, obuf and gate are rewritten by the next segment
+  }
+  store_tile<D, NT>(Hg, S, L);
+}
+
+template <typename T, int D, int NT>
+cudaError_t launch_seq(const PrefillParams& p, cudaStream_t stream) {
+  using SL = SeqSmem<D, NT>;
+  auto kern = gdn_prefill_seq_kernel<T, D, NT>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SL::kBytes));
+  if (e != cudaSuccess) return e;
+  kern<<<p.n * p.Hv, NT, SL::kBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent(const RecParams& p, int dtype, int D, bool verify,
+                             cudaStream_t stream) {
+  if (dtype == GDN_DTYPE_BF16) return launch_rec_typed<__nv_bfloat16>(p, D, verify, stream);
+  return launch_rec_typed<float>(p, D, verify, stream);
+}
+
+cudaError_t launch_prefill_sequential(const PrefillParams& p, int dtype, cudaStream_t stream) {
+  if (dtype == GDN_DTYPE_BF16) {
+    if (p.D == 128) return launch_seq<__nv_bfloat16, 128, 512>(p, stream);
+    return launch_seq<__nv_bfloat16, 16, 64>(p, stream);
+  }
+  if (p.D == 128) return launch_seq<float, 128, 512>(p, stream);
+  return launch_seq<float, 16, 64>(p, stream);
+}
+
+}  // namespace gdn

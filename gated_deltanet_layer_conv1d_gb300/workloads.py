@@ -131,29 +131,29 @@ def tiny_check(q_scale_one: bool = False, prefill_tokens: int = 64, decode_steps
 
 
 def batched_decode(n: int = 128, steps: int = 1, shape: LayerShape = FULL,
-                   seed: int = SEED) -> Workload:
-    """n sequences x 1 token per step; f32 state and bf16 conv state ~N(0, 0.1); bf16
-    activations.  `tokens` is step 0, `steps` the following steps."""
+                   seed: int = SEED, bf16: bool = True) -> Workload:
+    """n sequences x 1 token per step; f32 state and conv state ~N(0, 0.1); bf16 (or f32)
+    activations and conv state.  `tokens` is step 0, `steps` the following steps."""
     rng = np.random.default_rng(seed)
     w = make_weights(rng, shape)
-    H0, conv0 = make_states(rng, shape, n, bf16=True)
-    all_steps = [make_tokens(rng, shape, n, bf16=True) for _ in range(steps)]
+    H0, conv0 = make_states(rng, shape, n, bf16=bf16)
+    all_steps = [make_tokens(rng, shape, n, bf16=bf16) for _ in range(steps)]
     perm = rng.permutation(n).astype(np.int32)
-    return Workload(f"batched_decode_{n}seq", shape, True, w, H0, conv0,
+    return Workload(f"batched_decode_{n}seq", shape, bf16, w, H0, conv0,
                     np.ones(n, np.int32), all_steps[0], all_steps[1:],
                     extra={"slot_perm": perm})
 
 
 def ragged_verify(n: int = 128, k_lo: int = 2, k_hi: int = 16, shape: LayerShape = FULL,
-                  seed: int = SEED) -> Workload:
+                  seed: int = SEED, bf16: bool = True) -> Workload:
     """n sequences with k_i ~ U{k_lo..k_hi} draft tokens each; states ~N(0, 0.1)."""
     rng = np.random.default_rng(seed)
     w = make_weights(rng, shape)
     ks = rng.integers(k_lo, k_hi + 1, size=n).astype(np.int32)
-    H0, conv0 = make_states(rng, shape, n, bf16=True)
-    tok = make_tokens(rng, shape, int(ks.sum()), bf16=True)
+    H0, conv0 = make_states(rng, shape, n, bf16=bf16)
+    tok = make_tokens(rng, shape, int(ks.sum()), bf16=bf16)
     perm = rng.permutation(n).astype(np.int32)
-    return Workload(f"ragged_verify_{n}seq", shape, True, w, H0, conv0, ks, tok,
+    return Workload(f"ragged_verify_{n}seq", shape, bf16, w, H0, conv0, ks, tok,
                     extra={"slot_perm": perm})
 
 

@@ -1,0 +1,245 @@
+/*
+ * gdn.h -- C ABI of libgdn.so, the Gated DeltaNet (GDN) token mixer for GB300 (sm_103a).
+ *
+ * One GDN layer's token mixer, as the `qwen3_ssm` layer of the reference engine runs it:
+ *   causal depthwise conv over the raw [Q|K|V] channels, SiLU, per-key-head L2 norm of
+ *   q and k (layer_struct.rs, Qwen3SsmLayer::conv1d_l2norm_f32_k);
+ *   gates alpha = exp(-exp(A_log) * softplus(a + dt_bias)), beta = sigmoid(b)
+ *   (layer_struct.rs, ba_gates_k / compute_gdn_gates_k);
+ *   the gated delta rule on an f32 state S (d_v x d_k) per value head,
+ *       S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   o_t = S_t q_t
+ *   (layer_struct.rs, gdn_f32_k and its strided / WY / prefill variants);
+ *   the Z-gated RMSNorm y = o / sqrt(mean(o^2) + eps) * w * SiLU(z)
+ *   (layer_struct.rs, gated_rms_norm_f32_k).
+ *
+ * Conventions shared by every entry point
+ *   - Ownership: the caller owns every buffer.  The library allocates nothing, keeps no
+ *     state between calls and never synchronises; every GPU call is enqueued on `stream`.
+ *   - Errors: arguments are validated on the host first; on any error the call returns
+ *     a nonzero gdn_status and launches nothing (trait_layer.rs, the module invariant
+ *     that a refused mode "returns an error and launches nothing").  Problems only the
+ *     device can see (a NULL or misaligned table entry, a slot out of range, bad
+ *     cu_seqlens, a bounded wait that ran out) are written by the kernel to the
+ *     caller's device status word `*status_dev` -- the first error wins, the kernel
+ *     skips the affected work and returns normally; it never traps.  The caller zeroes
+ *     the word before the call and reads it afterwards.
+ *   - Pointers marked "device" are CUDA device (or managed) memory; "host" is host memory.
+ *   - Row strides are in ELEMENTS of the activation dtype.
+ *   - Supported shapes: (d_k, d_v) in {(16, 16), (128, 128)}, d_conv = 4,
+ *     n_v_heads a multiple of n_k_heads with G = n_v_heads / n_k_heads <= 4.
+ *
+ * Layouts (readings of the reference pages; the design notes list each one)
+ *   raw QKV row  [conv_dim] = [Q: n_k_heads*d_k | K: n_k_heads*d_k | V: n_v_heads*d_v],
+ *                each head's channels contiguous (layer_struct.rs, Qwen3SsmLayer doc:
+ *                the QKVZ projection is brought into [Q | K | V | Z] order);
+ *   Z row        [n_v_heads*d_v];   a, b rows [n_v_heads];
+ *   value head h reads key head h / G;
+ *   h state of one sequence [n_v_heads][d_k][d_v] f32, element (i, j) = S[j][i]
+ *                (layer_struct.rs, h_state_bytes = nv * kd * vd values);
+ *   conv state of one sequence [conv_dim][d_conv] in the activation dtype, the last
+ *                d_conv raw inputs of each channel, oldest first (layer_struct.rs,
+ *                conv_state_bytes = conv_dim * d_conv values); conv_w[c][d_conv-1]
+ *                multiplies the newest input;
+ *   y row        [n_v_heads*d_v] in the activation dtype.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+/* A CUDA stream: the same type as cudaStream_t.  NULL is the legacy default stream. */
+typedef struct CUstream_st* gdn_stream_t;
+
+typedef int32_t gdn_status;
+
+/* Host-side status codes (returned). */
+#define GDN_OK 0
+#define GDN_ERR_INVALID_ARGUMENT 1   /* a count, size, stride, eps or enum out of range */
+#define GDN_ERR_UNSUPPORTED_DIMS 2   /* head dims / conv width / G not built (see above) */
+#define GDN_ERR_NULL_POINTER 3       /* a required pointer is NULL */
+#define GDN_ERR_MISALIGNED 4         /* a pointer or stride breaks the alignment rule */
+#define GDN_ERR_BAD_K 5              /* a verify k outside 2..16 */
+#define GDN_ERR_TOO_MANY_SEQS 6      /* more than GDN_MAX_SEQS sequences in one call */
+#define GDN_ERR_WORKSPACE_TOO_SMALL 7
+#define GDN_ERR_CUDA 8               /* a CUDA runtime call (launch, attribute) failed */
+/* Device-side codes (written to *status_dev by a kernel). */
+#define GDN_ERR_BAD_TABLE_ENTRY 16   /* verify: a needed table entry is NULL or not 16-B aligned */
+#define GDN_ERR_BAD_SLOT 17          /* a slot index outside [0, n_slots) */
+#define GDN_ERR_BAD_SEQLENS 18       /* cu_seqlens not monotone / not matching the sizes */
+#define GDN_ERR_TIMEOUT 19           /* a bounded device-side wait ran out */
+
+/* Activation dtypes (raw QKV, Z, a, b, the conv state and the output y). */
+#define GDN_DTYPE_F32 0
+#define GDN_DTYPE_BF16 1
+
+/* Most sequences one batched decode or verify call holds, and the WY pointer-table
+ * layout of the batched verify (transformer_layer.rs, VERIFY_WY_TABLE_SEQS = 128,
+ * VERIFY_WY_TABLES_PER_LAYER = 16, VERIFY_WY_TABLE_STRIDE_BYTES = SEQS * 8,
+ * VERIFY_WY_LAYER_STRIDE_BYTES = TABLES * TABLE_STRIDE): per layer, 16 tables of 128
+ * u64 entries lie back to back; table 0 holds each sequence's h state, table t + 1 its
+ * intermediate t; entries a call does not use stay zero; strides do not depend on k. */
+#define GDN_MAX_SEQS 128
+#define GDN_VERIFY_WY_TABLE_SEQS 128
+#define GDN_VERIFY_WY_TABLES_PER_LAYER 16
+#define GDN_VERIFY_WY_TABLE_STRIDE_BYTES (GDN_VERIFY_WY_TABLE_SEQS * 8)
+#define GDN_VERIFY_WY_LAYER_STRIDE_BYTES \
+  (GDN_VERIFY_WY_TABLES_PER_LAYER * GDN_VERIFY_WY_TABLE_STRIDE_BYTES)
+#define GDN_VERIFY_K_MIN 2
+#define GDN_VERIFY_K_MAX 16
+#define GDN_PREFILL_CHUNK 64
+
+typedef struct {
+  int32_t n_k_heads; /* H_k */
+  int32_t n_v_heads; /* H_v, a multiple of H_k */
+  int32_t d_k;
+  int32_t d_v;
+  int32_t d_conv;    /* conv width; 4 */
+  float q_scale;     /* q <- q / sqrt(sum q^2 + l2_eps) * q_scale */
+  float l2_eps;      /* >= 0 */
+  float norm_eps;    /* gated RMSNorm epsilon, >= 0 */
+} gdn_dims;
+
+/* Layer parameters, all f32 device memory. */
+typedef struct {
+  const float* conv_w;  /* [conv_dim][d_conv] */
+  const float* A_log;   /* [n_v_heads] */
+  const float* dt_bias; /* [n_v_heads] */
+  const float* norm_w;  /* [d_v], shared by all value heads */
+} gdn_weights;
+
+/* Per-token activations, device memory, rows in token order (sequence-major when a call
+ * holds several sequences).  Base pointers of qkv and z are 16-byte aligned and their
+ * row strides (in elements) are multiples of 16 bytes; a and b are element aligned. */
+typedef struct {
+  const void* qkv;    /* [T][qkv_stride], the first conv_dim elements of a row are used */
+  int64_t qkv_stride;
+  const void* z;      /* [T][z_stride], the first n_v_heads*d_v elements are used */
+  int64_t z_stride;
+  const void* a;      /* [T][ab_stride], decay logits (first n_v_heads elements) */
+  const void* b;      /* [T][ab_stride], write-strength logits */
+  int64_t ab_stride;
+  int32_t dtype;      /* GDN_DTYPE_*: dtype of qkv, z, a, b, the conv state and y */
+} gdn_inputs;
+
+/* Batched single-token decode across n sequences (trait_layer.rs,
+ * TransformerLayer::decode_batched / decode_multi_seq; layer_struct.rs, the strided
+ * conv1d_l2norm_f32_strided_k, gdn_f32_strided_norm_k and
+ * gated_rms_norm_f32_strided_k, here fused into one launch).
+ *   inputs    : n rows, row i is sequence i's token.
+ *   h_pool    : device [n_slots][n_v_heads][d_k][d_v] f32, 16-B aligned; the state of
+ *               sequence i is slot slots_dev[i], read and written in place.
+ *   conv_pool : device [n_slots][conv_dim][d_conv] in inputs->dtype, updated in place.
+ *   slots_dev : device int32 [n]; distinct slots (a repeated slot races).
+ *   y         : device [n][n_v_heads*d_v] in inputs->dtype.
+ *   core_out  : device f32 [n][n_v_heads][d_v] (o before the norm), or NULL.
+ *   status_dev: device int32 status word (see conventions).
+ * Returns GDN_ERR_TOO_MANY_SEQS for n > GDN_MAX_SEQS; n == 0 is a no-op. */
+GDN_API gdn_status gdn_decode_batched(const gdn_dims* dims, const gdn_weights* weights,
+                              const gdn_inputs* inputs, int32_t n, float* h_pool,
+                              void* conv_pool, int32_t n_slots, const int32_t* slots_dev,
+                              void* y, float* core_out, int32_t* status_dev,
+                              gdn_stream_t stream);
+
+/* Ragged speculative verify: sequence i runs ks_host[i] draft tokens in one launch
+ * (trait_layer.rs, TransformerLayer::decode_verify_multi; layer_struct.rs, the
+ * pointer-table wyN kernels gdn_wyn_table_k and the snapshot-writing
+ * gdn_f32_strided_norm_snap_k).  Sequence i starts from the state that table 0 entry i
+ * points to, and after its t+1-th token (t = 0 .. k_i-2) writes the state to table t+1
+ * entry i ("intermediate t"); the state after all k_i tokens is written back to table 0
+ * entry i.  Intermediate t equals t+1 sequential decode steps.
+ *   n          : 1 .. GDN_MAX_SEQS sequences.
+ *   ks_host    : host int32 [n], each in 2..16; rows are sequence-major, sequence i
+ *                owns rows sum(ks[:i]) .. + ks[i] of inputs, y and core_out.
+ *   wy_tables_dev: device u64 [16][128], this layer's slice.  Each entry used points to
+ *                a [n_v_heads][d_k][d_v] f32 state, 16-B aligned.  Entries the call does
+ *                not use are never read.  A NULL or misaligned needed entry sets
+ *                GDN_ERR_BAD_TABLE_ENTRY and that sequence is skipped.  The tables
+ *                themselves are never written.
+ *   conv_pool, n_slots, slots_dev: as in decode; the conv state ends after all k_i
+ *                tokens.
+ *   conv_inter : device [n][15][conv_dim][d_conv] in inputs->dtype, or NULL: the conv
+ *                state after token t+1 (t = 0 .. k_i-2), for rolling back to an
+ *                accepted prefix.
+ *   y, core_out, status_dev: as in decode, with sum(ks) rows. */
+GDN_API gdn_status gdn_verify_multi(const gdn_dims* dims, const gdn_weights* weights,
+                            const gdn_inputs* inputs, int32_t n, const int32_t* ks_host,
+                            const uint64_t* wy_tables_dev, void* conv_pool, int32_t n_slots,
+                            const int32_t* slots_dev, void* conv_inter, void* y,
+                            float* core_out, int32_t* status_dev, gdn_stream_t stream);
+
+/* Conv + SiLU + L2 norm of q and k (q also scaled) for T tokens of n sequences in one
+ * launch, updating each sequence's conv state to its last d_conv raw inputs
+ * (layer_struct.rs, conv1d_l2norm_f32_strided_k; trait_layer.rs,
+ * LayerSplitPrefill::prefill_phase1_conv1d_one / prefill_phase1_l2_batched).
+ *   cu_seqlens_dev: device int32 [n+1], cu[0] = 0, non-decreasing, cu[n] = total_tokens.
+ *   qkv_out    : device f32 [total_tokens][conv_dim]: normalised q, normalised k, raw
+ *                conv+SiLU v, in the [Q|K|V] channel order. */
+GDN_API gdn_status gdn_conv_step(const gdn_dims* dims, const gdn_weights* weights,
+                         const gdn_inputs* inputs, int32_t n, const int32_t* cu_seqlens_dev,
+                         int32_t total_tokens, void* conv_pool, int32_t n_slots,
+                         const int32_t* slots_dev, float* qkv_out, int32_t* status_dev,
+                         gdn_stream_t stream);
+
+/* Chunked (WY-form) prefill of n variable-length sequences (trait_layer.rs,
+ * LayerSplitPrefill::prefill_gdn_full_batched_fla_varlen; layer_struct.rs, the FLA
+ * chunked prefill gdn_prefill_fla_recompute_wu_k -> state spine chunk_delta_h ->
+ * chunk_fwd_o, and gated_rms_norm_prefill_k).  Chunk length 64.
+ *   cu_seqlens_dev : device int32 [n+1] (as in gdn_conv_step); total_tokens = cu[n],
+ *                    max_seqlen >= every length.
+ *   h_state_ptrs_dev: device u64 [n], each a 16-B aligned [n_v_heads][d_k][d_v] f32
+ *                    state, read as the initial state and overwritten with the final.
+ *   conv_pool, n_slots, slots_dev: as in decode.
+ *   y, core_out    : [total_tokens] rows, as in decode.
+ *   workspace      : device scratch of at least gdn_prefill_workspace_bytes(...) bytes,
+ *                    256-B aligned; its contents on entry do not matter. */
+GDN_API gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* weights,
+                               const gdn_inputs* inputs, int32_t n,
+                               const int32_t* cu_seqlens_dev, int32_t total_tokens,
+                               int32_t max_seqlen, int32_t chunk,
+                               const uint64_t* h_state_ptrs_dev, void* conv_pool,
+                               int32_t n_slots, const int32_t* slots_dev, void* y,
+                               float* core_out, void* workspace, size_t workspace_bytes,
+                               int32_t* status_dev, gdn_stream_t stream);
+
+/* Bytes of workspace gdn_prefill_chunked needs for these sizes (0 on invalid input). */
+GDN_API size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t n, int32_t total_tokens,
+                                   int32_t max_seqlen, int32_t chunk);
+
+/* Z-gated RMSNorm of T rows (layer_struct.rs, gated_rms_norm_f32_k: f32 input):
+ *   y[t][h*d_v + j] = o[t][h][j] / sqrt(mean_j o[t][h][:]^2 + eps) * w[j] * SiLU(z[t][h*d_v + j])
+ *   o : device f32 [T][n_v_heads][d_v];  z : device [T][z_stride] in `dtype`;
+ *   w : device f32 [d_v];  y : device [T][n_v_heads*d_v] in `dtype`.  d_v in {16, 128}. */
+GDN_API gdn_status gdn_gated_rmsnorm(const float* o, const void* z, int64_t z_stride, const float* w,
+                             float eps, int32_t T, int32_t n_v_heads, int32_t d_v,
+                             int32_t dtype, void* y, gdn_stream_t stream);
+
+/* Host helper: fills one layer's WY pointer tables in HOST memory
+ * (transformer_layer.rs, the VERIFY_WY_* layout; the engine's upload_verify_wy_tables
+ * stages them only for k in 2..16).  Zero-fills all 16 x 128 entries, then sets
+ * table 0 entry i = h_ptrs[i] and table t+1 entry i = inter_ptrs[i*15 + t] for
+ * t < ks[i] - 1.  Returns GDN_ERR_BAD_K for a k outside 2..16 (tables left zero). */
+GDN_API gdn_status gdn_wy_tables_fill(uint64_t* host_tables, int32_t n, const int32_t* ks,
+                              const uint64_t* h_ptrs, const uint64_t* inter_ptrs);
+
+/* A static, human-readable name of a status code. */
+GDN_API const char* gdn_status_string(gdn_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+GDN_API int32_t gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

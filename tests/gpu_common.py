@@ -1,0 +1,74 @@
+"""Helpers shared by the GPU parity tests: build/load, oracle runs, comparisons.
+
+Tolerances (written here once, used by every parity test):
+  * bf16 outputs y: ||y_gpu - bf16(y_oracle)||_2 / ||bf16(y_oracle)||_2 <= 2e-3 per tensor;
+  * f32 outputs (core o, f32 y): relative L2 <= 1e-4;
+  * f32 state: ||S_gpu - S_oracle||_F / ||S_oracle||_F <= 1e-4 per sequence;
+  * conv state, slot indexing, table memory: bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_layer_conv1d_gb300 import workloads as wl
+
+Y_BF16_TOL = 2e-3
+F32_TOL = 1e-4
+STATE_TOL = 1e-4
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from gated_deltanet_layer_conv1d_gb300 import _build
+    _build.build()
+    oracle.build()
+
+
+def rel_l2(a, b) -> float:
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
+
+
+def assert_y_close(y_gpu: torch.Tensor, y_orc: np.ndarray, what="y"):
+    y = y_gpu.float().cpu().numpy().astype(np.float64)
+    if y_gpu.dtype == torch.bfloat16:
+        ref = wl.round_bf16(y_orc.astype(np.float32)).astype(np.float64)
+        tol = Y_BF16_TOL
+    else:
+        ref, tol = y_orc, F32_TOL
+    assert np.isfinite(y).all(), f"{what}: non-finite"
+    e = rel_l2(y, ref)
+    assert e <= tol, f"{what}: rel L2 {e:.3e} > {tol:.0e}"
+    return e
+
+
+def assert_state_close(H_gpu, H_orc, what="state"):
+    H = np.asarray(H_gpu, np.float64)
+    e = rel_l2(H, H_orc)
+    assert e <= STATE_TOL, f"{what}: rel Frobenius {e:.3e} > {STATE_TOL:.0e}"
+    return e
+
+
+def odims(shape: wl.LayerShape) -> oracle.Dims:
+    return oracle.Dims(shape.n_k_heads, shape.n_v_heads, shape.d_k, shape.d_v, shape.d_conv,
+                       float(np.float32(shape.q_scale)), float(np.float32(shape.l2_eps)),
+                       float(np.float32(shape.norm_eps)))
+
+
+def oracle_seqs(w: wl.Workload, token_rows: dict, lens, H0=None, conv0=None, idx=None,
+                snapshots=False):
+    """Runs the oracle over sequences whose token rows are sequence-major in token_rows."""
+    H0 = w.H0 if H0 is None else H0
+    conv0 = w.conv0 if conv0 is None else conv0
+    off = np.concatenate([[0], np.cumsum(lens)])
+    idx = range(len(lens)) if idx is None else idx
+    seqs = []
+    for i in idx:
+        sl = slice(int(off[i]), int(off[i + 1]))
+        seqs.append(dict(qkv=token_rows["qkv"][sl], z=token_rows["z"][sl], a=token_rows["a"][sl],
+                         b=token_rows["b"][sl], conv_state=conv0[i], H=H0[i]))
+    return oracle.mixer_batch(odims(w.shape), w.weights, seqs, snapshots=snapshots)

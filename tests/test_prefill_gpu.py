@@ -1,0 +1,173 @@
+"""GPU parity of gdn_prefill_chunked, gdn_conv_step and gdn_gated_rmsnorm against the
+fp64 oracle (trait_layer.rs LayerSplitPrefill::prefill_gdn_full_batched_fla_varlen,
+prefill_phase1_conv1d_one / prefill_phase1_l2_batched; layer_struct.rs
+gated_rms_norm_f32_k)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_layer_conv1d_gb300 import device as dev
+from gated_deltanet_layer_conv1d_gb300 import gdn
+from gated_deltanet_layer_conv1d_gb300 import workloads as wl
+from tests.gpu_common import (assert_state_close, assert_y_close, odims, oracle_seqs,
+                              require_gpu, rel_l2, F32_TOL)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def run_prefill(w: wl.Workload, slot_perm=None):
+    d = torch.device("cuda")
+    sh = w.shape
+    dims = dev.dims_of(sh)
+    h_pool, conv_pool, slots = dev.states_to(w, d, slot_perm)
+    sl = slots.long().cpu().numpy()
+    hsz = sh.n_v_heads * sh.d_k * sh.d_v * 4
+    hp = torch.tensor([h_pool.data_ptr() + int(s) * hsz for s in sl], dtype=torch.int64, device=d)
+    cu = torch.from_numpy(w.cu_seqlens).to(d)
+    T = int(w.lens.sum())
+    ws_bytes = gdn.gdn_prefill_workspace_bytes(dims, w.n, T, int(w.lens.max()))
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=d) if ws_bytes else None
+    y = torch.empty((T, sh.n_v_heads * sh.d_v), dtype=dev.act_dtype(w), device=d)
+    core = torch.empty((T, sh.n_v_heads, sh.d_v), dtype=torch.float32, device=d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    gdn.gdn_prefill_chunked(dims, dev.weights_to(w, d), dev.tokens_to(w.tokens, dev.act_dtype(w), d),
+                            w.n, cu, T, int(w.lens.max()), hp, conv_pool, h_pool.shape[0], slots,
+                            y, core, ws, status)
+    torch.cuda.synchronize()
+    return dict(status=int(status.item()), y=y, core=core, h_pool=h_pool, conv_pool=conv_pool,
+                slots=slots)
+
+
+def check_prefill(w, r, state_tol_scale=1.0):
+    assert r["status"] == 0, gdn.status_string(r["status"])
+    res = oracle_seqs(w, w.tokens, [int(x) for x in w.lens])
+    assert_y_close(r["y"], np.concatenate([x.y for x in res]), "prefill y")
+    e = rel_l2(r["core"].cpu().numpy(), np.concatenate([x.o for x in res]))
+    assert e <= F32_TOL * state_tol_scale, f"core o: {e:.3e}"
+    sl = r["slots"].long()
+    H = r["h_pool"][sl].cpu().numpy()
+    conv = r["conv_pool"][sl].float().cpu().numpy()
+    for i, x in enumerate(res):
+        assert_state_close(H[i], x.H, f"state seq {i}")
+        np.testing.assert_array_equal(conv[i], x.conv_state)
+    return res
+
+
+def test_tiny_prefill_then_decode_f32():
+    """64-token prefill from zero state, then 8 decode steps, f32 throughout."""
+    for q_one in (False, True):
+        w = wl.tiny_check(q_scale_one=q_one)
+        r = run_prefill(w)
+        check_prefill(w, r)
+        d = torch.device("cuda")
+        dims = dev.dims_of(w.shape)
+        weights = dev.weights_to(w, d)
+        status = torch.zeros(1, dtype=torch.int32, device=d)
+        ys = []
+        for tok in w.steps:
+            y = torch.empty((1, 32), dtype=torch.float32, device=d)
+            gdn.gdn_decode_batched(dims, weights, dev.tokens_to(tok, torch.float32, d), 1,
+                                   r["h_pool"], r["conv_pool"], 1, r["slots"], y, None, status)
+            ys.append(y)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        all_tok = {k: np.concatenate([w.tokens[k]] + [s[k] for s in w.steps]) for k in w.tokens}
+        res = oracle_seqs(w, all_tok, [72])[0]
+        assert_y_close(torch.cat(ys), res.y[64:], "decode y after prefill")
+        assert_state_close(r["h_pool"][0].cpu().numpy(), res.H, "state after 72 tokens")
+        np.testing.assert_array_equal(r["conv_pool"][0].cpu().numpy(), res.conv_state)
+
+
+def test_varlen_prefill_tiny_bf16():
+    w = wl.varlen_prefill([1, 5, 70, 3, 64, 65], shape=wl.TINY, seed=9)
+    check_prefill(w, run_prefill(w, slot_perm=[3, 0, 5, 1, 2, 4]))
+
+
+def test_varlen_prefill_full_small():
+    w = wl.varlen_prefill([100, 7, 129, 64], seed=11)
+    check_prefill(w, run_prefill(w))
+
+
+@pytest.mark.slow
+def test_long_prefill_8192():
+    w = wl.long_prefill(8192)
+    check_prefill(w, run_prefill(w))
+
+
+def test_prefill_bad_seqlens_sets_status():
+    w = wl.varlen_prefill([5, 6], shape=wl.TINY, seed=12)
+    w_cu = w.cu_seqlens.copy()
+    d = torch.device("cuda")
+    sh = w.shape
+    h_pool, conv_pool, slots = dev.states_to(w, d)
+    hp = torch.tensor([h_pool[i].data_ptr() for i in range(2)], dtype=torch.int64, device=d)
+    cu = torch.from_numpy(np.array([0, 9, 7], np.int32)).to(d)  # decreasing: invalid
+    y = torch.zeros((11, 32), dtype=torch.bfloat16, device=d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    gdn.gdn_prefill_chunked(dev.dims_of(sh), dev.weights_to(w, d),
+                            dev.tokens_to(w.tokens, torch.bfloat16, d), 2, cu, 11, 9, hp,
+                            conv_pool, 2, slots, y, None, None, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 18  # GDN_ERR_BAD_SEQLENS
+    assert w_cu[-1] == 11
+
+
+@pytest.mark.parametrize("shape,lens,bf16", [(wl.TINY, [3, 1, 9], False),
+                                             (wl.FULL, [5, 70, 2], True)])
+def test_conv_step(shape, lens, bf16):
+    rng = np.random.default_rng(13)
+    w = wl.varlen_prefill(lens, shape=shape, seed=13)
+    if not bf16:
+        w.bf16 = False
+        w.tokens = wl.make_tokens(rng, shape, int(sum(lens)), bf16=False)
+        w.conv0 = rng.standard_normal(w.conv0.shape).astype(np.float32)
+    d = torch.device("cuda")
+    _, conv_pool, slots = dev.states_to(w, d)
+    cu = torch.from_numpy(w.cu_seqlens).to(d)
+    T = int(sum(lens))
+    out = torch.empty((T, shape.conv_dim), dtype=torch.float32, device=d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    gdn.gdn_conv_step(dev.dims_of(shape), dev.weights_to(w, d),
+                      dev.tokens_to(w.tokens, dev.act_dtype(w), d), len(lens), cu, T, conv_pool,
+                      len(lens), slots, out, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    od = odims(shape)
+    got = out.cpu().numpy()
+    off = w.cu_seqlens
+    for i in range(len(lens)):
+        xc, st, _ = oracle.conv(w.weights["conv_w"], w.conv0[i], w.tokens["qkv"][off[i]:off[i + 1]])
+        qn, kn, v = oracle.l2norm_split(od, xc)
+        g = got[off[i]:off[i + 1]]
+        Hk, dk = shape.n_k_heads, shape.d_k
+        np.testing.assert_allclose(g[:, :Hk * dk], qn.reshape(len(qn), -1), rtol=2e-5, atol=2e-6)
+        np.testing.assert_allclose(g[:, Hk * dk:2 * Hk * dk], kn.reshape(len(kn), -1), rtol=2e-5,
+                                   atol=2e-6)
+        np.testing.assert_allclose(g[:, 2 * Hk * dk:], v.reshape(len(v), -1), rtol=2e-5,
+                                   atol=2e-5)
+        np.testing.assert_array_equal(conv_pool[i].float().cpu().numpy(), st)
+
+
+@pytest.mark.parametrize("shape,bf16", [(wl.TINY, False), (wl.FULL, True)])
+def test_gated_rmsnorm(shape, bf16):
+    rng = np.random.default_rng(14)
+    T, Hv, dv = 33, shape.n_v_heads, shape.d_v
+    o = rng.standard_normal((T, Hv, dv)).astype(np.float32)
+    z = rng.standard_normal((T, Hv * dv)).astype(np.float32)
+    if bf16:
+        z = wl.round_bf16(z)
+    w = (1 + 0.1 * rng.standard_normal(dv)).astype(np.float32)
+    d = torch.device("cuda")
+    dt = torch.bfloat16 if bf16 else torch.float32
+    y = torch.empty((T, Hv * dv), dtype=dt, device=d)
+    gdn.gdn_gated_rmsnorm(torch.from_numpy(o).to(d), torch.from_numpy(z).to(d, dt),
+                          torch.from_numpy(w).to(d), 1e-6, y)
+    torch.cuda.synchronize()
+    ref = oracle.gated_rmsnorm(o, z, w, float(np.float32(1e-6)))
+    assert_y_close(y, ref, "gated rmsnorm")
