@@ -90,6 +90,14 @@ gdn_status check_pools(const void* conv_pool, int32_t n_slots, const int32_t* sl
   return GDN_OK;
 }
 
+// A launcher refuses a shape whose shared-memory plan does not fit with
+// cudaErrorInvalidConfiguration before launching anything.
+gdn_status status_of(cudaError_t e) {
+  if (e == cudaSuccess) return GDN_OK;
+  if (e == cudaErrorInvalidConfiguration) return GDN_ERR_UNSUPPORTED_DIMS;
+  return GDN_ERR_CUDA;
+}
+
 #define GDN_TRY(expr)                \
   do {                               \
     const gdn_status s_ = (expr);    \
@@ -173,7 +181,7 @@ gdn_status gdn_decode_batched(const gdn_dims* dims, const gdn_weights* weights,
   p.status = status_dev;
   p.n_items = n * p.Hk;
   const cudaError_t e = launch_recurrent(p, inputs->dtype, dims->d_k, false, stream);
-  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  return status_of(e);
 }
 
 gdn_status gdn_verify_multi(const gdn_dims* dims, const gdn_weights* weights,
@@ -221,7 +229,7 @@ gdn_status gdn_verify_multi(const gdn_dims* dims, const gdn_weights* weights,
   std::stable_sort(order, order + n, [&](int a, int b) { return ks_host[a] > ks_host[b]; });
   for (int i = 0; i < n; ++i) p.order[i] = uint8_t(order[i]);
   const cudaError_t e = launch_recurrent(p, inputs->dtype, dims->d_k, true, stream);
-  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  return status_of(e);
 }
 
 gdn_status gdn_conv_step(const gdn_dims* dims, const gdn_weights* weights,

@@ -44,6 +44,7 @@ namespace gdn {
 namespace {
 
 constexpr int kW = 4;  // conv width
+constexpr size_t kMaxSmemPerBlock = 232448;  // 227 KiB opt-in shared memory per CTA
 
 template <int D, int NT>
 struct RecMap {
@@ -211,19 +212,34 @@ __device__ __forceinline__ void norm_tokens(const float* o, const float* z, int 
 // ======================================================================================
 // decode / verify
 // ======================================================================================
-template <int D, int NT, int KMAX, int STAGES>
+template <int D, int NT, int KMAX, int STAGES, typename T>
 struct RecSmem {
   using Map = RecMap<D, NT>;
+  // Decode prefetches the next item's raw inputs into shared memory while the current
+  // item runs; verify (k tokens per item) amortises the prologue and skips it.
+  static constexpr bool kPrefetch = (KMAX == 1);
   static constexpr size_t kTile = size_t(D) * D * sizeof(float);
   static constexpr size_t kStage = 0;
   static constexpr size_t kRed = kStage + STAGES * kTile;                  // [2][2][RB][D]
   static constexpr size_t kObuf = kRed + size_t(2) * 2 * Map::RB * D * 4;  // [KMAX][D]
-  static constexpr size_t kBar = kObuf + size_t(KMAX) * D * 4;             // [STAGES] u64
+  static constexpr size_t kNw = kObuf + size_t(KMAX) * D * 4;              // [D] norm_w
+  static constexpr size_t kBar = kNw + size_t(D) * 4;                      // [STAGES] u64
   static constexpr size_t kGate = kBar + 8 * ((STAGES + 1) / 2 * 2);       // [KMAX][kMaxG][2]
   static constexpr size_t kKq = kGate + size_t(KMAX) * kMaxG * 2 * 4;      // [KMAX]
   static constexpr size_t kXs = kKq + ((size_t(KMAX) * 4 + 15) / 16) * 16;
-  // xs: [KMAX][(2 + 2G) D] = q | k | v of G heads | z of G heads, per token
-  static size_t bytes(int G) { return kXs + size_t(KMAX) * (2 + 2 * G) * D * 4; }
+  // xs: [KMAX][(2 + 2G) D] f32 = q | k | v of G heads | z of G heads, per token
+  __host__ __device__ static size_t xs_bytes(int G) { return size_t(KMAX) * (2 + 2 * G) * D * 4; }
+  // raw (prefetch only): conv state [CH][4] T | conv_w [CH][4] f32 | x [KMAX][CH] T |
+  // z [KMAX][G D] T, CH = (2 + G) D
+  __host__ __device__ static size_t raw_cs(int) { return 0; }
+  __host__ __device__ static size_t raw_w(int G) { return raw_cs(G) + size_t(2 + G) * D * 4 * sizeof(T); }
+  __host__ __device__ static size_t raw_x(int G) { return raw_w(G) + size_t(2 + G) * D * 4 * 4; }
+  __host__ __device__ static size_t raw_z(int G) { return raw_x(G) + size_t(KMAX) * (2 + G) * D * sizeof(T); }
+  __host__ __device__ static size_t raw_bytes(int G) {
+    return kPrefetch ? raw_z(G) + size_t(KMAX) * G * D * sizeof(T) : 0;
+  }
+  __host__ __device__ static size_t kRaw(int G) { return kXs + xs_bytes(G); }
+  __host__ __device__ static size_t bytes(int G) { return kRaw(G) + raw_bytes(G); }
 };
 
 // The item this CTA owns in round r: a zig-zag over the item list.
@@ -280,12 +296,13 @@ template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY>
 __global__ void __launch_bounds__(NT, 1)
     gdn_recurrent_kernel(const __grid_constant__ RecParams p) {
   using Map = RecMap<D, NT>;
-  using SL = RecSmem<D, NT, KMAX, STAGES>;
+  using SL = RecSmem<D, NT, KMAX, STAGES, T>;
   using A = Act<T>;
   extern __shared__ __align__(128) unsigned char smem[];
   float* stage = reinterpret_cast<float*>(smem + SL::kStage);
   float* red = reinterpret_cast<float*>(smem + SL::kRed);
   float* obuf = reinterpret_cast<float*>(smem + SL::kObuf);
+  float* nw_s = reinterpret_cast<float*>(smem + SL::kNw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SL::kBar);
   float* gate = reinterpret_cast<float*>(smem + SL::kGate);
   float* kq_s = reinterpret_cast<float*>(smem + SL::kKq);
@@ -298,12 +315,73 @@ __global__ void __launch_bounds__(NT, 1)
   const int CHX = CH + G * D;   // plus the z channels
   const int P = gridDim.x, cta = blockIdx.x;
   const int rounds = (p.n_items + P - 1) / P;
+  unsigned char* raw = smem + SL::kRaw(G);
+  T* raw_cs = reinterpret_cast<T*>(raw + SL::raw_cs(G));
+  float* raw_w = reinterpret_cast<float*>(raw + SL::raw_w(G));
+  T* raw_x = reinterpret_cast<T*>(raw + SL::raw_x(G));
+  T* raw_z = reinterpret_cast<T*>(raw + SL::raw_z(G));
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
     fence_mbar_init();
   }
-  __syncthreads();
+  for (int j = tid; j < D; j += NT) nw_s[j] = p.norm_w[j];
+
+  // Global channel of item-local conv channel lc: q | k | v of the G value heads.
+  auto global_channel = [&](int kh, int lc) -> int {
+    if (lc < D) return kh * D + lc;
+    if (lc < 2 * D) return Hk * D + kh * D + (lc - D);
+    return 2 * Hk * D + kh * G * D + (lc - 2 * D);
+  };
+  // First round at or after r whose item can run (rounds if none).
+  auto next_valid = [&](int r, Item& it) -> int {
+    for (; r < rounds; ++r) {
+      const int j = item_at(cta, r, P);
+      if (j < p.n_items && item_decode<VERIFY>(p, j, it) == 0) return r;
+    }
+    return rounds;
+  };
+  // Prefetch path: starts the async copies of an item's raw prologue inputs and loads its
+  // gate logits into registers (threads < k*G).
+  float ra = 0.f, rbv = 0.f;
+  auto prefetch = [&](const Item& it) {
+    const int k = it.k;
+    const int lens[3] = {D, D, G * D};
+    const int lstart[3] = {0, D, 2 * D};
+    for (int seg = 0; seg < 3; ++seg) {
+      const int gc = global_channel(it.kh, lstart[seg]);
+      const size_t cs_bytes = size_t(lens[seg]) * kW * sizeof(T);
+      const unsigned char* cs_src = reinterpret_cast<const unsigned char*>(p.conv_pool) +
+                                    (size_t(it.slot) * p.conv_dim + gc) * kW * sizeof(T);
+      unsigned char* cs_dst = reinterpret_cast<unsigned char*>(raw_cs) + size_t(lstart[seg]) * kW * sizeof(T);
+      for (size_t c = tid; c < cs_bytes / 16; c += NT) cp_async16(cs_dst + c * 16, cs_src + c * 16);
+      const size_t w_bytes = size_t(lens[seg]) * kW * 4;
+      const unsigned char* w_src = reinterpret_cast<const unsigned char*>(p.conv_w + size_t(gc) * kW);
+      unsigned char* w_dst = reinterpret_cast<unsigned char*>(raw_w + size_t(lstart[seg]) * kW);
+      for (size_t c = tid; c < w_bytes / 16; c += NT) cp_async16(w_dst + c * 16, w_src + c * 16);
+      const size_t x_bytes = size_t(lens[seg]) * sizeof(T);
+      for (int t = 0; t < k; ++t) {
+        const unsigned char* x_src = reinterpret_cast<const unsigned char*>(
+            reinterpret_cast<const T*>(p.qkv) + size_t(it.row0 + t) * p.qkv_stride + gc);
+        unsigned char* x_dst = reinterpret_cast<unsigned char*>(raw_x + size_t(t) * CH + lstart[seg]);
+        for (size_t c = tid; c < x_bytes / 16; c += NT) cp_async16(x_dst + c * 16, x_src + c * 16);
+      }
+    }
+    const size_t z_bytes = size_t(G) * D * sizeof(T);
+    for (int t = 0; t < k; ++t) {
+      const unsigned char* z_src = reinterpret_cast<const unsigned char*>(
+          reinterpret_cast<const T*>(p.z) + size_t(it.row0 + t) * p.z_stride + it.kh * G * D);
+      unsigned char* z_dst = reinterpret_cast<unsigned char*>(raw_z + size_t(t) * G * D);
+      for (size_t c = tid; c < z_bytes / 16; c += NT) cp_async16(z_dst + c * 16, z_src + c * 16);
+    }
+    cp_async_commit();
+    if (tid < k * G) {
+      const int t = tid / G, g = tid - t * G;
+      const size_t ro = size_t(it.row0 + t) * p.ab_stride + it.kh * G + g;
+      ra = A::to_f(reinterpret_cast<const T*>(p.a)[ro]);
+      rbv = A::to_f(reinterpret_cast<const T*>(p.b)[ro]);
+    }
+  };
 
   // ---- producer cursor (thread 0 only): the next (round, value head) to load.  It walks
   // the same item sequence as the consumer loop below and skips the same bad items.
@@ -345,74 +423,125 @@ __global__ void __launch_bounds__(NT, 1)
                  reinterpret_cast<const unsigned char*>(src) + off, kPiece, &bar[s]);
     }
   };
+  __syncthreads();  // barriers initialised, norm_w staged
   if (tid == 0)
     for (int s = 0; s < STAGES; ++s) prod_issue(s);
 
-  int q = 0;  // tiles consumed by this CTA
-  for (int r = 0; r < rounds; ++r) {
-    const int j = item_at(cta, r, P);
-    if (j >= p.n_items) continue;
-    Item it;
-    const int bad = item_decode<VERIFY>(p, j, it);
-    if (bad) {
-      if (tid == 0) report(p.status, bad);
-      continue;
+  // Bad items are reported here, once, by the consumer side.
+  if (tid == 0) {
+    for (int r = 0; r < rounds; ++r) {
+      const int j = item_at(cta, r, P);
+      Item it;
+      if (j < p.n_items) {
+        const int bad = item_decode<VERIFY>(p, j, it);
+        if (bad) report(p.status, bad);
+      }
     }
+  }
+
+  Item nxt;
+  int r_next = next_valid(0, nxt);
+  if constexpr (SL::kPrefetch) {
+    if (r_next < rounds) prefetch(nxt);
+  }
+  int q = 0;  // tiles consumed by this CTA
+  while (r_next < rounds) {
+    const Item it = nxt;
     const int k = it.k;
+    r_next = next_valid(r_next + 1, nxt);
 
     // ---------------- item prologue: conv + SiLU (+ state update), z, gates, L2 norms
-    for (int lc = tid; lc < CHX; lc += NT) {
-      if (lc >= CH) {  // z channel: staged as f32
-        const int zc = lc - CH;
-        const T* zp = reinterpret_cast<const T*>(p.z) + size_t(it.row0) * p.z_stride +
-                      it.kh * G * D + zc;
-        for (int t = 0; t < k; ++t) xs[t * CHX + lc] = A::to_f(zp[size_t(t) * p.z_stride]);
-        continue;
+    if constexpr (SL::kPrefetch) {
+      cp_async_wait_all();
+      if (tid < k * G) {  // gates from the prefetched logits
+        const int t = tid / G, g = tid - t * G;
+        const int h = it.kh * G + g;
+        float al, be;
+        gates_f(ra, rbv, p.A_log[h], p.dt_bias[h], &al, &be);
+        gate[(t * kMaxG + g) * 2 + 0] = al;
+        gate[(t * kMaxG + g) * 2 + 1] = be;
       }
-      int gc;
-      if (lc < D) gc = it.kh * D + lc;
-      else if (lc < 2 * D) gc = Hk * D + it.kh * D + (lc - D);
-      else gc = 2 * Hk * D + it.kh * G * D + (lc - 2 * D);
-      T* cs = reinterpret_cast<T*>(p.conv_pool) + (size_t(it.slot) * p.conv_dim + gc) * kW;
-      const float4 w4 = *reinterpret_cast<const float4*>(p.conv_w + size_t(gc) * kW);
-      float buf[kW + KMAX];
-      const float4 s4 = A::load4(cs);
-      buf[0] = s4.x; buf[1] = s4.y; buf[2] = s4.z; buf[3] = s4.w;
-      const T* xrow = reinterpret_cast<const T*>(p.qkv) + size_t(it.row0) * p.qkv_stride + gc;
+      __syncthreads();  // raw inputs of `it` visible to every thread
+      for (int lc = tid; lc < CHX; lc += NT) {
+        if (lc >= CH) {
+          const int zc = lc - CH;
+          for (int t = 0; t < k; ++t) xs[t * CHX + lc] = A::to_f(raw_z[t * G * D + zc]);
+          continue;
+        }
+        const float4 w4 = *reinterpret_cast<const float4*>(raw_w + size_t(lc) * kW);
+        const float4 s4 = A::load4(raw_cs + size_t(lc) * kW);
+        float buf[kW + KMAX];
+        buf[0] = s4.x; buf[1] = s4.y; buf[2] = s4.z; buf[3] = s4.w;
 #pragma unroll
-      for (int t = 0; t < KMAX; ++t)
-        if (t < k) buf[kW + t] = A::to_f(xrow[size_t(t) * p.qkv_stride]);
+        for (int t = 0; t < KMAX; ++t)
+          if (t < k) buf[kW + t] = A::to_f(raw_x[t * CH + lc]);
 #pragma unroll
-      for (int t = 0; t < KMAX; ++t) {
-        if (t < k) {
-          // window of token t: the last kW raw inputs, buf[t+1 .. t+4]
-          const float acc = w4.x * buf[t + 1] + w4.y * buf[t + 2] + w4.z * buf[t + 3] +
-                            w4.w * buf[t + 4];
-          xs[t * CHX + lc] = silu_f(acc);
-          if (VERIFY && p.conv_inter && t < k - 1) {
-            T* ci = reinterpret_cast<T*>(p.conv_inter) +
-                    ((size_t(it.seq) * (GDN_VERIFY_WY_TABLES_PER_LAYER - 1) + t) * p.conv_dim + gc) * kW;
-            A::store4(ci, make_float4(buf[t + 1], buf[t + 2], buf[t + 3], buf[t + 4]));
+        for (int t = 0; t < KMAX; ++t)
+          if (t < k)
+            xs[t * CHX + lc] = silu_f(w4.x * buf[t + 1] + w4.y * buf[t + 2] + w4.z * buf[t + 3] +
+                                      w4.w * buf[t + 4]);
+        float4 ns = s4;
+#pragma unroll
+        for (int t = 1; t <= KMAX; ++t)
+          if (t == k) ns = make_float4(buf[t], buf[t + 1], buf[t + 2], buf[t + 3]);
+        T* cs = reinterpret_cast<T*>(p.conv_pool) +
+                (size_t(it.slot) * p.conv_dim + global_channel(it.kh, lc)) * kW;
+        A::store4(cs, ns);  // exact copies of raw inputs
+      }
+      __syncthreads();  // raw buffer consumed: start the next item's copies
+      if (r_next < rounds) prefetch(nxt);
+    } else {
+      __syncthreads();  // every warp is done with the previous item's xs and gates
+      for (int lc = tid; lc < CHX; lc += NT) {
+        if (lc >= CH) {  // z channel: staged as f32
+          const int zc = lc - CH;
+          const T* zp = reinterpret_cast<const T*>(p.z) + size_t(it.row0) * p.z_stride +
+                        it.kh * G * D + zc;
+          for (int t = 0; t < k; ++t) xs[t * CHX + lc] = A::to_f(zp[size_t(t) * p.z_stride]);
+          continue;
+        }
+        const int gc = global_channel(it.kh, lc);
+        T* cs = reinterpret_cast<T*>(p.conv_pool) + (size_t(it.slot) * p.conv_dim + gc) * kW;
+        const float4 w4 = *reinterpret_cast<const float4*>(p.conv_w + size_t(gc) * kW);
+        float buf[kW + KMAX];
+        const float4 s4 = A::load4(cs);
+        buf[0] = s4.x; buf[1] = s4.y; buf[2] = s4.z; buf[3] = s4.w;
+        const T* xrow = reinterpret_cast<const T*>(p.qkv) + size_t(it.row0) * p.qkv_stride + gc;
+#pragma unroll
+        for (int t = 0; t < KMAX; ++t)
+          if (t < k) buf[kW + t] = A::to_f(xrow[size_t(t) * p.qkv_stride]);
+#pragma unroll
+        for (int t = 0; t < KMAX; ++t) {
+          if (t < k) {
+            // window of token t: the last kW raw inputs, buf[t+1 .. t+4]
+            const float acc = w4.x * buf[t + 1] + w4.y * buf[t + 2] + w4.z * buf[t + 3] +
+                              w4.w * buf[t + 4];
+            xs[t * CHX + lc] = silu_f(acc);
+            if (VERIFY && p.conv_inter && t < k - 1) {
+              T* ci = reinterpret_cast<T*>(p.conv_inter) +
+                      ((size_t(it.seq) * (GDN_VERIFY_WY_TABLES_PER_LAYER - 1) + t) * p.conv_dim + gc) * kW;
+              A::store4(ci, make_float4(buf[t + 1], buf[t + 2], buf[t + 3], buf[t + 4]));
+            }
           }
         }
-      }
-      float4 ns = s4;
+        float4 ns = s4;
 #pragma unroll
-      for (int t = 1; t <= KMAX; ++t)
-        if (t == k) ns = make_float4(buf[t], buf[t + 1], buf[t + 2], buf[t + 3]);
-      A::store4(cs, ns);  // exact copies of raw inputs
+        for (int t = 1; t <= KMAX; ++t)
+          if (t == k) ns = make_float4(buf[t], buf[t + 1], buf[t + 2], buf[t + 3]);
+        A::store4(cs, ns);  // exact copies of raw inputs
+      }
+      for (int idx = tid; idx < k * G; idx += NT) {
+        const int t = idx / G, g = idx - t * G;
+        const int h = it.kh * G + g;
+        const size_t ro = size_t(it.row0 + t) * p.ab_stride + h;
+        float al, be;
+        gates_f(A::to_f(reinterpret_cast<const T*>(p.a)[ro]),
+                A::to_f(reinterpret_cast<const T*>(p.b)[ro]), p.A_log[h], p.dt_bias[h], &al, &be);
+        gate[(t * kMaxG + g) * 2 + 0] = al;
+        gate[(t * kMaxG + g) * 2 + 1] = be;
+      }
+      __syncthreads();
     }
-    for (int idx = tid; idx < k * G; idx += NT) {
-      const int t = idx / G, g = idx - t * G;
-      const int h = it.kh * G + g;
-      const size_t ro = size_t(it.row0 + t) * p.ab_stride + h;
-      float al, be;
-      gates_f(A::to_f(reinterpret_cast<const T*>(p.a)[ro]),
-              A::to_f(reinterpret_cast<const T*>(p.b)[ro]), p.A_log[h], p.dt_bias[h], &al, &be);
-      gate[(t * kMaxG + g) * 2 + 0] = al;
-      gate[(t * kMaxG + g) * 2 + 1] = be;
-    }
-    __syncthreads();
     l2norm_tokens<D, Map::NW>(xs, CHX, k, p.q_scale, p.l2_eps, kq_s, L.warp, L.lane);
     __syncthreads();
 
@@ -449,7 +578,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (VERIFY || t == k - 1) store_tile<D, NT>(state_dst<D, VERIFY>(p, it, h, t), S, L);
       }
       __syncthreads();  // obuf complete
-      norm_tokens<T, D, Map::NW>(obuf, xs + CH + g * D, CHX, k, it.row0, h, p.norm_w,
+      norm_tokens<T, D, Map::NW>(obuf, xs + CH + g * D, CHX, k, it.row0, h, nw_s,
                                  p.norm_eps, p.Hv, reinterpret_cast<T*>(p.y), p.core_out,
                                  L.warp, L.lane);
     }
@@ -458,9 +587,10 @@ __global__ void __launch_bounds__(NT, 1)
 
 template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY>
 cudaError_t launch_rec(const RecParams& p, cudaStream_t stream) {
-  using SL = RecSmem<D, NT, KMAX, STAGES>;
+  using SL = RecSmem<D, NT, KMAX, STAGES, T>;
   auto kern = gdn_recurrent_kernel<T, D, NT, KMAX, STAGES, VERIFY>;
   const size_t smem = SL::bytes(p.G);
+  if (smem > kMaxSmemPerBlock) return cudaErrorInvalidConfiguration;  // shape not supported
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
