@@ -226,7 +226,14 @@ struct RecSmem {
   static constexpr size_t kBar = kNw + size_t(D) * 4;                      // [STAGES] u64
   static constexpr size_t kGate = kBar + 8 * ((STAGES + 1) / 2 * 2);       // [KMAX][kMaxG][2]
   static constexpr size_t kKq = kGate + size_t(KMAX) * kMaxG * 2 * 4;      // [KMAX]
-  static constexpr size_t kXs = kKq + ((size_t(KMAX) * 4 + 15) / 16) * 16;
+  // Per-launch staging so no global load sits on the per-head critical path:
+  // slot of each sequence, whether its item can run (0 = yes, else the GDN_ERR_* code),
+  // its table-0 pointer (verify), and the current item's 16 table entries (verify).
+  static constexpr size_t kSlots = kKq + ((size_t(KMAX) * 4 + 15) / 16) * 16;  // [128] i32
+  static constexpr size_t kValid = kSlots + GDN_MAX_SEQS * 4;                  // [128] i32
+  static constexpr size_t kTab0 = kValid + GDN_MAX_SEQS * 4;                   // [128] u64
+  static constexpr size_t kTabItem = kTab0 + GDN_MAX_SEQS * 8;                 // [16] u64
+  static constexpr size_t kXs = kTabItem + GDN_VERIFY_WY_TABLES_PER_LAYER * 8;
   // xs: [KMAX][(2 + 2G) D] f32 = q | k | v of G heads | z of G heads, per token
   __host__ __device__ static size_t xs_bytes(int G) { return size_t(KMAX) * (2 + 2 * G) * D * 4; }
   // raw (prefetch only): conv state [CH][4] T | conv_w [CH][4] f32 | x [KMAX][CH] T |
@@ -251,44 +258,53 @@ struct Item {
   int seq, kh, k, row0, slot;
 };
 
-// Decodes item j and checks everything the device must check before touching memory.
-// Returns 0 if the item can run, else the GDN_ERR_* code.
+// Checks a sequence before any of its memory is touched: 0 if it can run, else the
+// GDN_ERR_* code (slot out of range; a needed table entry NULL or misaligned).
 template <bool VERIFY>
-__device__ __forceinline__ int item_decode(const RecParams& p, int j, Item& it) {
-  const int rank = j / p.Hk;
-  it.kh = j - rank * p.Hk;
-  it.seq = VERIFY ? int(p.order[rank]) : rank;
-  it.k = VERIFY ? int(p.ks[it.seq]) : 1;
-  it.row0 = VERIFY ? int(p.row_off[it.seq]) : it.seq;
-  it.slot = p.slots[it.seq];
-  if (it.slot < 0 || it.slot >= p.n_slots) return GDN_ERR_BAD_SLOT;
+__device__ __forceinline__ int seq_check(const RecParams& p, int seq) {
+  const int slot = p.slots[seq];
+  if (slot < 0 || slot >= p.n_slots) return GDN_ERR_BAD_SLOT;
   if (VERIFY) {
-    for (int t = 0; t < it.k; ++t) {
-      const uint64_t e = p.tables[t * GDN_VERIFY_WY_TABLE_SEQS + it.seq];
+    const int k = p.ks[seq];
+    for (int t = 0; t < k; ++t) {
+      const uint64_t e = p.tables[t * GDN_VERIFY_WY_TABLE_SEQS + seq];
       if (e == 0 || (e & 15u) != 0) return GDN_ERR_BAD_TABLE_ENTRY;
     }
   }
   return 0;
 }
 
-// The state of value head h of an item: written after token t (t = k-1: final state).
+// Decodes item j from the launch's staged per-sequence data (shared memory only).
+// Returns 0 if the item can run, else its GDN_ERR_* code.
+template <bool VERIFY>
+__device__ __forceinline__ int item_decode(const RecParams& p, int j, const int32_t* slots_s,
+                                           const int32_t* valid_s, Item& it) {
+  const int rank = j / p.Hk;
+  it.kh = j - rank * p.Hk;
+  it.seq = VERIFY ? int(p.order[rank]) : rank;
+  it.k = VERIFY ? int(p.ks[it.seq]) : 1;
+  it.row0 = VERIFY ? int(p.row_off[it.seq]) : it.seq;
+  it.slot = slots_s[it.seq];
+  return valid_s[it.seq];
+}
+
+// The state of value head h of an item, written after token t (t = k-1: final state).
+// tab_item: the item's 16 table entries (verify).
 template <int D, bool VERIFY>
-__device__ __forceinline__ float* state_dst(const RecParams& p, const Item& it, int h, int t) {
+__device__ __forceinline__ float* state_dst(const RecParams& p, const Item& it,
+                                            const uint64_t* tab_item, int h, int t) {
   if (VERIFY) {
     const int table = (t == it.k - 1) ? 0 : t + 1;
-    const uint64_t e = p.tables[table * GDN_VERIFY_WY_TABLE_SEQS + it.seq];
-    return reinterpret_cast<float*>(e) + size_t(h) * D * D;
+    return reinterpret_cast<float*>(tab_item[table]) + size_t(h) * D * D;
   }
   return p.h_pool + (size_t(it.slot) * p.Hv + h) * D * D;
 }
 
 // The state of value head h of an item as read at its start.
 template <int D, bool VERIFY>
-__device__ __forceinline__ const float* state_src(const RecParams& p, const Item& it, int h) {
-  if (VERIFY) {
-    const uint64_t e = p.tables[it.seq];  // table 0
-    return reinterpret_cast<const float*>(e) + size_t(h) * D * D;
-  }
+__device__ __forceinline__ const float* state_src(const RecParams& p, const Item& it,
+                                                  const uint64_t* tab0_s, int h) {
+  if (VERIFY) return reinterpret_cast<const float*>(tab0_s[it.seq]) + size_t(h) * D * D;
   return p.h_pool + (size_t(it.slot) * p.Hv + h) * D * D;
 }
 
@@ -307,6 +323,10 @@ __global__ void __launch_bounds__(NT, 1)
   float* gate = reinterpret_cast<float*>(smem + SL::kGate);
   float* kq_s = reinterpret_cast<float*>(smem + SL::kKq);
   float* xs = reinterpret_cast<float*>(smem + SL::kXs);
+  int32_t* slots_s = reinterpret_cast<int32_t*>(smem + SL::kSlots);
+  int32_t* valid_s = reinterpret_cast<int32_t*>(smem + SL::kValid);
+  uint64_t* tab0_s = reinterpret_cast<uint64_t*>(smem + SL::kTab0);
+  uint64_t* tab_item = reinterpret_cast<uint64_t*>(smem + SL::kTabItem);
 
   const int tid = threadIdx.x;
   const Lane<D, NT> L(tid);
@@ -326,6 +346,11 @@ __global__ void __launch_bounds__(NT, 1)
     fence_mbar_init();
   }
   for (int j = tid; j < D; j += NT) nw_s[j] = p.norm_w[j];
+  for (int i = tid; i < p.n; i += NT) {
+    slots_s[i] = p.slots[i];
+    valid_s[i] = seq_check<VERIFY>(p, i);
+    if (VERIFY) tab0_s[i] = p.tables[i];
+  }
 
   // Global channel of item-local conv channel lc: q | k | v of the G value heads.
   auto global_channel = [&](int kh, int lc) -> int {
@@ -337,13 +362,13 @@ __global__ void __launch_bounds__(NT, 1)
   auto next_valid = [&](int r, Item& it) -> int {
     for (; r < rounds; ++r) {
       const int j = item_at(cta, r, P);
-      if (j < p.n_items && item_decode<VERIFY>(p, j, it) == 0) return r;
+      if (j < p.n_items && item_decode<VERIFY>(p, j, slots_s, valid_s, it) == 0) return r;
     }
     return rounds;
   };
   // Prefetch path: starts the async copies of an item's raw prologue inputs and loads its
   // gate logits into registers (threads < k*G).
-  float ra = 0.f, rbv = 0.f;
+  float ra = 0.f, rbv = 0.f, rAl = 0.f, rDt = 0.f;
   auto prefetch = [&](const Item& it) {
     const int k = it.k;
     const int lens[3] = {D, D, G * D};
@@ -380,6 +405,8 @@ __global__ void __launch_bounds__(NT, 1)
       const size_t ro = size_t(it.row0 + t) * p.ab_stride + it.kh * G + g;
       ra = A::to_f(reinterpret_cast<const T*>(p.a)[ro]);
       rbv = A::to_f(reinterpret_cast<const T*>(p.b)[ro]);
+      rAl = p.A_log[it.kh * G + g];
+      rDt = p.dt_bias[it.kh * G + g];
     }
   };
 
@@ -393,7 +420,7 @@ __global__ void __launch_bounds__(NT, 1)
     while (pr < rounds) {
       if (!pvalid) {
         const int j = item_at(cta, pr, P);
-        if (j < p.n_items && item_decode<VERIFY>(p, j, pit) == 0) {
+        if (j < p.n_items && item_decode<VERIFY>(p, j, slots_s, valid_s, pit) == 0) {
           pvalid = true;
           pg = 0;
         } else {
@@ -402,7 +429,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       if (pg < G) {
-        *src = state_src<D, VERIFY>(p, pit, pit.kh * G + pg);
+        *src = state_src<D, VERIFY>(p, pit, tab0_s, pit.kh * G + pg);
         ++pg;
         return true;
       }
@@ -433,7 +460,7 @@ __global__ void __launch_bounds__(NT, 1)
       const int j = item_at(cta, r, P);
       Item it;
       if (j < p.n_items) {
-        const int bad = item_decode<VERIFY>(p, j, it);
+        const int bad = item_decode<VERIFY>(p, j, slots_s, valid_s, it);
         if (bad) report(p.status, bad);
       }
     }
@@ -455,9 +482,8 @@ __global__ void __launch_bounds__(NT, 1)
       cp_async_wait_all();
       if (tid < k * G) {  // gates from the prefetched logits
         const int t = tid / G, g = tid - t * G;
-        const int h = it.kh * G + g;
         float al, be;
-        gates_f(ra, rbv, p.A_log[h], p.dt_bias[h], &al, &be);
+        gates_f(ra, rbv, rAl, rDt, &al, &be);
         gate[(t * kMaxG + g) * 2 + 0] = al;
         gate[(t * kMaxG + g) * 2 + 1] = be;
       }
@@ -491,7 +517,8 @@ __global__ void __launch_bounds__(NT, 1)
       __syncthreads();  // raw buffer consumed: start the next item's copies
       if (r_next < rounds) prefetch(nxt);
     } else {
-      __syncthreads();  // every warp is done with the previous item's xs and gates
+      __syncthreads();  // every warp is done with the previous item's xs, gates, tables
+      if (VERIFY && tid < k) tab_item[tid] = p.tables[tid * GDN_VERIFY_WY_TABLE_SEQS + it.seq];
       for (int lc = tid; lc < CHX; lc += NT) {
         if (lc >= CH) {  // z channel: staged as f32
           const int zc = lc - CH;
@@ -575,7 +602,8 @@ __global__ void __launch_bounds__(NT, 1)
         token_update<D, NT>(S, L, xq, xq + D, xq + (2 + g) * D, gate[(t * kMaxG + g) * 2 + 0],
                             gate[(t * kMaxG + g) * 2 + 1], kq_s[t],
                             red + (t & 1) * 2 * Map::RB * D, obuf + t * D);
-        if (VERIFY || t == k - 1) store_tile<D, NT>(state_dst<D, VERIFY>(p, it, h, t), S, L);
+        if (VERIFY || t == k - 1)
+          store_tile<D, NT>(state_dst<D, VERIFY>(p, it, tab_item, h, t), S, L);
       }
       __syncthreads();  // obuf complete
       norm_tokens<T, D, Map::NW>(obuf, xs + CH + g * D, CHX, k, it.row0, h, nw_s,

@@ -1,0 +1,108 @@
+// tcgen05.cuh -- thin inline-PTX wrappers for the 5th-generation tensor cores (sm_100+):
+// tensor-memory allocation, shared-memory matrix descriptors, bf16 MMA into TMEM,
+// completion through an mbarrier, and TMEM <-> register moves.
+//
+// Operand convention used throughout this library: every MMA operand is a K-major bf16
+// tile in shared memory with the 128-byte swizzle.  A tile of R rows x Kd elements
+// (Kd a multiple of 64) is stored as Kd/64 column blocks of [R][64] elements; inside a
+// block row r occupies 128 bytes and its 16-byte chunk c sits at chunk c ^ (r % 8).
+// Tiles start on 1024-byte boundaries.  The accumulator of an M = 128 MMA holds row m in
+// TMEM lane m and column n in TMEM column n (f32).
+#pragma once
+
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace gdn {
+namespace tc {
+
+// Byte offset of element (r, k) of a K-major, 128B-swizzled bf16 tile with R rows.
+__host__ __device__ __forceinline__ uint32_t sw128_offset(int R, int r, int k) {
+  return uint32_t((k >> 6) * R * 128 + r * 128 + ((((k & 63) >> 3) ^ (r & 7)) << 4) +
+                  ((k & 7) << 1));
+}
+
+// Shared-memory matrix descriptor: K-major, SWIZZLE_128B, 8-row groups 1024 B apart.
+// `addr` is the shared-window address of the first element the MMA reads (the tile
+// base plus the K offset of this instruction, within the 128-byte swizzle row).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= uint64_t((addr >> 4) & 0x3FFFu);          // start address
+  d |= uint64_t(1u) << 16;                        // leading byte offset (unused here)
+  d |= uint64_t((1024u >> 4) & 0x3FFFu) << 32;    // stride byte offset: 8 rows x 128 B
+  d |= uint64_t(1u) << 46;                        // descriptor version for sm_100
+  d |= uint64_t(2u) << 61;                        // layout: SWIZZLE_128B
+  return d;
+}
+
+// Descriptor of the K sub-block starting at element k0 (a multiple of 16) of a tile.
+__device__ __forceinline__ uint64_t desc_at(uint32_t tile_addr, int R, int k0) {
+  return desc_sw128(tile_addr + uint32_t((k0 >> 6) * R * 128 + (k0 & 63) * 2));
+}
+
+// Instruction descriptor of kind::f16: bf16 A and B (both K-major), f32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4)                       // D format: f32
+         | (1u << 7)                     // A format: bf16
+         | (1u << 10)                    // B format: bf16
+         | (uint32_t(N >> 3) << 17)      // N / 8
+         | (uint32_t(M >> 4) << 24);     // M / 16
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T for one K = 16 step (issued by one thread).
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+
+// Arrives once on `bar` when every MMA this thread issued before has completed.
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Tensor-memory allocation: executed by one whole warp.  The TMEM address lands in *slot.
+__device__ __forceinline__ void alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               ::"r"(smem_u32(slot)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// 32 lanes x 32 bits, 16 consecutive columns: thread t of warp w gets lane 32*(w%4)+t.
+// The wait is part of the same statement, so no use of the values can precede it.
+__device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+
+}  // namespace tc
+}  // namespace gdn

@@ -26,7 +26,8 @@
  *   - Pointers marked "device" are CUDA device (or managed) memory; "host" is host memory.
  *   - Row strides are in ELEMENTS of the activation dtype.
  *   - Supported shapes: (d_k, d_v) in {(16, 16), (128, 128)}, d_conv = 4,
- *     n_v_heads a multiple of n_k_heads with G = n_v_heads / n_k_heads <= 4.
+ *     n_v_heads a multiple of n_k_heads with G = n_v_heads / n_k_heads <= 4 (<= 3 for
+ *     gdn_verify_multi, whose per-token staging must fit in shared memory).
  *
  * Layouts (readings of the reference pages; the design notes list each one)
  *   raw QKV row  [conv_dim] = [Q: n_k_heads*d_k | K: n_k_heads*d_k | V: n_v_heads*d_v],
