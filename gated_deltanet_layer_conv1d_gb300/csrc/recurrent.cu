@@ -80,11 +80,15 @@ struct Lane {
 // L.col0..+3).  xq, xk: the normalised q, k of the token in shared memory; xv: its v;
 // red: this token's reduction buffer [2][RB][D] (alternate per token); orow: where the
 // (rb == 0, rs == 0) threads put o.  Contains one __syncthreads.
-template <int D, int NT>
-__device__ __forceinline__ void token_update(float4 (&S)[RecMap<D, NT>::M], const Lane<D, NT>& L,
+//
+// NAMED selects the barrier: named barrier 1 over the NT compute threads (kernels with a
+// separate producer warp) or __syncthreads.  `flag` is OR-reduced by that barrier; if any
+// thread raised it, every thread gets true back and the update is not applied.
+template <int D, int NT, bool NAMED = false>
+__device__ __forceinline__ bool token_update(float4 (&S)[RecMap<D, NT>::M], const Lane<D, NT>& L,
                                              const float* xq, const float* xk, const float* xv,
                                              float al, float be, float kq, float* red,
-                                             float* orow) {
+                                             float* orow, bool flag = false) {
   using Map = RecMap<D, NT>;
   float kr[Map::M];
   float4 u = make_float4(0.f, 0.f, 0.f, 0.f), pp = u;
@@ -111,7 +115,8 @@ __device__ __forceinline__ void token_update(float4 (&S)[RecMap<D, NT>::M], cons
     *reinterpret_cast<float4*>(red + L.rb * D + L.col0) = u;
     *reinterpret_cast<float4*>(red + (Map::RB + L.rb) * D + L.col0) = pp;
   }
-  __syncthreads();
+  const bool abort = NAMED ? named_sync_or(1, NT, flag) : (__syncthreads_or(flag) != 0);
+  if (abort) return true;
   float4 U = make_float4(0.f, 0.f, 0.f, 0.f), PP = U;
 #pragma unroll
   for (int b = 0; b < Map::RB; ++b) {
@@ -141,6 +146,7 @@ __device__ __forceinline__ void token_update(float4 (&S)[RecMap<D, NT>::M], cons
     S[m].z = al * S[m].z + kr[m] * dl.z;
     S[m].w = al * S[m].w + kr[m] * dl.w;
   }
+  return false;
 }
 
 template <int D, int NT>
@@ -223,8 +229,11 @@ struct RecSmem {
   static constexpr size_t kRed = kStage + STAGES * kTile;                  // [2][2][RB][D]
   static constexpr size_t kObuf = kRed + size_t(2) * 2 * Map::RB * D * 4;  // [KMAX][D]
   static constexpr size_t kNw = kObuf + size_t(KMAX) * D * 4;              // [D] norm_w
-  static constexpr size_t kBar = kNw + size_t(D) * 4;                      // [STAGES] u64
-  static constexpr size_t kGate = kBar + 8 * ((STAGES + 1) / 2 * 2);       // [KMAX][kMaxG][2]
+  // mbarriers: full[STAGES] | empty[STAGES] | raw_full | raw_empty, then two counters
+  // (tiles and raw blocks the producer has started), read only when a wait gives up.
+  static constexpr size_t kBar = kNw + size_t(D) * 4;
+  static constexpr size_t kIssued = kBar + 8 * (2 * STAGES + 2);           // [2] i32
+  static constexpr size_t kGate = kIssued + 16;                            // [KMAX][kMaxG][2]
   static constexpr size_t kKq = kGate + size_t(KMAX) * kMaxG * 2 * 4;      // [KMAX]
   // Per-launch staging so no global load sits on the per-head critical path:
   // slot of each sequence, whether its item can run (0 = yes, else the GDN_ERR_* code),
@@ -308,18 +317,28 @@ __device__ __forceinline__ const float* state_src(const RecParams& p, const Item
   return p.h_pool + (size_t(it.slot) * p.Hv + h) * D * D;
 }
 
+// Thread roles: threads [0, NT) compute (16 warps at d = 128), the last warp produces.
+// Lane 0 of the producer warp streams every state tile into the stage ring (full/empty
+// mbarriers per stage) and, for decode, each item's raw prologue inputs into a staging
+// block (raw_full/raw_empty), with bulk async copies.  Compute threads synchronise only
+// with named barrier 1; a stage is released by one mbarrier arrive per compute warp.
 template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NT + 32, 1)
     gdn_recurrent_kernel(const __grid_constant__ RecParams p) {
   using Map = RecMap<D, NT>;
   using SL = RecSmem<D, NT, KMAX, STAGES, T>;
   using A = Act<T>;
+  constexpr int NWC = NT / 32;  // compute warps
   extern __shared__ __align__(128) unsigned char smem[];
   float* stage = reinterpret_cast<float*>(smem + SL::kStage);
   float* red = reinterpret_cast<float*>(smem + SL::kRed);
   float* obuf = reinterpret_cast<float*>(smem + SL::kObuf);
   float* nw_s = reinterpret_cast<float*>(smem + SL::kNw);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SL::kBar);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SL::kBar);
+  uint64_t* empty = full + STAGES;
+  uint64_t* raw_full = full + 2 * STAGES;
+  uint64_t* raw_empty = raw_full + 1;
+  volatile int32_t* issued_s = reinterpret_cast<volatile int32_t*>(smem + SL::kIssued);
   float* gate = reinterpret_cast<float*>(smem + SL::kGate);
   float* kq_s = reinterpret_cast<float*>(smem + SL::kKq);
   float* xs = reinterpret_cast<float*>(smem + SL::kXs);
@@ -329,7 +348,6 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* tab_item = reinterpret_cast<uint64_t*>(smem + SL::kTabItem);
 
   const int tid = threadIdx.x;
-  const Lane<D, NT> L(tid);
   const int G = p.G, Hk = p.Hk;
   const int CH = (2 + G) * D;   // conv channels of one item
   const int CHX = CH + G * D;   // plus the z channels
@@ -342,15 +360,23 @@ __global__ void __launch_bounds__(NT, 1)
   T* raw_z = reinterpret_cast<T*>(raw + SL::raw_z(G));
 
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NWC);
+    }
+    mbar_init(raw_full, 1);
+    mbar_init(raw_empty, 1);
+    issued_s[0] = 0;
+    issued_s[1] = 0;
     fence_mbar_init();
   }
-  for (int j = tid; j < D; j += NT) nw_s[j] = p.norm_w[j];
-  for (int i = tid; i < p.n; i += NT) {
+  for (int j = tid; j < D; j += NT + 32) nw_s[j] = p.norm_w[j];
+  for (int i = tid; i < p.n; i += NT + 32) {
     slots_s[i] = p.slots[i];
     valid_s[i] = seq_check<VERIFY>(p, i);
     if (VERIFY) tab0_s[i] = p.tables[i];
   }
+  __syncthreads();  // the only CTA-wide barrier: barriers initialised, staging done
 
   // Global channel of item-local conv channel lc: q | k | v of the G value heads.
   auto global_channel = [&](int kh, int lc) -> int {
@@ -366,95 +392,99 @@ __global__ void __launch_bounds__(NT, 1)
     }
     return rounds;
   };
-  // Prefetch path: starts the async copies of an item's raw prologue inputs and loads its
-  // gate logits into registers (threads < k*G).
-  float ra = 0.f, rbv = 0.f, rAl = 0.f, rDt = 0.f;
-  auto prefetch = [&](const Item& it) {
-    const int k = it.k;
-    const int lens[3] = {D, D, G * D};
-    const int lstart[3] = {0, D, 2 * D};
-    for (int seg = 0; seg < 3; ++seg) {
-      const int gc = global_channel(it.kh, lstart[seg]);
-      const size_t cs_bytes = size_t(lens[seg]) * kW * sizeof(T);
-      const unsigned char* cs_src = reinterpret_cast<const unsigned char*>(p.conv_pool) +
-                                    (size_t(it.slot) * p.conv_dim + gc) * kW * sizeof(T);
-      unsigned char* cs_dst = reinterpret_cast<unsigned char*>(raw_cs) + size_t(lstart[seg]) * kW * sizeof(T);
-      for (size_t c = tid; c < cs_bytes / 16; c += NT) cp_async16(cs_dst + c * 16, cs_src + c * 16);
-      const size_t w_bytes = size_t(lens[seg]) * kW * 4;
-      const unsigned char* w_src = reinterpret_cast<const unsigned char*>(p.conv_w + size_t(gc) * kW);
-      unsigned char* w_dst = reinterpret_cast<unsigned char*>(raw_w + size_t(lstart[seg]) * kW);
-      for (size_t c = tid; c < w_bytes / 16; c += NT) cp_async16(w_dst + c * 16, w_src + c * 16);
-      const size_t x_bytes = size_t(lens[seg]) * sizeof(T);
-      for (int t = 0; t < k; ++t) {
-        const unsigned char* x_src = reinterpret_cast<const unsigned char*>(
-            reinterpret_cast<const T*>(p.qkv) + size_t(it.row0 + t) * p.qkv_stride + gc);
-        unsigned char* x_dst = reinterpret_cast<unsigned char*>(raw_x + size_t(t) * CH + lstart[seg]);
-        for (size_t c = tid; c < x_bytes / 16; c += NT) cp_async16(x_dst + c * 16, x_src + c * 16);
-      }
-    }
-    const size_t z_bytes = size_t(G) * D * sizeof(T);
-    for (int t = 0; t < k; ++t) {
-      const unsigned char* z_src = reinterpret_cast<const unsigned char*>(
-          reinterpret_cast<const T*>(p.z) + size_t(it.row0 + t) * p.z_stride + it.kh * G * D);
-      unsigned char* z_dst = reinterpret_cast<unsigned char*>(raw_z + size_t(t) * G * D);
-      for (size_t c = tid; c < z_bytes / 16; c += NT) cp_async16(z_dst + c * 16, z_src + c * 16);
-    }
-    cp_async_commit();
-    if (tid < k * G) {
-      const int t = tid / G, g = tid - t * G;
-      const size_t ro = size_t(it.row0 + t) * p.ab_stride + it.kh * G + g;
-      ra = A::to_f(reinterpret_cast<const T*>(p.a)[ro]);
-      rbv = A::to_f(reinterpret_cast<const T*>(p.b)[ro]);
-      rAl = p.A_log[it.kh * G + g];
-      rDt = p.dt_bias[it.kh * G + g];
-    }
-  };
 
-  // ---- producer cursor (thread 0 only): the next (round, value head) to load.  It walks
-  // the same item sequence as the consumer loop below and skips the same bad items.
-  int pr = 0, pg = 0;
-  int issued = 0;  // tiles the producer has started
-  Item pit;
-  bool pvalid = false;
-  auto prod_next = [&](const float** src) -> bool {
-    while (pr < rounds) {
-      if (!pvalid) {
-        const int j = item_at(cta, pr, P);
-        if (j < p.n_items && item_decode<VERIFY>(p, j, slots_s, valid_s, pit) == 0) {
-          pvalid = true;
-          pg = 0;
-        } else {
-          ++pr;
-          continue;
-        }
-      }
-      if (pg < G) {
-        *src = state_src<D, VERIFY>(p, pit, tab0_s, pit.kh * G + pg);
-        ++pg;
-        return true;
-      }
-      pvalid = false;
-      ++pr;
-    }
-    return false;
-  };
-  auto prod_issue = [&](int s) {
-    const float* src;
-    if (prod_next(&src)) {
-      ++issued;
-      mbar_arrive_expect_tx(&bar[s], uint32_t(SL::kTile));
+  // =========================================================================== producer
+  if (tid >= NT) {
+    if (tid != NT) return;
+    auto issue_tile = [&](int s, const Item& it, int g) {
+      const float* src = state_src<D, VERIFY>(p, it, tab0_s, it.kh * G + g);
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&full[s], uint32_t(SL::kTile));
       constexpr uint32_t kPiece = SL::kTile >= 16384 ? 16384u : uint32_t(SL::kTile);
 #pragma unroll
       for (uint32_t off = 0; off < SL::kTile; off += kPiece)
         bulk_g2s(reinterpret_cast<unsigned char*>(stage) + s * SL::kTile + off,
-                 reinterpret_cast<const unsigned char*>(src) + off, kPiece, &bar[s]);
+                 reinterpret_cast<const unsigned char*>(src) + off, kPiece, &full[s]);
+      issued_s[0] = issued_s[0] + 1;
+    };
+    // The raw prologue inputs of one item as contiguous blocks: conv state, conv
+    // weights and raw qkv of its q | k | v channel ranges, and z of its value heads.
+    auto issue_raw = [&](const Item& it) {
+      const int k = it.k;
+      const int lens[3] = {D, D, G * D};
+      const int lstart[3] = {0, D, 2 * D};
+      uint32_t total = uint32_t(CH) * kW * sizeof(T) + uint32_t(CH) * kW * 4 +
+                       uint32_t(k) * CH * sizeof(T) + uint32_t(k) * G * D * sizeof(T);
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(raw_full, total);
+      for (int seg = 0; seg < 3; ++seg) {
+        const int gc = global_channel(it.kh, lstart[seg]);
+        bulk_g2s(reinterpret_cast<unsigned char*>(raw_cs) + size_t(lstart[seg]) * kW * sizeof(T),
+                 reinterpret_cast<const T*>(p.conv_pool) + (size_t(it.slot) * p.conv_dim + gc) * kW,
+                 uint32_t(lens[seg]) * kW * sizeof(T), raw_full);
+        bulk_g2s(raw_w + size_t(lstart[seg]) * kW, p.conv_w + size_t(gc) * kW,
+                 uint32_t(lens[seg]) * kW * 4, raw_full);
+        for (int t = 0; t < k; ++t)
+          bulk_g2s(raw_x + size_t(t) * CH + lstart[seg],
+                   reinterpret_cast<const T*>(p.qkv) + size_t(it.row0 + t) * p.qkv_stride + gc,
+                   uint32_t(lens[seg]) * sizeof(T), raw_full);
+      }
+      for (int t = 0; t < k; ++t)
+        bulk_g2s(raw_z + size_t(t) * G * D,
+                 reinterpret_cast<const T*>(p.z) + size_t(it.row0 + t) * p.z_stride + it.kh * G * D,
+                 uint32_t(G) * D * sizeof(T), raw_full);
+      issued_s[1] = issued_s[1] + 1;
+    };
+    auto advance = [&](int& r, int& g, Item& it) {
+      if (++g == G) {
+        g = 0;
+        r = next_valid(r + 1, it);
+      }
+    };
+    Item it_raw, it_i, it_x;
+    int r_raw = next_valid(0, it_raw);
+    if (SL::kPrefetch && r_raw < rounds) {
+      issue_raw(it_raw);
+      r_raw = next_valid(r_raw + 1, it_raw);
     }
-  };
-  __syncthreads();  // barriers initialised, norm_w staged
-  if (tid == 0)
-    for (int s = 0; s < STAGES; ++s) prod_issue(s);
+    int r_i = next_valid(0, it_i), g_i = 0;  // next tile to issue
+    for (int s = 0; s < STAGES && r_i < rounds; ++s) {
+      issue_tile(s, it_i, g_i);
+      advance(r_i, g_i, it_i);
+    }
+    int r_x = next_valid(0, it_x), g_x = 0;  // tile the consumers take next
+    int x = 0, items = 0;
+    while (r_x < rounds) {
+      if (SL::kPrefetch && g_x == 0) {
+        // the consumers read raw inputs of item `items` before its first tile
+        if (!mbar_wait_bounded(raw_empty, uint32_t(items) & 1u)) {
+          report(p.status, GDN_ERR_TIMEOUT);
+          return;
+        }
+        if (r_raw < rounds) {
+          issue_raw(it_raw);
+          r_raw = next_valid(r_raw + 1, it_raw);
+        }
+        ++items;
+      }
+      if (r_i < rounds) {
+        const int s = x % STAGES;
+        if (!mbar_wait_bounded(&empty[s], uint32_t(x / STAGES) & 1u)) {
+          report(p.status, GDN_ERR_TIMEOUT);
+          return;
+        }
+        issue_tile(s, it_i, g_i);
+        advance(r_i, g_i, it_i);
+      }
+      ++x;
+      advance(r_x, g_x, it_x);
+    }
+    return;
+  }
 
-  // Bad items are reported here, once, by the consumer side.
+  // =========================================================================== compute
+  const Lane<D, NT> L(tid);
+  // Bad items are reported once, here.
   if (tid == 0) {
     for (int r = 0; r < rounds; ++r) {
       const int j = item_at(cta, r, P);
@@ -465,13 +495,33 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
   }
+  int q = 0, m = 0;  // tiles and items consumed by this CTA
+  // A bounded wait gave up: let this CTA's copies still in flight land, then stop.
+  auto drain = [&](int q_from) {
+    if (tid != 0) return;
+    report(p.status, GDN_ERR_TIMEOUT);
+    const int nt = issued_s[0], nr = issued_s[1];
+    for (int x = q_from; x < nt; ++x)
+      mbar_wait_bounded(&full[x % STAGES], uint32_t(x / STAGES) & 1u, kWaitBudgetNs / 8);
+    if (nr > m) mbar_wait_bounded(raw_full, uint32_t(m) & 1u, kWaitBudgetNs / 8);
+  };
+  // Gate logits and per-head gate parameters of an item, loaded ahead into registers
+  // (threads < k*G; decode).
+  float ra = 0.f, rbv = 0.f, rAl = 0.f, rDt = 0.f;
+  auto load_scalars = [&](const Item& it) {
+    if (tid < it.k * G) {
+      const int t = tid / G, g = tid - t * G;
+      const size_t ro = size_t(it.row0 + t) * p.ab_stride + it.kh * G + g;
+      ra = A::to_f(reinterpret_cast<const T*>(p.a)[ro]);
+      rbv = A::to_f(reinterpret_cast<const T*>(p.b)[ro]);
+      rAl = p.A_log[it.kh * G + g];
+      rDt = p.dt_bias[it.kh * G + g];
+    }
+  };
 
   Item nxt;
   int r_next = next_valid(0, nxt);
-  if constexpr (SL::kPrefetch) {
-    if (r_next < rounds) prefetch(nxt);
-  }
-  int q = 0;  // tiles consumed by this CTA
+  if (SL::kPrefetch && r_next < rounds) load_scalars(nxt);
   while (r_next < rounds) {
     const Item it = nxt;
     const int k = it.k;
@@ -479,7 +529,7 @@ __global__ void __launch_bounds__(NT, 1)
 
     // ---------------- item prologue: conv + SiLU (+ state update), z, gates, L2 norms
     if constexpr (SL::kPrefetch) {
-      cp_async_wait_all();
+      const bool ok = mbar_wait_bounded(raw_full, uint32_t(m) & 1u);
       if (tid < k * G) {  // gates from the prefetched logits
         const int t = tid / G, g = tid - t * G;
         float al, be;
@@ -487,7 +537,10 @@ __global__ void __launch_bounds__(NT, 1)
         gate[(t * kMaxG + g) * 2 + 0] = al;
         gate[(t * kMaxG + g) * 2 + 1] = be;
       }
-      __syncthreads();  // raw inputs of `it` visible to every thread
+      if (named_sync_or(1, NT, !ok)) {
+        drain(q);
+        return;
+      }
       for (int lc = tid; lc < CHX; lc += NT) {
         if (lc >= CH) {
           const int zc = lc - CH;
@@ -514,10 +567,11 @@ __global__ void __launch_bounds__(NT, 1)
                 (size_t(it.slot) * p.conv_dim + global_channel(it.kh, lc)) * kW;
         A::store4(cs, ns);  // exact copies of raw inputs
       }
-      __syncthreads();  // raw buffer consumed: start the next item's copies
-      if (r_next < rounds) prefetch(nxt);
+      named_sync(1, NT);  // raw block consumed
+      if (tid == 0) mbar_arrive(raw_empty);
+      if (r_next < rounds) load_scalars(nxt);
     } else {
-      __syncthreads();  // every warp is done with the previous item's xs, gates, tables
+      named_sync(1, NT);  // every warp is done with the previous item's xs, gates, tables
       if (VERIFY && tid < k) tab_item[tid] = p.tables[tid * GDN_VERIFY_WY_TABLE_SEQS + it.seq];
       for (int lc = tid; lc < CHX; lc += NT) {
         if (lc >= CH) {  // z channel: staged as f32
@@ -567,45 +621,39 @@ __global__ void __launch_bounds__(NT, 1)
         gate[(t * kMaxG + g) * 2 + 0] = al;
         gate[(t * kMaxG + g) * 2 + 1] = be;
       }
-      __syncthreads();
+      named_sync(1, NT);
     }
+    ++m;
     l2norm_tokens<D, Map::NW>(xs, CHX, k, p.q_scale, p.l2_eps, kq_s, L.warp, L.lane);
-    __syncthreads();
+    named_sync(1, NT);
 
     // ---------------- value heads of the item
     for (int g = 0; g < G; ++g) {
       const int h = it.kh * G + g;
       const int s = q % STAGES;
-      const uint32_t parity = uint32_t(q / STAGES) & 1u;
-      const bool ok = mbar_wait_bounded(&bar[s], parity);
+      const bool ok = mbar_wait_bounded(&full[s], uint32_t(q / STAGES) & 1u);
       float4 S[Map::M];
       const float* tile = stage + size_t(s) * D * D;
 #pragma unroll
-      for (int m = 0; m < Map::M; ++m)
-        S[m] = *reinterpret_cast<const float4*>(tile + L.row(m) * D + L.col0);
-      if (__syncthreads_or(!ok)) {
-        if (tid == 0) {
-          report(p.status, GDN_ERR_TIMEOUT);
-          // Let this CTA's copies still in flight land before it exits (bounded).
-          for (int x = q; x < issued; ++x)
-            mbar_wait_bounded(&bar[x % STAGES], uint32_t(x / STAGES) & 1u, kWaitBudgetNs / 8);
-        }
-        return;
-      }
+      for (int mm = 0; mm < Map::M; ++mm)
+        S[mm] = *reinterpret_cast<const float4*>(tile + L.row(mm) * D + L.col0);
+      __syncwarp();
+      if (L.lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
       ++q;
-      if (tid == 0) {
-        fence_proxy_async_smem();
-        prod_issue(s);  // refill the stage just emptied
-      }
       for (int t = 0; t < k; ++t) {
         const float* xq = xs + t * CHX;
-        token_update<D, NT>(S, L, xq, xq + D, xq + (2 + g) * D, gate[(t * kMaxG + g) * 2 + 0],
-                            gate[(t * kMaxG + g) * 2 + 1], kq_s[t],
-                            red + (t & 1) * 2 * Map::RB * D, obuf + t * D);
+        if (token_update<D, NT, true>(S, L, xq, xq + D, xq + (2 + g) * D,
+                                      gate[(t * kMaxG + g) * 2 + 0],
+                                      gate[(t * kMaxG + g) * 2 + 1], kq_s[t],
+                                      red + (t & 1) * 2 * Map::RB * D, obuf + t * D,
+                                      t == 0 && !ok)) {
+          drain(q - 1);
+          return;
+        }
         if (VERIFY || t == k - 1)
           store_tile<D, NT>(state_dst<D, VERIFY>(p, it, tab_item, h, t), S, L);
       }
-      __syncthreads();  // obuf complete
+      named_sync(1, NT);  // obuf complete
       norm_tokens<T, D, Map::NW>(obuf, xs + CH + g * D, CHX, k, it.row0, h, nw_s,
                                  p.norm_eps, p.Hv, reinterpret_cast<T*>(p.y), p.core_out,
                                  L.warp, L.lane);
@@ -623,7 +671,7 @@ cudaError_t launch_rec(const RecParams& p, cudaStream_t stream) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   const int P = p.n_items < sm_count() ? p.n_items : sm_count();
-  kern<<<P, NT, smem, stream>>>(p);
+  kern<<<P, NT + 32, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
