@@ -584,32 +584,31 @@ __global__ void __launch_bounds__(NT + 32, 1)
         const int gc = global_channel(it.kh, lc);
         T* cs = reinterpret_cast<T*>(p.conv_pool) + (size_t(it.slot) * p.conv_dim + gc) * kW;
         const float4 w4 = *reinterpret_cast<const float4*>(p.conv_w + size_t(gc) * kW);
-        float buf[kW + KMAX];
-        const float4 s4 = A::load4(cs);
-        buf[0] = s4.x; buf[1] = s4.y; buf[2] = s4.z; buf[3] = s4.w;
+        // win: the last kW raw inputs, oldest first; each token shifts its input in.
+        float4 win = A::load4(cs);
         const T* xrow = reinterpret_cast<const T*>(p.qkv) + size_t(it.row0) * p.qkv_stride + gc;
+        constexpr int kGrp = KMAX < 4 ? KMAX : 4;  // raw loads in flight together
+        for (int t0 = 0; t0 < k; t0 += kGrp) {
+          float xg[kGrp];
 #pragma unroll
-        for (int t = 0; t < KMAX; ++t)
-          if (t < k) buf[kW + t] = A::to_f(xrow[size_t(t) * p.qkv_stride]);
+          for (int u = 0; u < kGrp; ++u)
+            if (t0 + u < k) xg[u] = A::to_f(xrow[size_t(t0 + u) * p.qkv_stride]);
 #pragma unroll
-        for (int t = 0; t < KMAX; ++t) {
-          if (t < k) {
-            // window of token t: the last kW raw inputs, buf[t+1 .. t+4]
-            const float acc = w4.x * buf[t + 1] + w4.y * buf[t + 2] + w4.z * buf[t + 3] +
-                              w4.w * buf[t + 4];
-            xs[t * CHX + lc] = silu_f(acc);
-            if (VERIFY && p.conv_inter && t < k - 1) {
-              T* ci = reinterpret_cast<T*>(p.conv_inter) +
-                      ((size_t(it.seq) * (GDN_VERIFY_WY_TABLES_PER_LAYER - 1) + t) * p.conv_dim + gc) * kW;
-              A::store4(ci, make_float4(buf[t + 1], buf[t + 2], buf[t + 3], buf[t + 4]));
+          for (int u = 0; u < kGrp; ++u) {
+            const int t = t0 + u;
+            if (t < k) {
+              win = make_float4(win.y, win.z, win.w, xg[u]);
+              xs[t * CHX + lc] =
+                  silu_f(w4.x * win.x + w4.y * win.y + w4.z * win.z + w4.w * win.w);
+              if (VERIFY && p.conv_inter && t < k - 1) {
+                T* ci = reinterpret_cast<T*>(p.conv_inter) +
+                        ((size_t(it.seq) * (GDN_VERIFY_WY_TABLES_PER_LAYER - 1) + t) * p.conv_dim + gc) * kW;
+                A::store4(ci, win);
+              }
             }
           }
         }
-        float4 ns = s4;
-#pragma unroll
-        for (int t = 1; t <= KMAX; ++t)
-          if (t == k) ns = make_float4(buf[t], buf[t + 1], buf[t + 2], buf[t + 3]);
-        A::store4(cs, ns);  // exact copies of raw inputs
+        A::store4(cs, win);  // exact copies of the last kW raw inputs
       }
       for (int idx = tid; idx < k * G; idx += NT) {
         const int t = idx / G, g = idx - t * G;
