@@ -36,16 +36,33 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
   return d;
 }
 
+// MN-major, SWIZZLE_128B: the operand is stored [K rows][MN elements] with 64-element
+// (128-byte) MN blocks `lbo_bytes` apart; 8 K rows span 1024 bytes.  `addr` points at the
+// first K row the instruction reads (advance 16 rows = 2048 bytes per K = 16 step).
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t addr, uint32_t lbo_bytes) {
+  uint64_t d = 0;
+  d |= uint64_t((addr >> 4) & 0x3FFFu);
+  d |= uint64_t((lbo_bytes >> 4) & 0x3FFFu) << 16;  // stride between 64-element MN blocks
+  d |= uint64_t((1024u >> 4) & 0x3FFFu) << 32;      // stride between 8-row K groups
+  d |= uint64_t(1u) << 46;
+  d |= uint64_t(2u) << 61;
+  return d;
+}
+
 // Descriptor of the K sub-block starting at element k0 (a multiple of 16) of a tile.
 __device__ __forceinline__ uint64_t desc_at(uint32_t tile_addr, int R, int k0) {
   return desc_sw128(tile_addr + uint32_t((k0 >> 6) * R * 128 + (k0 & 63) * 2));
 }
 
-// Instruction descriptor of kind::f16: bf16 A and B (both K-major), f32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+// Instruction descriptor of kind::f16: bf16 A and B, f32 accumulator; A and B K-major
+// unless a_mn / b_mn select MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn = false,
+                                                  bool b_mn = false) {
   return (1u << 4)                       // D format: f32
          | (1u << 7)                     // A format: bf16
          | (1u << 10)                    // B format: bf16
+         | (uint32_t(a_mn) << 15)        // A major-ness
+         | (uint32_t(b_mn) << 16)        // B major-ness
          | (uint32_t(N >> 3) << 17)      // N / 8
          | (uint32_t(M >> 4) << 24);     // M / 16
 }
