@@ -13,6 +13,8 @@
 //   gated_rms_norm_f32_k / gated_rms_norm_prefill_k).
 #include "common.cuh"
 #include "kernels.h"
+#include "prefill_layout.cuh"
+#include "tcgen05.cuh"
 
 namespace gdn {
 namespace {
@@ -92,9 +94,42 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const __grid_con
         const float r = (is_q ? p.q_scale : 1.f) * rsqrtf(ss + p.l2_eps);
         y.x *= r; y.y *= r; y.z *= r; y.w *= r;
       }
-      const size_t o = size_t(t) * p.conv_dim + qd * 4;
-      if (p.out_bf16) Act<__nv_bfloat16>::store4(reinterpret_cast<__nv_bfloat16*>(p.out) + o, y);
-      else *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) = y;
+      if (p.out_mode == 2) {
+        // prefill workspace: the channel's place in its 128B-swizzled [64][128] tile
+        const PrefillLayout lay{p.Hk, p.Hv};
+        const size_t cs = PrefillLayout::base(t0, seq) + size_t(pos / PrefillLayout::kC);
+        const int r = pos % PrefillLayout::kC;
+        const int c = qd * 4;
+        size_t off;
+        if (c < 2 * p.Hk * D) {
+          const int head = c / D, i = c % D;
+          off = (head < p.Hk ? lay.qk(cs, head, 1) : lay.qk(cs, head - p.Hk, 0)) +
+                tc::sw128_offset(PrefillLayout::kC, r, i);
+        } else {
+          const int c2 = c - 2 * p.Hk * D;
+          off = lay.v(cs, c2 / D) + tc::sw128_offset(PrefillLayout::kC, r, c2 % D);
+        }
+        Act<__nv_bfloat16>::store4(
+            reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<unsigned char*>(p.workspace) + off), y);
+      } else {
+        const size_t o = size_t(t) * p.conv_dim + qd * 4;
+        if (p.out_bf16) Act<__nv_bfloat16>::store4(reinterpret_cast<__nv_bfloat16*>(p.out) + o, y);
+        else *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) = y;
+      }
+    }
+  }
+  if (p.out_mode == 2) {
+    // log(alpha) and beta of this token for every value head
+    const PrefillLayout lay{p.Hk, p.Hv};
+    const size_t cs = PrefillLayout::base(t0, seq) + size_t(pos / PrefillLayout::kC);
+    const int r = pos % PrefillLayout::kC;
+    for (int h = threadIdx.x; h < p.Hv; h += kConvThreads) {
+      const size_t ro = size_t(t) * p.ab_stride + h;
+      const float av = A::to_f(reinterpret_cast<const T*>(p.a)[ro]);
+      const float bv = A::to_f(reinterpret_cast<const T*>(p.b)[ro]);
+      float* g = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(p.workspace) + lay.gate(cs, h));
+      g[r] = -expf(p.A_log[h]) * softplus_f(av + p.dt_bias[h]);
+      g[PrefillLayout::kC + r] = sigmoid_f(bv);
     }
   }
 }
@@ -175,6 +210,12 @@ cudaError_t conv_typed(const ConvParams& p, cudaStream_t stream) {
 cudaError_t launch_conv_step(const ConvParams& p, int dtype, cudaStream_t stream) {
   if (dtype == GDN_DTYPE_BF16) return conv_typed<__nv_bfloat16>(p, stream);
   return conv_typed<float>(p, stream);
+}
+
+cudaError_t launch_prefill_prep(const ConvParams& p, cudaStream_t stream) {
+  if (p.total_tokens > 0)
+    gdn_conv_kernel<__nv_bfloat16, 128><<<p.total_tokens, kConvThreads, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_conv_state_update(const ConvParams& p, int dtype, cudaStream_t stream) {

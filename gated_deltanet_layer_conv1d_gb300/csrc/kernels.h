@@ -58,8 +58,19 @@ struct ConvParams {
   void* out;
   int32_t out_bf16;
   int32_t* status;
+  // Chunked-prefill pre-pass only (out_mode == 2): gates and the workspace tiles.
+  int32_t out_mode;  // 0: f32 rows / 1: bf16 rows (out_bf16), 2: prefill workspace tiles
+  const float* A_log;
+  const float* dt_bias;
+  const void* a;
+  const void* b;
+  int64_t ab_stride;
+  void* workspace;
 };
 cudaError_t launch_conv_step(const ConvParams& p, int dtype, cudaStream_t stream);
+// Pre-pass of the tensor-core prefill: conv, SiLU, L2 norms and gates of every token into
+// the workspace tiles (bf16 activations, d = 128).
+cudaError_t launch_prefill_prep(const ConvParams& p, cudaStream_t stream);
 
 cudaError_t launch_gated_rmsnorm(const float* o, const void* z, int64_t z_stride,
                                  const float* w, float eps, int T, int Hv, int D, int dtype,

@@ -1,17 +1,55 @@
 // prefill.cu -- dispatch of the GDN prefill (sm_103a).
+//
+// d_k = d_v = 128 with bf16 activations: the tensor-core chunked path -- a pre-pass
+// (conv, SiLU, L2 norms, gates of every token into the workspace tiles), then one
+// tcgen05 chunk kernel per (sequence, value head).  Every other shape or dtype: the
+// token-sequential kernel.  The conv-state update runs after either (see abi.cu).
 #include "common.cuh"
 #include "kernels.h"
+#include "prefill_layout.cuh"
 
 namespace gdn {
 
 cudaError_t launch_prefill_sequential(const PrefillParams& p, int dtype, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream);
 
 size_t prefill_workspace_bytes(int Hk, int Hv, int D, int n, int total_tokens, int max_seqlen) {
-  (void)Hk; (void)Hv; (void)D; (void)n; (void)total_tokens; (void)max_seqlen;
-  return 0;
+  (void)max_seqlen;
+  if (D != 128) return 0;
+  const PrefillLayout lay{Hk, Hv};
+  return PrefillLayout::slots(n, total_tokens) * lay.slot_bytes();
 }
 
 cudaError_t launch_prefill(const PrefillParams& p, int dtype, cudaStream_t stream) {
+  if (p.D == 128 && dtype == GDN_DTYPE_BF16) {
+    ConvParams c{};
+    c.Hk = p.Hk;
+    c.Hv = p.Hv;
+    c.D = p.D;
+    c.conv_dim = p.conv_dim;
+    c.n = p.n;
+    c.n_slots = p.n_slots;
+    c.total_tokens = p.total_tokens;
+    c.q_scale = p.q_scale;
+    c.l2_eps = p.l2_eps;
+    c.conv_w = p.conv_w;
+    c.qkv = p.qkv;
+    c.qkv_stride = p.qkv_stride;
+    c.cu_seqlens = p.cu_seqlens;
+    c.conv_pool = p.conv_pool;
+    c.slots = p.slots;
+    c.status = p.status;
+    c.out_mode = 2;
+    c.A_log = p.A_log;
+    c.dt_bias = p.dt_bias;
+    c.a = p.a;
+    c.b = p.b;
+    c.ab_stride = p.ab_stride;
+    c.workspace = p.workspace;
+    cudaError_t e = launch_prefill_prep(c, stream);
+    if (e != cudaSuccess) return e;
+    return launch_prefill_tc(p, stream);
+  }
   return launch_prefill_sequential(p, dtype, stream);
 }
 

@@ -1,0 +1,469 @@
+// prefill_tc.cu -- chunked (WY / UT-transform) prefill of the gated delta rule on the
+// 5th-generation tensor cores (tcgen05, accumulators in TMEM), d_k = d_v = 128, chunk 64.
+//
+// The method (layer_struct.rs, the FLA chunked prefill: gdn_prefill_fla_recompute_wu_k ->
+// the chunk_delta_h state spine -> gdn_prefill_fla_chunk_fwd_o_k; here one fused kernel per
+// (sequence, value head)).  Inside a chunk of L tokens, with g_r = sum_{s<=r} log alpha_s:
+//   A   = strict_lower(beta_r (k_r . k_s) e^{g_r - g_s}),   T = (I + A)^{-1}
+//   W   = T diag(beta e^g) K,   U = T diag(beta) V,   Delta = U - W H0      (H0 = S0^T)
+//   O   = diag(e^g) Q H0 + lower_incl(Q K^T e^{g_r - g_s}) Delta
+//   H_L = e^{g_L} H0 + (diag(e^{g_L - g}) K)^T Delta
+// Every product is computed transposed so that M = 128 (one TMEM lane per accumulator row):
+//   MMA0  [K;Q] K^T            (M 128 = 64 keys + 64 queries, N 64, K 128)
+//   MMA_W W^T = K^T (T diag(beta e^g))^T      (A = K MN-major, N 64, K 64)
+//   MMA_U U^T = V^T (T diag(beta))^T          (A = V MN-major)
+//   MMA1  (W H0)^T = H0^T W^T,   MMA2  (Q H0)^T = H0^T Q^T     (N 64, K 128)
+//   MMA3  (P Delta)^T = Delta^T P^T           (N 64, K 64)
+//   MMA4  (K~^T Delta)^T = (Delta^T diag(e^{g_L - g})) K        (B = K MN-major, N 128, K 64)
+// All per-token scalings are folded into T's columns, Delta's columns or the epilogue, so
+// the q, k, v tiles come straight from the pre-pass workspace (one bulk copy each).
+// H0 lives in registers (f32) of the 8 warps: thread (w, l) owns row j = 32 (w % 4) + l of
+// H^T and columns i in [64 (w / 4), +64); its bf16 copy is the A operand of MMA1/MMA2.
+// T = (I + A)^{-1} is computed on CUDA cores by blocked forward substitution (16 x 16
+// diagonal blocks, then the off-diagonal blocks level by level).
+#include "common.cuh"
+#include "kernels.h"
+#include "prefill_layout.cuh"
+#include "tcgen05.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kC = 64;
+constexpr int kD = 128;
+constexpr int kThreads = 256;
+
+// Shared memory (offsets from a 1024-aligned base).
+struct TcSmem {
+  static constexpr uint32_t kAQK = 0;            // [128][128] bf16: rows 0-63 k_hat, 64-127 q_hat
+  static constexpr uint32_t kV = 32768;          // [64][128] bf16 v (MN-major A of MMA_U)
+  static constexpr uint32_t kHT = 49152;         // [128][128] bf16 H^T
+  static constexpr uint32_t kW = 81920;          // [64][128] bf16 W
+  static constexpr uint32_t kTw = 98304;         // [64][64] bf16 T diag(beta e^g)
+  static constexpr uint32_t kTu = 106496;        // [64][64] bf16 T diag(beta)
+  static constexpr uint32_t kP = 114688;         // [64][64] bf16 P
+  static constexpr uint32_t kDT = 122880;        // [128][64] bf16 Delta^T
+  static constexpr uint32_t kDTs = 139264;       // [128][64] bf16 Delta^T diag(e^{g_L - g})
+  static constexpr uint32_t kAm = 155648;        // [64][64] f32 A
+  static constexpr uint32_t kTf = 172032;        // [64][64] f32 T
+  static constexpr uint32_t kY = 188416;         // [3][16][16] f32 scratch of the inverse
+  static constexpr uint32_t kGate = 191488;      // [2][64] f32 log(alpha), beta (bulk copied)
+  static constexpr uint32_t kG = 192000;         // [64] f32 cumulative log decay g
+  static constexpr uint32_t kB = 192256;         // [64] f32 beta (0 past the chunk end)
+  static constexpr uint32_t kMisc = 192512;      // bars, tmem slot, scan carry
+  static constexpr uint32_t kBytes = 192640;
+  static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024
+};
+
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  uint4 u;
+  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+  __nv_bfloat162 c = __floats2bfloat162_rn(v[4], v[5]), d = __floats2bfloat162_rn(v[6], v[7]);
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  u.z = *reinterpret_cast<uint32_t*>(&c);
+  u.w = *reinterpret_cast<uint32_t*>(&d);
+  return u;
+}
+
+// TMEM columns of the accumulators (512 allocated).
+constexpr uint32_t kT0 = 0;     // MMA0: [K;Q] K^T          (64 cols)
+constexpr uint32_t kTW = 64;    // MMA_W: W^T               (64)
+constexpr uint32_t kTU = 128;   // MMA_U: U^T               (64)
+constexpr uint32_t kTD = 192;   // MMA1: (W H0)^T           (64)
+constexpr uint32_t kT2 = 256;   // MMA2: (Q H0)^T           (64)
+constexpr uint32_t kT3 = 320;   // MMA3: (P Delta)^T        (64)
+constexpr uint32_t kT4 = 384;   // MMA4: (K~^T Delta)^T     (128)
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
+  using S = TcSmem;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  float* Am = reinterpret_cast<float*>(sm + S::kAm);
+  float* Tf = reinterpret_cast<float*>(sm + S::kTf);
+  float* Ys = reinterpret_cast<float*>(sm + S::kY);
+  float* gate = reinterpret_cast<float*>(sm + S::kGate);
+  float* G_s = reinterpret_cast<float*>(sm + S::kG);
+  float* B_s = reinterpret_cast<float*>(sm + S::kB);
+  float* Os = reinterpret_cast<float*>(sm + S::kAQK);  // output staging, after MMA4
+  uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + S::kMisc);
+  uint64_t* bar_mma = bar_load + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_mma + 1);
+  float* carry = reinterpret_cast<float*>(tslot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int seq = blockIdx.x / p.Hv, h = blockIdx.x % p.Hv, kh = h / p.G;
+  const int t_begin = p.cu_seqlens[seq], t_end = p.cu_seqlens[seq + 1];
+  const int len = t_end - t_begin;
+  const uint64_t hp = p.h_ptrs[seq];
+  {
+    int bad = 0;
+    if (t_begin < 0 || len < 0 || t_end > p.total_tokens || len > p.max_seqlen)
+      bad = GDN_ERR_BAD_SEQLENS;
+    else if (hp == 0 || (hp & 15u) != 0)
+      bad = GDN_ERR_BAD_TABLE_ENTRY;
+    if (bad) {
+      if (tid == 0) report(p.status, bad);
+      return;
+    }
+  }
+  if (len == 0) return;  // nothing to do: the state stays as it is
+
+  const PrefillLayout lay{p.Hk, p.Hv};
+  const size_t slot0 = PrefillLayout::base(t_begin, seq);
+  const unsigned char* ws = reinterpret_cast<const unsigned char*>(p.workspace);
+  const int nc = (len + kC - 1) / kC;
+
+  if (tid == 0) {
+    mbar_init(bar_load, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tc::alloc(tslot, 512);
+
+  // H0 (f32) into registers: H^T row j, columns i0 .. i0 + 63.
+  const int q4 = warp & 3, half = warp >> 2;
+  const int j = 32 * q4 + lane;
+  const int i0 = 64 * half;
+  float* Hg = reinterpret_cast<float*>(hp) + size_t(h) * kD * kD;
+  float Hr[64];
+#pragma unroll
+  for (int ii = 0; ii < 64; ++ii) Hr[ii] = Hg[(i0 + ii) * kD + j];
+  auto write_HT = [&]() {
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8)
+      *reinterpret_cast<uint4*>(sm + S::kHT + tc::sw128_offset(128, j, i0 + 8 * c8)) =
+          pack8_bf16(Hr + 8 * c8);
+  };
+  write_HT();
+  fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const uint32_t tl = uint32_t(32 * q4) << 16;  // this warp's TMEM lane quarter
+  uint32_t load_phase = 0, mma_phase = 0;
+  bool bad = false;
+  // Every thread waits for the MMAs committed so far.
+  auto mma_wait = [&]() {
+    bad |= !mbar_wait_bounded(bar_mma, mma_phase);
+    mma_phase ^= 1u;
+    tc::fence_after_sync();
+  };
+  // Barrier that also agrees on a failed wait; true means stop.
+  auto sync_or_stop = [&]() -> bool {
+    tc::fence_before_sync();
+    const bool stop = __syncthreads_or(bad) != 0;
+    tc::fence_after_sync();
+    return stop;
+  };
+
+  bool aborted = false;
+  for (int c = 0; c < nc; ++c) {
+    const int t0 = c * kC;
+    const int L = (len - t0) < kC ? (len - t0) : kC;
+    const size_t cs = slot0 + size_t(c);
+
+    // ---- 1. this chunk's k_hat, q_hat, v tiles and gates
+    if (tid == 0) {
+      const unsigned char* kimg = ws + lay.qk(cs, kh, 0);
+      const unsigned char* qimg = ws + lay.qk(cs, kh, 1);
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar_load, 3u * 16384u + 512u);
+      bulk_g2s(sm + S::kAQK, kimg, 8192, bar_load);
+      bulk_g2s(sm + S::kAQK + 16384, kimg + 8192, 8192, bar_load);
+      bulk_g2s(sm + S::kAQK + 8192, qimg, 8192, bar_load);
+      bulk_g2s(sm + S::kAQK + 24576, qimg + 8192, 8192, bar_load);
+      bulk_g2s(sm + S::kV, ws + lay.v(cs, h), 16384, bar_load);
+      bulk_g2s(gate, ws + lay.gate(cs, h), 512, bar_load);
+    }
+    bad |= !mbar_wait_bounded(bar_load, load_phase);
+    load_phase ^= 1u;
+
+    // ---- 2. rows past the end of the sequence are zero; decay prefix sums
+    if (L < kC) {
+      const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+      for (int idx = tid; idx < (kC - L) * 16; idx += kThreads) {
+        const int row = L + idx / 16, ch = idx % 16, blk = ch / 8, c16 = ch % 8;
+        *reinterpret_cast<uint4*>(sm + S::kAQK + blk * 16384 + row * 128 + c16 * 16) = zero;
+        *reinterpret_cast<uint4*>(sm + S::kAQK + blk * 16384 + (kC + row) * 128 + c16 * 16) = zero;
+        *reinterpret_cast<uint4*>(sm + S::kV + blk * 8192 + row * 128 + c16 * 16) = zero;
+      }
+    }
+    if (tid < kC) {
+      float v = tid < L ? gate[tid] : 0.f;
+      const float be = tid < L ? gate[kC + tid] : 0.f;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += u;
+      }
+      if (tid == 31) carry[0] = v;
+      named_sync(2, kC);
+      if (tid >= 32) v += carry[0];
+      G_s[tid] = v;
+      B_s[tid] = be;
+    }
+    fence_proxy_async_smem();
+    if (sync_or_stop()) { aborted = true; break; }
+    const float gL = G_s[L - 1];
+
+    // ---- 3. MMA0: [K;Q] K^T
+    if (tid == 0) {
+#pragma unroll
+      for (int k0 = 0; k0 < kD; k0 += 16)
+        tc::mma_bf16(tmem + kT0, tc::desc_at(sb + S::kAQK, 128, k0),
+                     tc::desc_at(sb + S::kAQK, 128, k0), tc::idesc_bf16(128, 64), k0 > 0);
+      tc::commit(bar_mma);
+    }
+    mma_wait();
+
+    // ---- 4. A (f32) from the K K^T rows, P (bf16) from the Q K^T rows
+    {
+      float v[32];
+      tc::ld16(tmem + tl + kT0 + 32 * half, *reinterpret_cast<float(*)[16]>(v));
+      tc::ld16(tmem + tl + kT0 + 32 * half + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      const int row = 32 * q4 + lane;
+      if (row < kC) {
+        const int r = row;
+        const float gr = G_s[r], br = B_s[r];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const int s = 32 * half + u;
+          Am[r * kC + s] = (s < r && r < L) ? br * v[u] * expf(gr - G_s[s]) : 0.f;
+        }
+      } else {
+        const int r = row - kC;
+        const float gr = G_s[r];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const int s = 32 * half + u;
+          v[u] = (s <= r && r < L) ? v[u] * expf(gr - G_s[s]) : 0.f;
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8)
+          *reinterpret_cast<uint4*>(sm + S::kP + tc::sw128_offset(64, r, 32 * half + 8 * c8)) =
+              pack8_bf16(v + 8 * c8);
+      }
+    }
+    if (sync_or_stop()) { aborted = true; break; }
+
+    // ---- 5. T = (I + A)^{-1}: diagonal 16 x 16 blocks, then the blocks below them
+    if (warp < 4) {
+      if (lane < 16) {
+        const int b0 = 16 * warp;
+        float X[16];
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+          float acc = (rr == lane) ? 1.f : 0.f;
+#pragma unroll
+          for (int ss = 0; ss < rr; ++ss) acc -= Am[(b0 + rr) * kC + b0 + ss] * X[ss];
+          X[rr] = acc;
+        }
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) Tf[(b0 + rr) * kC + b0 + lane] = X[rr];
+      }
+    } else {
+      // blocks above the diagonal are zero
+      for (int e = tid - 128; e < 6 * 256; e += 128) {
+        const int blk = e / 256, a = (e % 256) / 16, bb = e % 16;
+        const int I = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        Tf[(16 * I + a) * kC + 16 * J + bb] = 0.f;
+      }
+    }
+    __syncthreads();
+    for (int d = 1; d < 4; ++d) {
+      const int nblk = 4 - d;  // blocks (I, J = I - d), I = d .. 3
+      for (int e = tid; e < nblk * 256; e += kThreads) {
+        const int I = d + e / 256, J = I - d, a = (e % 256) / 16, bb = e % 16;
+        float acc = 0.f;
+        for (int K = J; K < I; ++K)
+#pragma unroll
+          for (int n = 0; n < 16; ++n)
+            acc += Am[(16 * I + a) * kC + 16 * K + n] * Tf[(16 * K + n) * kC + 16 * J + bb];
+        Ys[e] = acc;
+      }
+      __syncthreads();
+      for (int e = tid; e < nblk * 256; e += kThreads) {
+        const int I = d + e / 256, J = I - d, a = (e % 256) / 16, bb = e % 16;
+        const float* y = Ys + (e / 256) * 256;
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) acc += Tf[(16 * I + a) * kC + 16 * I + m] * y[m * 16 + bb];
+        Tf[(16 * I + a) * kC + 16 * J + bb] = -acc;
+      }
+      __syncthreads();
+    }
+    // T diag(beta e^g) and T diag(beta), bf16, [r][s]
+    for (int cid = tid; cid < kC * 8; cid += kThreads) {
+      const int r = cid / 8, s0 = (cid % 8) * 8;
+      float tw[8], tu[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float tv = Tf[r * kC + s0 + u];
+        tu[u] = tv * B_s[s0 + u];
+        tw[u] = tu[u] * expf(G_s[s0 + u]);
+      }
+      *reinterpret_cast<uint4*>(sm + S::kTw + tc::sw128_offset(64, r, s0)) = pack8_bf16(tw);
+      *reinterpret_cast<uint4*>(sm + S::kTu + tc::sw128_offset(64, r, s0)) = pack8_bf16(tu);
+    }
+    fence_proxy_async_smem();
+    if (sync_or_stop()) { aborted = true; break; }
+
+    // ---- 6. W^T = K^T (T diag(beta e^g))^T, U^T = V^T (T diag(beta))^T
+    if (tid == 0) {
+#pragma unroll
+      for (int s0 = 0; s0 < kC; s0 += 16) {
+        tc::mma_bf16(tmem + kTW, tc::desc_mn_sw128(sb + S::kAQK + s0 * 128, 16384),
+                     tc::desc_at(sb + S::kTw, 64, s0), tc::idesc_bf16(128, 64, true, false),
+                     s0 > 0);
+        tc::mma_bf16(tmem + kTU, tc::desc_mn_sw128(sb + S::kV + s0 * 128, 8192),
+                     tc::desc_at(sb + S::kTu, 64, s0), tc::idesc_bf16(128, 64, true, false),
+                     s0 > 0);
+      }
+      tc::commit(bar_mma);
+    }
+    mma_wait();
+
+    // ---- 7. W [r][i] from W^T (lane i)
+    {
+      float v[32];
+      tc::ld16(tmem + tl + kTW + 32 * half, *reinterpret_cast<float(*)[16]>(v));
+      tc::ld16(tmem + tl + kTW + 32 * half + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      const int i = 32 * q4 + lane;
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        *reinterpret_cast<__nv_bfloat16*>(sm + S::kW + tc::sw128_offset(64, 32 * half + u, i)) =
+            __float2bfloat16_rn(v[u]);
+    }
+    fence_proxy_async_smem();
+    if (sync_or_stop()) { aborted = true; break; }
+
+    // ---- 8. (W H0)^T = H0^T W^T and (Q H0)^T = H0^T Q^T
+    if (tid == 0) {
+#pragma unroll
+      for (int k0 = 0; k0 < kD; k0 += 16) {
+        tc::mma_bf16(tmem + kTD, tc::desc_at(sb + S::kHT, 128, k0),
+                     tc::desc_at(sb + S::kW, 64, k0), tc::idesc_bf16(128, 64), k0 > 0);
+        tc::mma_bf16(tmem + kT2, tc::desc_at(sb + S::kHT, 128, k0),
+                     tc::desc_at(sb + S::kAQK + 8192, 128, k0), tc::idesc_bf16(128, 64),
+                     k0 > 0);
+      }
+      tc::commit(bar_mma);
+    }
+    mma_wait();
+
+    // ---- 9. Delta^T = U^T - (W H0)^T, and its decay-weighted copy
+    {
+      float du[32], dd[32];
+      tc::ld16(tmem + tl + kTU + 32 * half, *reinterpret_cast<float(*)[16]>(du));
+      tc::ld16(tmem + tl + kTU + 32 * half + 16, *reinterpret_cast<float(*)[16]>(du + 16));
+      tc::ld16(tmem + tl + kTD + 32 * half, *reinterpret_cast<float(*)[16]>(dd));
+      tc::ld16(tmem + tl + kTD + 32 * half + 16, *reinterpret_cast<float(*)[16]>(dd + 16));
+      float ds[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) {
+        du[u] -= dd[u];
+        ds[u] = du[u] * expf(gL - G_s[32 * half + u]);
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        const uint32_t off = tc::sw128_offset(128, j, 32 * half + 8 * c8);
+        *reinterpret_cast<uint4*>(sm + S::kDT + off) = pack8_bf16(du + 8 * c8);
+        *reinterpret_cast<uint4*>(sm + S::kDTs + off) = pack8_bf16(ds + 8 * c8);
+      }
+    }
+    fence_proxy_async_smem();
+    if (sync_or_stop()) { aborted = true; break; }
+
+    // ---- 10. (P Delta)^T = Delta^T P^T and (K~^T Delta)^T = (Delta^T e^{g_L - g}) K
+    if (tid == 0) {
+#pragma unroll
+      for (int s0 = 0; s0 < kC; s0 += 16) {
+        tc::mma_bf16(tmem + kT3, tc::desc_at(sb + S::kDT, 128, s0),
+                     tc::desc_at(sb + S::kP, 64, s0), tc::idesc_bf16(128, 64), s0 > 0);
+        tc::mma_bf16(tmem + kT4, tc::desc_at(sb + S::kDTs, 128, s0),
+                     tc::desc_mn_sw128(sb + S::kAQK + s0 * 128, 16384),
+                     tc::idesc_bf16(128, 128, false, true), s0 > 0);
+      }
+      tc::commit(bar_mma);
+    }
+    mma_wait();
+
+    // ---- 11. H update (registers + bf16 copy) and the chunk outputs
+    {
+      const float eL = expf(gL);
+#pragma unroll
+      for (int c16 = 0; c16 < 4; ++c16) {
+        float v[16];
+        tc::ld16(tmem + tl + kT4 + i0 + 16 * c16, v);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) Hr[16 * c16 + u] = eL * Hr[16 * c16 + u] + v[u];
+      }
+      write_HT();
+      float d2[32], d3[32];
+      tc::ld16(tmem + tl + kT2 + 32 * half, *reinterpret_cast<float(*)[16]>(d2));
+      tc::ld16(tmem + tl + kT2 + 32 * half + 16, *reinterpret_cast<float(*)[16]>(d2 + 16));
+      tc::ld16(tmem + tl + kT3 + 32 * half, *reinterpret_cast<float(*)[16]>(d3));
+      tc::ld16(tmem + tl + kT3 + 32 * half + 16, *reinterpret_cast<float(*)[16]>(d3 + 16));
+#pragma unroll
+      for (int u = 0; u < 32; ++u) {
+        const int r = 32 * half + u;
+        Os[r * kD + j] = expf(G_s[r]) * d2[u] + d3[u];
+      }
+    }
+    fence_proxy_async_smem();
+    if (sync_or_stop()) { aborted = true; break; }
+
+    // ---- 12. gated RMSNorm of the chunk's outputs, one warp per token
+    for (int r = warp; r < L; r += kThreads / 32) {
+      const int row = t_begin + t0 + r;
+      const int jj = lane * 4;
+      const float4 o = *reinterpret_cast<const float4*>(Os + r * kD + jj);
+      const float ss = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
+      const float inv = rsqrtf(ss / float(kD) + p.norm_eps);
+      const float4 w4 = *reinterpret_cast<const float4*>(p.norm_w + jj);
+      const float4 z4 = Act<__nv_bfloat16>::load4(
+          reinterpret_cast<const __nv_bfloat16*>(p.z) + size_t(row) * p.z_stride + h * kD + jj);
+      float4 yv;
+      yv.x = o.x * inv * w4.x * silu_f(z4.x);
+      yv.y = o.y * inv * w4.y * silu_f(z4.y);
+      yv.z = o.z * inv * w4.z * silu_f(z4.z);
+      yv.w = o.w * inv * w4.w * silu_f(z4.w);
+      Act<__nv_bfloat16>::store4(
+          reinterpret_cast<__nv_bfloat16*>(p.y) + size_t(row) * p.Hv * kD + h * kD + jj, yv);
+      if (p.core_out)
+        *reinterpret_cast<float4*>(p.core_out + (size_t(row) * p.Hv + h) * kD + jj) = o;
+    }
+    __syncthreads();  // Os (the q/k tile region) is free for the next chunk's copies
+  }
+
+  if (aborted) {
+    if (tid == 0) report(p.status, GDN_ERR_TIMEOUT);
+  } else {
+#pragma unroll
+    for (int ii = 0; ii < 64; ++ii) Hg[(i0 + ii) * kD + j] = Hr[ii];
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::dealloc(tmem, 512);
+}
+
+}  // namespace
+
+size_t prefill_tc_smem_bytes() { return TcSmem::kAlloc; }
+
+cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
+  auto kern = gdn_prefill_tc_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(TcSmem::kAlloc));
+  if (e != cudaSuccess) return e;
+  if (p.n > 0) kern<<<p.n * p.Hv, kThreads, TcSmem::kAlloc, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

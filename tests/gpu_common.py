@@ -16,6 +16,11 @@ from gated_deltanet_layer_conv1d_gb300 import workloads as wl
 Y_BF16_TOL = 2e-3
 F32_TOL = 1e-4
 STATE_TOL = 1e-4
+# The tensor-core chunked prefill multiplies bf16 operands (q, k, v, T, W, Delta, P and a
+# bf16 copy of the state); each carries a relative rounding of 2^-9, so its f32 state and
+# core output are held to the bf16 class, 2e-3, instead of 1e-4.
+TC_STATE_TOL = 2e-3
+TC_CORE_TOL = 2e-3
 
 
 def require_gpu():
@@ -46,10 +51,10 @@ def assert_y_close(y_gpu: torch.Tensor, y_orc: np.ndarray, what="y"):
     return e
 
 
-def assert_state_close(H_gpu, H_orc, what="state"):
+def assert_state_close(H_gpu, H_orc, what="state", tol=STATE_TOL):
     H = np.asarray(H_gpu, np.float64)
     e = rel_l2(H, H_orc)
-    assert e <= STATE_TOL, f"{what}: rel Frobenius {e:.3e} > {STATE_TOL:.0e}"
+    assert e <= tol, f"{what}: rel Frobenius {e:.3e} > {tol:.0e}"
     return e
 
 
