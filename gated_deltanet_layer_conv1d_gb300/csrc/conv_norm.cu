@@ -11,6 +11,8 @@
 //   old state ordered before the write of the new one.
 // gdn_gated_rmsnorm_kernel: one warp per (token, value head) (layer_struct.rs,
 //   gated_rms_norm_f32_k / gated_rms_norm_prefill_k).
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "prefill_layout.cuh"
@@ -109,8 +111,12 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const __grid_con
           const int c2 = c - 2 * p.Hk * D;
           off = lay.v(cs, c2 / D) + tc::sw128_offset(PrefillLayout::kC, r, c2 % D);
         }
-        Act<__nv_bfloat16>::store4(
-            reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<unsigned char*>(p.workspace) + off), y);
+        // fp16 operand of the tensor-core chunk kernel
+        const __half2 lo = __floats2half2_rn(y.x, y.y), hi = __floats2half2_rn(y.z, y.w);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&lo);
+        u.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(p.workspace) + off) = u;
       } else {
         const size_t o = size_t(t) * p.conv_dim + qd * 4;
         if (p.out_bf16) Act<__nv_bfloat16>::store4(reinterpret_cast<__nv_bfloat16*>(p.out) + o, y);

@@ -3,7 +3,7 @@
 //
 // The workspace holds, per 64-token "chunk slot", the operand tiles of that chunk exactly
 // as the chunk kernel wants them in shared memory, so each arrives with one bulk copy:
-//   for every key head:   k_hat tile, q_hat tile  ([64 tokens][128] bf16, 128B-swizzled,
+//   for every key head:   k_hat tile, q_hat tile  ([64 tokens][128] fp16, 128B-swizzled,
 //                         K-major, i.e. two [64][64] column blocks)
 //   for every value head: v tile (same layout)
 //   for every value head: log(alpha)[64], beta[64] (f32)
@@ -20,7 +20,7 @@ namespace gdn {
 
 struct PrefillLayout {
   static constexpr int kC = 64;                       // chunk length
-  static constexpr size_t kTile = size_t(64) * 128 * 2;  // one bf16 [64][128] tile
+  static constexpr size_t kTile = size_t(64) * 128 * 2;  // one fp16 [64][128] tile
   int Hk, Hv;
   __host__ __device__ size_t slot_bytes() const {
     return size_t(Hk) * 2 * kTile + size_t(Hv) * kTile + size_t(Hv) * 2 * kC * 4;

@@ -17,10 +17,15 @@
 //   MMA4  (K~^T Delta)^T = (Delta^T diag(e^{g_L - g})) K        (B = K MN-major, N 128, K 64)
 // All per-token scalings are folded into T's columns, Delta's columns or the epilogue, so
 // the q, k, v tiles come straight from the pre-pass workspace (one bulk copy each).
+// Operands are fp16 (kind::f16, f32 accumulation): every operand here is bounded
+// (normalised q and k, O(1) v, T, P, Delta and state), and fp16's 11-bit significand
+// keeps the rounding of the inputs and of T, P and Delta eight times below bf16's.
 // H0 lives in registers (f32) of the 8 warps: thread (w, l) owns row j = 32 (w % 4) + l of
-// H^T and columns i in [64 (w / 4), +64); its bf16 copy is the A operand of MMA1/MMA2.
+// H^T and columns i in [64 (w / 4), +64); its fp16 copy is the A operand of MMA1/MMA2.
 // T = (I + A)^{-1} is computed on CUDA cores by blocked forward substitution (16 x 16
 // diagonal blocks, then the off-diagonal blocks level by level).
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "prefill_layout.cuh"
@@ -35,15 +40,15 @@ constexpr int kThreads = 256;
 
 // Shared memory (offsets from a 1024-aligned base).
 struct TcSmem {
-  static constexpr uint32_t kAQK = 0;            // [128][128] bf16: rows 0-63 k_hat, 64-127 q_hat
-  static constexpr uint32_t kV = 32768;          // [64][128] bf16 v (MN-major A of MMA_U)
-  static constexpr uint32_t kHT = 49152;         // [128][128] bf16 H^T
-  static constexpr uint32_t kW = 81920;          // [64][128] bf16 W
-  static constexpr uint32_t kTw = 98304;         // [64][64] bf16 T diag(beta e^g)
-  static constexpr uint32_t kTu = 106496;        // [64][64] bf16 T diag(beta)
-  static constexpr uint32_t kP = 114688;         // [64][64] bf16 P
-  static constexpr uint32_t kDT = 122880;        // [128][64] bf16 Delta^T
-  static constexpr uint32_t kDTs = 139264;       // [128][64] bf16 Delta^T diag(e^{g_L - g})
+  static constexpr uint32_t kAQK = 0;            // [128][128] f16: rows 0-63 k_hat, 64-127 q_hat
+  static constexpr uint32_t kV = 32768;          // [64][128] f16 v (MN-major A of MMA_U)
+  static constexpr uint32_t kHT = 49152;         // [128][128] f16 H^T
+  static constexpr uint32_t kW = 81920;          // [64][128] f16 W
+  static constexpr uint32_t kTw = 98304;         // [64][64] f16 T diag(beta e^g)
+  static constexpr uint32_t kTu = 106496;        // [64][64] f16 T diag(beta)
+  static constexpr uint32_t kP = 114688;         // [64][64] f16 P
+  static constexpr uint32_t kDT = 122880;        // [128][64] f16 Delta^T
+  static constexpr uint32_t kDTs = 139264;       // [128][64] f16 Delta^T diag(e^{g_L - g})
   static constexpr uint32_t kAm = 155648;        // [64][64] f32 A
   static constexpr uint32_t kTf = 172032;        // [64][64] f32 T
   static constexpr uint32_t kY = 188416;         // [3][16][16] f32 scratch of the inverse
@@ -55,10 +60,10 @@ struct TcSmem {
   static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024
 };
 
-__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+__device__ __forceinline__ uint4 pack8_h(const float* v) {
   uint4 u;
-  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
-  __nv_bfloat162 c = __floats2bfloat162_rn(v[4], v[5]), d = __floats2bfloat162_rn(v[6], v[7]);
+  __half2 a = __floats2half2_rn(v[0], v[1]), b = __floats2half2_rn(v[2], v[3]);
+  __half2 c = __floats2half2_rn(v[4], v[5]), d = __floats2half2_rn(v[6], v[7]);
   u.x = *reinterpret_cast<uint32_t*>(&a);
   u.y = *reinterpret_cast<uint32_t*>(&b);
   u.z = *reinterpret_cast<uint32_t*>(&c);
@@ -136,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int c8 = 0; c8 < 8; ++c8)
       *reinterpret_cast<uint4*>(sm + S::kHT + tc::sw128_offset(128, j, i0 + 8 * c8)) =
-          pack8_bf16(Hr + 8 * c8);
+          pack8_h(Hr + 8 * c8);
   };
   write_HT();
   fence_proxy_async_smem();
@@ -215,13 +220,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
 #pragma unroll
       for (int k0 = 0; k0 < kD; k0 += 16)
-        tc::mma_bf16(tmem + kT0, tc::desc_at(sb + S::kAQK, 128, k0),
-                     tc::desc_at(sb + S::kAQK, 128, k0), tc::idesc_bf16(128, 64), k0 > 0);
+        tc::mma_f16(tmem + kT0, tc::desc_at(sb + S::kAQK, 128, k0),
+                     tc::desc_at(sb + S::kAQK, 128, k0), tc::idesc_f16(128, 64), k0 > 0);
       tc::commit(bar_mma);
     }
     mma_wait();
 
-    // ---- 4. A (f32) from the K K^T rows, P (bf16) from the Q K^T rows
+    // ---- 4. A (f32) from the K K^T rows, P (fp16) from the Q K^T rows
     {
       float v[32];
       tc::ld16(tmem + tl + kT0 + 32 * half, *reinterpret_cast<float(*)[16]>(v));
@@ -246,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8)
           *reinterpret_cast<uint4*>(sm + S::kP + tc::sw128_offset(64, r, 32 * half + 8 * c8)) =
-              pack8_bf16(v + 8 * c8);
+              pack8_h(v + 8 * c8);
       }
     }
     if (sync_or_stop()) { aborted = true; break; }
@@ -298,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncthreads();
     }
-    // T diag(beta e^g) and T diag(beta), bf16, [r][s]
+    // T diag(beta e^g) and T diag(beta), fp16, [r][s]
     for (int cid = tid; cid < kC * 8; cid += kThreads) {
       const int r = cid / 8, s0 = (cid % 8) * 8;
       float tw[8], tu[8];
@@ -308,8 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tu[u] = tv * B_s[s0 + u];
         tw[u] = tu[u] * expf(G_s[s0 + u]);
       }
-      *reinterpret_cast<uint4*>(sm + S::kTw + tc::sw128_offset(64, r, s0)) = pack8_bf16(tw);
-      *reinterpret_cast<uint4*>(sm + S::kTu + tc::sw128_offset(64, r, s0)) = pack8_bf16(tu);
+      *reinterpret_cast<uint4*>(sm + S::kTw + tc::sw128_offset(64, r, s0)) = pack8_h(tw);
+      *reinterpret_cast<uint4*>(sm + S::kTu + tc::sw128_offset(64, r, s0)) = pack8_h(tu);
     }
     fence_proxy_async_smem();
     if (sync_or_stop()) { aborted = true; break; }
@@ -318,11 +323,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
 #pragma unroll
       for (int s0 = 0; s0 < kC; s0 += 16) {
-        tc::mma_bf16(tmem + kTW, tc::desc_mn_sw128(sb + S::kAQK + s0 * 128, 16384),
-                     tc::desc_at(sb + S::kTw, 64, s0), tc::idesc_bf16(128, 64, true, false),
+        tc::mma_f16(tmem + kTW, tc::desc_mn_sw128(sb + S::kAQK + s0 * 128, 16384),
+                     tc::desc_at(sb + S::kTw, 64, s0), tc::idesc_f16(128, 64, true, false),
                      s0 > 0);
-        tc::mma_bf16(tmem + kTU, tc::desc_mn_sw128(sb + S::kV + s0 * 128, 8192),
-                     tc::desc_at(sb + S::kTu, 64, s0), tc::idesc_bf16(128, 64, true, false),
+        tc::mma_f16(tmem + kTU, tc::desc_mn_sw128(sb + S::kV + s0 * 128, 8192),
+                     tc::desc_at(sb + S::kTu, 64, s0), tc::idesc_f16(128, 64, true, false),
                      s0 > 0);
       }
       tc::commit(bar_mma);
@@ -337,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i = 32 * q4 + lane;
 #pragma unroll
       for (int u = 0; u < 32; ++u)
-        *reinterpret_cast<__nv_bfloat16*>(sm + S::kW + tc::sw128_offset(64, 32 * half + u, i)) =
-            __float2bfloat16_rn(v[u]);
+        *reinterpret_cast<__half*>(sm + S::kW + tc::sw128_offset(64, 32 * half + u, i)) =
+            __float2half_rn(v[u]);
     }
     fence_proxy_async_smem();
     if (sync_or_stop()) { aborted = true; break; }
@@ -347,10 +352,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
 #pragma unroll
       for (int k0 = 0; k0 < kD; k0 += 16) {
-        tc::mma_bf16(tmem + kTD, tc::desc_at(sb + S::kHT, 128, k0),
-                     tc::desc_at(sb + S::kW, 64, k0), tc::idesc_bf16(128, 64), k0 > 0);
-        tc::mma_bf16(tmem + kT2, tc::desc_at(sb + S::kHT, 128, k0),
-                     tc::desc_at(sb + S::kAQK + 8192, 128, k0), tc::idesc_bf16(128, 64),
+        tc::mma_f16(tmem + kTD, tc::desc_at(sb + S::kHT, 128, k0),
+                     tc::desc_at(sb + S::kW, 64, k0), tc::idesc_f16(128, 64), k0 > 0);
+        tc::mma_f16(tmem + kT2, tc::desc_at(sb + S::kHT, 128, k0),
+                     tc::desc_at(sb + S::kAQK + 8192, 128, k0), tc::idesc_f16(128, 64),
                      k0 > 0);
       }
       tc::commit(bar_mma);
@@ -373,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
         const uint32_t off = tc::sw128_offset(128, j, 32 * half + 8 * c8);
-        *reinterpret_cast<uint4*>(sm + S::kDT + off) = pack8_bf16(du + 8 * c8);
-        *reinterpret_cast<uint4*>(sm + S::kDTs + off) = pack8_bf16(ds + 8 * c8);
+        *reinterpret_cast<uint4*>(sm + S::kDT + off) = pack8_h(du + 8 * c8);
+        *reinterpret_cast<uint4*>(sm + S::kDTs + off) = pack8_h(ds + 8 * c8);
       }
     }
     fence_proxy_async_smem();
@@ -384,17 +389,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
 #pragma unroll
       for (int s0 = 0; s0 < kC; s0 += 16) {
-        tc::mma_bf16(tmem + kT3, tc::desc_at(sb + S::kDT, 128, s0),
-                     tc::desc_at(sb + S::kP, 64, s0), tc::idesc_bf16(128, 64), s0 > 0);
-        tc::mma_bf16(tmem + kT4, tc::desc_at(sb + S::kDTs, 128, s0),
+        tc::mma_f16(tmem + kT3, tc::desc_at(sb + S::kDT, 128, s0),
+                     tc::desc_at(sb + S::kP, 64, s0), tc::idesc_f16(128, 64), s0 > 0);
+        tc::mma_f16(tmem + kT4, tc::desc_at(sb + S::kDTs, 128, s0),
                      tc::desc_mn_sw128(sb + S::kAQK + s0 * 128, 16384),
-                     tc::idesc_bf16(128, 128, false, true), s0 > 0);
+                     tc::idesc_f16(128, 128, false, true), s0 > 0);
       }
       tc::commit(bar_mma);
     }
     mma_wait();
 
-    // ---- 11. H update (registers + bf16 copy) and the chunk outputs
+    // ---- 11. H update (registers + fp16 copy) and the chunk outputs
     {
       const float eL = expf(gL);
 #pragma unroll

@@ -54,21 +54,26 @@ __device__ __forceinline__ uint64_t desc_at(uint32_t tile_addr, int R, int k0) {
   return desc_sw128(tile_addr + uint32_t((k0 >> 6) * R * 128 + (k0 & 63) * 2));
 }
 
-// Instruction descriptor of kind::f16: bf16 A and B, f32 accumulator; A and B K-major
-// unless a_mn / b_mn select MN-major.
+// Instruction descriptor of kind::f16 with an f32 accumulator: A and B both bf16 (or both
+// fp16 when `fp16`), K-major unless a_mn / b_mn select MN-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn = false,
-                                                  bool b_mn = false) {
+                                                  bool b_mn = false, bool fp16 = false) {
   return (1u << 4)                       // D format: f32
-         | (1u << 7)                     // A format: bf16
-         | (1u << 10)                    // B format: bf16
+         | (uint32_t(!fp16) << 7)        // A format: 1 = bf16, 0 = fp16
+         | (uint32_t(!fp16) << 10)       // B format: 1 = bf16, 0 = fp16
          | (uint32_t(a_mn) << 15)        // A major-ness
          | (uint32_t(b_mn) << 16)        // B major-ness
          | (uint32_t(N >> 3) << 17)      // N / 8
          | (uint32_t(M >> 4) << 24);     // M / 16
 }
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn = false,
+                                                 bool b_mn = false) {
+  return idesc_bf16(M, N, a_mn, b_mn, true);
+}
 
-// D[tmem] (+)= A[smem] * B[smem]^T for one K = 16 step (issued by one thread).
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+// D[tmem] (+)= A[smem] * B[smem]^T for one K = 16 step of kind::f16 (bf16 or fp16
+// operands as the instruction descriptor says), issued by one thread.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, bool accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"

@@ -16,11 +16,12 @@ from gated_deltanet_layer_conv1d_gb300 import workloads as wl
 Y_BF16_TOL = 2e-3
 F32_TOL = 1e-4
 STATE_TOL = 1e-4
-# The tensor-core chunked prefill multiplies bf16 operands (q, k, v, T, W, Delta, P and a
-# bf16 copy of the state); each carries a relative rounding of 2^-9, so its f32 state and
-# core output are held to the bf16 class, 2e-3, instead of 1e-4.
-TC_STATE_TOL = 2e-3
-TC_CORE_TOL = 2e-3
+# The tensor-core chunked prefill multiplies fp16 operands (q, k, v, T, W, Delta, P and an
+# fp16 copy of the state), each rounded to 2^-11 relative; the oracle's own operand-rounding
+# emulation puts the resulting f32 state and core-output error near 4e-4, so they are held
+# to 1e-3 instead of the 1e-4 of the f32 paths.
+TC_STATE_TOL = 1e-3
+TC_CORE_TOL = 1e-3
 
 
 def require_gpu():
