@@ -146,6 +146,7 @@ const char* gdn_status_string(gdn_status s) {
     case GDN_ERR_TOO_MANY_SEQS: return "too many sequences";
     case GDN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case GDN_ERR_CUDA: return "CUDA runtime error";
+    case GDN_ERR_SCRATCH_TOO_SMALL: return "call needs more than the library's static scratch";
     case GDN_ERR_BAD_TABLE_ENTRY: return "null or misaligned state pointer";
     case GDN_ERR_BAD_SLOT: return "slot out of range";
     case GDN_ERR_BAD_SEQLENS: return "bad cu_seqlens";

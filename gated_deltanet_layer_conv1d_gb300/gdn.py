@@ -29,7 +29,8 @@ PREFILL_CHUNK = 64
 # Symbols include/gdn.h declares.
 EXPORTS = ("gdn_decode_batched", "gdn_verify_multi", "gdn_conv_step", "gdn_prefill_chunked",
            "gdn_prefill_workspace_bytes", "gdn_gated_rmsnorm", "gdn_wy_tables_fill",
-           "gdn_status_string", "gdn_version")
+           "gdn_status_string", "gdn_version", "gdn_prefill_chunked_noalloc")
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class GdnError(RuntimeError):
@@ -75,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_conv_step.argtypes = [D, W, IN, I32, P, I32, P, I32, P, P, P, P]
         L.gdn_prefill_chunked.argtypes = [D, W, IN, I32, P, I32, I32, I32, P, P, I32, P, P, P,
                                           P, SZ, P, P]
+        L.gdn_prefill_chunked_noalloc.argtypes = [D, W, IN, I32, P, I32, I32, I32, P, P, I32, P,
+                                                  P, P, P, P]
         L.gdn_prefill_workspace_bytes.argtypes = [D, I32, I32, I32, I32]
         L.gdn_prefill_workspace_bytes.restype = SZ
         L.gdn_gated_rmsnorm.argtypes = [P, P, I64, P, ctypes.c_float, I32, I32, I32, I32, P, P]
@@ -195,6 +198,20 @@ def gdn_prefill_chunked(dims: gdn_dims, weights: Weights, inputs: Inputs, n: int
         ctypes.byref(dims), ctypes.byref(w), ctypes.byref(i), n, _ptr(cu_seqlens), total_tokens,
         max_seqlen, chunk, _ptr(h_state_ptrs), _ptr(conv_pool), n_slots, _ptr(slots), _ptr(y),
         _ptr(core_out), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)))
+
+
+def gdn_prefill_chunked_noalloc(dims: gdn_dims, weights: Weights, inputs: Inputs, n: int,
+                                cu_seqlens, total_tokens: int, max_seqlen: int, h_state_ptrs,
+                                conv_pool, n_slots: int, slots, y, core_out=None, status=None,
+                                stream=None, chunk: int = PREFILL_CHUNK):
+    """gdn_prefill_chunked without a workspace argument, for callers that cannot allocate
+    device memory when they prefill: the library's own fixed scratch (NOALLOC_SCRATCH_BYTES
+    per GPU) stands in for it.  Calls that overlap on the GPU race on that scratch."""
+    w, i = weights.c(), inputs.c()
+    _check("gdn_prefill_chunked_noalloc", lib().gdn_prefill_chunked_noalloc(
+        ctypes.byref(dims), ctypes.byref(w), ctypes.byref(i), n, _ptr(cu_seqlens), total_tokens,
+        max_seqlen, chunk, _ptr(h_state_ptrs), _ptr(conv_pool), n_slots, _ptr(slots), _ptr(y),
+        _ptr(core_out), _ptr(status), _stream(stream)))
 
 
 def gdn_gated_rmsnorm(o, z, w, eps: float, y, stream=None):

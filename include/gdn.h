@@ -74,6 +74,7 @@ typedef int32_t gdn_status;
 #define GDN_ERR_TOO_MANY_SEQS 6      /* more than GDN_MAX_SEQS sequences in one call */
 #define GDN_ERR_WORKSPACE_TOO_SMALL 7
 #define GDN_ERR_CUDA 8               /* a CUDA runtime call (launch, attribute) failed */
+#define GDN_ERR_SCRATCH_TOO_SMALL 9  /* the call needs more than the library's static scratch */
 /* Device-side codes (written to *status_dev by a kernel). */
 #define GDN_ERR_BAD_TABLE_ENTRY 16   /* verify: a needed table entry is NULL or not 16-B aligned */
 #define GDN_ERR_BAD_SLOT 17          /* a slot index outside [0, n_slots) */
@@ -216,6 +217,35 @@ GDN_API gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* 
 /* Bytes of workspace gdn_prefill_chunked needs for these sizes (0 on invalid input). */
 GDN_API size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t n, int32_t total_tokens,
                                    int32_t max_seqlen, int32_t chunk);
+
+/* Allocation-free variant of gdn_prefill_chunked (the reference pages have no counterpart).
+ * Some callers cannot allocate device memory at the time they prefill: a serving engine that
+ * reserved nearly all of HBM at start-up for its own state and KV pools (a cudaMalloc would
+ * fail, or fragment memory the engine manages), or a plug-in running under a host runtime
+ * that owns every allocation and hands out no scratch.  This entry point takes the same
+ * arguments as gdn_prefill_chunked minus the workspace and uses instead a scratch array the
+ * library keeps in device memory: GDN_NOALLOC_SCRATCH_BYTES (64 MiB) per GPU, held by every
+ * GPU that loads the library until the process exits.  It calls no allocator.
+ *   - Sizes: a call whose gdn_prefill_workspace_bytes(...) exceeds the scratch returns
+ *     GDN_ERR_SCRATCH_TOO_SMALL and launches nothing (at H_k = 16, H_v = 32, d = 128 the
+ *     scratch holds 63 chunk slots, e.g. one sequence of about 3,900 tokens).
+ *   - Set-up: the first call on a device, with that device current, looks up the scratch's
+ *     device address (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     Its failure returns GDN_ERR_CUDA.
+ *   - Sharing: every call on a device uses the same array and leaves its contents behind;
+ *     nothing in it needs to start at zero.  Calls that overlap on the GPU (other streams,
+ *     other host threads) race on it: serialise them.
+ *   - Results are the same as gdn_prefill_chunked's for the same arguments. */
+GDN_API gdn_status gdn_prefill_chunked_noalloc(const gdn_dims* dims, const gdn_weights* weights,
+                                               const gdn_inputs* inputs, int32_t n,
+                                               const int32_t* cu_seqlens_dev,
+                                               int32_t total_tokens, int32_t max_seqlen,
+                                               int32_t chunk, const uint64_t* h_state_ptrs_dev,
+                                               void* conv_pool, int32_t n_slots,
+                                               const int32_t* slots_dev, void* y,
+                                               float* core_out, int32_t* status_dev,
+                                               gdn_stream_t stream);
+#define GDN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
 /* Z-gated RMSNorm of T rows (layer_struct.rs, gated_rms_norm_f32_k: f32 input):
  *   y[t][h*d_v + j] = o[t][h][j] / sqrt(mean_j o[t][h][:]^2 + eps) * w[j] * SiLU(z[t][h*d_v + j])
