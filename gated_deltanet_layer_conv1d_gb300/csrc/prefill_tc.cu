@@ -49,16 +49,23 @@ struct TcSmem {
   static constexpr uint32_t kP = 114688;         // [64][64] f16 P
   static constexpr uint32_t kDT = 122880;        // [128][64] f16 Delta^T
   static constexpr uint32_t kDTs = 139264;       // [128][64] f16 Delta^T diag(e^{g_L - g})
-  static constexpr uint32_t kAm = 155648;        // [64][64] f32 A
-  static constexpr uint32_t kTf = 172032;        // [64][64] f32 T
-  static constexpr uint32_t kY = 188416;         // [3][16][16] f32 scratch of the inverse
-  static constexpr uint32_t kGate = 191488;      // [2][64] f32 log(alpha), beta (bulk copied)
-  static constexpr uint32_t kG = 192000;         // [64] f32 cumulative log decay g
-  static constexpr uint32_t kB = 192256;         // [64] f32 beta (0 past the chunk end)
-  static constexpr uint32_t kMisc = 192512;      // bars, tmem slot, scan carry
-  static constexpr uint32_t kBytes = 192640;
+  static constexpr int kAS = 65;                 // row stride of A: odd, so column writes
+                                                 // from 32 lanes hit 32 banks
+  static constexpr uint32_t kAm = 155648;        // [64][65] f32 A
+  static constexpr uint32_t kTf = 172288;        // [64][64] f32 T
+  static constexpr uint32_t kOs = kAm;           // [64][128] f32 outputs (A and T are dead then)
+  static constexpr uint32_t kY = 188672;         // [3][16][16] f32 scratch of the inverse
+  static constexpr uint32_t kZ = 191744;         // [2][64][128] bf16 z rows, double-buffered
+  static constexpr uint32_t kNW = 224512;        // [128] f32 norm weight
+  static constexpr uint32_t kGate = 225024;      // [2][64] f32 log(alpha), beta (bulk copied)
+  static constexpr uint32_t kG = 225536;         // [64] f32 cumulative log decay g
+  static constexpr uint32_t kB = 225792;         // [64] f32 beta (0 past the chunk end)
+  static constexpr uint32_t kMisc = 226048;      // bars, tmem slot, scan carry
+  static constexpr uint32_t kBytes = 226176;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024
 };
+static_assert(TcSmem::kOs + 64 * 128 * 4 <= TcSmem::kY, "output staging fits in A and T");
+static_assert(TcSmem::kAm + 64 * TcSmem::kAS * 4 <= TcSmem::kTf, "A fits");
 
 __device__ __forceinline__ uint4 pack8_h(const float* v) {
   uint4 u;
@@ -93,7 +100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* gate = reinterpret_cast<float*>(sm + S::kGate);
   float* G_s = reinterpret_cast<float*>(sm + S::kG);
   float* B_s = reinterpret_cast<float*>(sm + S::kB);
-  float* Os = reinterpret_cast<float*>(sm + S::kAQK);  // output staging, after MMA4
+  float* NW = reinterpret_cast<float*>(sm + S::kNW);
+  float* Os = reinterpret_cast<float*>(sm + S::kOs);  // output staging, after the inverse
   uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + S::kMisc);
   uint64_t* bar_mma = bar_load + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_mma + 1);
@@ -144,11 +152,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           pack8_h(Hr + 8 * c8);
   };
   write_HT();
+  if (tid < kD) NW[tid] = p.norm_w[tid];
   fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
+  // The q_hat / k_hat / v tiles, gates and z rows of chunk c into shared memory (thread 0).
+  auto issue_loads = [&](int c) {
+    const int t0 = c * kC;
+    const int L = (len - t0) < kC ? (len - t0) : kC;
+    const size_t cs = slot0 + size_t(c);
+    const unsigned char* kimg = ws + lay.qk(cs, kh, 0);
+    const unsigned char* qimg = ws + lay.qk(cs, kh, 1);
+    unsigned char* zdst = sm + S::kZ + (c & 1) * 16384;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar_load, 3u * 16384u + 512u + uint32_t(L) * 256u);
+    bulk_g2s(sm + S::kAQK, kimg, 8192, bar_load);
+    bulk_g2s(sm + S::kAQK + 16384, kimg + 8192, 8192, bar_load);
+    bulk_g2s(sm + S::kAQK + 8192, qimg, 8192, bar_load);
+    bulk_g2s(sm + S::kAQK + 24576, qimg + 8192, 8192, bar_load);
+    bulk_g2s(sm + S::kV, ws + lay.v(cs, h), 16384, bar_load);
+    bulk_g2s(gate, ws + lay.gate(cs, h), 512, bar_load);
+    const __nv_bfloat16* zsrc = reinterpret_cast<const __nv_bfloat16*>(p.z) +
+                                size_t(t_begin + t0) * p.z_stride + size_t(h) * kD;
+    for (int r = 0; r < L; ++r)
+      bulk_g2s(zdst + r * 256, zsrc + size_t(r) * p.z_stride, 256, bar_load);
+  };
+  if (tid == 0) issue_loads(0);
   const uint32_t tl = uint32_t(32 * q4) << 16;  // this warp's TMEM lane quarter
   uint32_t load_phase = 0, mma_phase = 0;
   bool bad = false;
@@ -170,21 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int c = 0; c < nc; ++c) {
     const int t0 = c * kC;
     const int L = (len - t0) < kC ? (len - t0) : kC;
-    const size_t cs = slot0 + size_t(c);
 
-    // ---- 1. this chunk's k_hat, q_hat, v tiles and gates
-    if (tid == 0) {
-      const unsigned char* kimg = ws + lay.qk(cs, kh, 0);
-      const unsigned char* qimg = ws + lay.qk(cs, kh, 1);
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar_load, 3u * 16384u + 512u);
-      bulk_g2s(sm + S::kAQK, kimg, 8192, bar_load);
-      bulk_g2s(sm + S::kAQK + 16384, kimg + 8192, 8192, bar_load);
-      bulk_g2s(sm + S::kAQK + 8192, qimg, 8192, bar_load);
-      bulk_g2s(sm + S::kAQK + 24576, qimg + 8192, 8192, bar_load);
-      bulk_g2s(sm + S::kV, ws + lay.v(cs, h), 16384, bar_load);
-      bulk_g2s(gate, ws + lay.gate(cs, h), 512, bar_load);
-    }
+    // ---- 1. this chunk's tiles, gates and z rows (issued during the previous chunk)
     bad |= !mbar_wait_bounded(bar_load, load_phase);
     load_phase ^= 1u;
 
@@ -238,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           const int s = 32 * half + u;
-          Am[r * kC + s] = (s < r && r < L) ? br * v[u] * expf(gr - G_s[s]) : 0.f;
+          Am[r * S::kAS + s] = (s < r && r < L) ? br * v[u] * expf(gr - G_s[s]) : 0.f;
         }
       } else {
         const int r = row - kC;
@@ -265,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rr = 0; rr < 16; ++rr) {
           float acc = (rr == lane) ? 1.f : 0.f;
 #pragma unroll
-          for (int ss = 0; ss < rr; ++ss) acc -= Am[(b0 + rr) * kC + b0 + ss] * X[ss];
+          for (int ss = 0; ss < rr; ++ss) acc -= Am[(b0 + rr) * S::kAS + b0 + ss] * X[ss];
           X[rr] = acc;
         }
 #pragma unroll
@@ -281,25 +299,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncthreads();
+    // Block (I, J = I - d) of T: T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ.  A thread computes a
+    // 1 x 4 strip (row a, columns bb..bb+3) of one block: one broadcast A load and one
+    // 16-byte T load per four FMAs.
     for (int d = 1; d < 4; ++d) {
       const int nblk = 4 - d;  // blocks (I, J = I - d), I = d .. 3
-      for (int e = tid; e < nblk * 256; e += kThreads) {
-        const int I = d + e / 256, J = I - d, a = (e % 256) / 16, bb = e % 16;
-        float acc = 0.f;
+      const int e = tid;       // strip e: block e / 64, row (e % 64) / 4, columns 4 (e % 4)
+      if (e < nblk * 64) {
+        const int I = d + e / 64, J = I - d, a = (e % 64) / 4, bb = 4 * (e % 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int K = J; K < I; ++K)
 #pragma unroll
-          for (int n = 0; n < 16; ++n)
-            acc += Am[(16 * I + a) * kC + 16 * K + n] * Tf[(16 * K + n) * kC + 16 * J + bb];
-        Ys[e] = acc;
+          for (int n = 0; n < 16; ++n) {
+            const float av = Am[(16 * I + a) * S::kAS + 16 * K + n];
+            const float4 t4 = *reinterpret_cast<const float4*>(Tf + (16 * K + n) * kC + 16 * J + bb);
+            acc.x += av * t4.x; acc.y += av * t4.y; acc.z += av * t4.z; acc.w += av * t4.w;
+          }
+        *reinterpret_cast<float4*>(Ys + (e / 64) * 256 + a * 16 + bb) = acc;
       }
       __syncthreads();
-      for (int e = tid; e < nblk * 256; e += kThreads) {
-        const int I = d + e / 256, J = I - d, a = (e % 256) / 16, bb = e % 16;
-        const float* y = Ys + (e / 256) * 256;
-        float acc = 0.f;
+      if (e < nblk * 64) {
+        const int I = d + e / 64, J = I - d, a = (e % 64) / 4, bb = 4 * (e % 4);
+        const float* y = Ys + (e / 64) * 256;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int m = 0; m < 16; ++m) acc += Tf[(16 * I + a) * kC + 16 * I + m] * y[m * 16 + bb];
-        Tf[(16 * I + a) * kC + 16 * J + bb] = -acc;
+        for (int m = 0; m < 16; ++m) {
+          const float tv = Tf[(16 * I + a) * kC + 16 * I + m];
+          const float4 y4 = *reinterpret_cast<const float4*>(y + m * 16 + bb);
+          acc.x += tv * y4.x; acc.y += tv * y4.y; acc.z += tv * y4.z; acc.w += tv * y4.w;
+        }
+        *reinterpret_cast<float4*>(Tf + (16 * I + a) * kC + 16 * J + bb) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
       }
       __syncthreads();
     }
@@ -398,6 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::commit(bar_mma);
     }
     mma_wait();
+    // Every MMA of this chunk has completed and the q/k, v and gate buffers are no longer
+    // read: start the next chunk's loads now, behind this chunk's epilogue.
+    if (tid == 0 && c + 1 < nc) issue_loads(c + 1);
 
     // ---- 11. H update (registers + fp16 copy) and the chunk outputs
     {
@@ -431,9 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4 o = *reinterpret_cast<const float4*>(Os + r * kD + jj);
       const float ss = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
       const float inv = rsqrtf(ss / float(kD) + p.norm_eps);
-      const float4 w4 = *reinterpret_cast<const float4*>(p.norm_w + jj);
+      const float4 w4 = *reinterpret_cast<const float4*>(NW + jj);
       const float4 z4 = Act<__nv_bfloat16>::load4(
-          reinterpret_cast<const __nv_bfloat16*>(p.z) + size_t(row) * p.z_stride + h * kD + jj);
+          reinterpret_cast<const __nv_bfloat16*>(sm + S::kZ + (c & 1) * 16384) + r * kD + jj);
       float4 yv;
       yv.x = o.x * inv * w4.x * silu_f(z4.x);
       yv.y = o.y * inv * w4.y * silu_f(z4.y);
@@ -444,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.core_out)
         *reinterpret_cast<float4*>(p.core_out + (size_t(row) * p.Hv + h) * kD + jj) = o;
     }
-    __syncthreads();  // Os (the q/k tile region) is free for the next chunk's copies
+    __syncthreads();  // Os and this chunk's z buffer are read
   }
 
   if (aborted) {
