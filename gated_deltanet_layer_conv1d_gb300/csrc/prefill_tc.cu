@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* Tf = reinterpret_cast<float*>(sm + S::kTf);
   float* Ys = reinterpret_cast<float*>(sm + S::kY);
   float* gate = reinterpret_cast<float*>(sm + S::kGate);
-  float* G_s = reinterpret_cast<float*>(sm + S::kG);
+  float* G_s = reinterpret_cast<float*>(sm + S::kG);  // cumulative log2 decay
   float* B_s = reinterpret_cast<float*>(sm + S::kB);
   float* NW = reinterpret_cast<float*>(sm + S::kNW);
   float* Os = reinterpret_cast<float*>(sm + S::kOs);  // output staging, after the inverse
@@ -158,28 +158,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
-  // The q_hat / k_hat / v tiles, gates and z rows of chunk c into shared memory (thread 0).
+  // The q_hat / k_hat / v tiles, gates and z rows of chunk c into shared memory, issued by
+  // warp 0: lane 0 posts the byte count and the tile copies, then every lane copies z rows.
   auto issue_loads = [&](int c) {
     const int t0 = c * kC;
     const int L = (len - t0) < kC ? (len - t0) : kC;
     const size_t cs = slot0 + size_t(c);
-    const unsigned char* kimg = ws + lay.qk(cs, kh, 0);
-    const unsigned char* qimg = ws + lay.qk(cs, kh, 1);
     unsigned char* zdst = sm + S::kZ + (c & 1) * 16384;
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar_load, 3u * 16384u + 512u + uint32_t(L) * 256u);
-    bulk_g2s(sm + S::kAQK, kimg, 8192, bar_load);
-    bulk_g2s(sm + S::kAQK + 16384, kimg + 8192, 8192, bar_load);
-    bulk_g2s(sm + S::kAQK + 8192, qimg, 8192, bar_load);
-    bulk_g2s(sm + S::kAQK + 24576, qimg + 8192, 8192, bar_load);
-    bulk_g2s(sm + S::kV, ws + lay.v(cs, h), 16384, bar_load);
-    bulk_g2s(gate, ws + lay.gate(cs, h), 512, bar_load);
+    if (lane == 0) {
+      const unsigned char* kimg = ws + lay.qk(cs, kh, 0);
+      const unsigned char* qimg = ws + lay.qk(cs, kh, 1);
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar_load, 3u * 16384u + 512u + uint32_t(L) * 256u);
+      bulk_g2s(sm + S::kAQK, kimg, 8192, bar_load);
+      bulk_g2s(sm + S::kAQK + 16384, kimg + 8192, 8192, bar_load);
+      bulk_g2s(sm + S::kAQK + 8192, qimg, 8192, bar_load);
+      bulk_g2s(sm + S::kAQK + 24576, qimg + 8192, 8192, bar_load);
+      bulk_g2s(sm + S::kV, ws + lay.v(cs, h), 16384, bar_load);
+      bulk_g2s(gate, ws + lay.gate(cs, h), 512, bar_load);
+    }
+    __syncwarp();
     const __nv_bfloat16* zsrc = reinterpret_cast<const __nv_bfloat16*>(p.z) +
                                 size_t(t_begin + t0) * p.z_stride + size_t(h) * kD;
-    for (int r = 0; r < L; ++r)
+    for (int r = lane; r < L; r += 32)
       bulk_g2s(zdst + r * 256, zsrc + size_t(r) * p.z_stride, 256, bar_load);
   };
-  if (tid == 0) issue_loads(0);
+  if (warp == 0) issue_loads(0);
   const uint32_t tl = uint32_t(32 * q4) << 16;  // this warp's TMEM lane quarter
   uint32_t load_phase = 0, mma_phase = 0;
   bool bad = false;
@@ -217,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (tid < kC) {
-      float v = tid < L ? gate[tid] : 0.f;
+      // g in log2 units (log(alpha) * log2(e)), so each decay factor below is one exp2f
+      float v = tid < L ? gate[tid] * 1.4426950408889634f : 0.f;
       const float be = tid < L ? gate[kC + tid] : 0.f;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -256,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           const int s = 32 * half + u;
-          Am[r * S::kAS + s] = (s < r && r < L) ? br * v[u] * expf(gr - G_s[s]) : 0.f;
+          Am[r * S::kAS + s] = (s < r && r < L) ? br * v[u] * exp2f(gr - G_s[s]) : 0.f;
         }
       } else {
         const int r = row - kC;
@@ -264,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           const int s = 32 * half + u;
-          v[u] = (s <= r && r < L) ? v[u] * expf(gr - G_s[s]) : 0.f;
+          v[u] = (s <= r && r < L) ? v[u] * exp2f(gr - G_s[s]) : 0.f;
         }
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8)
@@ -281,10 +286,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         float X[16];
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
-          float acc = (rr == lane) ? 1.f : 0.f;
+          float acc0 = (rr == lane) ? 1.f : 0.f, acc1 = 0.f;
 #pragma unroll
-          for (int ss = 0; ss < rr; ++ss) acc -= Am[(b0 + rr) * S::kAS + b0 + ss] * X[ss];
-          X[rr] = acc;
+          for (int ss = 0; ss + 1 < rr; ss += 2) {
+            acc0 -= Am[(b0 + rr) * S::kAS + b0 + ss] * X[ss];
+            acc1 -= Am[(b0 + rr) * S::kAS + b0 + ss + 1] * X[ss + 1];
+          }
+          if (rr & 1) acc0 -= Am[(b0 + rr) * S::kAS + b0 + rr - 1] * X[rr - 1];
+          X[rr] = acc0 + acc1;
         }
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) Tf[(b0 + rr) * kC + b0 + lane] = X[rr];
@@ -341,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < 8; ++u) {
         const float tv = Tf[r * kC + s0 + u];
         tu[u] = tv * B_s[s0 + u];
-        tw[u] = tu[u] * expf(G_s[s0 + u]);
+        tw[u] = tu[u] * exp2f(G_s[s0 + u]);
       }
       *reinterpret_cast<uint4*>(sm + S::kTw + tc::sw128_offset(64, r, s0)) = pack8_h(tw);
       *reinterpret_cast<uint4*>(sm + S::kTu + tc::sw128_offset(64, r, s0)) = pack8_h(tu);
@@ -403,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 32; ++u) {
         du[u] -= dd[u];
-        ds[u] = du[u] * expf(gL - G_s[32 * half + u]);
+        ds[u] = du[u] * exp2f(gL - G_s[32 * half + u]);
       }
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
@@ -430,11 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_wait();
     // Every MMA of this chunk has completed and the q/k, v and gate buffers are no longer
     // read: start the next chunk's loads now, behind this chunk's epilogue.
-    if (tid == 0 && c + 1 < nc) issue_loads(c + 1);
+    if (warp == 0 && c + 1 < nc) issue_loads(c + 1);
 
     // ---- 11. H update (registers + fp16 copy) and the chunk outputs
     {
-      const float eL = expf(gL);
+      const float eL = exp2f(gL);
 #pragma unroll
       for (int c16 = 0; c16 < 4; ++c16) {
         float v[16];
@@ -451,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 32; ++u) {
         const int r = 32 * half + u;
-        Os[r * kD + j] = expf(G_s[r]) * d2[u] + d3[u];
+        Os[r * kD + j] = exp2f(G_s[r]) * d2[u] + d3[u];
       }
     }
     fence_proxy_async_smem();
