@@ -305,6 +305,74 @@ def prefill_mode(device, steps, tc_peak):
                          "hbm_GBps": round(prefill_bytes(T) / (ms * 1e-3) / 1e9, 1)}}
 
 
+PREFILL_FLOPS_PER_TOKEN = prefill_flops(64) / 64
+
+
+def mixed_mode(device, steps, hbm_peak, tc_peak):
+    """Mixed serving step: 32 sequences prefilling U{512..4096} tokens on one stream next to
+    a 96-sequence ragged verify (k ~ U{2..16}) on another; tokens/s over both."""
+    import torch
+
+    from gated_deltanet_layer_conv1d_gb300 import device as dev
+    from gated_deltanet_layer_conv1d_gb300 import gdn
+    from gated_deltanet_layer_conv1d_gb300 import workloads as wl
+    pre, ver = wl.mixed_serving()
+    dims, weights = dev.dims_of(pre.shape), dev.weights_to(pre, device)
+    # prefill side
+    ph, pc, ps = dev.states_to(pre, device)
+    hsz = 32 * 128 * 128 * 4
+    php = torch.tensor([ph.data_ptr() + i * hsz for i in range(pre.n)], dtype=torch.int64,
+                       device=device)
+    cu = torch.from_numpy(pre.cu_seqlens).to(device)
+    T = int(pre.lens.sum())
+    Lmax = int(pre.lens.max())
+    pin = dev.tokens_to(pre.tokens, torch.bfloat16, device)
+    py = torch.empty((T, 4096), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(gdn.gdn_prefill_workspace_bytes(dims, pre.n, T, Lmax), dtype=torch.uint8,
+                     device=device)
+    # verify side
+    ks = [int(k) for k in ver.lens]
+    vh, vc, vs = dev.states_to(ver, device)
+    inter = torch.empty((ver.n, 15, 32, 128, 128), dtype=torch.float32, device=device)
+    tables = dev.wy_tables_to(ks, [vh.data_ptr() + i * hsz for i in range(ver.n)],
+                              [[inter[i, t].data_ptr() for t in range(15)] for i in range(ver.n)],
+                              device)
+    vin = dev.tokens_to(ver.tokens, torch.bfloat16, device)
+    vy = torch.empty((sum(ks), 4096), dtype=torch.bfloat16, device=device)
+    status = torch.zeros(2, dtype=torch.int32, device=device)
+    main = torch.cuda.current_stream(device)
+    s_pre, s_ver = torch.cuda.Stream(device), torch.cuda.Stream(device)
+
+    def fn(i):
+        fork = torch.cuda.Event()
+        fork.record(main)
+        s_pre.wait_event(fork)
+        s_ver.wait_event(fork)
+        gdn.gdn_prefill_chunked(dims, weights, pin, pre.n, cu, T, Lmax, php, pc, pre.n, ps, py,
+                                None, ws, status[0:1], s_pre)
+        gdn.gdn_verify_multi(dims, weights, vin, ver.n, ks, tables, vc, ver.n, vs, None, vy,
+                             None, status[1:2], s_ver)
+        for st in (s_pre, s_ver):
+            done = torch.cuda.Event()
+            done.record(st)
+            main.wait_event(done)
+
+    ms = time_loop(torch, main, fn, steps, 2)
+    assert int(status.abs().sum().item()) == 0
+    tokens = T + sum(ks)
+    fl = PREFILL_FLOPS_PER_TOKEN * T
+    byts = verify_bytes(ks) + prefill_bytes(T)
+    return {"workload": "mixed_32prefill_U512to4096_96verify_k2to16", "tokens_per_step": tokens,
+            "prefill_tokens": T, "verify_tokens": sum(ks), "ms_per_step": round(ms, 4),
+            "value": round(tokens / (ms * 1e-3), 1), "unit": "tokens/s", "streams": 2,
+            "roofline": {"tensor": {"achieved": round(fl / (ms * 1e-3) / 1e12, 2),
+                                    "peak": tc_peak, "unit": "TFLOP/s",
+                                    "frac": round(fl / (ms * 1e-3) / 1e12 / tc_peak, 4)},
+                         "hbm": {"achieved": round(byts / (ms * 1e-3) / 1e9, 1),
+                                 "peak": hbm_peak, "unit": "GB/s",
+                                 "frac": round(byts / (ms * 1e-3) / 1e9 / hbm_peak, 4)}}}
+
+
 def cpu_baseline_decode(n_seq=N_SEQ, tokens=4):
     """The fp64 oracle on this host's cores: n_seq sequences x `tokens` decode tokens of
     the headline workload (one oracle call per sequence, sequences on OpenMP threads)."""
@@ -464,6 +532,7 @@ def main():
     if not args.no_modes and rank == 0:
         modes["ragged_verify"] = verify_mode(device, max(10, min(200, args.steps // 10)), hbm_peak)
         modes["chunked_prefill"] = prefill_mode(device, 5, tc_peak)
+        modes["mixed_serving"] = mixed_mode(device, 3, hbm_peak, tc_peak)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline_decode()

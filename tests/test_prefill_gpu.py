@@ -203,3 +203,49 @@ def test_gated_rmsnorm(shape, bf16):
     torch.cuda.synchronize()
     ref = oracle.gated_rmsnorm(o, z, w, float(np.float32(1e-6)))
     assert_y_close(y, ref, "gated rmsnorm")
+
+
+def test_mixed_serving_step_two_streams():
+    """32 varlen prefills (U{512..4096}) on one stream next to a 96-sequence ragged verify on
+    another, as one serving step; sampled sequences are compared with the oracle."""
+    pre, ver = wl.mixed_serving()
+    d = torch.device("cuda")
+    dims, weights = dev.dims_of(pre.shape), dev.weights_to(pre, d)
+    ph, pc, ps = dev.states_to(pre, d)
+    hsz = 32 * 128 * 128 * 4
+    php = torch.tensor([ph.data_ptr() + i * hsz for i in range(pre.n)], dtype=torch.int64, device=d)
+    cu = torch.from_numpy(pre.cu_seqlens).to(d)
+    T, Lmax = int(pre.lens.sum()), int(pre.lens.max())
+    py = torch.empty((T, 4096), dtype=torch.bfloat16, device=d)
+    ws = torch.empty(gdn.gdn_prefill_workspace_bytes(dims, pre.n, T, Lmax), dtype=torch.uint8,
+                     device=d)
+    ks = [int(k) for k in ver.lens]
+    vh, vc, vs = dev.states_to(ver, d)
+    inter = torch.zeros((ver.n, 15, 32, 128, 128), dtype=torch.float32, device=d)
+    tables = dev.wy_tables_to(ks, [vh.data_ptr() + i * hsz for i in range(ver.n)],
+                              [[inter[i, t].data_ptr() for t in range(15)] for i in range(ver.n)], d)
+    vy = torch.empty((sum(ks), 4096), dtype=torch.bfloat16, device=d)
+    status = torch.zeros(2, dtype=torch.int32, device=d)
+    s_pre, s_ver = torch.cuda.Stream(d), torch.cuda.Stream(d)
+    torch.cuda.synchronize()
+    gdn.gdn_prefill_chunked(dims, weights, dev.tokens_to(pre.tokens, torch.bfloat16, d), pre.n, cu,
+                            T, Lmax, php, pc, pre.n, ps, py, None, ws, status[0:1], s_pre)
+    gdn.gdn_verify_multi(dims, weights, dev.tokens_to(ver.tokens, torch.bfloat16, d), ver.n, ks,
+                         tables, vc, ver.n, vs, None, vy, None, status[1:2], s_ver)
+    torch.cuda.synchronize()
+    assert int(status.abs().sum().item()) == 0
+    # prefill: the four shortest sequences in full
+    off = pre.cu_seqlens
+    idx = [int(i) for i in np.argsort(pre.lens)[:4]]
+    res = oracle_seqs(pre, pre.tokens, [int(x) for x in pre.lens], idx=idx)
+    H = ph.cpu().numpy()
+    for i, x in zip(idx, res):
+        assert_y_close(py[off[i]:off[i + 1]], x.y, f"prefill y seq {i}")
+        assert_state_close(H[i], x.H, f"prefill state seq {i}", TC_STATE_TOL)
+        np.testing.assert_array_equal(pc[i].float().cpu().numpy(), x.conv_state)
+    # verify: every sequence's outputs and final state, intermediates of a sample
+    resv = oracle_seqs(ver, ver.tokens, ks)
+    assert_y_close(vy, np.concatenate([x.y for x in resv]), "verify y")
+    Hv = vh.cpu().numpy()
+    for i, x in enumerate(resv):
+        assert_state_close(Hv[i], x.H, f"verify state seq {i}")
