@@ -227,11 +227,13 @@ def test_mixed_serving_step_two_streams():
     vy = torch.empty((sum(ks), 4096), dtype=torch.bfloat16, device=d)
     status = torch.zeros(2, dtype=torch.int32, device=d)
     s_pre, s_ver = torch.cuda.Stream(d), torch.cuda.Stream(d)
-    torch.cuda.synchronize()
-    gdn.gdn_prefill_chunked(dims, weights, dev.tokens_to(pre.tokens, torch.bfloat16, d), pre.n, cu,
-                            T, Lmax, php, pc, pre.n, ps, py, None, ws, status[0:1], s_pre)
-    gdn.gdn_verify_multi(dims, weights, dev.tokens_to(ver.tokens, torch.bfloat16, d), ver.n, ks,
-                         tables, vc, ver.n, vs, None, vy, None, status[1:2], s_ver)
+    pin = dev.tokens_to(pre.tokens, torch.bfloat16, d)
+    vin = dev.tokens_to(ver.tokens, torch.bfloat16, d)
+    torch.cuda.synchronize()  # every input is on the device before either side stream starts
+    gdn.gdn_prefill_chunked(dims, weights, pin, pre.n, cu, T, Lmax, php, pc, pre.n, ps, py, None,
+                            ws, status[0:1], s_pre)
+    gdn.gdn_verify_multi(dims, weights, vin, ver.n, ks, tables, vc, ver.n, vs, None, vy, None,
+                         status[1:2], s_ver)
     torch.cuda.synchronize()
     assert int(status.abs().sum().item()) == 0
     # prefill: the four shortest sequences in full
