@@ -60,6 +60,18 @@ __device__ __forceinline__ float softplus_f(float x) {
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
 __device__ __forceinline__ float silu_f(float x) { return x / (1.f + expf(-x)); }
 
+// SiLU with the fast exponential and division (relative error ~1e-6, far below the bf16
+// rounding of the outputs it feeds).
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+
+// 2^x with the hardware approximation (ex2.approx, relative error below 2^-22; subnormal
+// results flush to zero).
+__device__ __forceinline__ float exp2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // The decay and write-strength gates of one (token, value head).
 __device__ __forceinline__ void gates_f(float a, float b, float A_log, float dt_bias,
                                         float* alpha, float* beta) {

@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           const int s = 32 * half + u;
-          Am[r * S::kAS + s] = (s < r && r < L) ? br * v[u] * exp2f(gr - G_s[s]) : 0.f;
+          Am[r * S::kAS + s] = (s < r && r < L) ? br * v[u] * exp2_fast(gr - G_s[s]) : 0.f;
         }
       } else {
         const int r = row - kC;
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           const int s = 32 * half + u;
-          v[u] = (s <= r && r < L) ? v[u] * exp2f(gr - G_s[s]) : 0.f;
+          v[u] = (s <= r && r < L) ? v[u] * exp2_fast(gr - G_s[s]) : 0.f;
         }
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8)
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < 8; ++u) {
         const float tv = Tf[r * kC + s0 + u];
         tu[u] = tv * B_s[s0 + u];
-        tw[u] = tu[u] * exp2f(G_s[s0 + u]);
+        tw[u] = tu[u] * exp2_fast(G_s[s0 + u]);
       }
       *reinterpret_cast<uint4*>(sm + S::kTw + tc::sw128_offset(64, r, s0)) = pack8_h(tw);
       *reinterpret_cast<uint4*>(sm + S::kTu + tc::sw128_offset(64, r, s0)) = pack8_h(tu);
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 32; ++u) {
         du[u] -= dd[u];
-        ds[u] = du[u] * exp2f(gL - G_s[32 * half + u]);
+        ds[u] = du[u] * exp2_fast(gL - G_s[32 * half + u]);
       }
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- 11. H update (registers + fp16 copy) and the chunk outputs
     {
-      const float eL = exp2f(gL);
+      const float eL = exp2_fast(gL);
 #pragma unroll
       for (int c16 = 0; c16 < 4; ++c16) {
         float v[16];
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 32; ++u) {
         const int r = 32 * half + u;
-        Os[r * kD + j] = exp2f(G_s[r]) * d2[u] + d3[u];
+        Os[r * kD + j] = exp2_fast(G_s[r]) * d2[u] + d3[u];
       }
     }
     fence_proxy_async_smem();
@@ -477,10 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4 z4 = Act<__nv_bfloat16>::load4(
           reinterpret_cast<const __nv_bfloat16*>(sm + S::kZ + (c & 1) * 16384) + r * kD + jj);
       float4 yv;
-      yv.x = o.x * inv * w4.x * silu_f(z4.x);
-      yv.y = o.y * inv * w4.y * silu_f(z4.y);
-      yv.z = o.z * inv * w4.z * silu_f(z4.z);
-      yv.w = o.w * inv * w4.w * silu_f(z4.w);
+      yv.x = o.x * inv * w4.x * silu_fast(z4.x);
+      yv.y = o.y * inv * w4.y * silu_fast(z4.y);
+      yv.z = o.z * inv * w4.z * silu_fast(z4.z);
+      yv.w = o.w * inv * w4.w * silu_fast(z4.w);
       Act<__nv_bfloat16>::store4(
           reinterpret_cast<__nv_bfloat16*>(p.y) + size_t(row) * p.Hv * kD + h * kD + jj, yv);
       if (p.core_out)
