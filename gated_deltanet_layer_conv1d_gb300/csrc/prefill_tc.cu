@@ -158,32 +158,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
-  // The q_hat / k_hat / v tiles, gates and z rows of chunk c into shared memory, issued by
-  // warp 0: lane 0 posts the byte count and the tile copies, then every lane copies z rows.
+  // The q_hat / k_hat / v tiles and gates of chunk c into shared memory: bulk copies issued
+  // by thread 0, completing on bar_load.
   auto issue_loads = [&](int c) {
+    const size_t cs = slot0 + size_t(c);
+    const unsigned char* kimg = ws + lay.qk(cs, kh, 0);
+    const unsigned char* qimg = ws + lay.qk(cs, kh, 1);
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar_load, 3u * 16384u + 512u);
+    bulk_g2s(sm + S::kAQK, kimg, 8192, bar_load);
+    bulk_g2s(sm + S::kAQK + 16384, kimg + 8192, 8192, bar_load);
+    bulk_g2s(sm + S::kAQK + 8192, qimg, 8192, bar_load);
+    bulk_g2s(sm + S::kAQK + 24576, qimg + 8192, 8192, bar_load);
+    bulk_g2s(sm + S::kV, ws + lay.v(cs, h), 16384, bar_load);
+    bulk_g2s(gate, ws + lay.gate(cs, h), 512, bar_load);
+  };
+  // The z rows of chunk c (bf16, this value head's 128 columns) into z buffer c & 1: every
+  // thread copies 16-byte pieces with cp.async; each waits for its own before the barrier
+  // that precedes the norm.
+  auto issue_z = [&](int c) {
     const int t0 = c * kC;
     const int L = (len - t0) < kC ? (len - t0) : kC;
-    const size_t cs = slot0 + size_t(c);
     unsigned char* zdst = sm + S::kZ + (c & 1) * 16384;
-    if (lane == 0) {
-      const unsigned char* kimg = ws + lay.qk(cs, kh, 0);
-      const unsigned char* qimg = ws + lay.qk(cs, kh, 1);
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar_load, 3u * 16384u + 512u + uint32_t(L) * 256u);
-      bulk_g2s(sm + S::kAQK, kimg, 8192, bar_load);
-      bulk_g2s(sm + S::kAQK + 16384, kimg + 8192, 8192, bar_load);
-      bulk_g2s(sm + S::kAQK + 8192, qimg, 8192, bar_load);
-      bulk_g2s(sm + S::kAQK + 24576, qimg + 8192, 8192, bar_load);
-      bulk_g2s(sm + S::kV, ws + lay.v(cs, h), 16384, bar_load);
-      bulk_g2s(gate, ws + lay.gate(cs, h), 512, bar_load);
+    const unsigned char* zsrc = reinterpret_cast<const unsigned char*>(
+        reinterpret_cast<const __nv_bfloat16*>(p.z) + size_t(t_begin + t0) * p.z_stride +
+        size_t(h) * kD);
+    for (int e = tid; e < L * 16; e += kThreads) {
+      const int r = e / 16, piece = e % 16;
+      cp_async16(zdst + r * 256 + piece * 16, zsrc + size_t(r) * p.z_stride * 2 + piece * 16);
     }
-    __syncwarp();
-    const __nv_bfloat16* zsrc = reinterpret_cast<const __nv_bfloat16*>(p.z) +
-                                size_t(t_begin + t0) * p.z_stride + size_t(h) * kD;
-    for (int r = lane; r < L; r += 32)
-      bulk_g2s(zdst + r * 256, zsrc + size_t(r) * p.z_stride, 256, bar_load);
+    cp_async_commit();
   };
-  if (warp == 0) issue_loads(0);
+  if (tid == 0) issue_loads(0);
+  issue_z(0);
   const uint32_t tl = uint32_t(32 * q4) << 16;  // this warp's TMEM lane quarter
   uint32_t load_phase = 0, mma_phase = 0;
   bool bad = false;
@@ -439,7 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_wait();
     // Every MMA of this chunk has completed and the q/k, v and gate buffers are no longer
     // read: start the next chunk's loads now, behind this chunk's epilogue.
-    if (warp == 0 && c + 1 < nc) issue_loads(c + 1);
+    if (c + 1 < nc) {
+      if (tid == 0) issue_loads(c + 1);
+      issue_z(c + 1);
+    }
 
     // ---- 11. H update (registers + fp16 copy) and the chunk outputs
     {
@@ -463,6 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         Os[r * kD + j] = exp2_fast(G_s[r]) * d2[u] + d3[u];
       }
     }
+    // this chunk's z rows: the last group of this thread's own copies still in flight is
+    // the next chunk's, so wait until at most one group remains
+    if (c + 1 < nc) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else asm volatile("cp.async.wait_group 0;" ::: "memory");
     fence_proxy_async_smem();
     if (sync_or_stop()) { aborted = true; break; }
 
