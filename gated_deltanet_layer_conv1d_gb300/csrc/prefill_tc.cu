@@ -78,6 +78,25 @@ __device__ __forceinline__ uint4 pack8_h(const float* v) {
   return u;
 }
 
+// Warp-level TF32 MMA (m16n8k8, row-major A, column-major B, f32 accumulate) for the small
+// 16 x 16 block products of the triangular inverse.  Fragment of lane l (g = l / 4,
+// t = l % 4): A (16 x 8) a0 (g, t), a1 (g + 8, t), a2 (g, t + 4), a3 (g + 8, t + 4);
+// B (8 x 8) b0 (t, g), b1 (t + 4, g); D (16 x 8) d0 (g, 2t), d1 (g, 2t + 1), d2 (g + 8, 2t),
+// d3 (g + 8, 2t + 1).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // TMEM columns of the accumulators (512 allocated).
 constexpr uint32_t kT0 = 0;     // MMA0: [K;Q] K^T          (64 cols)
 constexpr uint32_t kTW = 64;    // MMA_W: W^T               (64)
@@ -315,37 +334,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncthreads();
-    // Block (I, J = I - d) of T: T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ.  A thread computes a
-    // 1 x 4 strip (row a, columns bb..bb+3) of one block: one broadcast A load and one
-    // 16-byte T load per four FMAs.
+    // Block (I, J = I - d) of T: T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ, one warp per block,
+    // as TF32 warp MMAs over 16 x 8 output halves.
     for (int d = 1; d < 4; ++d) {
-      const int nblk = 4 - d;  // blocks (I, J = I - d), I = d .. 3
-      const int e = tid;       // strip e: block e / 64, row (e % 64) / 4, columns 4 (e % 4)
-      if (e < nblk * 64) {
-        const int I = d + e / 64, J = I - d, a = (e % 64) / 4, bb = 4 * (e % 4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int K = J; K < I; ++K)
+      if (warp < 4 - d) {
+        const int I = d + warp, J = I - d;
+        const int g = lane >> 2, t = lane & 3;
+        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int k0 = 16 * J; k0 < 16 * I; k0 += 8) {
+          const float* ar = Am + (16 * I + g) * S::kAS + k0 + t;
+          const uint32_t a[4] = {to_tf32(ar[0]), to_tf32(ar[8 * S::kAS]), to_tf32(ar[4]),
+                                 to_tf32(ar[8 * S::kAS + 4])};
 #pragma unroll
-          for (int n = 0; n < 16; ++n) {
-            const float av = Am[(16 * I + a) * S::kAS + 16 * K + n];
-            const float4 t4 = *reinterpret_cast<const float4*>(Tf + (16 * K + n) * kC + 16 * J + bb);
-            acc.x += av * t4.x; acc.y += av * t4.y; acc.z += av * t4.z; acc.w += av * t4.w;
+          for (int nt = 0; nt < 2; ++nt) {
+            const float* br = Tf + (k0 + t) * kC + 16 * J + 8 * nt + g;
+            mma_tf32(y[nt], a, to_tf32(br[0]), to_tf32(br[4 * kC]));
           }
-        *reinterpret_cast<float4*>(Ys + (e / 64) * 256 + a * 16 + bb) = acc;
-      }
-      __syncthreads();
-      if (e < nblk * 64) {
-        const int I = d + e / 64, J = I - d, a = (e % 64) / 4, bb = 4 * (e % 4);
-        const float* y = Ys + (e / 64) * 256;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float tv = Tf[(16 * I + a) * kC + 16 * I + m];
-          const float4 y4 = *reinterpret_cast<const float4*>(y + m * 16 + bb);
-          acc.x += tv * y4.x; acc.y += tv * y4.y; acc.z += tv * y4.z; acc.w += tv * y4.w;
         }
-        *reinterpret_cast<float4*>(Tf + (16 * I + a) * kC + 16 * J + bb) =
-            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        float* Yw = Ys + warp * 256;  // Y of this block, [16][16]
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          Yw[g * 16 + 8 * nt + 2 * t] = y[nt][0];
+          Yw[g * 16 + 8 * nt + 2 * t + 1] = y[nt][1];
+          Yw[(g + 8) * 16 + 8 * nt + 2 * t] = y[nt][2];
+          Yw[(g + 8) * 16 + 8 * nt + 2 * t + 1] = y[nt][3];
+        }
+        __syncwarp();
+        float tt[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int k0 = 0; k0 < 16; k0 += 8) {
+          const float* ar = Tf + (16 * I + g) * kC + 16 * I + k0 + t;
+          const uint32_t a[4] = {to_tf32(ar[0]), to_tf32(ar[8 * kC]), to_tf32(ar[4]),
+                                 to_tf32(ar[8 * kC + 4])};
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+            mma_tf32(tt[nt], a, to_tf32(Yw[(k0 + t) * 16 + 8 * nt + g]),
+                     to_tf32(Yw[(k0 + t + 4) * 16 + 8 * nt + g]));
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          float* tr = Tf + (16 * I + g) * kC + 16 * J + 8 * nt + 2 * t;
+          tr[0] = -tt[nt][0];
+          tr[1] = -tt[nt][1];
+          tr[8 * kC] = -tt[nt][2];
+          tr[8 * kC + 1] = -tt[nt][3];
+        }
       }
       __syncthreads();
     }
@@ -481,7 +514,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (sync_or_stop()) { aborted = true; break; }
 
     // ---- 12. gated RMSNorm of the chunk's outputs, one warp per token
-    for (int r = warp; r < L; r += kThreads / 32) {
+#pragma unroll
+    for (int rr = 0; rr < kC / (kThreads / 32); ++rr) {
+      const int r = warp + rr * (kThreads / 32);
+      if (r >= L) break;
       const int row = t_begin + t0 + r;
       const int jj = lane * 4;
       const float4 o = *reinterpret_cast<const float4*>(Os + r * kD + jj);
