@@ -234,19 +234,19 @@ def time_loop(torch, stream, fn, steps, warmup):
     return e0.elapsed_time(e1) / steps
 
 
-def verify_mode(device, steps, hbm_peak):
+def verify_mode(device, steps, hbm_peak, warmup=3, n=N_SEQ):
     import torch
 
     from gated_deltanet_layer_conv1d_gb300 import device as dev
     from gated_deltanet_layer_conv1d_gb300 import gdn
     from gated_deltanet_layer_conv1d_gb300 import workloads as wl
-    w = wl.ragged_verify(n=N_SEQ)
+    w = wl.ragged_verify(n=n)
     ks = [int(k) for k in w.lens]
     h_pool, conv_pool, slots = dev.states_to(w, device)
-    inter = torch.empty((N_SEQ, 15, 32, 128, 128), dtype=torch.float32, device=device)
+    inter = torch.empty((n, 15, 32, 128, 128), dtype=torch.float32, device=device)
     hsz = 32 * 128 * 128 * 4
-    tables = dev.wy_tables_to(ks, [h_pool.data_ptr() + i * hsz for i in range(N_SEQ)],
-                              [[inter[i, t].data_ptr() for t in range(15)] for i in range(N_SEQ)],
+    tables = dev.wy_tables_to(ks, [h_pool.data_ptr() + i * hsz for i in range(n)],
+                              [[inter[i, t].data_ptr() for t in range(15)] for i in range(n)],
                               device)
     inp = dev.tokens_to(w.tokens, torch.bfloat16, device)
     y = torch.empty((sum(ks), 4096), dtype=torch.bfloat16, device=device)
@@ -255,14 +255,14 @@ def verify_mode(device, steps, hbm_peak):
     stream = torch.cuda.current_stream(device)
 
     def fn(i):
-        gdn.gdn_verify_multi(dims, weights, inp, N_SEQ, ks, tables, conv_pool, N_SEQ, slots,
+        gdn.gdn_verify_multi(dims, weights, inp, n, ks, tables, conv_pool, n, slots,
                              None, y, None, status, stream)
 
-    ms = time_loop(torch, stream, fn, steps, 3)
+    ms = time_loop(torch, stream, fn, steps, warmup)
     assert int(status.item()) == 0
     byts = verify_bytes(ks)
     gbs = byts / (ms * 1e-3) / 1e9
-    return {"workload": f"ragged_verify_{N_SEQ}seq_k2to16", "tokens_per_step": sum(ks),
+    return {"workload": f"ragged_verify_{n}seq_k2to16", "tokens_per_step": sum(ks),
             "ms_per_step": round(ms, 4), "value": round(sum(ks) / (ms * 1e-3), 1),
             "unit": "tokens/s", "gpu_launches_per_step": 1,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
@@ -270,7 +270,7 @@ def verify_mode(device, steps, hbm_peak):
                          "algorithmic_bytes": byts}}
 
 
-def prefill_mode(device, steps, tc_peak):
+def prefill_mode(device, steps, tc_peak, warmup=2):
     import torch
 
     from gated_deltanet_layer_conv1d_gb300 import device as dev
@@ -293,7 +293,7 @@ def prefill_mode(device, steps, tc_peak):
         gdn.gdn_prefill_chunked(dims, weights, inp, 1, cu, T, T, hp, conv_pool, 1, slots, y,
                                 None, ws, status, stream)
 
-    ms = time_loop(torch, stream, fn, steps, 2)
+    ms = time_loop(torch, stream, fn, steps, warmup)
     assert int(status.item()) == 0
     fl = prefill_flops(T)
     tfs = fl / (ms * 1e-3) / 1e12
@@ -447,8 +447,10 @@ def main():
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-modes", action="store_true", help="skip the verify / prefill lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--profile", action="store_true",
-                    help="only the timed decode loop (for profiler captures)")
+    ap.add_argument("--profile", nargs="?", const="decode", default=None,
+                    choices=["decode", "verify", "verify-small", "prefill"],
+                    help="only one timed loop of one mode (for profiler captures); "
+                         "verify-small runs 32 sequences")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -474,6 +476,15 @@ def main():
     gdn.lib()
 
     hbm_peak, tc_peak, peak_src = peaks()
+    if args.profile in ("verify", "verify-small", "prefill"):
+        if args.profile == "prefill":
+            r = prefill_mode(device, args.steps, tc_peak, warmup=args.warmup)
+        else:
+            r = verify_mode(device, args.steps, hbm_peak, warmup=args.warmup,
+                            n=32 if args.profile == "verify-small" else N_SEQ)
+        if rank == 0:
+            print(json.dumps({"profile_run": args.profile, "ms_per_step": r["ms_per_step"]}))
+        return
     bench = DecodeBench(device)
     for i in range(args.warmup):
         bench.step(i)
