@@ -1,9 +1,11 @@
 // prefill.cu -- dispatch of the GDN prefill (sm_103a).
 //
 // d_k = d_v = 128 with bf16 activations: the tensor-core chunked path -- a pre-pass
-// (conv, SiLU, L2 norms, gates of every token into the workspace tiles), then one
-// tcgen05 chunk kernel per (sequence, value head).  Every other shape or dtype: the
-// token-sequential kernel.  The conv-state update runs after either (see abi.cu).
+// (conv, SiLU, L2 norms, gates of every token into the workspace tiles), the chunk kernel
+// (every chunk's W, U, P and K~ at once), the state spine (chunk after chunk per sequence
+// and value head, writing the core output O) and the gated RMSNorm of O.  Every other
+// shape or dtype: the token-sequential kernel.  The conv-state update runs after either
+// (see abi.cu).
 #include "common.cuh"
 #include "kernels.h"
 #include "prefill_layout.cuh"
@@ -17,7 +19,7 @@ size_t prefill_workspace_bytes(int Hk, int Hv, int D, int n, int total_tokens, i
   (void)max_seqlen;
   if (D != 128) return 0;
   const PrefillLayout lay{Hk, Hv};
-  return PrefillLayout::slots(n, total_tokens) * lay.slot_bytes();
+  return lay.total_bytes(n, total_tokens);
 }
 
 cudaError_t launch_prefill(const PrefillParams& p, int dtype, cudaStream_t stream) {
@@ -48,7 +50,16 @@ cudaError_t launch_prefill(const PrefillParams& p, int dtype, cudaStream_t strea
     c.workspace = p.workspace;
     cudaError_t e = launch_prefill_prep(c, stream);
     if (e != cudaSuccess) return e;
-    return launch_prefill_tc(p, stream);
+    // The spine writes the core output into the caller's buffer, else into the workspace.
+    PrefillParams q = p;
+    if (!q.core_out)
+      q.core_out = reinterpret_cast<float*>(
+          static_cast<unsigned char*>(p.workspace) +
+          PrefillLayout{p.Hk, p.Hv}.o_offset(p.n, p.total_tokens));
+    e = launch_prefill_tc(q, stream);
+    if (e != cudaSuccess) return e;
+    return launch_gated_rmsnorm(q.core_out, p.z, p.z_stride, p.norm_w, p.norm_eps,
+                                p.total_tokens, p.Hv, p.D, GDN_DTYPE_BF16, p.y, stream);
   }
   return launch_prefill_sequential(p, dtype, stream);
 }

@@ -2,28 +2,36 @@
 // 5th-generation tensor cores (tcgen05, accumulators in TMEM), d_k = d_v = 128, chunk 64.
 //
 // The method (layer_struct.rs, the FLA chunked prefill: gdn_prefill_fla_recompute_wu_k ->
-// the chunk_delta_h state spine -> gdn_prefill_fla_chunk_fwd_o_k; here one fused kernel per
-// (sequence, value head)).  Inside a chunk of L tokens, with g_r = sum_{s<=r} log alpha_s:
+// the chunk_delta_h state spine -> gdn_prefill_fla_chunk_fwd_o_k).  Inside a chunk of L
+// tokens, with g_r = sum_{s<=r} log alpha_s:
 //   A   = strict_lower(beta_r (k_r . k_s) e^{g_r - g_s}),   T = (I + A)^{-1}
 //   W   = T diag(beta e^g) K,   U = T diag(beta) V,   Delta = U - W H0      (H0 = S0^T)
-//   O   = diag(e^g) Q H0 + lower_incl(Q K^T e^{g_r - g_s}) Delta
-//   H_L = e^{g_L} H0 + (diag(e^{g_L - g}) K)^T Delta
-// Every product is computed transposed so that M = 128 (one TMEM lane per accumulator row):
-//   MMA0  [K;Q] K^T            (M 128 = 64 keys + 64 queries, N 64, K 128)
-//   MMA_W W^T = K^T (T diag(beta e^g))^T      (A = K MN-major, N 64, K 64)
-//   MMA_U U^T = V^T (T diag(beta))^T          (A = V MN-major)
-//   MMA1  (W H0)^T = H0^T W^T,   MMA2  (Q H0)^T = H0^T Q^T     (N 64, K 128)
-//   MMA3  (P Delta)^T = Delta^T P^T           (N 64, K 64)
-//   MMA4  (K~^T Delta)^T = (Delta^T diag(e^{g_L - g})) K        (B = K MN-major, N 128, K 64)
-// All per-token scalings are folded into T's columns, Delta's columns or the epilogue, so
-// the q, k, v tiles come straight from the pre-pass workspace (one bulk copy each).
+//   O   = diag(e^g) Q H0 + P Delta,    P  = lower_incl(Q K^T e^{g_r - g_s})
+//   H_L = e^{g_L} H0 + K~^T Delta,     K~ = diag(e^{g_L - g}) K
+//
+// Two kernels follow the pre-pass (which leaves the normalised q, k, v tiles and the gates
+// in the workspace):
+//
+// gdn_prefill_chunk_kernel -- everything that does not depend on the state, for every
+//   (chunk, value head) at once:
+//     MMA0  [K;Q] K^T            (M 128 = 64 keys + 64 queries, N 64, K 128) -> A and P
+//     T = (I + A)^{-1} on CUDA cores (16 x 16 diagonal blocks, then the blocks below them
+//       level by level with warp-level TF32 MMAs)
+//     MMA_W W^T = K^T (T diag(beta e^g))^T,  MMA_U U^T = V^T (T diag(beta))^T  (N 64, K 64)
+//   and writes W, K~, P, g and U to the workspace.
+// gdn_prefill_spine_kernel<NCOL> -- the state recurrence, chunk after chunk, for one
+//   (sequence, value head) and NCOL of its 128 value columns (columns of H never mix, so
+//   the 128 / NCOL slices run in separate CTAs).  Per chunk, two MMAs:
+//     MMA_a [Q;W] H0             (M 128 = 64 query rows + 64 W rows, N NCOL, K 128)
+//     MMA_b K~^T Delta and [P;*] Delta  (M 128, N NCOL, K 64; rows past P are ignored)
+//   with Delta and the new H written back as fp16 operands between them; it writes the
+//   core output O.  The next chunk's operands arrive by bulk copy into the other of two
+//   buffers meanwhile.  The gated RMSNorm of O follows as its own kernel.
+//
 // Operands are fp16 (kind::f16, f32 accumulation): every operand here is bounded
 // (normalised q and k, O(1) v, T, P, Delta and state), and fp16's 11-bit significand
-// keeps the rounding of the inputs and of T, P and Delta eight times below bf16's.
-// H0 lives in registers (f32) of the 8 warps: thread (w, l) owns row j = 32 (w % 4) + l of
-// H^T and columns i in [64 (w / 4), +64); its fp16 copy is the A operand of MMA1/MMA2.
-// T = (I + A)^{-1} is computed on CUDA cores by blocked forward substitution (16 x 16
-// diagonal blocks, then the off-diagonal blocks level by level).
+// keeps the rounding of the inputs and of T, P and Delta eight times below bf16's.  The
+// state itself stays f32 in registers from the first chunk to the last.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -36,36 +44,7 @@ namespace {
 
 constexpr int kC = 64;
 constexpr int kD = 128;
-constexpr int kThreads = 256;
-
-// Shared memory (offsets from a 1024-aligned base).
-struct TcSmem {
-  static constexpr uint32_t kAQK = 0;            // [128][128] f16: rows 0-63 k_hat, 64-127 q_hat
-  static constexpr uint32_t kV = 32768;          // [64][128] f16 v (MN-major A of MMA_U)
-  static constexpr uint32_t kHT = 49152;         // [128][128] f16 H^T
-  static constexpr uint32_t kW = 81920;          // [64][128] f16 W
-  static constexpr uint32_t kTw = 98304;         // [64][64] f16 T diag(beta e^g)
-  static constexpr uint32_t kTu = 106496;        // [64][64] f16 T diag(beta)
-  static constexpr uint32_t kP = 114688;         // [64][64] f16 P
-  static constexpr uint32_t kDT = 122880;        // [128][64] f16 Delta^T
-  static constexpr uint32_t kDTs = 139264;       // [128][64] f16 Delta^T diag(e^{g_L - g})
-  static constexpr int kAS = 65;                 // row stride of A: odd, so column writes
-                                                 // from 32 lanes hit 32 banks
-  static constexpr uint32_t kAm = 155648;        // [64][65] f32 A
-  static constexpr uint32_t kTf = 172288;        // [64][64] f32 T
-  static constexpr uint32_t kOs = kAm;           // [64][128] f32 outputs (A and T are dead then)
-  static constexpr uint32_t kY = 188672;         // [3][16][16] f32 scratch of the inverse
-  static constexpr uint32_t kZ = 191744;         // [2][64][128] bf16 z rows, double-buffered
-  static constexpr uint32_t kNW = 224512;        // [128] f32 norm weight
-  static constexpr uint32_t kGate = 225024;      // [2][64] f32 log(alpha), beta (bulk copied)
-  static constexpr uint32_t kG = 225536;         // [64] f32 cumulative log decay g
-  static constexpr uint32_t kB = 225792;         // [64] f32 beta (0 past the chunk end)
-  static constexpr uint32_t kMisc = 226048;      // bars, tmem slot, scan carry
-  static constexpr uint32_t kBytes = 226176;
-  static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024
-};
-static_assert(TcSmem::kOs + 64 * 128 * 4 <= TcSmem::kY, "output staging fits in A and T");
-static_assert(TcSmem::kAm + 64 * TcSmem::kAS * 4 <= TcSmem::kTf, "A fits");
+constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint4 pack8_h(const float* v) {
   uint4 u;
@@ -97,18 +76,80 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// TMEM columns of the accumulators (512 allocated).
-constexpr uint32_t kT0 = 0;     // MMA0: [K;Q] K^T          (64 cols)
-constexpr uint32_t kTW = 64;    // MMA_W: W^T               (64)
-constexpr uint32_t kTU = 128;   // MMA_U: U^T               (64)
-constexpr uint32_t kTD = 192;   // MMA1: (W H0)^T           (64)
-constexpr uint32_t kT2 = 256;   // MMA2: (Q H0)^T           (64)
-constexpr uint32_t kT3 = 320;   // MMA3: (P Delta)^T        (64)
-constexpr uint32_t kT4 = 384;   // MMA4: (K~^T Delta)^T     (128)
+// Both kernels check their sequence's token range and state pointer the same way.
+__device__ __forceinline__ int check_seq(const PrefillParams& p, int t_begin, int t_end,
+                                         uint64_t hp) {
+  const int len = t_end - t_begin;
+  if (t_begin < 0 || len < 0 || t_end > p.total_tokens || len > p.max_seqlen)
+    return GDN_ERR_BAD_SEQLENS;
+  if (hp == 0 || (hp & 15u) != 0) return GDN_ERR_BAD_TABLE_ENTRY;
+  return 0;
+}
 
-__global__ void __launch_bounds__(kThreads, 1)
-    gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
-  using S = TcSmem;
+// ------------------------------------------------------------------------------------
+// Chunk kernel: one CTA of 256 threads per (chunk slot, value head).
+
+constexpr int kPrepThreads = 256;
+
+struct PrepSmem {
+  static constexpr uint32_t kAQK = 0;        // [128][128] f16: rows 0-63 k_hat, 64-127 q_hat;
+                                             // later K~ in the k rows, P in q block 0
+  static constexpr uint32_t kP = 8192;       // [64][64] f16 P (q block 0, dead after MMA0)
+  static constexpr uint32_t kV = 32768;      // [64][128] f16 v (MN-major A of MMA_U)
+  static constexpr int kAS = 65;             // row stride of A: odd, so column writes from
+                                             // 32 lanes hit 32 banks
+  static constexpr uint32_t kAm = 49152;     // [64][65] f32 A
+  static constexpr uint32_t kTw = kAm;       // [64][64] f16 T diag(beta e^g) (A is dead)
+  static constexpr uint32_t kTu = kAm + 8192;  // [64][64] f16 T diag(beta)
+  static constexpr uint32_t kTf = 66560;     // [64][64] f32 T
+  static constexpr uint32_t kWi = kTf;       // [64][128] f16 W image (T is dead)
+  static constexpr uint32_t kY = 82944;      // [3][16][16] f32 scratch of the inverse
+  static constexpr uint32_t kGate = 86016;   // [2][64] f32 log(alpha), beta (bulk copied)
+  static constexpr uint32_t kG = 86528;      // [64] f32 cumulative log2 decay g
+  static constexpr uint32_t kB = 86784;      // [64] f32 beta (0 past the chunk end)
+  static constexpr uint32_t kMisc = 87040;   // bars, tmem slot, scan carry
+  static constexpr uint32_t kBytes = 87168;
+  static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024
+};
+static_assert(PrepSmem::kAm + 64 * PrepSmem::kAS * 4 <= PrepSmem::kTf, "A fits");
+static_assert(PrepSmem::kTf + 64 * 64 * 4 <= PrepSmem::kY, "T fits");
+static_assert(PrepSmem::kY + 3 * 256 * 4 <= PrepSmem::kGate, "inverse scratch fits");
+
+// TMEM columns of the chunk kernel (256 allocated, so two CTAs share an SM).
+constexpr uint32_t kT0 = 0;     // MMA0: [K;Q] K^T   (64 cols)
+constexpr uint32_t kTW = 64;    // MMA_W: W^T        (64)
+constexpr uint32_t kTU = 128;   // MMA_U: U^T        (64)
+
+__global__ void __launch_bounds__(kPrepThreads, 2)
+    gdn_prefill_chunk_kernel(const __grid_constant__ PrefillParams p) {
+  using S = PrepSmem;
+  const int cs = blockIdx.x / p.Hv, h = blockIdx.x % p.Hv, kh = h / p.G;
+  // The sequence that owns chunk slot cs: the last s with base(s) <= cs.
+  int seq = 0;
+  {
+    int lo = 0, hi = p.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (PrefillLayout::base(p.cu_seqlens[mid], mid) <= size_t(cs)) lo = mid;
+      else hi = mid - 1;
+    }
+    seq = lo;
+  }
+  const int t_begin = p.cu_seqlens[seq], t_end = p.cu_seqlens[seq + 1];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {
+    const int bad = check_seq(p, t_begin, t_end, p.h_ptrs[seq]);
+    if (bad) {
+      if (tid == 0) report(p.status, bad);
+      return;
+    }
+  }
+  const size_t slot0 = PrefillLayout::base(t_begin, seq);
+  const int len = t_end - t_begin, nc = (len + kC - 1) / kC;
+  if (size_t(cs) < slot0 || size_t(cs) - slot0 >= size_t(nc)) return;  // an unused slot
+  const int c = int(size_t(cs) - slot0);
+  const int L = (len - c * kC) < kC ? (len - c * kC) : kC;
+
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -117,73 +158,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* Tf = reinterpret_cast<float*>(sm + S::kTf);
   float* Ys = reinterpret_cast<float*>(sm + S::kY);
   float* gate = reinterpret_cast<float*>(sm + S::kGate);
-  float* G_s = reinterpret_cast<float*>(sm + S::kG);  // cumulative log2 decay
+  float* G_s = reinterpret_cast<float*>(sm + S::kG);
   float* B_s = reinterpret_cast<float*>(sm + S::kB);
-  float* NW = reinterpret_cast<float*>(sm + S::kNW);
-  float* Os = reinterpret_cast<float*>(sm + S::kOs);  // output staging, after the inverse
   uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + S::kMisc);
   uint64_t* bar_mma = bar_load + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_mma + 1);
   float* carry = reinterpret_cast<float*>(tslot + 1);
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int seq = blockIdx.x / p.Hv, h = blockIdx.x % p.Hv, kh = h / p.G;
-  const int t_begin = p.cu_seqlens[seq], t_end = p.cu_seqlens[seq + 1];
-  const int len = t_end - t_begin;
-  const uint64_t hp = p.h_ptrs[seq];
-  {
-    int bad = 0;
-    if (t_begin < 0 || len < 0 || t_end > p.total_tokens || len > p.max_seqlen)
-      bad = GDN_ERR_BAD_SEQLENS;
-    else if (hp == 0 || (hp & 15u) != 0)
-      bad = GDN_ERR_BAD_TABLE_ENTRY;
-    if (bad) {
-      if (tid == 0) report(p.status, bad);
-      return;
-    }
-  }
-  if (len == 0) return;  // nothing to do: the state stays as it is
-
   const PrefillLayout lay{p.Hk, p.Hv};
-  const size_t slot0 = PrefillLayout::base(t_begin, seq);
-  const unsigned char* ws = reinterpret_cast<const unsigned char*>(p.workspace);
-  const int nc = (len + kC - 1) / kC;
+  unsigned char* ws = reinterpret_cast<unsigned char*>(p.workspace);
 
   if (tid == 0) {
     mbar_init(bar_load, 1);
     mbar_init(bar_mma, 1);
     fence_mbar_init();
   }
-  if (warp == 0) tc::alloc(tslot, 512);
-
-  // H0 (f32) into registers: H^T row j, columns i0 .. i0 + 63.
-  const int q4 = warp & 3, half = warp >> 2;
-  const int j = 32 * q4 + lane;
-  const int i0 = 64 * half;
-  float* Hg = reinterpret_cast<float*>(hp) + size_t(h) * kD * kD;
-  float Hr[64];
-#pragma unroll
-  for (int ii = 0; ii < 64; ++ii) Hr[ii] = Hg[(i0 + ii) * kD + j];
-  auto write_HT = [&]() {
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8)
-      *reinterpret_cast<uint4*>(sm + S::kHT + tc::sw128_offset(128, j, i0 + 8 * c8)) =
-          pack8_h(Hr + 8 * c8);
-  };
-  write_HT();
-  if (tid < kD) NW[tid] = p.norm_w[tid];
-  fence_proxy_async_smem();
+  if (warp == 0) tc::alloc(tslot, 256);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
-  // The q_hat / k_hat / v tiles and gates of chunk c into shared memory: bulk copies issued
-  // by thread 0, completing on bar_load.
-  auto issue_loads = [&](int c) {
-    const size_t cs = slot0 + size_t(c);
+  if (tid == 0) {
     const unsigned char* kimg = ws + lay.qk(cs, kh, 0);
     const unsigned char* qimg = ws + lay.qk(cs, kh, 1);
-    fence_proxy_async_smem();
     mbar_arrive_expect_tx(bar_load, 3u * 16384u + 512u);
     bulk_g2s(sm + S::kAQK, kimg, 8192, bar_load);
     bulk_g2s(sm + S::kAQK + 16384, kimg + 8192, 8192, bar_load);
@@ -191,35 +188,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bulk_g2s(sm + S::kAQK + 24576, qimg + 8192, 8192, bar_load);
     bulk_g2s(sm + S::kV, ws + lay.v(cs, h), 16384, bar_load);
     bulk_g2s(gate, ws + lay.gate(cs, h), 512, bar_load);
-  };
-  // The z rows of chunk c (bf16, this value head's 128 columns) into z buffer c & 1: every
-  // thread copies 16-byte pieces with cp.async; each waits for its own before the barrier
-  // that precedes the norm.
-  auto issue_z = [&](int c) {
-    const int t0 = c * kC;
-    const int L = (len - t0) < kC ? (len - t0) : kC;
-    unsigned char* zdst = sm + S::kZ + (c & 1) * 16384;
-    const unsigned char* zsrc = reinterpret_cast<const unsigned char*>(
-        reinterpret_cast<const __nv_bfloat16*>(p.z) + size_t(t_begin + t0) * p.z_stride +
-        size_t(h) * kD);
-    for (int e = tid; e < L * 16; e += kThreads) {
-      const int r = e / 16, piece = e % 16;
-      cp_async16(zdst + r * 256 + piece * 16, zsrc + size_t(r) * p.z_stride * 2 + piece * 16);
-    }
-    cp_async_commit();
-  };
-  if (tid == 0) issue_loads(0);
-  issue_z(0);
+  }
+  const int q4 = warp & 3, half = warp >> 2;
   const uint32_t tl = uint32_t(32 * q4) << 16;  // this warp's TMEM lane quarter
-  uint32_t load_phase = 0, mma_phase = 0;
-  bool bad = false;
-  // Every thread waits for the MMAs committed so far.
+  bool bad = !mbar_wait_bounded(bar_load, 0);
+  uint32_t mma_phase = 0;
   auto mma_wait = [&]() {
     bad |= !mbar_wait_bounded(bar_mma, mma_phase);
     mma_phase ^= 1u;
     tc::fence_after_sync();
   };
-  // Barrier that also agrees on a failed wait; true means stop.
   auto sync_or_stop = [&]() -> bool {
     tc::fence_before_sync();
     const bool stop = __syncthreads_or(bad) != 0;
@@ -227,28 +205,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     return stop;
   };
 
-  bool aborted = false;
-  for (int c = 0; c < nc; ++c) {
-    const int t0 = c * kC;
-    const int L = (len - t0) < kC ? (len - t0) : kC;
-
-    // ---- 1. this chunk's tiles, gates and z rows (issued during the previous chunk)
-    bad |= !mbar_wait_bounded(bar_load, load_phase);
-    load_phase ^= 1u;
-
-    // ---- 2. rows past the end of the sequence are zero; decay prefix sums
+  do {
+    // ---- rows past the end of the sequence are zero; decay prefix sums
     if (L < kC) {
       const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-      for (int idx = tid; idx < (kC - L) * 16; idx += kThreads) {
+      for (int idx = tid; idx < (kC - L) * 16; idx += kPrepThreads) {
         const int row = L + idx / 16, ch = idx % 16, blk = ch / 8, c16 = ch % 8;
         *reinterpret_cast<uint4*>(sm + S::kAQK + blk * 16384 + row * 128 + c16 * 16) = zero;
-        *reinterpret_cast<uint4*>(sm + S::kAQK + blk * 16384 + (kC + row) * 128 + c16 * 16) = zero;
+        *reinterpret_cast<uint4*>(sm + S::kAQK + blk * 16384 + (kC + row) * 128 + c16 * 16) =
+            zero;
         *reinterpret_cast<uint4*>(sm + S::kV + blk * 8192 + row * 128 + c16 * 16) = zero;
       }
     }
     if (tid < kC) {
-      // g in log2 units (log(alpha) * log2(e)), so each decay factor below is one exp2f
-      float v = tid < L ? gate[tid] * 1.4426950408889634f : 0.f;
+      // g in log2 units, so each decay factor below is one exp2; rows past the end of the
+      // sequence add nothing, so they repeat g_{L-1}
+      float v = tid < L ? gate[tid] * kLog2e : 0.f;
       const float be = tid < L ? gate[kC + tid] : 0.f;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -260,12 +232,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid >= 32) v += carry[0];
       G_s[tid] = v;
       B_s[tid] = be;
+      reinterpret_cast<float*>(ws + lay.g(cs, h))[tid] = v;
     }
     fence_proxy_async_smem();
-    if (sync_or_stop()) { aborted = true; break; }
-    const float gL = G_s[L - 1];
+    if (sync_or_stop()) break;
+    const float gL = G_s[kC - 1];
 
-    // ---- 3. MMA0: [K;Q] K^T
+    // ---- MMA0: [K;Q] K^T
     if (tid == 0) {
 #pragma unroll
       for (int k0 = 0; k0 < kD; k0 += 16)
@@ -275,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mma_wait();
 
-    // ---- 4. A (f32) from the K K^T rows, P (fp16) from the Q K^T rows
+    // ---- A (f32) from the K K^T rows, P (fp16, over q block 0) from the Q K^T rows
     {
       float v[32];
       tc::ld16(tmem + tl + kT0 + 32 * half, *reinterpret_cast<float(*)[16]>(v));
@@ -303,9 +276,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               pack8_h(v + 8 * c8);
       }
     }
-    if (sync_or_stop()) { aborted = true; break; }
+    fence_proxy_async_smem();
+    if (sync_or_stop()) break;
+    if (tid == 0) {
+      bulk_s2g(ws + lay.p(cs, h), sm + S::kP, 8192);
+      bulk_commit();
+    }
 
-    // ---- 5. T = (I + A)^{-1}: diagonal 16 x 16 blocks, then the blocks below them
+    // ---- T = (I + A)^{-1}: diagonal 16 x 16 blocks, then the blocks below them
     if (warp < 4) {
       if (lane < 16) {
         const int b0 = 16 * warp;
@@ -382,8 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncthreads();
     }
-    // T diag(beta e^g) and T diag(beta), fp16, [r][s]
-    for (int cid = tid; cid < kC * 8; cid += kThreads) {
+    // T diag(beta e^g) and T diag(beta), fp16, [r][s] (over A, which is dead now)
+    for (int cid = tid; cid < kC * 8; cid += kPrepThreads) {
       const int r = cid / 8, s0 = (cid % 8) * 8;
       float tw[8], tu[8];
 #pragma unroll
@@ -396,9 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint4*>(sm + S::kTu + tc::sw128_offset(64, r, s0)) = pack8_h(tu);
     }
     fence_proxy_async_smem();
-    if (sync_or_stop()) { aborted = true; break; }
+    if (sync_or_stop()) break;
 
-    // ---- 6. W^T = K^T (T diag(beta e^g))^T, U^T = V^T (T diag(beta))^T
+    // ---- W^T = K^T (T diag(beta e^g))^T, U^T = V^T (T diag(beta))^T
     if (tid == 0) {
 #pragma unroll
       for (int s0 = 0; s0 < kC; s0 += 16) {
@@ -412,155 +390,347 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::commit(bar_mma);
     }
     mma_wait();
+    if (sync_or_stop()) break;
 
-    // ---- 7. W [r][i] from W^T (lane i)
+    // ---- W [r][i] (fp16 image, over T) from W^T (lane i); U [r][j] (f32, straight to the
+    // workspace) from U^T (lane j); K~ in place of the k rows, which no MMA reads any more
     {
+      const int i = 32 * q4 + lane;
       float v[32];
       tc::ld16(tmem + tl + kTW + 32 * half, *reinterpret_cast<float(*)[16]>(v));
       tc::ld16(tmem + tl + kTW + 32 * half + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-      const int i = 32 * q4 + lane;
 #pragma unroll
       for (int u = 0; u < 32; ++u)
-        *reinterpret_cast<__half*>(sm + S::kW + tc::sw128_offset(64, 32 * half + u, i)) =
+        *reinterpret_cast<__half*>(sm + S::kWi + tc::sw128_offset(64, 32 * half + u, i)) =
             __float2half_rn(v[u]);
+      tc::ld16(tmem + tl + kTU + 32 * half, *reinterpret_cast<float(*)[16]>(v));
+      tc::ld16(tmem + tl + kTU + 32 * half + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      float* Ug = reinterpret_cast<float*>(ws + lay.u(cs, h));
+#pragma unroll
+      for (int u = 0; u < 32; ++u) Ug[(32 * half + u) * kD + i] = v[u];
+    }
+    for (int idx = tid; idx < kC * 16; idx += kPrepThreads) {
+      const int blk = idx >> 9, row = (idx >> 3) & 63, c16 = idx & 7;
+      uint4* q = reinterpret_cast<uint4*>(sm + S::kAQK + blk * 16384 + row * 128 + c16 * 16);
+      const float sc = exp2_fast(gL - G_s[row]);
+      const uint4 raw = *q;
+      const __half2* hv = reinterpret_cast<const __half2*>(&raw);
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __half22float2(hv[e]);
+        f[2 * e] = x.x * sc;
+        f[2 * e + 1] = x.y * sc;
+      }
+      *q = pack8_h(f);
     }
     fence_proxy_async_smem();
-    if (sync_or_stop()) { aborted = true; break; }
-
-    // ---- 8. (W H0)^T = H0^T W^T and (Q H0)^T = H0^T Q^T
+    if (sync_or_stop()) break;
     if (tid == 0) {
-#pragma unroll
-      for (int k0 = 0; k0 < kD; k0 += 16) {
-        tc::mma_f16(tmem + kTD, tc::desc_at(sb + S::kHT, 128, k0),
-                     tc::desc_at(sb + S::kW, 64, k0), tc::idesc_f16(128, 64), k0 > 0);
-        tc::mma_f16(tmem + kT2, tc::desc_at(sb + S::kHT, 128, k0),
-                     tc::desc_at(sb + S::kAQK + 8192, 128, k0), tc::idesc_f16(128, 64),
-                     k0 > 0);
-      }
-      tc::commit(bar_mma);
+      bulk_s2g(ws + lay.w(cs, h), sm + S::kWi, 16384);
+      bulk_s2g(ws + lay.kt(cs, h), sm + S::kAQK, 8192);
+      bulk_s2g(ws + lay.kt(cs, h) + 8192, sm + S::kAQK + 16384, 8192);
+      bulk_commit();
     }
-    mma_wait();
+  } while (false);
 
-    // ---- 9. Delta^T = U^T - (W H0)^T, and its decay-weighted copy
-    {
-      float du[32], dd[32];
-      tc::ld16(tmem + tl + kTU + 32 * half, *reinterpret_cast<float(*)[16]>(du));
-      tc::ld16(tmem + tl + kTU + 32 * half + 16, *reinterpret_cast<float(*)[16]>(du + 16));
-      tc::ld16(tmem + tl + kTD + 32 * half, *reinterpret_cast<float(*)[16]>(dd));
-      tc::ld16(tmem + tl + kTD + 32 * half + 16, *reinterpret_cast<float(*)[16]>(dd + 16));
-      float ds[32];
-#pragma unroll
-      for (int u = 0; u < 32; ++u) {
-        du[u] -= dd[u];
-        ds[u] = du[u] * exp2_fast(gL - G_s[32 * half + u]);
-      }
-#pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        const uint32_t off = tc::sw128_offset(128, j, 32 * half + 8 * c8);
-        *reinterpret_cast<uint4*>(sm + S::kDT + off) = pack8_h(du + 8 * c8);
-        *reinterpret_cast<uint4*>(sm + S::kDTs + off) = pack8_h(ds + 8 * c8);
-      }
-    }
-    fence_proxy_async_smem();
-    if (sync_or_stop()) { aborted = true; break; }
-
-    // ---- 10. (P Delta)^T = Delta^T P^T and (K~^T Delta)^T = (Delta^T e^{g_L - g}) K
-    if (tid == 0) {
-#pragma unroll
-      for (int s0 = 0; s0 < kC; s0 += 16) {
-        tc::mma_f16(tmem + kT3, tc::desc_at(sb + S::kDT, 128, s0),
-                     tc::desc_at(sb + S::kP, 64, s0), tc::idesc_f16(128, 64), s0 > 0);
-        tc::mma_f16(tmem + kT4, tc::desc_at(sb + S::kDTs, 128, s0),
-                     tc::desc_mn_sw128(sb + S::kAQK + s0 * 128, 16384),
-                     tc::idesc_f16(128, 128, false, true), s0 > 0);
-      }
-      tc::commit(bar_mma);
-    }
-    mma_wait();
-    // Every MMA of this chunk has completed and the q/k, v and gate buffers are no longer
-    // read: start the next chunk's loads now, behind this chunk's epilogue.
-    if (c + 1 < nc) {
-      if (tid == 0) issue_loads(c + 1);
-      issue_z(c + 1);
-    }
-
-    // ---- 11. H update (registers + fp16 copy) and the chunk outputs
-    {
-      const float eL = exp2_fast(gL);
-#pragma unroll
-      for (int c16 = 0; c16 < 4; ++c16) {
-        float v[16];
-        tc::ld16(tmem + tl + kT4 + i0 + 16 * c16, v);
-#pragma unroll
-        for (int u = 0; u < 16; ++u) Hr[16 * c16 + u] = eL * Hr[16 * c16 + u] + v[u];
-      }
-      write_HT();
-      float d2[32], d3[32];
-      tc::ld16(tmem + tl + kT2 + 32 * half, *reinterpret_cast<float(*)[16]>(d2));
-      tc::ld16(tmem + tl + kT2 + 32 * half + 16, *reinterpret_cast<float(*)[16]>(d2 + 16));
-      tc::ld16(tmem + tl + kT3 + 32 * half, *reinterpret_cast<float(*)[16]>(d3));
-      tc::ld16(tmem + tl + kT3 + 32 * half + 16, *reinterpret_cast<float(*)[16]>(d3 + 16));
-#pragma unroll
-      for (int u = 0; u < 32; ++u) {
-        const int r = 32 * half + u;
-        Os[r * kD + j] = exp2_fast(G_s[r]) * d2[u] + d3[u];
-      }
-    }
-    // this chunk's z rows: the last group of this thread's own copies still in flight is
-    // the next chunk's, so wait until at most one group remains
-    if (c + 1 < nc) asm volatile("cp.async.wait_group 1;" ::: "memory");
-    else asm volatile("cp.async.wait_group 0;" ::: "memory");
-    fence_proxy_async_smem();
-    if (sync_or_stop()) { aborted = true; break; }
-
-    // ---- 12. gated RMSNorm of the chunk's outputs, one warp per token
-#pragma unroll
-    for (int rr = 0; rr < kC / (kThreads / 32); ++rr) {
-      const int r = warp + rr * (kThreads / 32);
-      if (r >= L) break;
-      const int row = t_begin + t0 + r;
-      const int jj = lane * 4;
-      const float4 o = *reinterpret_cast<const float4*>(Os + r * kD + jj);
-      const float ss = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
-      const float inv = rsqrtf(ss / float(kD) + p.norm_eps);
-      const float4 w4 = *reinterpret_cast<const float4*>(NW + jj);
-      const float4 z4 = Act<__nv_bfloat16>::load4(
-          reinterpret_cast<const __nv_bfloat16*>(sm + S::kZ + (c & 1) * 16384) + r * kD + jj);
-      float4 yv;
-      yv.x = o.x * inv * w4.x * silu_fast(z4.x);
-      yv.y = o.y * inv * w4.y * silu_fast(z4.y);
-      yv.z = o.z * inv * w4.z * silu_fast(z4.z);
-      yv.w = o.w * inv * w4.w * silu_fast(z4.w);
-      Act<__nv_bfloat16>::store4(
-          reinterpret_cast<__nv_bfloat16*>(p.y) + size_t(row) * p.Hv * kD + h * kD + jj, yv);
-      if (p.core_out)
-        *reinterpret_cast<float4*>(p.core_out + (size_t(row) * p.Hv + h) * kD + jj) = o;
-    }
-    __syncthreads();  // Os and this chunk's z buffer are read
-  }
-
-  if (aborted) {
-    if (tid == 0) report(p.status, GDN_ERR_TIMEOUT);
-  } else {
-#pragma unroll
-    for (int ii = 0; ii < 64; ++ii) Hg[(i0 + ii) * kD + j] = Hr[ii];
+  if (tid == 0) {
+    bulk_wait_all();
+    if (bad) report(p.status, GDN_ERR_TIMEOUT);
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::dealloc(tmem, 512);
+  if (warp == 0) tc::dealloc(tmem, 256);
+}
+
+// ------------------------------------------------------------------------------------
+// State spine: one CTA of 4 * NCOL threads per (sequence, value head, column slice).
+// Warp w serves TMEM lanes 32 (w % 4) .. + 31 and the 32 columns 32 (w / 4) .. + 31 of
+// its slice; lane l of it owns H row i = 32 (w % 4) + l over those columns.
+
+template <int NCOL>
+struct SpineSmem {
+  // One chunk's operands (two such buffers):
+  static constexpr uint32_t kQW = 0;       // [128][128] f16: rows 0-63 q_hat, 64-127 W
+  static constexpr uint32_t kP = 32768;    // [64][64] f16 P; an M = 128 operand starting
+                                           // here reads its rows 64-127 from K~ (unused)
+  static constexpr uint32_t kKt = 40960;   // [64][128] f16 K~ (MN-major A of K~^T Delta)
+  static constexpr uint32_t kGd = 57344;   // [64] f32 g
+  static constexpr uint32_t kStage = 58368;
+  static constexpr uint32_t kTx = 4 * 8192 + 8192 + 16384 + 256;  // bytes per fill
+  static constexpr uint32_t kHT = 2 * kStage;          // [NCOL][128] f16 H^T of the slice
+  static constexpr uint32_t kDT = kHT + NCOL * 256;    // [NCOL][64] f16 Delta^T
+  static constexpr uint32_t kMisc = kDT + NCOL * 128;  // bars, tmem slot
+  static constexpr uint32_t kBytes = kMisc + 64;
+  static constexpr uint32_t kAlloc = kBytes + 1024;
+  static constexpr uint32_t kTmemCols = NCOL == 32 ? 128 : (NCOL == 64 ? 256 : 512);
+};
+
+template <int NCOL>
+__global__ void __launch_bounds__(4 * NCOL, 1)
+    gdn_prefill_spine_kernel(const __grid_constant__ PrefillParams p) {
+  using S = SpineSmem<NCOL>;
+  constexpr int kNS = kD / NCOL;  // slices per head
+  constexpr int kIssuer = 64;     // warp 2, lane 0: not one of the output warps
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int slice = blockIdx.x % kNS, unit = blockIdx.x / kNS;
+  const int seq = unit / p.Hv, h = unit % p.Hv, kh = h / p.G;
+  const int t_begin = p.cu_seqlens[seq], t_end = p.cu_seqlens[seq + 1];
+  const uint64_t hp = p.h_ptrs[seq];
+  {
+    const int bad = check_seq(p, t_begin, t_end, hp);
+    if (bad) {
+      if (tid == 0) report(p.status, bad);
+      return;
+    }
+  }
+  const int len = t_end - t_begin;
+  if (len == 0) return;  // nothing to do: the state stays as it is
+  const int nc = (len + kC - 1) / kC;
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::kMisc);  // [2]
+  uint64_t* bar_mma = full + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_mma + 1);
+
+  const PrefillLayout lay{p.Hk, p.Hv};
+  const unsigned char* ws = reinterpret_cast<const unsigned char*>(p.workspace);
+  const size_t slot0 = PrefillLayout::base(t_begin, seq);
+
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tc::alloc(tslot, S::kTmemCols);
+
+  const int q4 = warp & 3, cg = warp >> 2;
+  const int row = 32 * q4 + lane;       // TMEM lane; the H row i of this thread
+  const int jl0 = 32 * cg;              // first column of this warp within the slice
+  const int col0 = NCOL * slice + jl0;  // ... and within the head
+  float* Hg = reinterpret_cast<float*>(hp) + size_t(h) * kD * kD;
+  float Hr[32];
+#pragma unroll
+  for (int u = 0; u < 32; u += 4) {
+    const float4 x = *reinterpret_cast<const float4*>(Hg + size_t(row) * kD + col0 + u);
+    Hr[u] = x.x;
+    Hr[u + 1] = x.y;
+    Hr[u + 2] = x.z;
+    Hr[u + 3] = x.w;
+  }
+  auto write_HT = [&]() {
+#pragma unroll
+    for (int u = 0; u < 32; ++u)
+      *reinterpret_cast<__half*>(sm + S::kHT + tc::sw128_offset(NCOL, jl0 + u, row)) =
+          __float2half_rn(Hr[u]);
+  };
+  write_HT();
+  fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const uint32_t tl = uint32_t(32 * q4) << 16;
+  constexpr uint32_t kTA = 0, kTH = NCOL, kTO = 2 * NCOL;
+
+  // Chunk c's operands into buffer c & 1 (issued by kIssuer, completing on full[c & 1]).
+  auto issue_loads = [&](int c) {
+    const size_t cs = slot0 + size_t(c);
+    unsigned char* st = sm + (c & 1) * S::kStage;
+    const unsigned char* qimg = ws + lay.qk(cs, kh, 1);
+    const unsigned char* wimg = ws + lay.w(cs, h);
+    mbar_arrive_expect_tx(&full[c & 1], S::kTx);
+    bulk_g2s(st + S::kQW, qimg, 8192, &full[c & 1]);
+    bulk_g2s(st + S::kQW + 8192, wimg, 8192, &full[c & 1]);
+    bulk_g2s(st + S::kQW + 16384, qimg + 8192, 8192, &full[c & 1]);
+    bulk_g2s(st + S::kQW + 24576, wimg + 8192, 8192, &full[c & 1]);
+    bulk_g2s(st + S::kP, ws + lay.p(cs, h), 8192, &full[c & 1]);
+    bulk_g2s(st + S::kKt, ws + lay.kt(cs, h), 16384, &full[c & 1]);
+    bulk_g2s(st + S::kGd, ws + lay.g(cs, h), 256, &full[c & 1]);
+  };
+  if (tid == kIssuer) issue_loads(0);
+  int issued = 0;  // last chunk whose loads were issued (meaningful in kIssuer)
+
+  uint32_t mma_phase = 0;
+  bool bad = false;
+  auto mma_wait = [&]() {
+    bad |= !mbar_wait_bounded(bar_mma, mma_phase);
+    mma_phase ^= 1u;
+    tc::fence_after_sync();
+  };
+  auto sync_or_stop = [&]() -> bool {
+    tc::fence_before_sync();
+    const bool stop = __syncthreads_or(bad) != 0;
+    tc::fence_after_sync();
+    return stop;
+  };
+
+  bool aborted = false;
+  int consumed = -1;
+  for (int c = 0; c < nc; ++c) {
+    const int t0 = c * kC;
+    const int L = (len - t0) < kC ? (len - t0) : kC;
+    const size_t cs = slot0 + size_t(c);
+    const uint32_t st = uint32_t(c & 1) * S::kStage;
+    // The other buffer was last read by chunk c - 1's MMAs (complete) and by this CTA's
+    // threads before the last barrier: refill it for chunk c + 1.
+    if (tid == kIssuer && c + 1 < nc) {
+      issue_loads(c + 1);
+      issued = c + 1;
+    }
+    bad |= !mbar_wait_bounded(&full[c & 1], uint32_t(c >> 1) & 1u);
+    consumed = c;
+    const float* gd = reinterpret_cast<const float*>(sm + st + S::kGd);
+
+    // U rows of this thread (W-row lanes 64..127), read ahead of the MMA
+    float X[32];
+    if (q4 >= 2) {
+      const int r = row - kC;
+      if (r < L) {
+        const float* Ug = reinterpret_cast<const float*>(ws + lay.u(cs, h)) + r * kD + col0;
+#pragma unroll
+        for (int u = 0; u < 32; u += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(Ug + u);
+          X[u] = x.x;
+          X[u + 1] = x.y;
+          X[u + 2] = x.z;
+          X[u + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) X[u] = 0.f;
+      }
+    }
+
+    // ---- MMA_a: [Q;W] H0
+    if (tid == kIssuer) {
+      if (!bad) {
+#pragma unroll
+        for (int k0 = 0; k0 < kD; k0 += 16)
+          tc::mma_f16(tmem + kTA, tc::desc_at(sb + st + S::kQW, 128, k0),
+                       tc::desc_at(sb + S::kHT, NCOL, k0), tc::idesc_f16(128, NCOL), k0 > 0);
+      }
+      tc::commit(bar_mma);
+    }
+    mma_wait();
+
+    // ---- Delta = U - W H0 (fp16 Delta^T for MMA_b); the Q H0 rows stay in registers
+    float eg = 0.f;
+    const float eL = exp2_fast(gd[kC - 1]);
+    {
+      float v[32];
+      tc::ld16(tmem + tl + kTA + jl0, *reinterpret_cast<float(*)[16]>(v));
+      tc::ld16(tmem + tl + kTA + jl0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      if (q4 >= 2) {
+        const int r = row - kC;
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+          *reinterpret_cast<__half*>(sm + S::kDT + tc::sw128_offset(NCOL, jl0 + u, r)) =
+              __float2half_rn(X[u] - v[u]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) X[u] = v[u];
+        eg = exp2_fast(gd[row]);
+      }
+    }
+    fence_proxy_async_smem();
+    if (sync_or_stop()) { aborted = true; break; }
+
+    // ---- MMA_b: K~^T Delta and [P;*] Delta
+    if (tid == kIssuer) {
+#pragma unroll
+      for (int s0 = 0; s0 < kC; s0 += 16) {
+        tc::mma_f16(tmem + kTH, tc::desc_mn_sw128(sb + st + S::kKt + s0 * 128, 8192),
+                     tc::desc_at(sb + S::kDT, NCOL, s0), tc::idesc_f16(128, NCOL, true, false),
+                     s0 > 0);
+        tc::mma_f16(tmem + kTO, tc::desc_at(sb + st + S::kP, 128, s0),
+                     tc::desc_at(sb + S::kDT, NCOL, s0), tc::idesc_f16(128, NCOL), s0 > 0);
+      }
+      tc::commit(bar_mma);
+    }
+    mma_wait();
+
+    // ---- H = e^{g_L} H + K~^T Delta (f32 registers, fp16 copy for the next MMA_a)
+    {
+      float v[32];
+      tc::ld16(tmem + tl + kTH + jl0, *reinterpret_cast<float(*)[16]>(v));
+      tc::ld16(tmem + tl + kTH + jl0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+#pragma unroll
+      for (int u = 0; u < 32; ++u) Hr[u] = eL * Hr[u] + v[u];
+      write_HT();
+    }
+    fence_proxy_async_smem();
+    if (sync_or_stop()) { aborted = true; break; }
+
+    // ---- O = e^g (Q H0) + P Delta for the query rows (lanes 0..63), behind the next MMA_a
+    if (q4 < 2) {
+      float v[32];
+      tc::ld16(tmem + tl + kTO + jl0, *reinterpret_cast<float(*)[16]>(v));
+      tc::ld16(tmem + tl + kTO + jl0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      if (row < L) {
+        float* o = p.core_out + (size_t(t_begin + t0 + row) * p.Hv + h) * kD + col0;
+#pragma unroll
+        for (int u = 0; u < 32; u += 4)
+          *reinterpret_cast<float4*>(o + u) =
+              make_float4(eg * X[u] + v[u], eg * X[u + 1] + v[u + 1], eg * X[u + 2] + v[u + 2],
+                          eg * X[u + 3] + v[u + 3]);
+      }
+    }
+  }
+
+  if (aborted) {
+    if (tid == kIssuer) {
+      report(p.status, GDN_ERR_TIMEOUT);
+      // a fill still in flight lands before this CTA's shared memory is released
+      if (issued > consumed) mbar_wait_bounded(&full[issued & 1], uint32_t(issued >> 1) & 1u);
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < 32; u += 4)
+      *reinterpret_cast<float4*>(Hg + size_t(row) * kD + col0 + u) =
+          make_float4(Hr[u], Hr[u + 1], Hr[u + 2], Hr[u + 3]);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::dealloc(tmem, S::kTmemCols);
+}
+
+template <int NCOL>
+cudaError_t launch_spine(const PrefillParams& p, cudaStream_t stream) {
+  auto kern = gdn_prefill_spine_kernel<NCOL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(SpineSmem<NCOL>::kAlloc));
+  if (e != cudaSuccess) return e;
+  kern<<<p.n * p.Hv * (kD / NCOL), 4 * NCOL, SpineSmem<NCOL>::kAlloc, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t prefill_tc_smem_bytes() { return TcSmem::kAlloc; }
-
+// Chunk kernel, then the spine; p.core_out must point at the f32 [total_tokens][Hv][128]
+// core output the spine writes.
 cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
-  auto kern = gdn_prefill_tc_kernel;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(TcSmem::kAlloc));
-  if (e != cudaSuccess) return e;
-  if (p.n > 0) kern<<<p.n * p.Hv, kThreads, TcSmem::kAlloc, stream>>>(p);
-  return cudaGetLastError();
+  if (p.n <= 0) return cudaSuccess;
+  {
+    auto kern = gdn_prefill_chunk_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(PrepSmem::kAlloc));
+    if (e != cudaSuccess) return e;
+    const size_t slots = PrefillLayout::slots(p.n, p.total_tokens);
+    kern<<<unsigned(slots * p.Hv), kPrepThreads, PrepSmem::kAlloc, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // Column slices per (sequence, head): as many as one wave of CTAs holds, since the
+  // spine's time is its chain of chunks, not its arithmetic.
+  const int units = p.n * p.Hv, sms = sm_count();
+  if (units * 4 <= sms) return launch_spine<32>(p, stream);
+  if (units * 2 <= sms) return launch_spine<64>(p, stream);
+  return launch_spine<128>(p, stream);
 }
 
 }  // namespace gdn

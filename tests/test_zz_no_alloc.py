@@ -66,7 +66,7 @@ def _same(ref, got):
 
 def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
     first = wl.varlen_prefill([100, 7, 129], seed=21)      # ragged chunks, 3 sequences
-    second = wl.varlen_prefill([1000, 64], seed=22)        # longer, more scratch than the first
+    second = wl.varlen_prefill([500, 64], seed=22)         # longer, more scratch than the first
     for w in (first, second):
         ref = _prefill(w, noalloc=False)
         got = _prefill(w, noalloc=True)
@@ -76,7 +76,7 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
 def test_noalloc_refuses_a_problem_larger_than_its_scratch():
     w = wl.varlen_prefill([64], seed=23)
     dims = dev.dims_of(w.shape)
-    too_many = 8192  # 130 chunk slots of about 1 MiB each: more than the 64 MiB scratch
+    too_many = 8192  # 130 chunk slots of about 3.3 MiB each: more than the 64 MiB scratch
     assert gdn.gdn_prefill_workspace_bytes(dims, 1, too_many, too_many) > gdn.NOALLOC_SCRATCH_BYTES
     d = torch.device("cuda")
     h_pool, conv_pool, slots = dev.states_to(w, d)
