@@ -448,7 +448,7 @@ def main():
     ap.add_argument("--no-modes", action="store_true", help="skip the verify / prefill lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--profile", nargs="?", const="decode", default=None,
-                    choices=["decode", "verify", "verify-small", "prefill"],
+                    choices=["decode", "verify", "verify-small", "prefill", "mixed"],
                     help="only one timed loop of one mode (for profiler captures); "
                          "verify-small runs 32 sequences")
     args = ap.parse_args()
@@ -476,9 +476,11 @@ def main():
     gdn.lib()
 
     hbm_peak, tc_peak, peak_src = peaks()
-    if args.profile in ("verify", "verify-small", "prefill"):
+    if args.profile in ("verify", "verify-small", "prefill", "mixed"):
         if args.profile == "prefill":
             r = prefill_mode(device, args.steps, tc_peak, warmup=args.warmup)
+        elif args.profile == "mixed":
+            r = mixed_mode(device, args.steps, hbm_peak, tc_peak)
         else:
             r = verify_mode(device, args.steps, hbm_peak, warmup=args.warmup,
                             n=32 if args.profile == "verify-small" else N_SEQ)

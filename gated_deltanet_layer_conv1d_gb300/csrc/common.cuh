@@ -188,9 +188,10 @@ __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t by
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// Waits until every bulk group this thread committed has completed (writes performed).
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+// Waits until every bulk group this thread committed has finished reading its shared-memory
+// source (the writes to global memory complete on their own, before the grid does).
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // Ampere-style async copy global -> shared of 16 bytes (both 16-B aligned), L2 only.

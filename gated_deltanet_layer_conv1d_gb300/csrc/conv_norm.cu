@@ -6,6 +6,10 @@
 //   is a shuffle reduction over the lanes of that head (layer_struct.rs,
 //   conv1d_l2norm_f32_strided_k / conv1d_prefill_k).  Inputs before a sequence's first
 //   token come from its conv state, which this kernel only reads.
+// gdn_prefill_tiles_kernel: the same conv, SiLU and L2 norms for the tensor-core prefill,
+//   one CTA per (64-token chunk, 8 heads), each warp walking one head's tokens in order
+//   with the conv window in registers; rows go to the fp16 tile images of the workspace
+//   and the gates next to them.
 // gdn_conv_state_kernel: afterwards, each sequence's conv state becomes its last d_conv
 //   raw inputs (exact copies).  Running it as a second launch keeps every read of the
 //   old state ordered before the write of the new one.
@@ -96,47 +100,150 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const __grid_con
         const float r = (is_q ? p.q_scale : 1.f) * rsqrtf(ss + p.l2_eps);
         y.x *= r; y.y *= r; y.z *= r; y.w *= r;
       }
-      if (p.out_mode == 2) {
-        // prefill workspace: the channel's place in its 128B-swizzled [64][128] tile
-        const PrefillLayout lay{p.Hk, p.Hv};
-        const size_t cs = PrefillLayout::base(t0, seq) + size_t(pos / PrefillLayout::kC);
-        const int r = pos % PrefillLayout::kC;
-        const int c = qd * 4;
-        size_t off;
-        if (c < 2 * p.Hk * D) {
-          const int head = c / D, i = c % D;
-          off = (head < p.Hk ? lay.qk(cs, head, 1) : lay.qk(cs, head - p.Hk, 0)) +
-                tc::sw128_offset(PrefillLayout::kC, r, i);
-        } else {
-          const int c2 = c - 2 * p.Hk * D;
-          off = lay.v(cs, c2 / D) + tc::sw128_offset(PrefillLayout::kC, r, c2 % D);
-        }
-        // fp16 operand of the tensor-core chunk kernel
-        const __half2 lo = __floats2half2_rn(y.x, y.y), hi = __floats2half2_rn(y.z, y.w);
-        uint2 u;
-        u.x = *reinterpret_cast<const uint32_t*>(&lo);
-        u.y = *reinterpret_cast<const uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(p.workspace) + off) = u;
-      } else {
-        const size_t o = size_t(t) * p.conv_dim + qd * 4;
-        if (p.out_bf16) Act<__nv_bfloat16>::store4(reinterpret_cast<__nv_bfloat16*>(p.out) + o, y);
-        else *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) = y;
-      }
+      const size_t o = size_t(t) * p.conv_dim + qd * 4;
+      if (p.out_bf16) Act<__nv_bfloat16>::store4(reinterpret_cast<__nv_bfloat16*>(p.out) + o, y);
+      else *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) = y;
     }
   }
-  if (p.out_mode == 2) {
-    // log(alpha) and beta of this token for every value head
-    const PrefillLayout lay{p.Hk, p.Hv};
-    const size_t cs = PrefillLayout::base(t0, seq) + size_t(pos / PrefillLayout::kC);
-    const int r = pos % PrefillLayout::kC;
-    for (int h = threadIdx.x; h < p.Hv; h += kConvThreads) {
-      const size_t ro = size_t(t) * p.ab_stride + h;
-      const float av = A::to_f(reinterpret_cast<const T*>(p.a)[ro]);
-      const float bv = A::to_f(reinterpret_cast<const T*>(p.b)[ro]);
-      float* g = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(p.workspace) + lay.gate(cs, h));
-      g[r] = -expf(p.A_log[h]) * softplus_f(av + p.dt_bias[h]);
-      g[PrefillLayout::kC + r] = sigmoid_f(bv);
+}
+
+// Pre-pass of the tensor-core prefill (bf16 activations, d = 128).  One CTA per (chunk
+// slot, group of kTileWarps heads), heads numbered as the qkv channels are laid out: q heads,
+// then k heads, then v heads.  Warp w takes one head and walks the chunk's tokens in order;
+// lane l holds the conv window of channels 4l .. 4l+3 in registers, so every raw input is
+// read once (plus 3 halo rows per chunk).  q and k rows are L2-normalised (a shuffle sum
+// over the warp, q also scaled by q_scale) and every row lands in its fp16 tile image.  CTAs
+// whose group holds value heads also write log(alpha) and beta of those heads.
+constexpr int kTileWarps = 8;
+constexpr int kTileBatch = 8;  // tokens whose raw inputs are loaded ahead of their use
+
+__global__ void __launch_bounds__(kTileWarps * 32, 2)
+    gdn_prefill_tiles_kernel(const __grid_constant__ ConvParams p) {
+  using A = Act<__nv_bfloat16>;
+  constexpr int D = 128, kC = PrefillLayout::kC;
+  const int n_heads = 2 * p.Hk + p.Hv;
+  const int groups = (n_heads + kTileWarps - 1) / kTileWarps;
+  const int cs = blockIdx.x / groups, grp = blockIdx.x % groups;
+  int seq = 0;
+  {
+    int lo = 0, hi = p.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (PrefillLayout::base(p.cu_seqlens[mid], mid) <= size_t(cs)) lo = mid;
+      else hi = mid - 1;
     }
+    seq = lo;
+  }
+  const int t0 = p.cu_seqlens[seq], t1 = p.cu_seqlens[seq + 1];
+  if (t0 < 0 || t1 < t0 || t1 > p.total_tokens) {
+    if (threadIdx.x == 0) report(p.status, GDN_ERR_BAD_SEQLENS);
+    return;
+  }
+  const size_t slot0 = PrefillLayout::base(t0, seq);
+  const int len = t1 - t0, nc = (len + kC - 1) / kC;
+  if (size_t(cs) < slot0 || size_t(cs) - slot0 >= size_t(nc)) return;  // an unused slot
+  const int pos0 = int(size_t(cs) - slot0) * kC;
+  const int L = (len - pos0) < kC ? (len - pos0) : kC;
+  const int slot = p.slots[seq];
+  if (slot < 0 || slot >= p.n_slots) {
+    if (threadIdx.x == 0) report(p.status, GDN_ERR_BAD_SLOT);
+    return;
+  }
+  const PrefillLayout lay{p.Hk, p.Hv};
+  unsigned char* ws = reinterpret_cast<unsigned char*>(p.workspace);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int head = grp * kTileWarps + warp;
+
+  if (head < n_heads) {
+    const int c = head * D + lane * 4;  // first channel of this lane
+    size_t tile;
+    float scale = 0.f;  // 0: v (not normalised)
+    if (head < p.Hk) {
+      tile = lay.qk(cs, head, 1);
+      scale = p.q_scale;
+    } else if (head < 2 * p.Hk) {
+      tile = lay.qk(cs, head - p.Hk, 0);
+      scale = 1.f;
+    } else {
+      tile = lay.v(cs, head - 2 * p.Hk);
+    }
+    const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(p.qkv);
+    const __nv_bfloat16* cst =
+        reinterpret_cast<const __nv_bfloat16*>(p.conv_pool) + size_t(slot) * p.conv_dim * kW;
+    const float4 w0 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 0) * kW);
+    const float4 w1 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 1) * kW);
+    const float4 w2 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 2) * kW);
+    const float4 w3 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 3) * kW);
+    // window entries 0..2: sequence positions pos0 - 3 .. pos0 - 1
+    float4 win[kW - 1];
+#pragma unroll
+    for (int j = 0; j < kW - 1; ++j) {
+      const int sp = pos0 - (kW - 1) + j;
+      if (sp >= 0) {
+        win[j] = A::load4(qkv + size_t(t0 + sp) * p.qkv_stride + c);
+      } else {
+        win[j].x = A::to_f(cst[size_t(c + 0) * kW + kW + sp]);
+        win[j].y = A::to_f(cst[size_t(c + 1) * kW + kW + sp]);
+        win[j].z = A::to_f(cst[size_t(c + 2) * kW + kW + sp]);
+        win[j].w = A::to_f(cst[size_t(c + 3) * kW + kW + sp]);
+      }
+    }
+    // raw bf16 inputs of batch b + 1 are in flight while batch b is computed
+    const __nv_bfloat16* xrow = qkv + size_t(t0 + pos0) * p.qkv_stride + c;
+    auto load_batch = [&](int r0, uint2 (&raw)[kTileBatch]) {
+#pragma unroll
+      for (int u = 0; u < kTileBatch; ++u)
+        raw[u] = (r0 + u < L) ? *reinterpret_cast<const uint2*>(xrow + size_t(r0 + u) * p.qkv_stride)
+                              : make_uint2(0u, 0u);
+    };
+    uint2 cur[kTileBatch], nxt[kTileBatch];
+    load_batch(0, cur);
+    for (int r0 = 0; r0 < L; r0 += kTileBatch) {
+      if (r0 + kTileBatch < L) load_batch(r0 + kTileBatch, nxt);
+#pragma unroll
+      for (int u = 0; u < kTileBatch; ++u) {
+        const int r = r0 + u;
+        if (r >= L) break;
+        const float2 xa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&cur[u].x));
+        const float2 xb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&cur[u].y));
+        const float4 x = make_float4(xa.x, xa.y, xb.x, xb.y);
+        float4 y;
+        y.x = silu_fast(w0.x * win[0].x + w0.y * win[1].x + w0.z * win[2].x + w0.w * x.x);
+        y.y = silu_fast(w1.x * win[0].y + w1.y * win[1].y + w1.z * win[2].y + w1.w * x.y);
+        y.z = silu_fast(w2.x * win[0].z + w2.y * win[1].z + w2.z * win[2].z + w2.w * x.z);
+        y.w = silu_fast(w3.x * win[0].w + w3.y * win[1].w + w3.z * win[2].w + w3.w * x.w);
+        win[0] = win[1];
+        win[1] = win[2];
+        win[2] = x;
+        if (scale != 0.f) {
+          const float ss = warp_sum(y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w);
+          const float rn = scale * rsqrtf(ss + p.l2_eps);
+          y.x *= rn;
+          y.y *= rn;
+          y.z *= rn;
+          y.w *= rn;
+        }
+        const __half2 lo = __floats2half2_rn(y.x, y.y), hi = __floats2half2_rn(y.z, y.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(ws + tile + tc::sw128_offset(kC, r, lane * 4)) = pk;
+      }
+#pragma unroll
+      for (int u = 0; u < kTileBatch; ++u) cur[u] = nxt[u];
+    }
+  }
+  // log(alpha) and beta of this group's value heads
+  for (int idx = threadIdx.x; idx < kC * kTileWarps; idx += kTileWarps * 32) {
+    const int r = idx / kTileWarps, hh = grp * kTileWarps + idx % kTileWarps;
+    if (r >= L || hh < 2 * p.Hk || hh >= n_heads) continue;
+    const int h = hh - 2 * p.Hk;
+    const size_t ro = size_t(t0 + pos0 + r) * p.ab_stride + h;
+    const float av = A::to_f(reinterpret_cast<const __nv_bfloat16*>(p.a)[ro]);
+    const float bv = A::to_f(reinterpret_cast<const __nv_bfloat16*>(p.b)[ro]);
+    float* g = reinterpret_cast<float*>(ws + lay.gate(cs, h));
+    g[r] = -expf(p.A_log[h]) * softplus_f(av + p.dt_bias[h]);
+    g[kC + r] = sigmoid_f(bv);
   }
 }
 
@@ -219,8 +326,10 @@ cudaError_t launch_conv_step(const ConvParams& p, int dtype, cudaStream_t stream
 }
 
 cudaError_t launch_prefill_prep(const ConvParams& p, cudaStream_t stream) {
-  if (p.total_tokens > 0)
-    gdn_conv_kernel<__nv_bfloat16, 128><<<p.total_tokens, kConvThreads, 0, stream>>>(p);
+  if (p.total_tokens == 0 || p.n == 0) return cudaSuccess;
+  const int groups = (2 * p.Hk + p.Hv + kTileWarps - 1) / kTileWarps;
+  const size_t slots = PrefillLayout::slots(p.n, p.total_tokens);
+  gdn_prefill_tiles_kernel<<<unsigned(slots * groups), kTileWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

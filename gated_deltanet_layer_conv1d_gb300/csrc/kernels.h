@@ -58,8 +58,7 @@ struct ConvParams {
   void* out;
   int32_t out_bf16;
   int32_t* status;
-  // Chunked-prefill pre-pass only (out_mode == 2): gates and the workspace tiles.
-  int32_t out_mode;  // 0: f32 rows / 1: bf16 rows (out_bf16), 2: prefill workspace tiles
+  // Chunked-prefill pre-pass only: gates and the workspace tiles.
   const float* A_log;
   const float* dt_bias;
   const void* a;

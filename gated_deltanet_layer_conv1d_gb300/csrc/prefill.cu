@@ -41,7 +41,6 @@ cudaError_t launch_prefill(const PrefillParams& p, int dtype, cudaStream_t strea
     c.conv_pool = p.conv_pool;
     c.slots = p.slots;
     c.status = p.status;
-    c.out_mode = 2;
     c.A_log = p.A_log;
     c.dt_bias = p.dt_bias;
     c.a = p.a;

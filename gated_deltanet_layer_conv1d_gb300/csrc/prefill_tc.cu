@@ -24,8 +24,8 @@
 //   the 128 / NCOL slices run in separate CTAs).  Per chunk, two MMAs:
 //     MMA_a [Q;W] H0             (M 128 = 64 query rows + 64 W rows, N NCOL, K 128)
 //     MMA_b K~^T Delta and [P;*] Delta  (M 128, N NCOL, K 64; rows past P are ignored)
-//   with Delta and the new H written back as fp16 operands between them; it writes the
-//   core output O.  The next chunk's operands arrive by bulk copy into the other of two
+//   with Delta and the new H written back between them as fp16 MN-major operands (each
+//   thread stores its own row, 16 bytes at a time); it writes the core output O.  The next chunk's operands arrive by bulk copy into the other of two
 //   buffers meanwhile.  The gated RMSNorm of O follows as its own kernel.
 //
 // Operands are fp16 (kind::f16, f32 accumulation): every operand here is bounded
@@ -405,9 +405,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             __float2half_rn(v[u]);
       tc::ld16(tmem + tl + kTU + 32 * half, *reinterpret_cast<float(*)[16]>(v));
       tc::ld16(tmem + tl + kTU + 32 * half + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-      float* Ug = reinterpret_cast<float*>(ws + lay.u(cs, h));
+      // U column group q4 (= i / 32), row r, column i % 32 = lane, in its swizzled place
+      float* Ug = reinterpret_cast<float*>(ws + lay.u(cs, h)) + q4 * (kC * 32);
 #pragma unroll
-      for (int u = 0; u < 32; ++u) Ug[(32 * half + u) * kD + i] = v[u];
+      for (int u = 0; u < 32; ++u) {
+        const int r = 32 * half + u;
+        Ug[r * 32 + ((((lane >> 2) ^ (r & 7))) << 2) + (lane & 3)] = v[u];
+      }
     }
     for (int idx = tid; idx < kC * 16; idx += kPrepThreads) {
       const int blk = idx >> 9, row = (idx >> 3) & 63, c16 = idx & 7;
@@ -435,7 +439,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   } while (false);
 
   if (tid == 0) {
-    bulk_wait_all();
+    bulk_wait_read();  // the shared memory the stores read is released with the CTA
     if (bad) report(p.status, GDN_ERR_TIMEOUT);
   }
   tc::fence_before_sync();
@@ -458,12 +462,14 @@ struct SpineSmem {
   static constexpr uint32_t kGd = 57344;   // [64] f32 g
   static constexpr uint32_t kStage = 58368;
   static constexpr uint32_t kTx = 4 * 8192 + 8192 + 16384 + 256;  // bytes per fill
-  static constexpr uint32_t kHT = 2 * kStage;          // [NCOL][128] f16 H^T of the slice
-  static constexpr uint32_t kDT = kHT + NCOL * 256;    // [NCOL][64] f16 Delta^T
-  static constexpr uint32_t kMisc = kDT + NCOL * 128;  // bars, tmem slot
+  static constexpr uint32_t kHT = 2 * kStage;          // [128][NCOL] f16 H slice (MN-major B)
+  static constexpr uint32_t kDT = kHT + NCOL * 256;    // [64][NCOL] f16 Delta (MN-major B)
+  static constexpr uint32_t kUs = kDT + NCOL * 128;    // [NCOL / 32][64][32] f32 U (swizzled)
+  static constexpr uint32_t kMisc = kUs + NCOL * 256;  // bars, tmem slot
   static constexpr uint32_t kBytes = kMisc + 64;
   static constexpr uint32_t kAlloc = kBytes + 1024;
-  static constexpr uint32_t kTmemCols = NCOL == 32 ? 128 : (NCOL == 64 ? 256 : 512);
+  static constexpr uint32_t kTmemCols = NCOL == 64 ? 256 : 512;
+  static_assert(NCOL == 64 || NCOL == 128, "whole 64-column blocks of the MN-major operands");
 };
 
 template <int NCOL>
@@ -494,7 +500,8 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
   const uint32_t sb = smem_u32(sm);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::kMisc);  // [2]
   uint64_t* bar_mma = full + 2;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_mma + 1);
+  uint64_t* ufull = full + 3;  // U of the current chunk
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(ufull + 1);
 
   const PrefillLayout lay{p.Hk, p.Hv};
   const unsigned char* ws = reinterpret_cast<const unsigned char*>(p.workspace);
@@ -504,6 +511,7 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
     mbar_init(bar_mma, 1);
+    mbar_init(ufull, 1);
     fence_mbar_init();
   }
   if (warp == 0) tc::alloc(tslot, S::kTmemCols);
@@ -522,11 +530,12 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     Hr[u + 2] = x.z;
     Hr[u + 3] = x.w;
   }
+  // fp16 H rows as the MN-major B operand of MMA_a: [K = i][N = j] in 64-column blocks
   auto write_HT = [&]() {
 #pragma unroll
-    for (int u = 0; u < 32; ++u)
-      *reinterpret_cast<__half*>(sm + S::kHT + tc::sw128_offset(NCOL, jl0 + u, row)) =
-          __float2half_rn(Hr[u]);
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(sm + S::kHT + tc::sw128_offset(128, row, jl0 + 8 * q)) =
+          pack8_h(Hr + 8 * q);
   };
   write_HT();
   fence_proxy_async_smem();
@@ -552,8 +561,18 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     bulk_g2s(st + S::kKt, ws + lay.kt(cs, h), 16384, &full[c & 1]);
     bulk_g2s(st + S::kGd, ws + lay.g(cs, h), 256, &full[c & 1]);
   };
-  if (tid == kIssuer) issue_loads(0);
-  int issued = 0;  // last chunk whose loads were issued (meaningful in kIssuer)
+  // Chunk c's U columns of this slice into the single U buffer (completing on ufull).
+  auto issue_u = [&](int c) {
+    mbar_arrive_expect_tx(ufull, NCOL * 256);
+    bulk_g2s(sm + S::kUs, ws + lay.u(slot0 + size_t(c), h) + size_t(slice) * NCOL * 256,
+             NCOL * 256, ufull);
+  };
+  if (tid == kIssuer) {
+    issue_loads(0);
+    issue_u(0);
+  }
+  int issued = 0;    // last chunk whose loads were issued (meaningful in kIssuer)
+  int u_issued = 0;  // ... and whose U was
 
   uint32_t mma_phase = 0;
   bool bad = false;
@@ -576,35 +595,9 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     const int L = (len - t0) < kC ? (len - t0) : kC;
     const size_t cs = slot0 + size_t(c);
     const uint32_t st = uint32_t(c & 1) * S::kStage;
-    // The other buffer was last read by chunk c - 1's MMAs (complete) and by this CTA's
-    // threads before the last barrier: refill it for chunk c + 1.
-    if (tid == kIssuer && c + 1 < nc) {
-      issue_loads(c + 1);
-      issued = c + 1;
-    }
     bad |= !mbar_wait_bounded(&full[c & 1], uint32_t(c >> 1) & 1u);
     consumed = c;
     const float* gd = reinterpret_cast<const float*>(sm + st + S::kGd);
-
-    // U rows of this thread (W-row lanes 64..127), read ahead of the MMA
-    float X[32];
-    if (q4 >= 2) {
-      const int r = row - kC;
-      if (r < L) {
-        const float* Ug = reinterpret_cast<const float*>(ws + lay.u(cs, h)) + r * kD + col0;
-#pragma unroll
-        for (int u = 0; u < 32; u += 4) {
-          const float4 x = *reinterpret_cast<const float4*>(Ug + u);
-          X[u] = x.x;
-          X[u + 1] = x.y;
-          X[u + 2] = x.z;
-          X[u + 3] = x.w;
-        }
-      } else {
-#pragma unroll
-        for (int u = 0; u < 32; ++u) X[u] = 0.f;
-      }
-    }
 
     // ---- MMA_a: [Q;W] H0
     if (tid == kIssuer) {
@@ -612,25 +605,45 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
 #pragma unroll
         for (int k0 = 0; k0 < kD; k0 += 16)
           tc::mma_f16(tmem + kTA, tc::desc_at(sb + st + S::kQW, 128, k0),
-                       tc::desc_at(sb + S::kHT, NCOL, k0), tc::idesc_f16(128, NCOL), k0 > 0);
+                       tc::desc_mn_sw128(sb + S::kHT + k0 * 128, 16384),
+                       tc::idesc_f16(128, NCOL, false, true), k0 > 0);
       }
       tc::commit(bar_mma);
+      // The other buffer was last read by chunk c - 1's MMAs (complete) and by this CTA's
+      // threads before the last barrier: refill it for chunk c + 1.
+      if (c + 1 < nc) {
+        issue_loads(c + 1);
+        issued = c + 1;
+      }
     }
     mma_wait();
 
     // ---- Delta = U - W H0 (fp16 Delta^T for MMA_b); the Q H0 rows stay in registers
     float eg = 0.f;
     const float eL = exp2_fast(gd[kC - 1]);
+    float X[32];
     {
       float v[32];
       tc::ld16(tmem + tl + kTA + jl0, *reinterpret_cast<float(*)[16]>(v));
       tc::ld16(tmem + tl + kTA + jl0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
       if (q4 >= 2) {
         const int r = row - kC;
+        bad |= !mbar_wait_bounded(ufull, uint32_t(c) & 1u);
+        const float* Us = reinterpret_cast<const float*>(sm + S::kUs) + cg * (kC * 32) + r * 32;
 #pragma unroll
-        for (int u = 0; u < 32; ++u)
-          *reinterpret_cast<__half*>(sm + S::kDT + tc::sw128_offset(NCOL, jl0 + u, r)) =
-              __float2half_rn(X[u] - v[u]);
+        for (int k = 0; k < 8; ++k) {
+          const float4 x = *reinterpret_cast<const float4*>(Us + ((k ^ (r & 7)) << 2));
+          X[4 * k] = x.x;
+          X[4 * k + 1] = x.y;
+          X[4 * k + 2] = x.z;
+          X[4 * k + 3] = x.w;
+        }
+#pragma unroll
+        for (int u = 0; u < 32; ++u) v[u] = X[u] - v[u];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(sm + S::kDT + tc::sw128_offset(64, r, jl0 + 8 * q)) =
+              pack8_h(v + 8 * q);
       } else {
 #pragma unroll
         for (int u = 0; u < 32; ++u) X[u] = v[u];
@@ -644,13 +657,18 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     if (tid == kIssuer) {
 #pragma unroll
       for (int s0 = 0; s0 < kC; s0 += 16) {
-        tc::mma_f16(tmem + kTH, tc::desc_mn_sw128(sb + st + S::kKt + s0 * 128, 8192),
-                     tc::desc_at(sb + S::kDT, NCOL, s0), tc::idesc_f16(128, NCOL, true, false),
-                     s0 > 0);
-        tc::mma_f16(tmem + kTO, tc::desc_at(sb + st + S::kP, 128, s0),
-                     tc::desc_at(sb + S::kDT, NCOL, s0), tc::idesc_f16(128, NCOL), s0 > 0);
+        const uint64_t bd = tc::desc_mn_sw128(sb + S::kDT + s0 * 128, 8192);
+        tc::mma_f16(tmem + kTH, tc::desc_mn_sw128(sb + st + S::kKt + s0 * 128, 8192), bd,
+                     tc::idesc_f16(128, NCOL, true, true), s0 > 0);
+        tc::mma_f16(tmem + kTO, tc::desc_at(sb + st + S::kP, 128, s0), bd,
+                     tc::idesc_f16(128, NCOL, false, true), s0 > 0);
       }
       tc::commit(bar_mma);
+      // this chunk's U has been read (before the barrier): fetch the next chunk's
+      if (c + 1 < nc) {
+        issue_u(c + 1);
+        u_issued = c + 1;
+      }
     }
     mma_wait();
 
@@ -685,8 +703,9 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
   if (aborted) {
     if (tid == kIssuer) {
       report(p.status, GDN_ERR_TIMEOUT);
-      // a fill still in flight lands before this CTA's shared memory is released
+      // fills still in flight land before this CTA's shared memory is released
       if (issued > consumed) mbar_wait_bounded(&full[issued & 1], uint32_t(issued >> 1) & 1u);
+      if (u_issued > consumed) mbar_wait_bounded(ufull, uint32_t(u_issued) & 1u);
     }
   } else {
 #pragma unroll
@@ -728,7 +747,6 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
   // Column slices per (sequence, head): as many as one wave of CTAs holds, since the
   // spine's time is its chain of chunks, not its arithmetic.
   const int units = p.n * p.Hv, sms = sm_count();
-  if (units * 4 <= sms) return launch_spine<32>(p, stream);
   if (units * 2 <= sms) return launch_spine<64>(p, stream);
   return launch_spine<128>(p, stream);
 }
