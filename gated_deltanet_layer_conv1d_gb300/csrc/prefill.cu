@@ -13,7 +13,7 @@
 namespace gdn {
 
 cudaError_t launch_prefill_sequential(const PrefillParams& p, int dtype, cudaStream_t stream);
-cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillParams& p, float* o_work, cudaStream_t stream);
 
 size_t prefill_workspace_bytes(int Hk, int Hv, int D, int n, int total_tokens, int max_seqlen) {
   (void)max_seqlen;
@@ -49,16 +49,9 @@ cudaError_t launch_prefill(const PrefillParams& p, int dtype, cudaStream_t strea
     c.workspace = p.workspace;
     cudaError_t e = launch_prefill_prep(c, stream);
     if (e != cudaSuccess) return e;
-    // The spine writes the core output into the caller's buffer, else into the workspace.
-    PrefillParams q = p;
-    if (!q.core_out)
-      q.core_out = reinterpret_cast<float*>(
-          static_cast<unsigned char*>(p.workspace) +
-          PrefillLayout{p.Hk, p.Hv}.o_offset(p.n, p.total_tokens));
-    e = launch_prefill_tc(q, stream);
-    if (e != cudaSuccess) return e;
-    return launch_gated_rmsnorm(q.core_out, p.z, p.z_stride, p.norm_w, p.norm_eps,
-                                p.total_tokens, p.Hv, p.D, GDN_DTYPE_BF16, p.y, stream);
+    float* o_work = reinterpret_cast<float*>(static_cast<unsigned char*>(p.workspace) +
+                                             PrefillLayout{p.Hk, p.Hv}.o_offset(p.n, p.total_tokens));
+    return launch_prefill_tc(p, o_work, stream);
   }
   return launch_prefill_sequential(p, dtype, stream);
 }

@@ -465,7 +465,12 @@ struct SpineSmem {
   static constexpr uint32_t kHT = 2 * kStage;          // [128][NCOL] f16 H slice (MN-major B)
   static constexpr uint32_t kDT = kHT + NCOL * 256;    // [64][NCOL] f16 Delta (MN-major B)
   static constexpr uint32_t kUs = kDT + NCOL * 128;    // [NCOL / 32][64][32] f32 U (swizzled)
-  static constexpr uint32_t kMisc = kUs + NCOL * 256;  // bars, tmem slot
+  // Gated norm in the spine (whole rows, NCOL = 128 only):
+  static constexpr bool kNorm = NCOL == 128;
+  static constexpr uint32_t kZ = kUs + NCOL * 256;     // [64][128] bf16 z rows (swizzled)
+  static constexpr uint32_t kRed = kZ + (kNorm ? 16384 : 0);   // [4][64] f32 partial sums
+  static constexpr uint32_t kNW = kRed + (kNorm ? 1024 : 0);   // [128] f32 norm weight
+  static constexpr uint32_t kMisc = kNW + (kNorm ? 512 : 0);   // bars, tmem slot
   static constexpr uint32_t kBytes = kMisc + 64;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static constexpr uint32_t kTmemCols = NCOL == 64 ? 256 : 512;
@@ -477,7 +482,9 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     gdn_prefill_spine_kernel(const __grid_constant__ PrefillParams p) {
   using S = SpineSmem<NCOL>;
   constexpr int kNS = kD / NCOL;  // slices per head
-  constexpr int kIssuer = 64;     // warp 2, lane 0: not one of the output warps
+  constexpr int kIssuer = 64;     // warp 2, lane 0: issues the MMAs
+  constexpr int kLoader = 96;     // warp 3, lane 0: issues the bulk copies
+  // (neither is in an output warp, whose work trails the chain)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int slice = blockIdx.x % kNS, unit = blockIdx.x / kNS;
   const int seq = unit / p.Hv, h = unit % p.Hv, kh = h / p.G;
@@ -538,6 +545,7 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
           pack8_h(Hr + 8 * q);
   };
   write_HT();
+  if (S::kNorm && tid < kD) reinterpret_cast<float*>(sm + S::kNW)[tid] = p.norm_w[tid];
   fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
@@ -567,12 +575,26 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     bulk_g2s(sm + S::kUs, ws + lay.u(slot0 + size_t(c), h) + size_t(slice) * NCOL * 256,
              NCOL * 256, ufull);
   };
-  if (tid == kIssuer) {
+  if (tid == kLoader) {
     issue_loads(0);
     issue_u(0);
   }
-  int issued = 0;    // last chunk whose loads were issued (meaningful in kIssuer)
+  int issued = 0;    // last chunk whose loads were issued (meaningful in kLoader)
   int u_issued = 0;  // ... and whose U was
+  // The z rows of chunk c (bf16, this head's 128 columns; 16-byte piece k of row r at
+  // k ^ (r % 16)): each output thread copies its own 64 bytes.
+  const __nv_bfloat16* zg = reinterpret_cast<const __nv_bfloat16*>(p.z);
+  auto issue_z = [&](int c) {
+    const int r = row, t0 = c * kC;
+    if (r < ((len - t0) < kC ? (len - t0) : kC)) {
+      const unsigned char* src = reinterpret_cast<const unsigned char*>(
+          zg + size_t(t_begin + t0 + r) * p.z_stride + size_t(h) * kD + jl0);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        cp_async16(sm + S::kZ + r * 256 + (((cg * 4 + k) ^ (r & 15)) << 4), src + 16 * k);
+    }
+    cp_async_commit();
+  };
 
   uint32_t mma_phase = 0;
   bool bad = false;
@@ -593,8 +615,14 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
   for (int c = 0; c < nc; ++c) {
     const int t0 = c * kC;
     const int L = (len - t0) < kC ? (len - t0) : kC;
-    const size_t cs = slot0 + size_t(c);
     const uint32_t st = uint32_t(c & 1) * S::kStage;
+    // The other buffer was last read by chunk c - 1's MMAs (complete) and by this CTA's
+    // threads before the last barrier: refill it for chunk c + 1.
+    if (tid == kLoader && c + 1 < nc) {
+      issue_loads(c + 1);
+      issued = c + 1;
+    }
+    if (S::kNorm && q4 < 2) issue_z(c);
     bad |= !mbar_wait_bounded(&full[c & 1], uint32_t(c >> 1) & 1u);
     consumed = c;
     const float* gd = reinterpret_cast<const float*>(sm + st + S::kGd);
@@ -609,12 +637,6 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
                        tc::idesc_f16(128, NCOL, false, true), k0 > 0);
       }
       tc::commit(bar_mma);
-      // The other buffer was last read by chunk c - 1's MMAs (complete) and by this CTA's
-      // threads before the last barrier: refill it for chunk c + 1.
-      if (c + 1 < nc) {
-        issue_loads(c + 1);
-        issued = c + 1;
-      }
     }
     mma_wait();
 
@@ -664,11 +686,11 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
                      tc::idesc_f16(128, NCOL, false, true), s0 > 0);
       }
       tc::commit(bar_mma);
-      // this chunk's U has been read (before the barrier): fetch the next chunk's
-      if (c + 1 < nc) {
-        issue_u(c + 1);
-        u_issued = c + 1;
-      }
+    }
+    // this chunk's U has been read (before the barrier): fetch the next chunk's
+    if (tid == kLoader && c + 1 < nc) {
+      issue_u(c + 1);
+      u_issued = c + 1;
     }
     mma_wait();
 
@@ -689,19 +711,53 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
       float v[32];
       tc::ld16(tmem + tl + kTO + jl0, *reinterpret_cast<float(*)[16]>(v));
       tc::ld16(tmem + tl + kTO + jl0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-      if (row < L) {
-        float* o = p.core_out + (size_t(t_begin + t0 + row) * p.Hv + h) * kD + col0;
+#pragma unroll
+      for (int u = 0; u < 32; ++u) v[u] = eg * X[u] + v[u];
+      const size_t orow = size_t(t_begin + t0 + row) * p.Hv + h;
+      if (p.core_out && row < L) {
+        float* o = p.core_out + orow * kD + col0;
 #pragma unroll
         for (int u = 0; u < 32; u += 4)
-          *reinterpret_cast<float4*>(o + u) =
-              make_float4(eg * X[u] + v[u], eg * X[u + 1] + v[u + 1], eg * X[u + 2] + v[u + 2],
-                          eg * X[u + 3] + v[u + 3]);
+          *reinterpret_cast<float4*>(o + u) = make_float4(v[u], v[u + 1], v[u + 2], v[u + 3]);
+      }
+      if constexpr (S::kNorm) {
+        // y = O / rms(O) * w * silu(z), the row's sum of squares over the 4 column groups
+        float* red = reinterpret_cast<float*>(sm + S::kRed);
+        const float* nw = reinterpret_cast<const float*>(sm + S::kNW) + jl0;
+        float ss = 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) ss += v[u] * v[u];
+        red[cg * kC + row] = ss;
+        named_sync(1, 8 * 32);
+        ss = red[row] + red[kC + row] + red[2 * kC + row] + red[3 * kC + row];
+        const float inv = rsqrtf(ss / float(kD) + p.norm_eps);
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        if (row < L) {
+          __nv_bfloat16* yo = reinterpret_cast<__nv_bfloat16*>(p.y) + orow * kD + jl0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 zr = *reinterpret_cast<const uint4*>(
+                sm + S::kZ + row * 256 + (((cg * 4 + k) ^ (row & 15)) << 4));
+            const __nv_bfloat162* z2 = reinterpret_cast<const __nv_bfloat162*>(&zr);
+            uint32_t out[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 zf = __bfloat1622float2(z2[e]);
+              const int u = 8 * k + 2 * e;
+              const __nv_bfloat162 yy = __floats2bfloat162_rn(
+                  v[u] * inv * nw[u] * silu_fast(zf.x), v[u + 1] * inv * nw[u + 1] * silu_fast(zf.y));
+              out[e] = *reinterpret_cast<const uint32_t*>(&yy);
+            }
+            *reinterpret_cast<uint4*>(yo + 8 * k) = make_uint4(out[0], out[1], out[2], out[3]);
+          }
+        }
       }
     }
   }
+  if (S::kNorm) asm volatile("cp.async.wait_group 0;" ::: "memory");
 
   if (aborted) {
-    if (tid == kIssuer) {
+    if (tid == kLoader) {
       report(p.status, GDN_ERR_TIMEOUT);
       // fills still in flight land before this CTA's shared memory is released
       if (issued > consumed) mbar_wait_bounded(&full[issued & 1], uint32_t(issued >> 1) & 1u);
@@ -730,9 +786,9 @@ cudaError_t launch_spine(const PrefillParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-// Chunk kernel, then the spine; p.core_out must point at the f32 [total_tokens][Hv][128]
-// core output the spine writes.
-cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
+// Chunk kernel, the spine and the gated norm.  o_work: f32 [total_tokens][Hv][128] room for
+// the core output when the caller passes none and the norm runs as its own kernel.
+cudaError_t launch_prefill_tc(const PrefillParams& p, float* o_work, cudaStream_t stream) {
   if (p.n <= 0) return cudaSuccess;
   {
     auto kern = gdn_prefill_chunk_kernel;
@@ -746,9 +802,17 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
   }
   // Column slices per (sequence, head): as many as one wave of CTAs holds, since the
   // spine's time is its chain of chunks, not its arithmetic.
+  // A whole-row spine (128 columns) applies the gated norm itself; two column slices per
+  // head double the CTAs when one wave would otherwise leave SMs idle, and leave the norm
+  // to its own kernel.
   const int units = p.n * p.Hv, sms = sm_count();
-  if (units * 2 <= sms) return launch_spine<64>(p, stream);
-  return launch_spine<128>(p, stream);
+  if (units * 2 > sms) return launch_spine<128>(p, stream);
+  PrefillParams q = p;
+  if (!q.core_out) q.core_out = o_work;
+  cudaError_t e = launch_spine<64>(q, stream);
+  if (e != cudaSuccess) return e;
+  return launch_gated_rmsnorm(q.core_out, p.z, p.z_stride, p.norm_w, p.norm_eps,
+                              p.total_tokens, p.Hv, kD, GDN_DTYPE_BF16, p.y, stream);
 }
 
 }  // namespace gdn
