@@ -93,34 +93,38 @@ constexpr int kPrepThreads = 256;
 
 struct PrepSmem {
   static constexpr uint32_t kAQK = 0;        // [128][128] f16: rows 0-63 k_hat, 64-127 q_hat;
-                                             // later K~ in the k rows, P in q block 0
+                                             // later K~ in the k rows, P in q block 0 and,
+                                             // once P is out, v in the two q blocks
   static constexpr uint32_t kP = 8192;       // [64][64] f16 P (q block 0, dead after MMA0)
-  static constexpr uint32_t kV = 32768;      // [64][128] f16 v (MN-major A of MMA_U)
+  static constexpr uint32_t kV = 8192;       // v, MN-major A of MMA_U: column blocks at
+                                             // 8192 and 24576 (16384 apart)
   static constexpr int kAS = 65;             // row stride of A: odd, so column writes from
                                              // 32 lanes hit 32 banks
-  static constexpr uint32_t kAm = 49152;     // [64][65] f32 A
+  static constexpr uint32_t kAm = 32768;     // [64][65] f32 A
   static constexpr uint32_t kTw = kAm;       // [64][64] f16 T diag(beta e^g) (A is dead)
   static constexpr uint32_t kTu = kAm + 8192;  // [64][64] f16 T diag(beta)
-  static constexpr uint32_t kTf = 66560;     // [64][64] f32 T
+  static constexpr uint32_t kTf = 50176;     // [64][64] f32 T
   static constexpr uint32_t kWi = kTf;       // [64][128] f16 W image (T is dead)
-  static constexpr uint32_t kY = 82944;      // [3][16][16] f32 scratch of the inverse
-  static constexpr uint32_t kGate = 86016;   // [2][64] f32 log(alpha), beta (bulk copied)
-  static constexpr uint32_t kG = 86528;      // [64] f32 cumulative log2 decay g
-  static constexpr uint32_t kB = 86784;      // [64] f32 beta (0 past the chunk end)
-  static constexpr uint32_t kMisc = 87040;   // bars, tmem slot, scan carry
-  static constexpr uint32_t kBytes = 87168;
+  static constexpr uint32_t kY = 66560;      // [3][16][16] f32 scratch of the inverse
+  static constexpr uint32_t kGate = 69632;   // [2][64] f32 log(alpha), beta (bulk copied)
+  static constexpr uint32_t kG = 70144;      // [64] f32 cumulative log2 decay g
+  static constexpr uint32_t kB = 70400;      // [64] f32 beta (0 past the chunk end)
+  static constexpr uint32_t kMisc = 70656;   // bars, tmem slot, scan carry
+  static constexpr uint32_t kBytes = 70784;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024
 };
 static_assert(PrepSmem::kAm + 64 * PrepSmem::kAS * 4 <= PrepSmem::kTf, "A fits");
 static_assert(PrepSmem::kTf + 64 * 64 * 4 <= PrepSmem::kY, "T fits");
 static_assert(PrepSmem::kY + 3 * 256 * 4 <= PrepSmem::kGate, "inverse scratch fits");
 
-// TMEM columns of the chunk kernel (256 allocated, so two CTAs share an SM).
+// TMEM columns of the chunk kernel (128 allocated, so three CTAs share an SM); MMA_W
+// reuses MMA0's columns, which are read before it is issued.
 constexpr uint32_t kT0 = 0;     // MMA0: [K;Q] K^T   (64 cols)
-constexpr uint32_t kTW = 64;    // MMA_W: W^T        (64)
-constexpr uint32_t kTU = 128;   // MMA_U: U^T        (64)
+constexpr uint32_t kTW = 0;     // MMA_W: W^T        (64)
+constexpr uint32_t kTU = 64;    // MMA_U: U^T        (64)
+constexpr uint32_t kPrepTmem = 128;
 
-__global__ void __launch_bounds__(kPrepThreads, 2)
+__global__ void __launch_bounds__(kPrepThreads, 3)
     gdn_prefill_chunk_kernel(const __grid_constant__ PrefillParams p) {
   using S = PrepSmem;
   const int cs = blockIdx.x / p.Hv, h = blockIdx.x % p.Hv, kh = h / p.G;
@@ -173,7 +177,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     mbar_init(bar_mma, 1);
     fence_mbar_init();
   }
-  if (warp == 0) tc::alloc(tslot, 256);
+  if (warp == 0) tc::alloc(tslot, kPrepTmem);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -181,12 +185,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   if (tid == 0) {
     const unsigned char* kimg = ws + lay.qk(cs, kh, 0);
     const unsigned char* qimg = ws + lay.qk(cs, kh, 1);
-    mbar_arrive_expect_tx(bar_load, 3u * 16384u + 512u);
+    mbar_arrive_expect_tx(bar_load, 2u * 16384u + 512u);
     bulk_g2s(sm + S::kAQK, kimg, 8192, bar_load);
     bulk_g2s(sm + S::kAQK + 16384, kimg + 8192, 8192, bar_load);
     bulk_g2s(sm + S::kAQK + 8192, qimg, 8192, bar_load);
     bulk_g2s(sm + S::kAQK + 24576, qimg + 8192, 8192, bar_load);
-    bulk_g2s(sm + S::kV, ws + lay.v(cs, h), 16384, bar_load);
     bulk_g2s(gate, ws + lay.gate(cs, h), 512, bar_load);
   }
   const int q4 = warp & 3, half = warp >> 2;
@@ -205,6 +208,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     return stop;
   };
 
+  bool v_issued = false;  // (thread 128)
   do {
     // ---- rows past the end of the sequence are zero; decay prefix sums
     if (L < kC) {
@@ -214,7 +218,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         *reinterpret_cast<uint4*>(sm + S::kAQK + blk * 16384 + row * 128 + c16 * 16) = zero;
         *reinterpret_cast<uint4*>(sm + S::kAQK + blk * 16384 + (kC + row) * 128 + c16 * 16) =
             zero;
-        *reinterpret_cast<uint4*>(sm + S::kV + blk * 8192 + row * 128 + c16 * 16) = zero;
       }
     }
     if (tid < kC) {
@@ -278,9 +281,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     }
     fence_proxy_async_smem();
     if (sync_or_stop()) break;
-    if (tid == 0) {
+    // P goes out; once it has been read, v comes into the q blocks (MMA0 is done with them)
+    if (tid == 128) {
+      v_issued = true;
       bulk_s2g(ws + lay.p(cs, h), sm + S::kP, 8192);
       bulk_commit();
+      bulk_wait_read();
+      mbar_arrive_expect_tx(bar_load, 16384u);
+      bulk_g2s(sm + S::kV, ws + lay.v(cs, h), 8192, bar_load);
+      bulk_g2s(sm + S::kV + 16384, ws + lay.v(cs, h) + 8192, 8192, bar_load);
     }
 
     // ---- T = (I + A)^{-1}: diagonal 16 x 16 blocks, then the blocks below them
@@ -360,6 +369,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       }
       __syncthreads();
     }
+    // v has arrived; its rows past the end of the sequence are zero
+    bad |= !mbar_wait_bounded(bar_load, 1);
+    if (L < kC) {
+      const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+      for (int idx = tid; idx < (kC - L) * 16; idx += kPrepThreads) {
+        const int row = L + idx / 16, ch = idx % 16, blk = ch / 8, c16 = ch % 8;
+        *reinterpret_cast<uint4*>(sm + S::kV + blk * 16384 + row * 128 + c16 * 16) = zero;
+      }
+    }
     // T diag(beta e^g) and T diag(beta), fp16, [r][s] (over A, which is dead now)
     for (int cid = tid; cid < kC * 8; cid += kPrepThreads) {
       const int r = cid / 8, s0 = (cid % 8) * 8;
@@ -383,7 +401,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         tc::mma_f16(tmem + kTW, tc::desc_mn_sw128(sb + S::kAQK + s0 * 128, 16384),
                      tc::desc_at(sb + S::kTw, 64, s0), tc::idesc_f16(128, 64, true, false),
                      s0 > 0);
-        tc::mma_f16(tmem + kTU, tc::desc_mn_sw128(sb + S::kV + s0 * 128, 8192),
+        tc::mma_f16(tmem + kTU, tc::desc_mn_sw128(sb + S::kV + s0 * 128, 16384),
                      tc::desc_at(sb + S::kTu, 64, s0), tc::idesc_f16(128, 64, true, false),
                      s0 > 0);
       }
@@ -442,9 +460,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     bulk_wait_read();  // the shared memory the stores read is released with the CTA
     if (bad) report(p.status, GDN_ERR_TIMEOUT);
   }
+  // after a stop, the v copy still lands before the shared memory is released
+  if (tid == 128 && v_issued) mbar_wait_bounded(bar_load, 1);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::dealloc(tmem, 256);
+  if (warp == 0) tc::dealloc(tmem, kPrepTmem);
 }
 
 // ------------------------------------------------------------------------------------
