@@ -7,9 +7,10 @@
 //   conv1d_l2norm_f32_strided_k / conv1d_prefill_k).  Inputs before a sequence's first
 //   token come from its conv state, which this kernel only reads.
 // gdn_prefill_tiles_kernel: the same conv, SiLU and L2 norms for the tensor-core prefill,
-//   one CTA per (64-token chunk, 8 heads), each warp walking one head's tokens in order
-//   with the conv window in registers; rows go to the fp16 tile images of the workspace
-//   and the gates next to them.
+//   one CTA per (half of a 64-token chunk, 8 heads): the raw rows arrive in shared memory
+//   by bulk copies, then each warp walks one head's tokens in order with the conv window
+//   in registers; rows go to the fp16 tile images of the workspace and the gates next to
+//   them.
 // gdn_conv_state_kernel: afterwards, each sequence's conv state becomes its last d_conv
 //   raw inputs (exact copies).  Running it as a second launch keeps every read of the
 //   old state ordered before the write of the new one.
@@ -108,22 +109,27 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const __grid_con
 }
 
 // Pre-pass of the tensor-core prefill (bf16 activations, d = 128).  One CTA per (chunk
-// slot, group of kTileWarps heads), heads numbered as the qkv channels are laid out: q heads,
-// then k heads, then v heads.  Warp w takes one head and walks the chunk's tokens in order;
-// lane l holds the conv window of channels 4l .. 4l+3 in registers, so every raw input is
-// read once (plus 3 halo rows per chunk).  q and k rows are L2-normalised (a shuffle sum
-// over the warp, q also scaled by q_scale) and every row lands in its fp16 tile image.  CTAs
-// whose group holds value heads also write log(alpha) and beta of those heads.
+// slot, half of the chunk, group of kTileWarps heads), heads numbered as the qkv channels
+// are laid out: q heads, then k heads, then v heads.  The CTA's 32 rows of the group's raw
+// channels, and the 3 rows before them, arrive in shared memory by one bulk copy per row,
+// all issued at once; then warp w walks head w's rows in order with the conv window of its
+// lane's 4 channels in registers.  q and k rows are L2-normalised (a shuffle sum over the
+// warp, q also scaled by q_scale) and every row lands in its fp16 tile image.  CTAs whose
+// group holds value heads also write log(alpha) and beta of those heads.
 constexpr int kTileWarps = 8;
-constexpr int kTileBatch = 8;  // tokens whose raw inputs are loaded ahead of their use
+constexpr int kTileRows = 32;  // rows per CTA: half a chunk
+constexpr uint32_t kTileRowBytes = kTileWarps * 128 * 2;
+constexpr uint32_t kTileSmem = (kTileRows + kW - 1) * kTileRowBytes + 16;  // rows + mbarrier
 
-__global__ void __launch_bounds__(kTileWarps * 32, 2)
+__global__ void __launch_bounds__(kTileWarps * 32)
     gdn_prefill_tiles_kernel(const __grid_constant__ ConvParams p) {
   using A = Act<__nv_bfloat16>;
   constexpr int D = 128, kC = PrefillLayout::kC;
+  extern __shared__ __align__(16) unsigned char tsm[];
   const int n_heads = 2 * p.Hk + p.Hv;
   const int groups = (n_heads + kTileWarps - 1) / kTileWarps;
-  const int cs = blockIdx.x / groups, grp = blockIdx.x % groups;
+  const int grp = blockIdx.x % groups, hf = (blockIdx.x / groups) & 1;
+  const int cs = blockIdx.x / (2 * groups);
   int seq = 0;
   {
     int lo = 0, hi = p.n - 1;
@@ -144,99 +150,43 @@ __global__ void __launch_bounds__(kTileWarps * 32, 2)
   if (size_t(cs) < slot0 || size_t(cs) - slot0 >= size_t(nc)) return;  // an unused slot
   const int pos0 = int(size_t(cs) - slot0) * kC;
   const int L = (len - pos0) < kC ? (len - pos0) : kC;
+  const int r_begin = hf * kTileRows;
+  if (r_begin >= L) return;  // a short last chunk has no second half
+  const int nrows = (L - r_begin) < kTileRows ? (L - r_begin) : kTileRows;
   const int slot = p.slots[seq];
   if (slot < 0 || slot >= p.n_slots) {
     if (threadIdx.x == 0) report(p.status, GDN_ERR_BAD_SLOT);
     return;
+  }
+  const int nh = (n_heads - grp * kTileWarps) < kTileWarps ? (n_heads - grp * kTileWarps)
+                                                          : kTileWarps;
+  const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(p.qkv);
+  // shared row j holds sequence position pos0 + r_begin - 3 + j (j < nrows + 3)
+  const int p_first = pos0 + r_begin - (kW - 1);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(tsm + (kTileRows + kW - 1) * kTileRowBytes);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int j0 = p_first < 0 ? -p_first : 0;  // rows before the sequence: conv state
+    const uint32_t bytes = uint32_t(nh) * D * 2;
+    mbar_arrive_expect_tx(bar, uint32_t(nrows + kW - 1 - j0) * bytes);
+    for (int j = j0; j < nrows + kW - 1; ++j)
+      bulk_g2s(tsm + j * kTileRowBytes,
+               qkv + size_t(t0 + p_first + j) * p.qkv_stride + size_t(grp) * kTileWarps * D,
+               bytes, bar);
   }
   const PrefillLayout lay{p.Hk, p.Hv};
   unsigned char* ws = reinterpret_cast<unsigned char*>(p.workspace);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int head = grp * kTileWarps + warp;
 
-  if (head < n_heads) {
-    const int c = head * D + lane * 4;  // first channel of this lane
-    size_t tile;
-    float scale = 0.f;  // 0: v (not normalised)
-    if (head < p.Hk) {
-      tile = lay.qk(cs, head, 1);
-      scale = p.q_scale;
-    } else if (head < 2 * p.Hk) {
-      tile = lay.qk(cs, head - p.Hk, 0);
-      scale = 1.f;
-    } else {
-      tile = lay.v(cs, head - 2 * p.Hk);
-    }
-    const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(p.qkv);
-    const __nv_bfloat16* cst =
-        reinterpret_cast<const __nv_bfloat16*>(p.conv_pool) + size_t(slot) * p.conv_dim * kW;
-    const float4 w0 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 0) * kW);
-    const float4 w1 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 1) * kW);
-    const float4 w2 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 2) * kW);
-    const float4 w3 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 3) * kW);
-    // window entries 0..2: sequence positions pos0 - 3 .. pos0 - 1
-    float4 win[kW - 1];
-#pragma unroll
-    for (int j = 0; j < kW - 1; ++j) {
-      const int sp = pos0 - (kW - 1) + j;
-      if (sp >= 0) {
-        win[j] = A::load4(qkv + size_t(t0 + sp) * p.qkv_stride + c);
-      } else {
-        win[j].x = A::to_f(cst[size_t(c + 0) * kW + kW + sp]);
-        win[j].y = A::to_f(cst[size_t(c + 1) * kW + kW + sp]);
-        win[j].z = A::to_f(cst[size_t(c + 2) * kW + kW + sp]);
-        win[j].w = A::to_f(cst[size_t(c + 3) * kW + kW + sp]);
-      }
-    }
-    // raw bf16 inputs of batch b + 1 are in flight while batch b is computed
-    const __nv_bfloat16* xrow = qkv + size_t(t0 + pos0) * p.qkv_stride + c;
-    auto load_batch = [&](int r0, uint2 (&raw)[kTileBatch]) {
-#pragma unroll
-      for (int u = 0; u < kTileBatch; ++u)
-        raw[u] = (r0 + u < L) ? *reinterpret_cast<const uint2*>(xrow + size_t(r0 + u) * p.qkv_stride)
-                              : make_uint2(0u, 0u);
-    };
-    uint2 cur[kTileBatch], nxt[kTileBatch];
-    load_batch(0, cur);
-    for (int r0 = 0; r0 < L; r0 += kTileBatch) {
-      if (r0 + kTileBatch < L) load_batch(r0 + kTileBatch, nxt);
-#pragma unroll
-      for (int u = 0; u < kTileBatch; ++u) {
-        const int r = r0 + u;
-        if (r >= L) break;
-        const float2 xa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&cur[u].x));
-        const float2 xb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&cur[u].y));
-        const float4 x = make_float4(xa.x, xa.y, xb.x, xb.y);
-        float4 y;
-        y.x = silu_fast(w0.x * win[0].x + w0.y * win[1].x + w0.z * win[2].x + w0.w * x.x);
-        y.y = silu_fast(w1.x * win[0].y + w1.y * win[1].y + w1.z * win[2].y + w1.w * x.y);
-        y.z = silu_fast(w2.x * win[0].z + w2.y * win[1].z + w2.z * win[2].z + w2.w * x.z);
-        y.w = silu_fast(w3.x * win[0].w + w3.y * win[1].w + w3.z * win[2].w + w3.w * x.w);
-        win[0] = win[1];
-        win[1] = win[2];
-        win[2] = x;
-        if (scale != 0.f) {
-          const float ss = warp_sum(y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w);
-          const float rn = scale * rsqrtf(ss + p.l2_eps);
-          y.x *= rn;
-          y.y *= rn;
-          y.z *= rn;
-          y.w *= rn;
-        }
-        const __half2 lo = __floats2half2_rn(y.x, y.y), hi = __floats2half2_rn(y.z, y.w);
-        uint2 pk;
-        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(ws + tile + tc::sw128_offset(kC, r, lane * 4)) = pk;
-      }
-#pragma unroll
-      for (int u = 0; u < kTileBatch; ++u) cur[u] = nxt[u];
-    }
-  }
-  // log(alpha) and beta of this group's value heads
-  for (int idx = threadIdx.x; idx < kC * kTileWarps; idx += kTileWarps * 32) {
-    const int r = idx / kTileWarps, hh = grp * kTileWarps + idx % kTileWarps;
-    if (r >= L || hh < 2 * p.Hk || hh >= n_heads) continue;
+  // log(alpha) and beta of this group's value heads, while the rows arrive
+  for (int idx = threadIdx.x; idx < kTileRows * kTileWarps; idx += kTileWarps * 32) {
+    const int r = r_begin + idx / kTileWarps, hh = grp * kTileWarps + idx % kTileWarps;
+    if (r >= r_begin + nrows || hh < 2 * p.Hk || hh >= n_heads) continue;
     const int h = hh - 2 * p.Hk;
     const size_t ro = size_t(t0 + pos0 + r) * p.ab_stride + h;
     const float av = A::to_f(reinterpret_cast<const __nv_bfloat16*>(p.a)[ro]);
@@ -244,6 +194,71 @@ __global__ void __launch_bounds__(kTileWarps * 32, 2)
     float* g = reinterpret_cast<float*>(ws + lay.gate(cs, h));
     g[r] = -expf(p.A_log[h]) * softplus_f(av + p.dt_bias[h]);
     g[kC + r] = sigmoid_f(bv);
+  }
+  if (warp >= nh) return;
+
+  const int c = head * D + lane * 4;  // first channel of this lane
+  size_t tile;
+  float scale = 0.f;  // 0: v (not normalised)
+  if (head < p.Hk) {
+    tile = lay.qk(cs, head, 1);
+    scale = p.q_scale;
+  } else if (head < 2 * p.Hk) {
+    tile = lay.qk(cs, head - p.Hk, 0);
+    scale = 1.f;
+  } else {
+    tile = lay.v(cs, head - 2 * p.Hk);
+  }
+  const float4 w0 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 0) * kW);
+  const float4 w1 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 1) * kW);
+  const float4 w2 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 2) * kW);
+  const float4 w3 = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 3) * kW);
+  float4 win[kW - 1];
+  if (p_first < 0) {
+    const __nv_bfloat16* cst =
+        reinterpret_cast<const __nv_bfloat16*>(p.conv_pool) + size_t(slot) * p.conv_dim * kW;
+#pragma unroll
+    for (int j = 0; j < kW - 1; ++j) {  // positions -3 .. -1: conv state entries 1 .. 3
+      win[j].x = A::to_f(cst[size_t(c + 0) * kW + 1 + j]);
+      win[j].y = A::to_f(cst[size_t(c + 1) * kW + 1 + j]);
+      win[j].z = A::to_f(cst[size_t(c + 2) * kW + 1 + j]);
+      win[j].w = A::to_f(cst[size_t(c + 3) * kW + 1 + j]);
+    }
+  }
+  if (!mbar_wait_bounded(bar, 0)) {
+    report(p.status, GDN_ERR_TIMEOUT);
+    return;
+  }
+  const unsigned char* col = tsm + warp * (D * 2) + lane * 8;
+  if (p_first >= 0) {
+#pragma unroll
+    for (int j = 0; j < kW - 1; ++j)
+      win[j] = A::load4(reinterpret_cast<const __nv_bfloat16*>(col + j * kTileRowBytes));
+  }
+  for (int r = 0; r < nrows; ++r) {
+    const float4 x =
+        A::load4(reinterpret_cast<const __nv_bfloat16*>(col + (r + kW - 1) * kTileRowBytes));
+    float4 y;
+    y.x = silu_fast(w0.x * win[0].x + w0.y * win[1].x + w0.z * win[2].x + w0.w * x.x);
+    y.y = silu_fast(w1.x * win[0].y + w1.y * win[1].y + w1.z * win[2].y + w1.w * x.y);
+    y.z = silu_fast(w2.x * win[0].z + w2.y * win[1].z + w2.z * win[2].z + w2.w * x.z);
+    y.w = silu_fast(w3.x * win[0].w + w3.y * win[1].w + w3.z * win[2].w + w3.w * x.w);
+    win[0] = win[1];
+    win[1] = win[2];
+    win[2] = x;
+    if (scale != 0.f) {
+      const float ss = warp_sum(y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w);
+      const float rn = scale * rsqrtf(ss + p.l2_eps);
+      y.x *= rn;
+      y.y *= rn;
+      y.z *= rn;
+      y.w *= rn;
+    }
+    const __half2 lo = __floats2half2_rn(y.x, y.y), hi = __floats2half2_rn(y.z, y.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(ws + tile + tc::sw128_offset(kC, r_begin + r, lane * 4)) = pk;
   }
 }
 
@@ -329,7 +344,10 @@ cudaError_t launch_prefill_prep(const ConvParams& p, cudaStream_t stream) {
   if (p.total_tokens == 0 || p.n == 0) return cudaSuccess;
   const int groups = (2 * p.Hk + p.Hv + kTileWarps - 1) / kTileWarps;
   const size_t slots = PrefillLayout::slots(p.n, p.total_tokens);
-  gdn_prefill_tiles_kernel<<<unsigned(slots * groups), kTileWarps * 32, 0, stream>>>(p);
+  cudaError_t e = cudaFuncSetAttribute(gdn_prefill_tiles_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTileSmem));
+  if (e != cudaSuccess) return e;
+  gdn_prefill_tiles_kernel<<<unsigned(slots * 2 * groups), kTileWarps * 32, kTileSmem, stream>>>(p);
   return cudaGetLastError();
 }
 

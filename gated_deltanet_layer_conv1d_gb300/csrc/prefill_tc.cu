@@ -480,14 +480,18 @@ struct SpineSmem {
                                            // here reads its rows 64-127 from K~ (unused)
   static constexpr uint32_t kKt = 40960;   // [64][128] f16 K~ (MN-major A of K~^T Delta)
   static constexpr uint32_t kGd = 57344;   // [64] f32 g
-  static constexpr uint32_t kStage = 58368;
-  static constexpr uint32_t kTx = 4 * 8192 + 8192 + 16384 + 256;  // bytes per fill
+  // The two-slice spine also keeps U in each buffer (one chunk ahead, like the rest); the
+  // whole-row spine has room for one U buffer only, refilled after each chunk's read.
+  static constexpr bool kUInStage = NCOL == 64;
+  static constexpr uint32_t kUst = 58368;  // [NCOL / 32][64][32] f32 U (swizzled), kUInStage
+  static constexpr uint32_t kStage = kUInStage ? kUst + NCOL * 256 : 58368;
+  static constexpr uint32_t kTx = 4 * 8192 + 8192 + 16384 + 256 + (kUInStage ? NCOL * 256 : 0);
   static constexpr uint32_t kHT = 2 * kStage;          // [128][NCOL] f16 H slice (MN-major B)
   static constexpr uint32_t kDT = kHT + NCOL * 256;    // [64][NCOL] f16 Delta (MN-major B)
-  static constexpr uint32_t kUs = kDT + NCOL * 128;    // [NCOL / 32][64][32] f32 U (swizzled)
+  static constexpr uint32_t kUs = kDT + NCOL * 128;    // the single U buffer, !kUInStage
   // Gated norm in the spine (whole rows, NCOL = 128 only):
   static constexpr bool kNorm = NCOL == 128;
-  static constexpr uint32_t kZ = kUs + NCOL * 256;     // [64][128] bf16 z rows (swizzled)
+  static constexpr uint32_t kZ = kUs + (kUInStage ? 0 : NCOL * 256);  // [64][128] bf16 z rows
   static constexpr uint32_t kRed = kZ + (kNorm ? 16384 : 0);   // [4][64] f32 partial sums
   static constexpr uint32_t kNW = kRed + (kNorm ? 1024 : 0);   // [128] f32 norm weight
   static constexpr uint32_t kMisc = kNW + (kNorm ? 512 : 0);   // bars, tmem slot
@@ -588,6 +592,9 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     bulk_g2s(st + S::kP, ws + lay.p(cs, h), 8192, &full[c & 1]);
     bulk_g2s(st + S::kKt, ws + lay.kt(cs, h), 16384, &full[c & 1]);
     bulk_g2s(st + S::kGd, ws + lay.g(cs, h), 256, &full[c & 1]);
+    if constexpr (S::kUInStage)
+      bulk_g2s(st + S::kUst, ws + lay.u(cs, h) + size_t(slice) * NCOL * 256, NCOL * 256,
+               &full[c & 1]);
   };
   // Chunk c's U columns of this slice into the single U buffer (completing on ufull).
   auto issue_u = [&](int c) {
@@ -597,7 +604,7 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
   };
   if (tid == kLoader) {
     issue_loads(0);
-    issue_u(0);
+    if (!S::kUInStage) issue_u(0);
   }
   int issued = 0;    // last chunk whose loads were issued (meaningful in kLoader)
   int u_issued = 0;  // ... and whose U was
@@ -670,8 +677,10 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
       tc::ld16(tmem + tl + kTA + jl0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
       if (q4 >= 2) {
         const int r = row - kC;
-        bad |= !mbar_wait_bounded(ufull, uint32_t(c) & 1u);
-        const float* Us = reinterpret_cast<const float*>(sm + S::kUs) + cg * (kC * 32) + r * 32;
+        if (!S::kUInStage) bad |= !mbar_wait_bounded(ufull, uint32_t(c) & 1u);
+        const float* Us = reinterpret_cast<const float*>(
+                              sm + (S::kUInStage ? st + S::kUst : S::kUs)) +
+                          cg * (kC * 32) + r * 32;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const float4 x = *reinterpret_cast<const float4*>(Us + ((k ^ (r & 7)) << 2));
@@ -708,7 +717,7 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
       tc::commit(bar_mma);
     }
     // this chunk's U has been read (before the barrier): fetch the next chunk's
-    if (tid == kLoader && c + 1 < nc) {
+    if (!S::kUInStage && tid == kLoader && c + 1 < nc) {
       issue_u(c + 1);
       u_issued = c + 1;
     }
@@ -781,7 +790,7 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
       report(p.status, GDN_ERR_TIMEOUT);
       // fills still in flight land before this CTA's shared memory is released
       if (issued > consumed) mbar_wait_bounded(&full[issued & 1], uint32_t(issued >> 1) & 1u);
-      if (u_issued > consumed) mbar_wait_bounded(ufull, uint32_t(u_issued) & 1u);
+      if (!S::kUInStage && u_issued > consumed) mbar_wait_bounded(ufull, uint32_t(u_issued) & 1u);
     }
   } else {
 #pragma unroll
