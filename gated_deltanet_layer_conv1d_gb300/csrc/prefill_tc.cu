@@ -254,8 +254,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
     // ---- A (f32) from the K K^T rows, P (fp16, over q block 0) from the Q K^T rows
     {
       float v[32];
-      tc::ld16(tmem + tl + kT0 + 32 * half, *reinterpret_cast<float(*)[16]>(v));
-      tc::ld16(tmem + tl + kT0 + 32 * half + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tc::ld32(tmem + tl + kT0 + 32 * half, v);
       const int row = 32 * q4 + lane;
       if (row < kC) {
         const int r = row;
@@ -415,14 +414,12 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
     {
       const int i = 32 * q4 + lane;
       float v[32];
-      tc::ld16(tmem + tl + kTW + 32 * half, *reinterpret_cast<float(*)[16]>(v));
-      tc::ld16(tmem + tl + kTW + 32 * half + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tc::ld32(tmem + tl + kTW + 32 * half, v);
 #pragma unroll
       for (int u = 0; u < 32; ++u)
         *reinterpret_cast<__half*>(sm + S::kWi + tc::sw128_offset(64, 32 * half + u, i)) =
             __float2half_rn(v[u]);
-      tc::ld16(tmem + tl + kTU + 32 * half, *reinterpret_cast<float(*)[16]>(v));
-      tc::ld16(tmem + tl + kTU + 32 * half + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tc::ld32(tmem + tl + kTU + 32 * half, v);
       // U column group q4 (= i / 32), row r, column i % 32 = lane, in its swizzled place
       float* Ug = reinterpret_cast<float*>(ws + lay.u(cs, h)) + q4 * (kC * 32);
 #pragma unroll
@@ -673,8 +670,7 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     float X[32];
     {
       float v[32];
-      tc::ld16(tmem + tl + kTA + jl0, *reinterpret_cast<float(*)[16]>(v));
-      tc::ld16(tmem + tl + kTA + jl0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tc::ld32(tmem + tl + kTA + jl0, v);
       if (q4 >= 2) {
         const int r = row - kC;
         if (!S::kUInStage) bad |= !mbar_wait_bounded(ufull, uint32_t(c) & 1u);
@@ -726,8 +722,7 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     // ---- H = e^{g_L} H + K~^T Delta (f32 registers, fp16 copy for the next MMA_a)
     {
       float v[32];
-      tc::ld16(tmem + tl + kTH + jl0, *reinterpret_cast<float(*)[16]>(v));
-      tc::ld16(tmem + tl + kTH + jl0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tc::ld32(tmem + tl + kTH + jl0, v);
 #pragma unroll
       for (int u = 0; u < 32; ++u) Hr[u] = eL * Hr[u] + v[u];
       write_HT();
@@ -738,8 +733,7 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     // ---- O = e^g (Q H0) + P Delta for the query rows (lanes 0..63), behind the next MMA_a
     if (q4 < 2) {
       float v[32];
-      tc::ld16(tmem + tl + kTO + jl0, *reinterpret_cast<float(*)[16]>(v));
-      tc::ld16(tmem + tl + kTO + jl0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tc::ld32(tmem + tl + kTO + jl0, v);
 #pragma unroll
       for (int u = 0; u < 32; ++u) v[u] = eg * X[u] + v[u];
       const size_t orow = size_t(t_begin + t0 + row) * p.Hv + h;
