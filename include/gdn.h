@@ -227,8 +227,10 @@ GDN_API size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t n, int3
  * library keeps in device memory: GDN_NOALLOC_SCRATCH_BYTES (64 MiB) per GPU, held by every
  * GPU that loads the library until the process exits.  It calls no allocator.
  *   - Sizes: a call whose gdn_prefill_workspace_bytes(...) exceeds the scratch returns
- *     GDN_ERR_SCRATCH_TOO_SMALL and launches nothing (at H_k = 16, H_v = 32, d = 128 the
- *     scratch holds 63 chunk slots, e.g. one sequence of about 3,900 tokens).
+ *     GDN_ERR_SCRATCH_TOO_SMALL and launches nothing.  At H_k = 16, H_v = 32, d = 128 each
+ *     64-token chunk slot takes 3.3 MiB (tiles, W, K~, P, U) and each token 16 KiB of f32
+ *     core output, so the scratch holds one sequence of up to 895 tokens, or several
+ *     shorter ones.
  *   - Set-up: the first call on a device, with that device current, looks up the scratch's
  *     device address (cudaGetSymbolAddress); make that first call before any stream capture.
  *     Its failure returns GDN_ERR_CUDA.
