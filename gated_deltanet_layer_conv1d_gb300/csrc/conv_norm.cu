@@ -294,29 +294,47 @@ __global__ void gdn_seqlens_check_kernel(const int32_t* cu, int n, int total, in
   }
 }
 
+// kRows rows per warp per pass, all their loads issued before any use, so each warp keeps
+// several independent rows in flight.
 template <typename T, int D>
 __global__ void gdn_gated_rmsnorm_kernel(const float* __restrict__ o, const T* __restrict__ z,
                                          int64_t z_stride, const float* __restrict__ w,
                                          float eps, int T_, int Hv, T* __restrict__ y) {
   using A = Act<T>;
+  constexpr int kRows = 4;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
-  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < T_ * Hv; r += warps) {
-    const int t = r / Hv, h = r - t * Hv;
-    const int j = lane * 4;
-    float4 ov = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (j < D) ov = *reinterpret_cast<const float4*>(o + size_t(r) * D + j);
-    const float ss = warp_sum(ov.x * ov.x + ov.y * ov.y + ov.z * ov.z + ov.w * ov.w);
-    if (j < D) {
-      const float inv = rsqrtf(ss / float(D) + eps);
-      const float4 w4 = *reinterpret_cast<const float4*>(w + j);
-      const float4 z4 = A::load4(z + size_t(t) * z_stride + h * D + j);
-      float4 yv;
-      yv.x = ov.x * inv * w4.x * silu_f(z4.x);
-      yv.y = ov.y * inv * w4.y * silu_f(z4.y);
-      yv.z = ov.z * inv * w4.z * silu_f(z4.z);
-      yv.w = ov.w * inv * w4.w * silu_f(z4.w);
-      A::store4(y + size_t(t) * Hv * D + h * D + j, yv);
+  const int j = lane * 4;
+  const bool live = j < D;
+  const float4 w4 = live ? *reinterpret_cast<const float4*>(w + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const int rows = T_ * Hv;
+  for (int r0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kRows; r0 < rows;
+       r0 += warps * kRows) {
+    float4 ov[kRows], z4[kRows];
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      const int r = r0 + k, t = r / Hv, h = r - t * Hv;
+      ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z4[k] = ov[k];
+      if (live && r < rows) {
+        ov[k] = *reinterpret_cast<const float4*>(o + size_t(r) * D + j);
+        z4[k] = A::load4(z + size_t(t) * z_stride + h * D + j);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      const int r = r0 + k, t = r / Hv, h = r - t * Hv;
+      const float ss =
+          warp_sum(ov[k].x * ov[k].x + ov[k].y * ov[k].y + ov[k].z * ov[k].z + ov[k].w * ov[k].w);
+      if (live && r < rows) {
+        const float inv = rsqrtf(ss / float(D) + eps);
+        float4 yv;
+        yv.x = ov[k].x * inv * w4.x * silu_f(z4[k].x);
+        yv.y = ov[k].y * inv * w4.y * silu_f(z4[k].y);
+        yv.z = ov[k].z * inv * w4.z * silu_f(z4[k].z);
+        yv.w = ov[k].w * inv * w4.w * silu_f(z4[k].w);
+        A::store4(y + size_t(t) * Hv * D + h * D + j, yv);
+      }
     }
   }
 }

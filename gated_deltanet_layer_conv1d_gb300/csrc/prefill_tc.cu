@@ -103,18 +103,20 @@ struct PrepSmem {
   static constexpr uint32_t kAm = 32768;     // [64][65] f32 A
   static constexpr uint32_t kTw = kAm;       // [64][64] f16 T diag(beta e^g) (A is dead)
   static constexpr uint32_t kTu = kAm + 8192;  // [64][64] f16 T diag(beta)
-  static constexpr uint32_t kTf = 50176;     // [64][64] f32 T
+  static constexpr int kTS = 72;             // row stride of T: the TF32 fragment reads of
+                                             // 8 rows x 4 columns hit distinct banks
+  static constexpr uint32_t kTf = 50176;     // [64][72] f32 T
   static constexpr uint32_t kWi = kTf;       // [64][128] f16 W image (T is dead)
-  static constexpr uint32_t kY = 66560;      // [3][16][16] f32 scratch of the inverse
-  static constexpr uint32_t kGate = 69632;   // [2][64] f32 log(alpha), beta (bulk copied)
-  static constexpr uint32_t kG = 70144;      // [64] f32 cumulative log2 decay g
-  static constexpr uint32_t kB = 70400;      // [64] f32 beta (0 past the chunk end)
-  static constexpr uint32_t kMisc = 70656;   // bars, tmem slot, scan carry
-  static constexpr uint32_t kBytes = 70784;
+  static constexpr uint32_t kY = 68608;      // [3][16][16] f32 scratch of the inverse
+  static constexpr uint32_t kGate = 71680;   // [2][64] f32 log(alpha), beta (bulk copied)
+  static constexpr uint32_t kG = 72192;      // [64] f32 cumulative log2 decay g
+  static constexpr uint32_t kB = 72448;      // [64] f32 beta (0 past the chunk end)
+  static constexpr uint32_t kMisc = 72704;   // bars, tmem slot, scan carry
+  static constexpr uint32_t kBytes = 72832;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024
 };
 static_assert(PrepSmem::kAm + 64 * PrepSmem::kAS * 4 <= PrepSmem::kTf, "A fits");
-static_assert(PrepSmem::kTf + 64 * 64 * 4 <= PrepSmem::kY, "T fits");
+static_assert(PrepSmem::kTf + 64 * PrepSmem::kTS * 4 <= PrepSmem::kY, "T fits");
 static_assert(PrepSmem::kY + 3 * 256 * 4 <= PrepSmem::kGate, "inverse scratch fits");
 
 // TMEM columns of the chunk kernel (128 allocated, so three CTAs share an SM); MMA_W
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
           X[rr] = acc0 + acc1;
         }
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) Tf[(b0 + rr) * kC + b0 + lane] = X[rr];
+        for (int rr = 0; rr < 16; ++rr) Tf[(b0 + rr) * S::kTS + b0 + lane] = X[rr];
       }
     } else {
       // blocks above the diagonal are zero
@@ -316,7 +318,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
         const int blk = e / 256, a = (e % 256) / 16, bb = e % 16;
         const int I = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
         const int J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-        Tf[(16 * I + a) * kC + 16 * J + bb] = 0.f;
+        Tf[(16 * I + a) * S::kTS + 16 * J + bb] = 0.f;
       }
     }
     __syncthreads();
@@ -333,8 +335,8 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
                                  to_tf32(ar[8 * S::kAS + 4])};
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
-            const float* br = Tf + (k0 + t) * kC + 16 * J + 8 * nt + g;
-            mma_tf32(y[nt], a, to_tf32(br[0]), to_tf32(br[4 * kC]));
+            const float* br = Tf + (k0 + t) * S::kTS + 16 * J + 8 * nt + g;
+            mma_tf32(y[nt], a, to_tf32(br[0]), to_tf32(br[4 * S::kTS]));
           }
         }
         float* Yw = Ys + warp * 256;  // Y of this block, [16][16]
@@ -349,9 +351,9 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
         float tt[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int k0 = 0; k0 < 16; k0 += 8) {
-          const float* ar = Tf + (16 * I + g) * kC + 16 * I + k0 + t;
-          const uint32_t a[4] = {to_tf32(ar[0]), to_tf32(ar[8 * kC]), to_tf32(ar[4]),
-                                 to_tf32(ar[8 * kC + 4])};
+          const float* ar = Tf + (16 * I + g) * S::kTS + 16 * I + k0 + t;
+          const uint32_t a[4] = {to_tf32(ar[0]), to_tf32(ar[8 * S::kTS]), to_tf32(ar[4]),
+                                 to_tf32(ar[8 * S::kTS + 4])};
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
             mma_tf32(tt[nt], a, to_tf32(Yw[(k0 + t) * 16 + 8 * nt + g]),
@@ -359,11 +361,11 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
         }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          float* tr = Tf + (16 * I + g) * kC + 16 * J + 8 * nt + 2 * t;
+          float* tr = Tf + (16 * I + g) * S::kTS + 16 * J + 8 * nt + 2 * t;
           tr[0] = -tt[nt][0];
           tr[1] = -tt[nt][1];
-          tr[8 * kC] = -tt[nt][2];
-          tr[8 * kC + 1] = -tt[nt][3];
+          tr[8 * S::kTS] = -tt[nt][2];
+          tr[8 * S::kTS + 1] = -tt[nt][3];
         }
       }
       __syncthreads();
@@ -381,10 +383,12 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
     for (int cid = tid; cid < kC * 8; cid += kPrepThreads) {
       const int r = cid / 8, s0 = (cid % 8) * 8;
       float tw[8], tu[8];
+      const float4 t0 = *reinterpret_cast<const float4*>(Tf + r * S::kTS + s0);
+      const float4 t1 = *reinterpret_cast<const float4*>(Tf + r * S::kTS + s0 + 4);
+      const float tv8[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const float tv = Tf[r * kC + s0 + u];
-        tu[u] = tv * B_s[s0 + u];
+        tu[u] = tv8[u] * B_s[s0 + u];
         tw[u] = tu[u] * exp2_fast(G_s[s0 + u]);
       }
       *reinterpret_cast<uint4*>(sm + S::kTw + tc::sw128_offset(64, r, s0)) = pack8_h(tw);
