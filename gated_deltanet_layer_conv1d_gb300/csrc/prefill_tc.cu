@@ -496,7 +496,7 @@ struct SpineSmem {
   static constexpr uint32_t kRed = kZ + (kNorm ? 16384 : 0);   // [4][64] f32 partial sums
   static constexpr uint32_t kNW = kRed + (kNorm ? 1024 : 0);   // [128] f32 norm weight
   static constexpr uint32_t kMisc = kNW + (kNorm ? 512 : 0);   // bars, tmem slot
-  static constexpr uint32_t kBytes = kMisc + 64;
+  static constexpr uint32_t kBytes = kMisc + 128;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static constexpr uint32_t kTmemCols = NCOL == 64 ? 256 : 512;
   static_assert(NCOL == 64 || NCOL == 128, "whole 64-column blocks of the MN-major operands");
@@ -530,10 +530,14 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
+  // full[b]: q_hat, W, g (and U) of buffer b; fullB[b]: P and K~ of buffer b, which only
+  // MMA_b reads
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::kMisc);  // [2]
-  uint64_t* bar_mma = full + 2;
-  uint64_t* ufull = full + 3;  // U of the current chunk
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(ufull + 1);
+  uint64_t* fullB = full + 2;                                    // [2]
+  uint64_t* bar_mma = full + 4;  // MMA_a, then K~^T Delta: the chain
+  uint64_t* bar_o = full + 5;    // [P;*] Delta: only the outputs wait for it
+  uint64_t* ufull = full + 6;    // U of the current chunk (whole-row spine)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(full + 7);
 
   const PrefillLayout lay{p.Hk, p.Hv};
   const unsigned char* ws = reinterpret_cast<const unsigned char*>(p.workspace);
@@ -542,7 +546,10 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
   if (tid == 0) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
+    mbar_init(&fullB[0], 1);
+    mbar_init(&fullB[1], 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_o, 1);
     mbar_init(ufull, 1);
     fence_mbar_init();
   }
@@ -585,17 +592,18 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     unsigned char* st = sm + (c & 1) * S::kStage;
     const unsigned char* qimg = ws + lay.qk(cs, kh, 1);
     const unsigned char* wimg = ws + lay.w(cs, h);
-    mbar_arrive_expect_tx(&full[c & 1], S::kTx);
+    mbar_arrive_expect_tx(&full[c & 1], S::kTx - 8192 - 16384);
     bulk_g2s(st + S::kQW, qimg, 8192, &full[c & 1]);
     bulk_g2s(st + S::kQW + 8192, wimg, 8192, &full[c & 1]);
     bulk_g2s(st + S::kQW + 16384, qimg + 8192, 8192, &full[c & 1]);
     bulk_g2s(st + S::kQW + 24576, wimg + 8192, 8192, &full[c & 1]);
-    bulk_g2s(st + S::kP, ws + lay.p(cs, h), 8192, &full[c & 1]);
-    bulk_g2s(st + S::kKt, ws + lay.kt(cs, h), 16384, &full[c & 1]);
     bulk_g2s(st + S::kGd, ws + lay.g(cs, h), 256, &full[c & 1]);
     if constexpr (S::kUInStage)
       bulk_g2s(st + S::kUst, ws + lay.u(cs, h) + size_t(slice) * NCOL * 256, NCOL * 256,
                &full[c & 1]);
+    mbar_arrive_expect_tx(&fullB[c & 1], 8192 + 16384);
+    bulk_g2s(st + S::kP, ws + lay.p(cs, h), 8192, &fullB[c & 1]);
+    bulk_g2s(st + S::kKt, ws + lay.kt(cs, h), 16384, &fullB[c & 1]);
   };
   // Chunk c's U columns of this slice into the single U buffer (completing on ufull).
   auto issue_u = [&](int c) {
@@ -704,17 +712,25 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     fence_proxy_async_smem();
     if (sync_or_stop()) { aborted = true; break; }
 
-    // ---- MMA_b: K~^T Delta and [P;*] Delta
+    // ---- MMA_b: K~^T Delta (the chain), then [P;*] Delta (the outputs)
     if (tid == kIssuer) {
+      bad |= !mbar_wait_bounded(&fullB[c & 1], uint32_t(c >> 1) & 1u);
+      if (!bad) {
 #pragma unroll
-      for (int s0 = 0; s0 < kC; s0 += 16) {
-        const uint64_t bd = tc::desc_mn_sw128(sb + S::kDT + s0 * 128, 8192);
-        tc::mma_f16(tmem + kTH, tc::desc_mn_sw128(sb + st + S::kKt + s0 * 128, 8192), bd,
-                     tc::idesc_f16(128, NCOL, true, true), s0 > 0);
-        tc::mma_f16(tmem + kTO, tc::desc_at(sb + st + S::kP, 128, s0), bd,
-                     tc::idesc_f16(128, NCOL, false, true), s0 > 0);
+        for (int s0 = 0; s0 < kC; s0 += 16)
+          tc::mma_f16(tmem + kTH, tc::desc_mn_sw128(sb + st + S::kKt + s0 * 128, 8192),
+                       tc::desc_mn_sw128(sb + S::kDT + s0 * 128, 8192),
+                       tc::idesc_f16(128, NCOL, true, true), s0 > 0);
       }
       tc::commit(bar_mma);
+      if (!bad) {
+#pragma unroll
+        for (int s0 = 0; s0 < kC; s0 += 16)
+          tc::mma_f16(tmem + kTO, tc::desc_at(sb + st + S::kP, 128, s0),
+                       tc::desc_mn_sw128(sb + S::kDT + s0 * 128, 8192),
+                       tc::idesc_f16(128, NCOL, false, true), s0 > 0);
+      }
+      tc::commit(bar_o);
     }
     // this chunk's U has been read (before the barrier): fetch the next chunk's
     if (!S::kUInStage && tid == kLoader && c + 1 < nc) {
@@ -736,6 +752,8 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
 
     // ---- O = e^g (Q H0) + P Delta for the query rows (lanes 0..63), behind the next MMA_a
     if (q4 < 2) {
+      bad |= !mbar_wait_bounded(bar_o, uint32_t(c) & 1u);
+      tc::fence_after_sync();
       float v[32];
       tc::ld32(tmem + tl + kTO + jl0, v);
 #pragma unroll
@@ -787,7 +805,11 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     if (tid == kLoader) {
       report(p.status, GDN_ERR_TIMEOUT);
       // fills still in flight land before this CTA's shared memory is released
-      if (issued > consumed) mbar_wait_bounded(&full[issued & 1], uint32_t(issued >> 1) & 1u);
+      if (issued > consumed) {
+        mbar_wait_bounded(&full[issued & 1], uint32_t(issued >> 1) & 1u);
+        mbar_wait_bounded(&fullB[issued & 1], uint32_t(issued >> 1) & 1u);
+      }
+      if (consumed >= 0) mbar_wait_bounded(&fullB[consumed & 1], uint32_t(consumed >> 1) & 1u);
       if (!S::kUInStage && u_issued > consumed) mbar_wait_bounded(ufull, uint32_t(u_issued) & 1u);
     }
   } else {
