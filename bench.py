@@ -6,8 +6,9 @@ step is one gdn_decode_batched call (conv + SiLU + L2, gates, gated delta rule, 
 RMSNorm: one fused kernel launch) over the 128 sequences.  Steps rotate over 4 state pools
 (4 x 256 MiB), so every step streams its state from HBM rather than L2.
 
-Also reported (key "modes"): the ragged verify of 128 sequences with k ~ U{2..16} and the
-8192-token chunked prefill, each with its own throughput and roofline fraction.
+Also reported (key "modes"): the ragged verify of 128 sequences with k ~ U{2..16}, the
+accepted-draft fold after it, the 8192-token chunked prefill and the mixed serving step,
+each with its own throughput and roofline fraction.
 
 `--impl reference` times the fp64 CPU oracle on this host's cores on a bounded sample of
 the same workload.  Under torchrun every rank runs an independent replica (the mixer has
@@ -265,6 +266,51 @@ def verify_mode(device, steps, hbm_peak, warmup=3, n=N_SEQ):
     return {"workload": f"ragged_verify_{n}seq_k2to16", "tokens_per_step": sum(ks),
             "ms_per_step": round(ms, 4), "value": round(sum(ks) / (ms * 1e-3), 1),
             "unit": "tokens/s", "gpu_launches_per_step": 1,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                         "algorithmic_bytes": byts}}
+
+
+def fold_mode(device, steps, hbm_peak, warmup=3, n=N_SEQ):
+    """The accepted-draft fold after a 128-sequence ragged verify (k ~ U{2..16}), m_i ~
+    U{1..k_i} accepted; the fold is repeated on the same verify output (it is idempotent)."""
+    import torch
+
+    from gated_deltanet_layer_conv1d_gb300 import device as dev
+    from gated_deltanet_layer_conv1d_gb300 import gdn
+    from gated_deltanet_layer_conv1d_gb300 import workloads as wl
+    w = wl.ragged_verify(n=n)
+    ks = [int(k) for k in w.lens]
+    rng = np.random.default_rng(1)
+    m = [int(rng.integers(1, k + 1)) for k in ks]
+    h_pool, conv_pool, slots = dev.states_to(w, device)
+    inter = torch.empty((n, 15, 32, 128, 128), dtype=torch.float32, device=device)
+    ci = torch.empty((n, 15, 8192, 4), dtype=torch.bfloat16, device=device)
+    hsz = 32 * 128 * 128 * 4
+    tables = dev.wy_tables_to(ks, [h_pool.data_ptr() + i * hsz for i in range(n)],
+                              [[inter[i, t].data_ptr() for t in range(15)] for i in range(n)],
+                              device)
+    inp = dev.tokens_to(w.tokens, torch.bfloat16, device)
+    y = torch.empty((sum(ks), 4096), dtype=torch.bfloat16, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    dims, weights = dev.dims_of(w.shape), dev.weights_to(w, device)
+    stream = torch.cuda.current_stream(device)
+    gdn.gdn_verify_multi(dims, weights, inp, n, ks, tables, conv_pool, n, slots, ci, y, None,
+                         status, stream)
+    acc = torch.tensor(m, dtype=torch.int32, device=device)
+
+    def fn(i):
+        gdn.gdn_fold_accepted(dims, n, ks, acc, tables, conv_pool, n, slots, ci,
+                              gdn.GDN_DTYPE_BF16, status, stream)
+
+    ms = time_loop(torch, stream, fn, steps, warmup)
+    assert int(status.item()) == 0
+    rolled = sum(1 for k, a in zip(ks, m) if a < k)
+    byts = rolled * 2 * (2 * 1024 * 1024 + 8192 * 4 * 2) + n * 4
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"workload": f"accepted_fold_{n}seq_k2to16", "sequences_rolled_back": rolled,
+            "ms_per_step": round(ms, 4), "value": round(n / (ms * 1e-3), 1),
+            "unit": "sequences/s", "gpu_launches_per_step": 1,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
                          "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
                          "algorithmic_bytes": byts}}
@@ -544,6 +590,7 @@ def main():
     modes = {}
     if not args.no_modes and rank == 0:
         modes["ragged_verify"] = verify_mode(device, max(10, min(200, args.steps // 10)), hbm_peak)
+        modes["accepted_fold"] = fold_mode(device, 50, hbm_peak)
         modes["chunked_prefill"] = prefill_mode(device, 5, tc_peak)
         modes["mixed_serving"] = mixed_mode(device, 3, hbm_peak, tc_peak)
     cpu = None

@@ -151,6 +151,7 @@ const char* gdn_status_string(gdn_status s) {
     case GDN_ERR_BAD_SLOT: return "slot out of range";
     case GDN_ERR_BAD_SEQLENS: return "bad cu_seqlens";
     case GDN_ERR_TIMEOUT: return "device wait timed out";
+    case GDN_ERR_BAD_ACCEPTED: return "accepted count outside 1..k";
     default: return "unknown status";
   }
 }
@@ -231,6 +232,43 @@ gdn_status gdn_verify_multi(const gdn_dims* dims, const gdn_weights* weights,
   for (int i = 0; i < n; ++i) p.order[i] = uint8_t(order[i]);
   const cudaError_t e = launch_recurrent(p, inputs->dtype, dims->d_k, true, stream);
   return status_of(e);
+}
+
+gdn_status gdn_fold_accepted(const gdn_dims* dims, int32_t n, const int32_t* ks_host,
+                             const int32_t* accepted_dev, const uint64_t* wy_tables_dev,
+                             void* conv_pool, int32_t n_slots, const int32_t* slots_dev,
+                             const void* conv_inter, int32_t dtype, int32_t* status_dev,
+                             gdn_stream_t stream) {
+  GDN_TRY(check_dims(dims));
+  if (n <= 0) return GDN_ERR_INVALID_ARGUMENT;
+  if (n > GDN_MAX_SEQS) return GDN_ERR_TOO_MANY_SEQS;
+  if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return GDN_ERR_INVALID_ARGUMENT;
+  if (!ks_host || !accepted_dev || !wy_tables_dev || !conv_inter || !status_dev)
+    return GDN_ERR_NULL_POINTER;
+  for (int i = 0; i < n; ++i)
+    if (ks_host[i] < GDN_VERIFY_K_MIN || ks_host[i] > GDN_VERIFY_K_MAX) return GDN_ERR_BAD_K;
+  GDN_TRY(check_pools(conv_pool, n_slots, slots_dev));
+  if (!aligned(accepted_dev, 4) || !aligned(wy_tables_dev, 8) || !aligned(conv_inter, 16) ||
+      !aligned(status_dev, 4))
+    return GDN_ERR_MISALIGNED;
+  FoldParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.Hv = dims->n_v_heads;
+  p.d_k = dims->d_k;
+  p.d_v = dims->d_v;
+  p.conv_dim = conv_dim_of(*dims);
+  p.d_conv = dims->d_conv;
+  p.esize = int32_t(esize(dtype));
+  p.n = n;
+  p.n_slots = n_slots;
+  p.accepted = accepted_dev;
+  p.tables = wy_tables_dev;
+  p.conv_pool = conv_pool;
+  p.slots = slots_dev;
+  p.conv_inter = conv_inter;
+  p.status = status_dev;
+  for (int i = 0; i < n; ++i) p.ks[i] = uint8_t(ks_host[i]);
+  return status_of(launch_fold(p, stream));
 }
 
 gdn_status gdn_conv_step(const gdn_dims* dims, const gdn_weights* weights,

@@ -104,6 +104,19 @@ size_t prefill_workspace_bytes(int Hk, int Hv, int D, int n, int total_tokens,
                                int max_seqlen);
 cudaError_t launch_prefill(const PrefillParams& p, int dtype, cudaStream_t stream);
 
+// Accepted-draft fold after a ragged verify.
+struct FoldParams {
+  int32_t Hv, d_k, d_v, conv_dim, d_conv, esize, n, n_slots;
+  const int32_t* accepted;  // [n] device
+  const uint64_t* tables;   // [16][128]
+  void* conv_pool;
+  const int32_t* slots;
+  const void* conv_inter;   // [n][15][conv_dim][d_conv]
+  int32_t* status;
+  uint8_t ks[GDN_MAX_SEQS];
+};
+cudaError_t launch_fold(const FoldParams& p, cudaStream_t stream);
+
 int sm_count();
 
 }  // namespace gdn

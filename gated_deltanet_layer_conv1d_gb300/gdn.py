@@ -29,7 +29,8 @@ PREFILL_CHUNK = 64
 # Symbols include/gdn.h declares.
 EXPORTS = ("gdn_decode_batched", "gdn_verify_multi", "gdn_conv_step", "gdn_prefill_chunked",
            "gdn_prefill_workspace_bytes", "gdn_gated_rmsnorm", "gdn_wy_tables_fill",
-           "gdn_status_string", "gdn_version", "gdn_prefill_chunked_noalloc")
+           "gdn_status_string", "gdn_version", "gdn_prefill_chunked_noalloc",
+           "gdn_fold_accepted")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -74,6 +75,7 @@ def lib() -> ctypes.CDLL:
         L.gdn_decode_batched.argtypes = [D, W, IN, I32, P, P, I32, P, P, P, P, P]
         L.gdn_verify_multi.argtypes = [D, W, IN, I32, P, P, P, I32, P, P, P, P, P, P]
         L.gdn_conv_step.argtypes = [D, W, IN, I32, P, I32, P, I32, P, P, P, P]
+        L.gdn_fold_accepted.argtypes = [D, I32, P, P, P, P, I32, P, P, I32, P, P]
         L.gdn_prefill_chunked.argtypes = [D, W, IN, I32, P, I32, I32, I32, P, P, I32, P, P, P,
                                           P, SZ, P, P]
         L.gdn_prefill_chunked_noalloc.argtypes = [D, W, IN, I32, P, I32, I32, I32, P, P, I32, P,
@@ -171,6 +173,15 @@ def gdn_verify_multi(dims: gdn_dims, weights: Weights, inputs: Inputs, n: int, k
         ctypes.byref(dims), ctypes.byref(w), ctypes.byref(i), n, ctypes.cast(ks, ctypes.c_void_p),
         _ptr(wy_tables), _ptr(conv_pool), n_slots, _ptr(slots), _ptr(conv_inter), _ptr(y),
         _ptr(core_out), _ptr(status), _stream(stream)))
+
+
+def gdn_fold_accepted(dims: gdn_dims, n: int, ks_host, accepted, wy_tables, conv_pool,
+                      n_slots: int, slots, conv_inter, dtype: int, status=None, stream=None):
+    ks = (ctypes.c_int32 * len(ks_host))(*[int(k) for k in ks_host])
+    _check("gdn_fold_accepted", lib().gdn_fold_accepted(
+        ctypes.byref(dims), n, ctypes.cast(ks, ctypes.c_void_p), _ptr(accepted), _ptr(wy_tables),
+        _ptr(conv_pool), n_slots, _ptr(slots), _ptr(conv_inter), int(dtype), _ptr(status),
+        _stream(stream)))
 
 
 def gdn_conv_step(dims: gdn_dims, weights: Weights, inputs: Inputs, n: int, cu_seqlens,

@@ -80,6 +80,7 @@ typedef int32_t gdn_status;
 #define GDN_ERR_BAD_SLOT 17          /* a slot index outside [0, n_slots) */
 #define GDN_ERR_BAD_SEQLENS 18       /* cu_seqlens not monotone / not matching the sizes */
 #define GDN_ERR_TIMEOUT 19           /* a bounded device-side wait ran out */
+#define GDN_ERR_BAD_ACCEPTED 20      /* fold: an accepted count outside 1..k */
 
 /* Activation dtypes (raw QKV, Z, a, b, the conv state and the output y). */
 #define GDN_DTYPE_F32 0
@@ -179,6 +180,29 @@ GDN_API gdn_status gdn_verify_multi(const gdn_dims* dims, const gdn_weights* wei
                             const uint64_t* wy_tables_dev, void* conv_pool, int32_t n_slots,
                             const int32_t* slots_dev, void* conv_inter, void* y,
                             float* core_out, int32_t* status_dev, gdn_stream_t stream);
+
+/* Folds the accepted drafts of a ragged verify into each sequence's state (trait_layer.rs,
+ * LayerWriteOnAccept::gdn_fold_accepted over the h-state table and a device table of
+ * accepted counts; layer_struct.rs, the fold kernel gdn_wy4_fold_k).  After
+ * gdn_verify_multi ran sequence i over k_i draft tokens, the caller accepted the first
+ * m_i = accepted_dev[i] of them (1 <= m_i <= k_i).  When m_i < k_i the state after m_i
+ * tokens replaces the state after all k_i: table 0 entry i receives a copy of the state
+ * table m_i entry i points to (intermediate m_i - 1), and the conv state of slot
+ * slots_dev[i] receives conv_inter[i][m_i - 1].  When m_i == k_i nothing is written.
+ *   n, ks_host  : the verify's sequence count and draft counts (each 2..16).
+ *   accepted_dev: device int32 [n]; a count outside 1..k_i sets GDN_ERR_BAD_ACCEPTED and
+ *                 that sequence is left as it is.
+ *   wy_tables_dev, conv_pool, n_slots, slots_dev: as passed to gdn_verify_multi; a NULL or
+ *                 misaligned table entry it needs sets GDN_ERR_BAD_TABLE_ENTRY.
+ *   conv_inter  : the conv intermediates that gdn_verify_multi wrote (required here),
+ *                 [n][15][conv_dim][d_conv] in `dtype`.
+ *   dtype       : the activation dtype of the verify (GDN_DTYPE_BF16 or GDN_DTYPE_F32). */
+GDN_API gdn_status gdn_fold_accepted(const gdn_dims* dims, int32_t n, const int32_t* ks_host,
+                                     const int32_t* accepted_dev,
+                                     const uint64_t* wy_tables_dev, void* conv_pool,
+                                     int32_t n_slots, const int32_t* slots_dev,
+                                     const void* conv_inter, int32_t dtype,
+                                     int32_t* status_dev, gdn_stream_t stream);
 
 /* Conv + SiLU + L2 norm of q and k (q also scaled) for T tokens of n sequences in one
  * launch, updating each sequence's conv state to its last d_conv raw inputs

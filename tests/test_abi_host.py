@@ -177,8 +177,32 @@ def test_gated_rmsnorm_refuses_bad_args(g):
     assert st(None, 0x1000, 4096, 0x1000, ctypes.c_float(1e-6), 4, 32, 128, 1, 0x1000, 0) == 3
 
 
+def test_fold_refuses_bad_arguments(g):
+    d = _dims(g)
+
+    def fold(n=2, ks=(3, 5), accepted=0xA0000, tables=0x70000, conv_pool=0x30000, n_slots=8,
+             slots=0x40000, conv_inter=0xB0000, dtype=1, status=0x60000):
+        g.gdn_fold_accepted(d, n, list(ks), accepted, tables, conv_pool, n_slots, slots,
+                            conv_inter, dtype, status, stream=0)
+
+    for kwargs, code in [(dict(n=0, ks=()), 1), (dict(n=129, ks=[2] * 129), 6),
+                         (dict(ks=(3, 17)), 5), (dict(ks=(1, 4)), 5), (dict(dtype=7), 1),
+                         (dict(accepted=None), 3), (dict(tables=None), 3),
+                         (dict(conv_inter=None), 3), (dict(status=None), 3),
+                         (dict(slots=None), 3), (dict(n_slots=0), 1),
+                         (dict(accepted=0xA0002), 4), (dict(conv_inter=0xB0008), 4),
+                         (dict(tables=0x70004), 4)]:
+        with pytest.raises(g.GdnError) as e:
+            fold(**kwargs)
+        assert e.value.status == code, kwargs
+    with pytest.raises(g.GdnError) as e:
+        g.gdn_fold_accepted(_dims(g, d_k=64, d_v=64), 2, [3, 5], 0xA0000, 0x70000, 0x30000, 8,
+                            0x40000, 0xB0000, 1, 0x60000, stream=0)
+    assert e.value.status == 2
+
+
 def test_status_strings(g):
-    for code in (0, 1, 2, 3, 4, 5, 6, 7, 8, 16, 17, 18, 19):
+    for code in (0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 16, 17, 18, 19, 20):
         s = g.status_string(code)
         assert s and s != "unknown status"
     assert g.status_string(12345) == "unknown status"
