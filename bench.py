@@ -7,8 +7,9 @@ RMSNorm: one fused kernel launch) over the 128 sequences.  Steps rotate over 4 s
 (4 x 256 MiB), so every step streams its state from HBM rather than L2.
 
 Also reported (key "modes"): the ragged verify of 128 sequences with k ~ U{2..16}, the
-accepted-draft fold after it, the 8192-token chunked prefill and the mixed serving step,
-each with its own throughput and roofline fraction.
+accepted-draft fold after it, the decode step on half-width (fp16) state pools, the
+8192-token chunked prefill and the mixed serving step, each with its own throughput and
+roofline fraction.
 
 `--impl reference` times the fp64 CPU oracle on this host's cores on a bounded sample of
 the same workload.  Under torchrun every rank runs an independent replica (the mixer has
@@ -266,6 +267,43 @@ def verify_mode(device, steps, hbm_peak, warmup=3, n=N_SEQ):
     return {"workload": f"ragged_verify_{n}seq_k2to16", "tokens_per_step": sum(ks),
             "ms_per_step": round(ms, 4), "value": round(sum(ks) / (ms * 1e-3), 1),
             "unit": "tokens/s", "gpu_launches_per_step": 1,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                         "algorithmic_bytes": byts}}
+
+
+def decode_h16_mode(device, steps, hbm_peak, warmup=3):
+    """Batched decode of 128 sequences on half-width (fp16) state pools: the same step as
+    the headline, with half the state bytes.  Four rotating pools (4 x 128 MiB), as there."""
+    import torch
+
+    from gated_deltanet_layer_conv1d_gb300 import device as dev
+    from gated_deltanet_layer_conv1d_gb300 import gdn
+    from gated_deltanet_layer_conv1d_gb300 import workloads as wl
+    w = wl.batched_decode(n=N_SEQ, steps=POOLS)
+    dims, weights = dev.dims_of(w.shape), dev.weights_to(w, device)
+    h_pool, conv_pool, _ = dev.states_to(w, device, n_slots=N_SEQ)
+    h16 = h_pool.half().repeat(POOLS, 1, 1, 1).contiguous()
+    conv_pool = conv_pool.repeat(POOLS, 1, 1).contiguous()
+    slots = [torch.arange(q * N_SEQ, (q + 1) * N_SEQ, dtype=torch.int32, device=device)
+             for q in range(POOLS)]
+    inputs = [dev.tokens_to(t, torch.bfloat16, device) for t in [w.tokens] + w.steps]
+    y = torch.empty((N_SEQ, 4096), dtype=torch.bfloat16, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def fn(i):
+        q = i % POOLS
+        gdn.gdn_decode_batched_h16(dims, weights, inputs[q], N_SEQ, h16, conv_pool,
+                                   POOLS * N_SEQ, slots[q], y, None, status, stream)
+
+    ms = time_loop(torch, stream, fn, steps, warmup)
+    assert int(status.item()) == 0
+    byts = N_SEQ * (DECODE_BYTES_PER_TOKEN - 2 * 1024 * 1024) + WEIGHT_BYTES
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"workload": "batched_decode_128seq_1tok_fp16_state_pool", "tokens_per_step": N_SEQ,
+            "ms_per_step": round(ms, 4), "value": round(N_SEQ / (ms * 1e-3), 1),
+            "unit": "tokens/s", "gpu_launches_per_step": 1, "state_dtype": "f16",
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
                          "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
                          "algorithmic_bytes": byts}}
@@ -591,6 +629,7 @@ def main():
     if not args.no_modes and rank == 0:
         modes["ragged_verify"] = verify_mode(device, max(10, min(200, args.steps // 10)), hbm_peak)
         modes["accepted_fold"] = fold_mode(device, 50, hbm_peak)
+        modes["decode_fp16_state"] = decode_h16_mode(device, 200, hbm_peak)
         modes["chunked_prefill"] = prefill_mode(device, 5, tc_peak)
         modes["mixed_serving"] = mixed_mode(device, 3, hbm_peak, tc_peak)
     cpu = None

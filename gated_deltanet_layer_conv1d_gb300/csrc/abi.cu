@@ -156,11 +156,11 @@ const char* gdn_status_string(gdn_status s) {
   }
 }
 
-gdn_status gdn_decode_batched(const gdn_dims* dims, const gdn_weights* weights,
-                              const gdn_inputs* inputs, int32_t n, float* h_pool,
+static gdn_status decode_impl(const gdn_dims* dims, const gdn_weights* weights,
+                              const gdn_inputs* inputs, int32_t n, void* h_pool,
                               void* conv_pool, int32_t n_slots, const int32_t* slots_dev,
                               void* y, float* core_out, int32_t* status_dev,
-                              gdn_stream_t stream) {
+                              gdn_stream_t stream, bool h16) {
   GDN_TRY(check_dims(dims));
   GDN_TRY(check_weights(weights));
   if (n < 0) return GDN_ERR_INVALID_ARGUMENT;
@@ -182,15 +182,34 @@ gdn_status gdn_decode_batched(const gdn_dims* dims, const gdn_weights* weights,
   p.core_out = core_out;
   p.status = status_dev;
   p.n_items = n * p.Hk;
-  const cudaError_t e = launch_recurrent(p, inputs->dtype, dims->d_k, false, stream);
+  const cudaError_t e = launch_recurrent(p, inputs->dtype, dims->d_k, false, h16, stream);
   return status_of(e);
 }
 
-gdn_status gdn_verify_multi(const gdn_dims* dims, const gdn_weights* weights,
+gdn_status gdn_decode_batched(const gdn_dims* dims, const gdn_weights* weights,
+                              const gdn_inputs* inputs, int32_t n, float* h_pool,
+                              void* conv_pool, int32_t n_slots, const int32_t* slots_dev,
+                              void* y, float* core_out, int32_t* status_dev,
+                              gdn_stream_t stream) {
+  return decode_impl(dims, weights, inputs, n, h_pool, conv_pool, n_slots, slots_dev, y,
+                     core_out, status_dev, stream, false);
+}
+
+gdn_status gdn_decode_batched_h16(const gdn_dims* dims, const gdn_weights* weights,
+                                  const gdn_inputs* inputs, int32_t n, void* h_pool,
+                                  void* conv_pool, int32_t n_slots, const int32_t* slots_dev,
+                                  void* y, float* core_out, int32_t* status_dev,
+                                  gdn_stream_t stream) {
+  return decode_impl(dims, weights, inputs, n, h_pool, conv_pool, n_slots, slots_dev, y,
+                     core_out, status_dev, stream, true);
+}
+
+static gdn_status verify_impl(const gdn_dims* dims, const gdn_weights* weights,
                             const gdn_inputs* inputs, int32_t n, const int32_t* ks_host,
                             const uint64_t* wy_tables_dev, void* conv_pool, int32_t n_slots,
                             const int32_t* slots_dev, void* conv_inter, void* y,
-                            float* core_out, int32_t* status_dev, gdn_stream_t stream) {
+                            float* core_out, int32_t* status_dev, gdn_stream_t stream,
+                              bool h16) {
   GDN_TRY(check_dims(dims));
   GDN_TRY(check_weights(weights));
   if (n <= 0) return GDN_ERR_INVALID_ARGUMENT;
@@ -230,19 +249,51 @@ gdn_status gdn_verify_multi(const gdn_dims* dims, const gdn_weights* weights,
   // Longest verify first, so the zig-zag deal balances the ragged work.
   std::stable_sort(order, order + n, [&](int a, int b) { return ks_host[a] > ks_host[b]; });
   for (int i = 0; i < n; ++i) p.order[i] = uint8_t(order[i]);
-  const cudaError_t e = launch_recurrent(p, inputs->dtype, dims->d_k, true, stream);
+  const cudaError_t e = launch_recurrent(p, inputs->dtype, dims->d_k, true, h16, stream);
   return status_of(e);
+}
+
+gdn_status gdn_verify_multi(const gdn_dims* dims, const gdn_weights* weights,
+                            const gdn_inputs* inputs, int32_t n, const int32_t* ks_host,
+                            const uint64_t* wy_tables_dev, void* conv_pool, int32_t n_slots,
+                            const int32_t* slots_dev, void* conv_inter, void* y,
+                            float* core_out, int32_t* status_dev, gdn_stream_t stream) {
+  return verify_impl(dims, weights, inputs, n, ks_host, wy_tables_dev, conv_pool, n_slots,
+                     slots_dev, conv_inter, y, core_out, status_dev, stream, false);
+}
+
+gdn_status gdn_verify_multi_h16(const gdn_dims* dims, const gdn_weights* weights,
+                                const gdn_inputs* inputs, int32_t n, const int32_t* ks_host,
+                                const uint64_t* wy_tables_dev, void* conv_pool,
+                                int32_t n_slots, const int32_t* slots_dev, void* conv_inter,
+                                void* y, float* core_out, int32_t* status_dev,
+                                gdn_stream_t stream) {
+  return verify_impl(dims, weights, inputs, n, ks_host, wy_tables_dev, conv_pool, n_slots,
+                     slots_dev, conv_inter, y, core_out, status_dev, stream, true);
+}
+
+gdn_status gdn_state_convert(const void* src, int32_t src_dtype, void* dst, int32_t dst_dtype,
+                             int64_t count, gdn_stream_t stream) {
+  const bool widen = src_dtype == GDN_DTYPE_F16 && dst_dtype == GDN_DTYPE_F32;
+  const bool narrow = src_dtype == GDN_DTYPE_F32 && dst_dtype == GDN_DTYPE_F16;
+  if (!widen && !narrow) return GDN_ERR_INVALID_ARGUMENT;
+  if (count < 0) return GDN_ERR_INVALID_ARGUMENT;
+  if (count == 0) return GDN_OK;
+  if (!src || !dst) return GDN_ERR_NULL_POINTER;
+  if (!aligned(src, 16) || !aligned(dst, 16)) return GDN_ERR_MISALIGNED;
+  return status_of(launch_state_convert(src, src_dtype, dst, dst_dtype, size_t(count), stream));
 }
 
 gdn_status gdn_fold_accepted(const gdn_dims* dims, int32_t n, const int32_t* ks_host,
                              const int32_t* accepted_dev, const uint64_t* wy_tables_dev,
                              void* conv_pool, int32_t n_slots, const int32_t* slots_dev,
-                             const void* conv_inter, int32_t dtype, int32_t* status_dev,
-                             gdn_stream_t stream) {
+                             const void* conv_inter, int32_t dtype, int32_t h_dtype,
+                             int32_t* status_dev, gdn_stream_t stream) {
   GDN_TRY(check_dims(dims));
   if (n <= 0) return GDN_ERR_INVALID_ARGUMENT;
   if (n > GDN_MAX_SEQS) return GDN_ERR_TOO_MANY_SEQS;
   if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return GDN_ERR_INVALID_ARGUMENT;
+  if (h_dtype != GDN_DTYPE_F32 && h_dtype != GDN_DTYPE_F16) return GDN_ERR_INVALID_ARGUMENT;
   if (!ks_host || !accepted_dev || !wy_tables_dev || !conv_inter || !status_dev)
     return GDN_ERR_NULL_POINTER;
   for (int i = 0; i < n; ++i)
@@ -259,6 +310,7 @@ gdn_status gdn_fold_accepted(const gdn_dims* dims, int32_t n, const int32_t* ks_
   p.conv_dim = conv_dim_of(*dims);
   p.d_conv = dims->d_conv;
   p.esize = int32_t(esize(dtype));
+  p.h_esize = h_dtype == GDN_DTYPE_F16 ? 2 : 4;
   p.n = n;
   p.n_slots = n_slots;
   p.accepted = accepted_dev;

@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(kFoldThreads) gdn_fold_kernel(const __grid_con
       if (threadIdx.x == 0 && part == 0) report(p.status, GDN_ERR_BAD_TABLE_ENTRY);
       return;
     }
-    const size_t tile = size_t(p.d_k) * p.d_v * 4;
+    const size_t tile = size_t(p.d_k) * p.d_v * p.h_esize;
     copy_block(reinterpret_cast<unsigned char*>(dst) + size_t(part) * tile,
                reinterpret_cast<const unsigned char*>(src) + size_t(part) * tile, tile);
   } else {

@@ -26,7 +26,7 @@ struct RecParams {
   const void* a;
   const void* b;
   int64_t ab_stride;
-  float* h_pool;           // decode: [n_slots][Hv][D][D]
+  void* h_pool;            // decode: [n_slots][Hv][D][D], f32 or fp16 elements
   const uint64_t* tables;  // verify: [16][128]
   void* conv_pool;         // [n_slots][conv_dim][4]
   const int32_t* slots;    // [n]
@@ -41,8 +41,12 @@ struct RecParams {
 };
 
 // Fused conv + L2 + gates + recurrence + gated norm, one launch for all sequences.
-cudaError_t launch_recurrent(const RecParams& p, int dtype, int D, bool verify,
+// h16: the state pool / tables hold fp16 elements (f32 arithmetic).
+cudaError_t launch_recurrent(const RecParams& p, int dtype, int D, bool verify, bool h16,
                              cudaStream_t stream);
+// Element-wise conversion between f32 and fp16 state pools (round to nearest even).
+cudaError_t launch_state_convert(const void* src, int src_dtype, void* dst, int dst_dtype,
+                                 size_t count, cudaStream_t stream);
 
 // Conv + SiLU + L2 norm over T tokens of n sequences -> f32 [T][conv_dim]
 // (or bf16 when out_bf16), then the conv-state update.
@@ -106,7 +110,7 @@ cudaError_t launch_prefill(const PrefillParams& p, int dtype, cudaStream_t strea
 
 // Accepted-draft fold after a ragged verify.
 struct FoldParams {
-  int32_t Hv, d_k, d_v, conv_dim, d_conv, esize, n, n_slots;
+  int32_t Hv, d_k, d_v, conv_dim, d_conv, esize, h_esize, n, n_slots;
   const int32_t* accepted;  // [n] device
   const uint64_t* tables;   // [16][128]
   void* conv_pool;

@@ -37,6 +37,8 @@
 // per (sequence, value head), in segments of 16 tokens (layer_struct.rs,
 // gdn_prefill_k: the sequential prefill recurrence).  It serves head sizes and dtypes
 // the tensor-core chunked prefill does not take.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -149,12 +151,33 @@ __device__ __forceinline__ bool token_update(float4 (&S)[RecMap<D, NT>::M], cons
   return false;
 }
 
-template <int D, int NT>
-__device__ __forceinline__ void store_tile(float* dst, const float4 (&S)[RecMap<D, NT>::M],
+// State elements: f32, or fp16 in a half-width pool (the arithmetic stays f32; a tile
+// is widened when it is read and rounded to nearest even when it is written).
+__device__ __forceinline__ float4 load_state4(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+__device__ __forceinline__ float4 load_state4(const __half* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void store_state4(float* p, float4 v) {
+  *reinterpret_cast<float4*>(p) = v;
+}
+__device__ __forceinline__ void store_state4(__half* p, float4 v) {
+  const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&a);
+  u.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+template <int D, int NT, typename SH = float>
+__device__ __forceinline__ void store_tile(SH* dst, const float4 (&S)[RecMap<D, NT>::M],
                                            const Lane<D, NT>& L) {
 #pragma unroll
-  for (int m = 0; m < RecMap<D, NT>::M; ++m)
-    *reinterpret_cast<float4*>(dst + L.row(m) * D + L.col0) = S[m];
+  for (int m = 0; m < RecMap<D, NT>::M; ++m) store_state4(dst + L.row(m) * D + L.col0, S[m]);
 }
 
 // L2-normalises q and k of `k` tokens held in shared memory (q at x + t*stride, k right
@@ -218,13 +241,13 @@ __device__ __forceinline__ void norm_tokens(const float* o, const float* z, int 
 // ======================================================================================
 // decode / verify
 // ======================================================================================
-template <int D, int NT, int KMAX, int STAGES, typename T>
+template <int D, int NT, int KMAX, int STAGES, typename T, typename SH = float>
 struct RecSmem {
   using Map = RecMap<D, NT>;
   // Decode prefetches the next item's raw inputs into shared memory while the current
   // item runs; verify (k tokens per item) amortises the prologue and skips it.
   static constexpr bool kPrefetch = (KMAX == 1);
-  static constexpr size_t kTile = size_t(D) * D * sizeof(float);
+  static constexpr size_t kTile = size_t(D) * D * sizeof(SH);
   static constexpr size_t kStage = 0;
   static constexpr size_t kRed = kStage + STAGES * kTile;                  // [2][2][RB][D]
   static constexpr size_t kObuf = kRed + size_t(2) * 2 * Map::RB * D * 4;  // [KMAX][D]
@@ -299,22 +322,22 @@ __device__ __forceinline__ int item_decode(const RecParams& p, int j, const int3
 
 // The state of value head h of an item, written after token t (t = k-1: final state).
 // tab_item: the item's 16 table entries (verify).
-template <int D, bool VERIFY>
-__device__ __forceinline__ float* state_dst(const RecParams& p, const Item& it,
-                                            const uint64_t* tab_item, int h, int t) {
+template <int D, bool VERIFY, typename SH>
+__device__ __forceinline__ SH* state_dst(const RecParams& p, const Item& it,
+                                         const uint64_t* tab_item, int h, int t) {
   if (VERIFY) {
     const int table = (t == it.k - 1) ? 0 : t + 1;
-    return reinterpret_cast<float*>(tab_item[table]) + size_t(h) * D * D;
+    return reinterpret_cast<SH*>(tab_item[table]) + size_t(h) * D * D;
   }
-  return p.h_pool + (size_t(it.slot) * p.Hv + h) * D * D;
+  return reinterpret_cast<SH*>(p.h_pool) + (size_t(it.slot) * p.Hv + h) * D * D;
 }
 
 // The state of value head h of an item as read at its start.
-template <int D, bool VERIFY>
-__device__ __forceinline__ const float* state_src(const RecParams& p, const Item& it,
-                                                  const uint64_t* tab0_s, int h) {
-  if (VERIFY) return reinterpret_cast<const float*>(tab0_s[it.seq]) + size_t(h) * D * D;
-  return p.h_pool + (size_t(it.slot) * p.Hv + h) * D * D;
+template <int D, bool VERIFY, typename SH>
+__device__ __forceinline__ const SH* state_src(const RecParams& p, const Item& it,
+                                               const uint64_t* tab0_s, int h) {
+  if (VERIFY) return reinterpret_cast<const SH*>(tab0_s[it.seq]) + size_t(h) * D * D;
+  return reinterpret_cast<const SH*>(p.h_pool) + (size_t(it.slot) * p.Hv + h) * D * D;
 }
 
 // Thread roles: threads [0, NT) compute (16 warps at d = 128), the last warp produces.
@@ -322,15 +345,15 @@ __device__ __forceinline__ const float* state_src(const RecParams& p, const Item
 // mbarriers per stage) and, for decode, each item's raw prologue inputs into a staging
 // block (raw_full/raw_empty), with bulk async copies.  Compute threads synchronise only
 // with named barrier 1; a stage is released by one mbarrier arrive per compute warp.
-template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY>
+template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY, typename SH>
 __global__ void __launch_bounds__(NT + 32, 1)
     gdn_recurrent_kernel(const __grid_constant__ RecParams p) {
   using Map = RecMap<D, NT>;
-  using SL = RecSmem<D, NT, KMAX, STAGES, T>;
+  using SL = RecSmem<D, NT, KMAX, STAGES, T, SH>;
   using A = Act<T>;
   constexpr int NWC = NT / 32;  // compute warps
   extern __shared__ __align__(128) unsigned char smem[];
-  float* stage = reinterpret_cast<float*>(smem + SL::kStage);
+  unsigned char* stage = smem + SL::kStage;
   float* red = reinterpret_cast<float*>(smem + SL::kRed);
   float* obuf = reinterpret_cast<float*>(smem + SL::kObuf);
   float* nw_s = reinterpret_cast<float*>(smem + SL::kNw);
@@ -397,13 +420,13 @@ __global__ void __launch_bounds__(NT + 32, 1)
   if (tid >= NT) {
     if (tid != NT) return;
     auto issue_tile = [&](int s, const Item& it, int g) {
-      const float* src = state_src<D, VERIFY>(p, it, tab0_s, it.kh * G + g);
+      const SH* src = state_src<D, VERIFY, SH>(p, it, tab0_s, it.kh * G + g);
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(&full[s], uint32_t(SL::kTile));
       constexpr uint32_t kPiece = SL::kTile >= 16384 ? 16384u : uint32_t(SL::kTile);
 #pragma unroll
       for (uint32_t off = 0; off < SL::kTile; off += kPiece)
-        bulk_g2s(reinterpret_cast<unsigned char*>(stage) + s * SL::kTile + off,
+        bulk_g2s(stage + s * SL::kTile + off,
                  reinterpret_cast<const unsigned char*>(src) + off, kPiece, &full[s]);
       issued_s[0] = issued_s[0] + 1;
     };
@@ -632,10 +655,9 @@ __global__ void __launch_bounds__(NT + 32, 1)
       const int s = q % STAGES;
       const bool ok = mbar_wait_bounded(&full[s], uint32_t(q / STAGES) & 1u);
       float4 S[Map::M];
-      const float* tile = stage + size_t(s) * D * D;
+      const SH* tile = reinterpret_cast<const SH*>(stage + size_t(s) * SL::kTile);
 #pragma unroll
-      for (int mm = 0; mm < Map::M; ++mm)
-        S[mm] = *reinterpret_cast<const float4*>(tile + L.row(mm) * D + L.col0);
+      for (int mm = 0; mm < Map::M; ++mm) S[mm] = load_state4(tile + L.row(mm) * D + L.col0);
       __syncwarp();
       if (L.lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
       ++q;
@@ -650,7 +672,7 @@ __global__ void __launch_bounds__(NT + 32, 1)
           return;
         }
         if (VERIFY || t == k - 1)
-          store_tile<D, NT>(state_dst<D, VERIFY>(p, it, tab_item, h, t), S, L);
+          store_tile<D, NT, SH>(state_dst<D, VERIFY, SH>(p, it, tab_item, h, t), S, L);
       }
       named_sync(1, NT);  // obuf complete
       norm_tokens<T, D, Map::NW>(obuf, xs + CH + g * D, CHX, k, it.row0, h, nw_s,
@@ -660,10 +682,10 @@ __global__ void __launch_bounds__(NT + 32, 1)
   }
 }
 
-template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY>
+template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY, typename SH>
 cudaError_t launch_rec(const RecParams& p, cudaStream_t stream) {
-  using SL = RecSmem<D, NT, KMAX, STAGES, T>;
-  auto kern = gdn_recurrent_kernel<T, D, NT, KMAX, STAGES, VERIFY>;
+  using SL = RecSmem<D, NT, KMAX, STAGES, T, SH>;
+  auto kern = gdn_recurrent_kernel<T, D, NT, KMAX, STAGES, VERIFY, SH>;
   const size_t smem = SL::bytes(p.G);
   if (smem > kMaxSmemPerBlock) return cudaErrorInvalidConfiguration;  // shape not supported
   cudaError_t e =
@@ -674,14 +696,14 @@ cudaError_t launch_rec(const RecParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, typename SH>
 cudaError_t launch_rec_typed(const RecParams& p, int D, bool verify, cudaStream_t stream) {
   if (D == 128) {
-    if (verify) return launch_rec<T, 128, 512, GDN_VERIFY_K_MAX, 2, true>(p, stream);
-    return launch_rec<T, 128, 512, 1, 3, false>(p, stream);
+    if (verify) return launch_rec<T, 128, 512, GDN_VERIFY_K_MAX, 2, true, SH>(p, stream);
+    return launch_rec<T, 128, 512, 1, 3, false, SH>(p, stream);
   }
-  if (verify) return launch_rec<T, 16, 64, GDN_VERIFY_K_MAX, 2, true>(p, stream);
-  return launch_rec<T, 16, 64, 1, 3, false>(p, stream);
+  if (verify) return launch_rec<T, 16, 64, GDN_VERIFY_K_MAX, 2, true, SH>(p, stream);
+  return launch_rec<T, 16, 64, 1, 3, false, SH>(p, stream);
 }
 
 // ======================================================================================
@@ -805,10 +827,15 @@ cudaError_t launch_seq(const PrefillParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_recurrent(const RecParams& p, int dtype, int D, bool verify,
+cudaError_t launch_recurrent(const RecParams& p, int dtype, int D, bool verify, bool h16,
                              cudaStream_t stream) {
-  if (dtype == GDN_DTYPE_BF16) return launch_rec_typed<__nv_bfloat16>(p, D, verify, stream);
-  return launch_rec_typed<float>(p, D, verify, stream);
+  if (h16) {
+    if (dtype == GDN_DTYPE_BF16)
+      return launch_rec_typed<__nv_bfloat16, __half>(p, D, verify, stream);
+    return launch_rec_typed<float, __half>(p, D, verify, stream);
+  }
+  if (dtype == GDN_DTYPE_BF16) return launch_rec_typed<__nv_bfloat16, float>(p, D, verify, stream);
+  return launch_rec_typed<float, float>(p, D, verify, stream);
 }
 
 cudaError_t launch_prefill_sequential(const PrefillParams& p, int dtype, cudaStream_t stream) {

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 GDN_OK = 0
 GDN_DTYPE_F32 = 0
 GDN_DTYPE_BF16 = 1
+GDN_DTYPE_F16 = 2  # h-state pools only
 MAX_SEQS = 128
 VERIFY_WY_TABLE_SEQS = 128
 VERIFY_WY_TABLES_PER_LAYER = 16
@@ -30,7 +31,8 @@ PREFILL_CHUNK = 64
 EXPORTS = ("gdn_decode_batched", "gdn_verify_multi", "gdn_conv_step", "gdn_prefill_chunked",
            "gdn_prefill_workspace_bytes", "gdn_gated_rmsnorm", "gdn_wy_tables_fill",
            "gdn_status_string", "gdn_version", "gdn_prefill_chunked_noalloc",
-           "gdn_fold_accepted")
+           "gdn_fold_accepted", "gdn_decode_batched_h16", "gdn_verify_multi_h16",
+           "gdn_state_convert")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -75,7 +77,10 @@ def lib() -> ctypes.CDLL:
         L.gdn_decode_batched.argtypes = [D, W, IN, I32, P, P, I32, P, P, P, P, P]
         L.gdn_verify_multi.argtypes = [D, W, IN, I32, P, P, P, I32, P, P, P, P, P, P]
         L.gdn_conv_step.argtypes = [D, W, IN, I32, P, I32, P, I32, P, P, P, P]
-        L.gdn_fold_accepted.argtypes = [D, I32, P, P, P, P, I32, P, P, I32, P, P]
+        L.gdn_fold_accepted.argtypes = [D, I32, P, P, P, P, I32, P, P, I32, I32, P, P]
+        L.gdn_decode_batched_h16.argtypes = L.gdn_decode_batched.argtypes
+        L.gdn_verify_multi_h16.argtypes = L.gdn_verify_multi.argtypes
+        L.gdn_state_convert.argtypes = [P, I32, P, I32, I64, P]
         L.gdn_prefill_chunked.argtypes = [D, W, IN, I32, P, I32, I32, I32, P, P, I32, P, P, P,
                                           P, SZ, P, P]
         L.gdn_prefill_chunked_noalloc.argtypes = [D, W, IN, I32, P, I32, I32, I32, P, P, I32, P,
@@ -176,12 +181,38 @@ def gdn_verify_multi(dims: gdn_dims, weights: Weights, inputs: Inputs, n: int, k
 
 
 def gdn_fold_accepted(dims: gdn_dims, n: int, ks_host, accepted, wy_tables, conv_pool,
-                      n_slots: int, slots, conv_inter, dtype: int, status=None, stream=None):
+                      n_slots: int, slots, conv_inter, dtype: int, status=None, stream=None,
+                      h_dtype: int = GDN_DTYPE_F32):
     ks = (ctypes.c_int32 * len(ks_host))(*[int(k) for k in ks_host])
     _check("gdn_fold_accepted", lib().gdn_fold_accepted(
         ctypes.byref(dims), n, ctypes.cast(ks, ctypes.c_void_p), _ptr(accepted), _ptr(wy_tables),
-        _ptr(conv_pool), n_slots, _ptr(slots), _ptr(conv_inter), int(dtype), _ptr(status),
-        _stream(stream)))
+        _ptr(conv_pool), n_slots, _ptr(slots), _ptr(conv_inter), int(dtype), int(h_dtype),
+        _ptr(status), _stream(stream)))
+
+
+def gdn_decode_batched_h16(dims: gdn_dims, weights: Weights, inputs: Inputs, n: int, h_pool,
+                           conv_pool, n_slots: int, slots, y, core_out=None, status=None,
+                           stream=None):
+    w, i = weights.c(), inputs.c()
+    _check("gdn_decode_batched_h16", lib().gdn_decode_batched_h16(
+        ctypes.byref(dims), ctypes.byref(w), ctypes.byref(i), n, _ptr(h_pool), _ptr(conv_pool),
+        n_slots, _ptr(slots), _ptr(y), _ptr(core_out), _ptr(status), _stream(stream)))
+
+
+def gdn_verify_multi_h16(dims: gdn_dims, weights: Weights, inputs: Inputs, n: int, ks_host,
+                         wy_tables, conv_pool, n_slots: int, slots, conv_inter, y,
+                         core_out=None, status=None, stream=None):
+    ks = (ctypes.c_int32 * len(ks_host))(*[int(k) for k in ks_host])
+    w, i = weights.c(), inputs.c()
+    _check("gdn_verify_multi_h16", lib().gdn_verify_multi_h16(
+        ctypes.byref(dims), ctypes.byref(w), ctypes.byref(i), n, ctypes.cast(ks, ctypes.c_void_p),
+        _ptr(wy_tables), _ptr(conv_pool), n_slots, _ptr(slots), _ptr(conv_inter), _ptr(y),
+        _ptr(core_out), _ptr(status), _stream(stream)))
+
+
+def gdn_state_convert(src, src_dtype: int, dst, dst_dtype: int, count: int, stream=None):
+    _check("gdn_state_convert", lib().gdn_state_convert(
+        _ptr(src), int(src_dtype), _ptr(dst), int(dst_dtype), int(count), _stream(stream)))
 
 
 def gdn_conv_step(dims: gdn_dims, weights: Weights, inputs: Inputs, n: int, cu_seqlens,

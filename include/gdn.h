@@ -85,6 +85,7 @@ typedef int32_t gdn_status;
 /* Activation dtypes (raw QKV, Z, a, b, the conv state and the output y). */
 #define GDN_DTYPE_F32 0
 #define GDN_DTYPE_BF16 1
+#define GDN_DTYPE_F16 2   /* h-state pools only (the *_h16 entry points, gdn_state_convert) */
 
 /* Most sequences one batched decode or verify call holds, and the WY pointer-table
  * layout of the batched verify (transformer_layer.rs, VERIFY_WY_TABLE_SEQS = 128,
@@ -196,13 +197,45 @@ GDN_API gdn_status gdn_verify_multi(const gdn_dims* dims, const gdn_weights* wei
  *                 misaligned table entry it needs sets GDN_ERR_BAD_TABLE_ENTRY.
  *   conv_inter  : the conv intermediates that gdn_verify_multi wrote (required here),
  *                 [n][15][conv_dim][d_conv] in `dtype`.
- *   dtype       : the activation dtype of the verify (GDN_DTYPE_BF16 or GDN_DTYPE_F32). */
+ *   dtype       : the activation dtype of the verify (GDN_DTYPE_BF16 or GDN_DTYPE_F32).
+ *   h_dtype     : the states' element type: GDN_DTYPE_F32, or GDN_DTYPE_F16 after
+ *                 gdn_verify_multi_h16. */
 GDN_API gdn_status gdn_fold_accepted(const gdn_dims* dims, int32_t n, const int32_t* ks_host,
                                      const int32_t* accepted_dev,
                                      const uint64_t* wy_tables_dev, void* conv_pool,
                                      int32_t n_slots, const int32_t* slots_dev,
-                                     const void* conv_inter, int32_t dtype,
+                                     const void* conv_inter, int32_t dtype, int32_t h_dtype,
                                      int32_t* status_dev, gdn_stream_t stream);
+
+/* Half-width h-state pools (layer_struct.rs: the FP16 h-state variants gdn_f16_norm_k,
+ * gdn_f16_strided_norm_half_k and gdn_wyn_f16_table_k, and the width converters
+ * ssm_h_f16_to_f32_k / ssm_h_f32_to_f16_k).  The same mixer on states stored as fp16
+ * [n_v_heads][d_k][d_v] (element (i, j) = S[j][i]), which halves the state traffic that
+ * dominates decode and verify.  The arithmetic stays f32: each head's state is widened when
+ * it is read and rounded to the nearest fp16 (ties to even) when it is written, once per
+ * token kept, so every stored state is the f32 update of the previous stored state,
+ * rounded.  Arguments and errors are those of gdn_decode_batched / gdn_verify_multi, with
+ * h_pool an fp16 pool and every table entry pointing to an fp16 state (16-B aligned).
+ * Prefill stays f32: widen a sequence's state with gdn_state_convert before
+ * gdn_prefill_chunked and narrow it after. */
+GDN_API gdn_status gdn_decode_batched_h16(const gdn_dims* dims, const gdn_weights* weights,
+                                          const gdn_inputs* inputs, int32_t n, void* h_pool,
+                                          void* conv_pool, int32_t n_slots,
+                                          const int32_t* slots_dev, void* y, float* core_out,
+                                          int32_t* status_dev, gdn_stream_t stream);
+GDN_API gdn_status gdn_verify_multi_h16(const gdn_dims* dims, const gdn_weights* weights,
+                                        const gdn_inputs* inputs, int32_t n,
+                                        const int32_t* ks_host, const uint64_t* wy_tables_dev,
+                                        void* conv_pool, int32_t n_slots,
+                                        const int32_t* slots_dev, void* conv_inter, void* y,
+                                        float* core_out, int32_t* status_dev,
+                                        gdn_stream_t stream);
+
+/* Converts `count` state elements between an f32 and an fp16 pool (src_dtype / dst_dtype =
+ * GDN_DTYPE_F32 and GDN_DTYPE_F16 in either order; round to nearest even when narrowing).
+ * src and dst are device memory, 16-B aligned, and must not overlap. */
+GDN_API gdn_status gdn_state_convert(const void* src, int32_t src_dtype, void* dst,
+                                     int32_t dst_dtype, int64_t count, gdn_stream_t stream);
 
 /* Conv + SiLU + L2 norm of q and k (q also scaled) for T tokens of n sequences in one
  * launch, updating each sequence's conv state to its last d_conv raw inputs

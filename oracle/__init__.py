@@ -60,6 +60,7 @@ class OrcDims(ctypes.Structure):
         ("q_scale", ctypes.c_double),
         ("l2_eps", ctypes.c_double),
         ("norm_eps", ctypes.c_double),
+        ("h_fp16", ctypes.c_int32),
     ]
 
 
@@ -73,6 +74,7 @@ class Dims:
     q_scale: float
     l2_eps: float
     norm_eps: float
+    h_fp16: bool = False  # store the state as binary16 after every token
 
     @property
     def conv_dim(self) -> int:
@@ -80,7 +82,7 @@ class Dims:
 
     def c(self) -> OrcDims:
         return OrcDims(self.n_k_heads, self.n_v_heads, self.d_k, self.d_v, self.d_conv,
-                       self.q_scale, self.l2_eps, self.norm_eps)
+                       self.q_scale, self.l2_eps, self.norm_eps, int(self.h_fp16))
 
 
 _D = ctypes.POINTER(ctypes.c_double)
@@ -95,6 +97,8 @@ def lib():
         L = ctypes.CDLL(_LIB)
         L.orc_softplus.restype = ctypes.c_double
         L.orc_softplus.argtypes = [ctypes.c_double]
+        L.orc_round_fp16.argtypes = [ctypes.c_double]
+        L.orc_round_fp16.restype = ctypes.c_double
         L.orc_gates.argtypes = [_I32, _I32, _D, _D, _D, _D, _D, _D]
         L.orc_conv.argtypes = [_I32, _I32, _I32, _D, _D, _D, _D, _D]
         L.orc_l2norm_split.argtypes = [ctypes.POINTER(OrcDims), _I32, _D, _D, _D, _D]
@@ -127,6 +131,11 @@ def _p(x):
 
 def max_threads() -> int:
     return int(lib().orc_max_threads())
+
+
+def round_fp16(x: float) -> float:
+    """The oracle's binary16 rounding (nearest, ties to even) of one value."""
+    return float(lib().orc_round_fp16(float(x)))
 
 
 def softplus(x: float) -> float:

@@ -36,7 +36,11 @@
 //     w[c][d_conv-1] multiplies the newest input.
 //
 // Everything is double precision.  No blocking, fusion or reordering beyond what the
-// definitions above state.
+// definitions above state.  One option changes storage, not arithmetic: with
+// OrcDims::h_fp16 set, the state is kept in a half-width pool (layer_struct.rs, the FP16
+// h-state variants gdn_f16_norm_k and gdn_wyn_f16_table_k): after every token the stored
+// state is rounded to the nearest IEEE binary16 value, while o is formed from the
+// unrounded update.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -69,7 +73,24 @@ struct OrcDims {
   double q_scale;     // multiplies q after its L2 norm
   double l2_eps;      // q <- q / sqrt(sum q^2 + l2_eps)
   double norm_eps;    // gated RMSNorm epsilon
+  int32_t h_fp16;     // 1: the state is stored as binary16 after every token
 };
+
+// Rounds x to the nearest IEEE 754 binary16 value, ties to even, returned as a double.
+// binary16 has an 11-bit significand: numbers in [2^(e-1), 2^e) are spaced 2^(e-11) for
+// e - 1 >= -14, and below 2^-14 (subnormals) the spacing stays 2^-24.  The largest finite
+// value is 65504; anything that rounds above it is infinite.
+double orc_round_fp16(double x) {
+  if (!std::isfinite(x) || x == 0.0) return x;
+  const double ax = std::fabs(x);
+  int e = 0;
+  std::frexp(ax, &e);  // ax = f 2^e, f in [0.5, 1)
+  const int ex = (e - 11 < -24) ? -24 : e - 11;
+  const double step = std::ldexp(1.0, ex);
+  double r = std::nearbyint(ax / step) * step;  // the default mode: nearest, ties to even
+  if (r > 65504.0) r = INFINITY;
+  return std::copysign(r, x);
+}
 
 int32_t orc_conv_dim(const OrcDims* d) {
   return 2 * d->n_k_heads * d->d_k + d->n_v_heads * d->d_v;
@@ -181,6 +202,8 @@ void orc_recurrence(const OrcDims* d, int32_t T, const double* qn, const double*
       orc_delta_step(dk, dv, Hh, qn + ((int64_t)t * Hk + kh) * dk, kn + ((int64_t)t * Hk + kh) * dk,
                      v + ((int64_t)t * Hv + h) * dv, alpha[(int64_t)t * Hv + h],
                      beta[(int64_t)t * Hv + h], o + ((int64_t)t * Hv + h) * dv);
+      if (d->h_fp16)
+        for (int64_t e = 0; e < hsz; ++e) Hh[e] = orc_round_fp16(Hh[e]);
       if (H_snap) std::memcpy(H_snap + ((int64_t)t * Hv + h) * hsz, Hh, sizeof(double) * hsz);
     }
   }

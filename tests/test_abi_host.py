@@ -181,12 +181,13 @@ def test_fold_refuses_bad_arguments(g):
     d = _dims(g)
 
     def fold(n=2, ks=(3, 5), accepted=0xA0000, tables=0x70000, conv_pool=0x30000, n_slots=8,
-             slots=0x40000, conv_inter=0xB0000, dtype=1, status=0x60000):
+             slots=0x40000, conv_inter=0xB0000, dtype=1, status=0x60000, h_dtype=0):
         g.gdn_fold_accepted(d, n, list(ks), accepted, tables, conv_pool, n_slots, slots,
-                            conv_inter, dtype, status, stream=0)
+                            conv_inter, dtype, status, stream=0, h_dtype=h_dtype)
 
     for kwargs, code in [(dict(n=0, ks=()), 1), (dict(n=129, ks=[2] * 129), 6),
                          (dict(ks=(3, 17)), 5), (dict(ks=(1, 4)), 5), (dict(dtype=7), 1),
+                         (dict(h_dtype=1), 1), (dict(dtype=2), 1),
                          (dict(accepted=None), 3), (dict(tables=None), 3),
                          (dict(conv_inter=None), 3), (dict(status=None), 3),
                          (dict(slots=None), 3), (dict(n_slots=0), 1),
@@ -199,6 +200,31 @@ def test_fold_refuses_bad_arguments(g):
         g.gdn_fold_accepted(_dims(g, d_k=64, d_v=64), 2, [3, 5], 0xA0000, 0x70000, 0x30000, 8,
                             0x40000, 0xB0000, 1, 0x60000, stream=0)
     assert e.value.status == 2
+
+
+def test_h16_entry_points_validate_like_the_f32_ones(g):
+    d = _dims(g)
+    for kwargs, code in [(dict(n=129), 6), (dict(h_pool=None), 3), (dict(h_pool=0x20004), 4)]:
+        args = dict(n=4, h_pool=0x20000)
+        args.update(kwargs)
+        with pytest.raises(g.GdnError) as e:
+            g.gdn_decode_batched_h16(d, _weights(g), _inputs(g), args["n"], args["h_pool"],
+                                     0x30000, 8, 0x40000, 0x50000, None, 0x60000, stream=0)
+        assert e.value.status == code, kwargs
+    with pytest.raises(g.GdnError) as e:
+        g.gdn_verify_multi_h16(d, _weights(g), _inputs(g), 2, [2, 17], 0x70000, 0x30000, 8,
+                               0x40000, None, 0x50000, None, 0x60000, stream=0)
+    assert e.value.status == 5
+
+
+def test_state_convert_refuses_bad_arguments(g):
+    for args, code in [((0x1000, 0, 0x2000, 0, 8), 1), ((0x1000, 2, 0x2000, 2, 8), 1),
+                       ((0x1000, 1, 0x2000, 2, 8), 1), ((0x1000, 0, 0x2000, 2, -1), 1),
+                       ((None, 0, 0x2000, 2, 8), 3), ((0x1008, 0, 0x2000, 2, 8), 4)]:
+        with pytest.raises(g.GdnError) as e:
+            g.gdn_state_convert(*args, stream=0)
+        assert e.value.status == code, args
+    g.gdn_state_convert(0x1000, 0, 0x2000, 2, 0, stream=0)  # nothing to do
 
 
 def test_status_strings(g):

@@ -384,3 +384,49 @@ def test_workload_bf16_rounding_is_ties_to_even():
     assert r[0] == 1.0 and r[1] == 1.0 and r[2] == np.float32(1.015625)
     assert r[3] == -2.0
     assert (r.view(np.uint32) & 0xFFFF).max() == 0
+
+
+# ---------------------------------------------------------------- binary16 state storage
+def test_round_fp16_matches_numpy_half_conversion():
+    rng = np.random.default_rng(11)
+    xs = np.concatenate([
+        rng.standard_normal(4000) * 10.0 ** rng.integers(-9, 6, 4000),  # normals, subnormals
+        np.array([0.0, -0.0, 65504.0, 65519.99, 65520.0, -65520.0, 1e6, 2.0 ** -24,
+                  2.0 ** -25, 3 * 2.0 ** -25, 2.0 ** -14, 2.0 ** -14 - 2.0 ** -25]),
+    ])
+    got = np.array([oracle.round_fp16(x) for x in xs])
+    with np.errstate(over="ignore"):  # values past 65504 become inf, as they should
+        ref = xs.astype(np.float16).astype(np.float64)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_round_fp16_ties_go_to_even():
+    u = 2.0 ** -10  # spacing of binary16 just above 1
+    assert oracle.round_fp16(1.0 + u / 2) == 1.0            # tie between 1 and 1+u: even is 1
+    assert oracle.round_fp16(1.0 + 3 * u / 2) == 1.0 + 2 * u  # tie: 1+2u has the even significand
+    assert oracle.round_fp16(2.0 ** -25) == 0.0              # half the smallest subnormal
+    assert oracle.round_fp16(3 * 2.0 ** -25) == 2.0 ** -23
+    assert math.isinf(oracle.round_fp16(65520.0))            # the tie above 65504 overflows
+
+
+def test_fp16_state_storage_rounds_every_stored_state_and_stays_close():
+    rng = np.random.default_rng(12)
+    dims = oracle.Dims(2, 4, 16, 16, 4, 0.25, 1e-6, 1e-6)
+    dims16 = oracle.Dims(2, 4, 16, 16, 4, 0.25, 1e-6, 1e-6, h_fp16=True)
+    T = 64
+    qn = rng.standard_normal((T, 2, 16)); qn /= np.linalg.norm(qn, axis=-1, keepdims=True)
+    kn = rng.standard_normal((T, 2, 16)); kn /= np.linalg.norm(kn, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, 4, 16))
+    al = rng.uniform(0.5, 1.0, (T, 4))
+    be = rng.uniform(0.0, 1.0, (T, 4))
+    H0 = rng.standard_normal((4, 16, 16)).astype(np.float16).astype(np.float64)
+    H, o, _ = oracle.recurrence(dims, qn, kn, v, al, be, H0)
+    H16, o16, snap = oracle.recurrence(dims16, qn, kn, v, al, be, H0, snapshots=True)
+    # every stored state is a binary16 value
+    np.testing.assert_array_equal(snap, snap.astype(np.float16).astype(np.float64))
+    np.testing.assert_array_equal(H16, snap[-1])
+    # one rounding per token: far from exact, and within 64 half-ulps of the exact result
+    e = np.linalg.norm(H16 - H) / np.linalg.norm(H)
+    assert 1e-5 < e < 64 * 2.0 ** -11
+    # the first output uses the unrounded update, so it equals the exact path's
+    np.testing.assert_allclose(o16[0], o[0], rtol=0, atol=1e-12)
