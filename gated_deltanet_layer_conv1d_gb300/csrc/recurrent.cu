@@ -250,12 +250,16 @@ struct RecSmem {
   static constexpr size_t kTile = size_t(D) * D * sizeof(SH);
   static constexpr size_t kStage = 0;
   static constexpr size_t kRed = kStage + STAGES * kTile;                  // [2][2][RB][D]
-  static constexpr size_t kObuf = kRed + size_t(2) * 2 * Map::RB * D * 4;  // [KMAX][D]
-  static constexpr size_t kNw = kObuf + size_t(KMAX) * D * 4;              // [D] norm_w
-  // mbarriers: full[STAGES] | empty[STAGES] | raw_full | raw_empty, then two counters
-  // (tiles and raw blocks the producer has started), read only when a wait gives up.
+  // Decode hands each head's output to a norm warp through a two-slot obuf.
+  static constexpr bool kNormWarp = (KMAX == 1);
+  static constexpr int kObufRows = KMAX > 2 ? KMAX : 2;
+  static constexpr size_t kObuf = kRed + size_t(2) * 2 * Map::RB * D * 4;  // [kObufRows][D]
+  static constexpr size_t kNw = kObuf + size_t(kObufRows) * D * 4;         // [D] norm_w
+  // mbarriers: full[STAGES] | empty[STAGES] | raw_full | raw_empty | nfull[2] | nfree[2],
+  // then two counters (tiles and raw blocks the producer has started), read only when a
+  // wait gives up.
   static constexpr size_t kBar = kNw + size_t(D) * 4;
-  static constexpr size_t kIssued = kBar + 8 * (2 * STAGES + 2);           // [2] i32
+  static constexpr size_t kIssued = kBar + 8 * (2 * STAGES + 6);           // [2] i32
   static constexpr size_t kGate = kIssued + 16;                            // [KMAX][kMaxG][2]
   static constexpr size_t kKq = kGate + size_t(KMAX) * kMaxG * 2 * 4;      // [KMAX]
   // Per-launch staging so no global load sits on the per-head critical path:
@@ -340,13 +344,21 @@ __device__ __forceinline__ const SH* state_src(const RecParams& p, const Item& i
   return reinterpret_cast<const SH*>(p.h_pool) + (size_t(it.slot) * p.Hv + h) * D * D;
 }
 
-// Thread roles: threads [0, NT) compute (16 warps at d = 128), the last warp produces.
+// Thread roles: threads [0, NT) compute (16 warps at d = 128), the next warp produces.
 // Lane 0 of the producer warp streams every state tile into the stage ring (full/empty
 // mbarriers per stage) and, for decode, each item's raw prologue inputs into a staging
 // block (raw_full/raw_empty), with bulk async copies.  Compute threads synchronise only
 // with named barrier 1; a stage is released by one mbarrier arrive per compute warp.
+// Decode has one more warp, which applies the gated RMSNorm to each head's output: the
+// compute warps that write a head's o arrive on nfull[slot], the norm warp copies o and z
+// to registers and arrives on nfree[slot], so the norm never sits on the chain of heads.
+template <int NT, int KMAX>
+__host__ __device__ constexpr int rec_threads() {
+  return NT + (KMAX == 1 ? 64 : 32);
+}
+
 template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY, typename SH>
-__global__ void __launch_bounds__(NT + 32, 1)
+__global__ void __launch_bounds__(rec_threads<NT, KMAX>(), 1)
     gdn_recurrent_kernel(const __grid_constant__ RecParams p) {
   using Map = RecMap<D, NT>;
   using SL = RecSmem<D, NT, KMAX, STAGES, T, SH>;
@@ -361,6 +373,9 @@ __global__ void __launch_bounds__(NT + 32, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* raw_full = full + 2 * STAGES;
   uint64_t* raw_empty = raw_full + 1;
+  uint64_t* nfull = raw_full + 2;  // [2] (decode)
+  uint64_t* nfree = raw_full + 4;  // [2] (decode)
+  constexpr int kThreads = rec_threads<NT, KMAX>();
   volatile int32_t* issued_s = reinterpret_cast<volatile int32_t*>(smem + SL::kIssued);
   float* gate = reinterpret_cast<float*>(smem + SL::kGate);
   float* kq_s = reinterpret_cast<float*>(smem + SL::kKq);
@@ -389,12 +404,16 @@ __global__ void __launch_bounds__(NT + 32, 1)
     }
     mbar_init(raw_full, 1);
     mbar_init(raw_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&nfull[b], Map::CB);  // the warps that write o: row block 0
+      mbar_init(&nfree[b], 1);
+    }
     issued_s[0] = 0;
     issued_s[1] = 0;
     fence_mbar_init();
   }
-  for (int j = tid; j < D; j += NT + 32) nw_s[j] = p.norm_w[j];
-  for (int i = tid; i < p.n; i += NT + 32) {
+  for (int j = tid; j < D; j += kThreads) nw_s[j] = p.norm_w[j];
+  for (int i = tid; i < p.n; i += kThreads) {
     slots_s[i] = p.slots[i];
     valid_s[i] = seq_check<VERIFY>(p, i);
     if (VERIFY) tab0_s[i] = p.tables[i];
@@ -415,6 +434,45 @@ __global__ void __launch_bounds__(NT + 32, 1)
     }
     return rounds;
   };
+
+  // =========================================================================== norm (decode)
+  if (SL::kNormWarp && tid >= NT + 32) {
+    using A = Act<T>;
+    const int lane = tid & 31, j = lane * 4;
+    int hq = 0;
+    Item it;
+    for (int r = next_valid(0, it); r < rounds; r = next_valid(r + 1, it)) {
+      for (int g = 0; g < G; ++g, ++hq) {
+        const int b = hq & 1;
+        if (!mbar_wait_bounded(&nfull[b], uint32_t(hq >> 1) & 1u)) {
+          if (lane == 0) report(p.status, GDN_ERR_TIMEOUT);
+          return;
+        }
+        float4 ov = make_float4(0.f, 0.f, 0.f, 0.f), z4 = ov;
+        if (j < D) {
+          ov = *reinterpret_cast<const float4*>(obuf + b * D + j);
+          z4 = *reinterpret_cast<const float4*>(xs + CH + g * D + j);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&nfree[b]);  // o and z are in registers
+        const float ss = warp_sum(ov.x * ov.x + ov.y * ov.y + ov.z * ov.z + ov.w * ov.w);
+        if (j < D) {
+          const int h = it.kh * G + g;
+          const float inv = rsqrtf(ss / float(D) + p.norm_eps);
+          const float4 w4 = *reinterpret_cast<const float4*>(nw_s + j);
+          float4 yv;
+          yv.x = ov.x * inv * w4.x * silu_f(z4.x);
+          yv.y = ov.y * inv * w4.y * silu_f(z4.y);
+          yv.z = ov.z * inv * w4.z * silu_f(z4.z);
+          yv.w = ov.w * inv * w4.w * silu_f(z4.w);
+          A::store4(reinterpret_cast<T*>(p.y) + size_t(it.row0) * p.Hv * D + h * D + j, yv);
+          if (p.core_out)
+            *reinterpret_cast<float4*>(p.core_out + (size_t(it.row0) * p.Hv + h) * D + j) = ov;
+        }
+      }
+    }
+    return;
+  }
 
   // =========================================================================== producer
   if (tid >= NT) {
@@ -560,7 +618,10 @@ __global__ void __launch_bounds__(NT + 32, 1)
         gate[(t * kMaxG + g) * 2 + 0] = al;
         gate[(t * kMaxG + g) * 2 + 1] = be;
       }
-      if (named_sync_or(1, NT, !ok)) {
+      // the norm warp has taken the previous item's z (and every earlier o) out of xs
+      const bool okn =
+          q == 0 || mbar_wait_bounded(&nfree[(q - 1) & 1], uint32_t((q - 1) >> 1) & 1u);
+      if (named_sync_or(1, NT, !ok || !okn)) {
         drain(q);
         return;
       }
@@ -653,7 +714,11 @@ __global__ void __launch_bounds__(NT + 32, 1)
     for (int g = 0; g < G; ++g) {
       const int h = it.kh * G + g;
       const int s = q % STAGES;
-      const bool ok = mbar_wait_bounded(&full[s], uint32_t(q / STAGES) & 1u);
+      const int hq = q;  // this head's index in the CTA's sequence of heads
+      bool ok = mbar_wait_bounded(&full[s], uint32_t(q / STAGES) & 1u);
+      // decode: obuf slot hq & 1 is free once the norm warp has taken head hq - 2
+      if (SL::kNormWarp && hq >= 2)
+        ok &= mbar_wait_bounded(&nfree[hq & 1], uint32_t((hq - 2) >> 1) & 1u);
       float4 S[Map::M];
       const SH* tile = reinterpret_cast<const SH*>(stage + size_t(s) * SL::kTile);
 #pragma unroll
@@ -666,7 +731,8 @@ __global__ void __launch_bounds__(NT + 32, 1)
         if (token_update<D, NT, true>(S, L, xq, xq + D, xq + (2 + g) * D,
                                       gate[(t * kMaxG + g) * 2 + 0],
                                       gate[(t * kMaxG + g) * 2 + 1], kq_s[t],
-                                      red + (t & 1) * 2 * Map::RB * D, obuf + t * D,
+                                      red + (t & 1) * 2 * Map::RB * D,
+                                      obuf + (SL::kNormWarp ? (hq & 1) : t) * D,
                                       t == 0 && !ok)) {
           drain(q - 1);
           return;
@@ -674,10 +740,17 @@ __global__ void __launch_bounds__(NT + 32, 1)
         if (VERIFY || t == k - 1)
           store_tile<D, NT, SH>(state_dst<D, VERIFY, SH>(p, it, tab_item, h, t), S, L);
       }
-      named_sync(1, NT);  // obuf complete
-      norm_tokens<T, D, Map::NW>(obuf, xs + CH + g * D, CHX, k, it.row0, h, nw_s,
-                                 p.norm_eps, p.Hv, reinterpret_cast<T*>(p.y), p.core_out,
-                                 L.warp, L.lane);
+      if constexpr (SL::kNormWarp) {
+        if (L.rb == 0) {  // this warp wrote part of o
+          __syncwarp();
+          if (L.lane == 0) mbar_arrive(&nfull[hq & 1]);
+        }
+      } else {
+        named_sync(1, NT);  // obuf complete
+        norm_tokens<T, D, Map::NW>(obuf, xs + CH + g * D, CHX, k, it.row0, h, nw_s,
+                                   p.norm_eps, p.Hv, reinterpret_cast<T*>(p.y), p.core_out,
+                                   L.warp, L.lane);
+      }
     }
   }
 }
@@ -692,7 +765,7 @@ cudaError_t launch_rec(const RecParams& p, cudaStream_t stream) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   const int P = p.n_items < sm_count() ? p.n_items : sm_count();
-  kern<<<P, NT + 32, smem, stream>>>(p);
+  kern<<<P, rec_threads<NT, KMAX>(), smem, stream>>>(p);
   return cudaGetLastError();
 }
 
