@@ -731,7 +731,9 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), 1)
         if (token_update<D, NT, true>(S, L, xq, xq + D, xq + (2 + g) * D,
                                       gate[(t * kMaxG + g) * 2 + 0],
                                       gate[(t * kMaxG + g) * 2 + 1], kq_s[t],
-                                      red + (t & 1) * 2 * Map::RB * D,
+                                      // decode alternates by head: no barrier separates
+                                      // one head's reduction reads from the next's writes
+                                      red + ((SL::kNormWarp ? hq : t) & 1) * 2 * Map::RB * D,
                                       obuf + (SL::kNormWarp ? (hq & 1) : t) * D,
                                       t == 0 && !ok)) {
           drain(q - 1);
