@@ -100,6 +100,22 @@ def ncu_traffic():
     return float(m_t.group(1))
 
 
+def slowest_rank(ms: float, device=None) -> float:
+    """The largest of every rank's time: replicas finish when the slowest one does."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job units per second: every rank's units over the slowest rank's time."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the GPU works."""
 
@@ -611,17 +627,14 @@ def main():
     sampler.stop()
     bench.check_status()
 
-    t = torch.tensor([ms_total], dtype=torch.float64, device=device)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_total = float(t.item())
+    ms_total = slowest_rank(ms_total, device)
     ms_step = ms_total / args.steps
-    tokens = N_SEQ * world * args.steps
-    value = tokens / (ms_total * 1e-3)
+    value = replica_throughput(N_SEQ * args.steps, world, ms_total)
     step_bytes = N_SEQ * DECODE_BYTES_PER_TOKEN + WEIGHT_BYTES
     achieved = step_bytes / (ms_step * 1e-3) / 1e9  # one kernel launch per step
     e2e_ms, h2d, d2h = bench.e2e(max(20, args.steps // 4), 5)
-    e2e = {"value": round(N_SEQ * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+    e2e_ms = slowest_rank(e2e_ms, device)
+    e2e = {"value": round(replica_throughput(N_SEQ, world, e2e_ms), 1), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": round(e2e_ms, 4)}
 
