@@ -46,9 +46,9 @@ DECODE_BYTES_PER_TOKEN = 4_194_304 + 131_072 + 32_896
 WEIGHT_BYTES = 131_840
 
 
-def verify_bytes(ks) -> int:
+def verify_bytes(ks, state_elem: int = 4) -> int:
     """Algorithmic bytes of one ragged verify launch (no conv intermediates)."""
-    state = 2 * 1024 * 1024
+    state = 32 * 128 * 128 * state_elem
     return int(sum(state + k * state + 131_072 + k * 32_896 for k in ks) + WEIGHT_BYTES)
 
 
@@ -252,7 +252,8 @@ def time_loop(torch, stream, fn, steps, warmup):
     return e0.elapsed_time(e1) / steps
 
 
-def verify_mode(device, steps, hbm_peak, warmup=3, n=N_SEQ):
+def verify_mode(device, steps, hbm_peak, warmup=3, n=N_SEQ, h16=False):
+    """The 128-sequence ragged verify; h16: on fp16 state pools and intermediates."""
     import torch
 
     from gated_deltanet_layer_conv1d_gb300 import device as dev
@@ -261,8 +262,11 @@ def verify_mode(device, steps, hbm_peak, warmup=3, n=N_SEQ):
     w = wl.ragged_verify(n=n)
     ks = [int(k) for k in w.lens]
     h_pool, conv_pool, slots = dev.states_to(w, device)
-    inter = torch.empty((n, 15, 32, 128, 128), dtype=torch.float32, device=device)
-    hsz = 32 * 128 * 128 * 4
+    sdt = torch.float16 if h16 else torch.float32
+    if h16:
+        h_pool = h_pool.half()
+    inter = torch.empty((n, 15, 32, 128, 128), dtype=sdt, device=device)
+    hsz = 32 * 128 * 128 * (2 if h16 else 4)
     tables = dev.wy_tables_to(ks, [h_pool.data_ptr() + i * hsz for i in range(n)],
                               [[inter[i, t].data_ptr() for t in range(15)] for i in range(n)],
                               device)
@@ -272,15 +276,17 @@ def verify_mode(device, steps, hbm_peak, warmup=3, n=N_SEQ):
     dims, weights = dev.dims_of(w.shape), dev.weights_to(w, device)
     stream = torch.cuda.current_stream(device)
 
+    run = gdn.gdn_verify_multi_h16 if h16 else gdn.gdn_verify_multi
+
     def fn(i):
-        gdn.gdn_verify_multi(dims, weights, inp, n, ks, tables, conv_pool, n, slots,
-                             None, y, None, status, stream)
+        run(dims, weights, inp, n, ks, tables, conv_pool, n, slots, None, y, None, status, stream)
 
     ms = time_loop(torch, stream, fn, steps, warmup)
     assert int(status.item()) == 0
-    byts = verify_bytes(ks)
+    byts = verify_bytes(ks, 2 if h16 else 4)
     gbs = byts / (ms * 1e-3) / 1e9
-    return {"workload": f"ragged_verify_{n}seq_k2to16", "tokens_per_step": sum(ks),
+    return {"workload": f"ragged_verify_{n}seq_k2to16" + ("_fp16_state_pool" if h16 else ""),
+            "tokens_per_step": sum(ks),
             "ms_per_step": round(ms, 4), "value": round(sum(ks) / (ms * 1e-3), 1),
             "unit": "tokens/s", "gpu_launches_per_step": 1,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
@@ -643,6 +649,8 @@ def main():
         modes["ragged_verify"] = verify_mode(device, max(10, min(200, args.steps // 10)), hbm_peak)
         modes["accepted_fold"] = fold_mode(device, 50, hbm_peak)
         modes["decode_fp16_state"] = decode_h16_mode(device, 200, hbm_peak)
+        modes["ragged_verify_fp16_state"] = verify_mode(device, max(10, min(200, args.steps // 10)),
+                                                        hbm_peak, h16=True)
         modes["chunked_prefill"] = prefill_mode(device, 5, tc_peak)
         modes["mixed_serving"] = mixed_mode(device, 3, hbm_peak, tc_peak)
     cpu = None
