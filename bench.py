@@ -201,33 +201,68 @@ class DecodeBench:
                                     self.status, self.stream)
 
     def e2e(self, steps: int, warmup: int):
-        """Same step with inputs copied in from pinned host memory and y read back."""
+        """The same step end to end: every step's inputs come in from pinned host memory and
+        its y goes back to pinned host memory, as a serving loop runs it.  Each step's
+        inputs travel as one block ([qkv | z | a | b] rows) on an input-copy stream and its
+        y on an output-copy stream, overlapping the neighbouring steps' kernels; two device
+        input and output buffers alternate."""
         torch = self.torch
-        host_in = [{k: getattr(x, k).cpu().pin_memory() for k in ("qkv", "z", "a", "b")}
-                   for x in self.inputs]
-        dev_in = self.inputs[0]
-        y_host = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host_in[0].values())
+        dev = self.y.device
+        n = N_SEQ
+        widths = {"qkv": 8192, "z": 4096, "a": 32, "b": 32}
+        offs, o = {}, 0
+        for k, wdt in widths.items():
+            offs[k] = o
+            o += n * wdt
+        total = o
+
+        def views(block):
+            return self.gdn.Inputs(*[block[offs[k]:offs[k] + n * widths[k]].view(n, widths[k])
+                                     for k in ("qkv", "z", "a", "b")])
+
+        host_blocks = []
+        for x in self.inputs:  # one pinned block per rotating pool
+            hb = torch.empty(total, dtype=torch.bfloat16).pin_memory()
+            for k in widths:
+                hb[offs[k]:offs[k] + n * widths[k]].copy_(getattr(x, k).reshape(-1).cpu())
+            host_blocks.append(hb)
+        dev_blocks = [torch.empty(total, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        dev_in = [views(b) for b in dev_blocks]
+        ys = [torch.empty_like(self.y) for _ in range(2)]
+        y_host = [torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory() for _ in range(2)]
+        h2d = total * 2
         d2h = self.y.numel() * self.y.element_size()
+        cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        computed = [torch.cuda.Event() for _ in range(2)]
+        released = [torch.cuda.Event() for _ in range(2)]
 
         def one(i):
-            src = host_in[i % POOLS]
-            for k in ("qkv", "z", "a", "b"):
-                getattr(dev_in, k).copy_(src[k], non_blocking=True)
-            self.gdn.gdn_decode_batched(self.dims, self.weights, dev_in, N_SEQ, self.h_pool,
+            b = i & 1
+            with torch.cuda.stream(cin):
+                if i >= 2:
+                    cin.wait_event(released[b])  # step i-2 is done with buffers b
+                dev_blocks[b].copy_(host_blocks[i % POOLS], non_blocking=True)
+                in_ready[b].record(cin)
+            self.stream.wait_event(in_ready[b])
+            self.gdn.gdn_decode_batched(self.dims, self.weights, dev_in[b], N_SEQ, self.h_pool,
                                         self.conv_pool, self.n_slots, self.slots[i % POOLS],
-                                        self.y, None, self.status, self.stream)
-            y_host.copy_(self.y, non_blocking=True)
+                                        ys[b], None, self.status, self.stream)
+            computed[b].record(self.stream)
+            with torch.cuda.stream(cout):
+                cout.wait_event(computed[b])
+                y_host[b].copy_(ys[b], non_blocking=True)
+                released[b].record(cout)
 
         for i in range(warmup):
             one(i)
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(self.stream)
+        t0.record(cin)  # before the first input copy
         for i in range(steps):
             one(i)
-        t1.record(self.stream)
+        t1.record(cout)  # after the last result copy, which follows every kernel
         torch.cuda.synchronize()
         ms = t0.elapsed_time(t1) / steps
         return ms, h2d, d2h
