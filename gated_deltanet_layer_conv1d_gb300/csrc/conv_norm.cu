@@ -329,10 +329,10 @@ __global__ void gdn_gated_rmsnorm_kernel(const float* __restrict__ o, const T* _
       if (live && r < rows) {
         const float inv = rsqrtf(ss / float(D) + eps);
         float4 yv;
-        yv.x = ov[k].x * inv * w4.x * silu_f(z4[k].x);
-        yv.y = ov[k].y * inv * w4.y * silu_f(z4[k].y);
-        yv.z = ov[k].z * inv * w4.z * silu_f(z4[k].z);
-        yv.w = ov[k].w * inv * w4.w * silu_f(z4[k].w);
+        yv.x = ov[k].x * inv * w4.x * silu_fast(z4[k].x);
+        yv.y = ov[k].y * inv * w4.y * silu_fast(z4[k].y);
+        yv.z = ov[k].z * inv * w4.z * silu_fast(z4[k].z);
+        yv.w = ov[k].w * inv * w4.w * silu_fast(z4[k].w);
         A::store4(y + size_t(t) * Hv * D + h * D + j, yv);
       }
     }
