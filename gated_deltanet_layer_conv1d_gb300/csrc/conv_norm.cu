@@ -235,30 +235,59 @@ __global__ void __launch_bounds__(kTileWarps * 32)
     for (int j = 0; j < kW - 1; ++j)
       win[j] = A::load4(reinterpret_cast<const __nv_bfloat16*>(col + j * kTileRowBytes));
   }
-  for (int r = 0; r < nrows; ++r) {
-    const float4 x =
-        A::load4(reinterpret_cast<const __nv_bfloat16*>(col + (r + kW - 1) * kTileRowBytes));
-    float4 y;
-    y.x = silu_fast(w0.x * win[0].x + w0.y * win[1].x + w0.z * win[2].x + w0.w * x.x);
-    y.y = silu_fast(w1.x * win[0].y + w1.y * win[1].y + w1.z * win[2].y + w1.w * x.y);
-    y.z = silu_fast(w2.x * win[0].z + w2.y * win[1].z + w2.z * win[2].z + w2.w * x.z);
-    y.w = silu_fast(w3.x * win[0].w + w3.y * win[1].w + w3.z * win[2].w + w3.w * x.w);
-    win[0] = win[1];
-    win[1] = win[2];
-    win[2] = x;
-    if (scale != 0.f) {
-      const float ss = warp_sum(y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w);
-      const float rn = scale * rsqrtf(ss + p.l2_eps);
-      y.x *= rn;
-      y.y *= rn;
-      y.z *= rn;
-      y.w *= rn;
+  // Four tokens per pass: their inputs are loaded first, the window rotates through
+  // registers, and the four L2 sums reduce side by side.
+  unsigned char* dst = ws + tile + (lane >> 4) * (kC * 128) + (lane * 4 & 7) * 2;
+  const int piece = (lane & 15) >> 1;  // 16-byte piece of the lane's 4 channels in a row
+  for (int r0 = 0; r0 < nrows; r0 += 4) {
+    float4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      x[u] = (r0 + u < nrows) ? A::load4(reinterpret_cast<const __nv_bfloat16*>(
+                                    col + (r0 + u + kW - 1) * kTileRowBytes))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 y[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4 a = u >= 3 ? x[u - 3] : win[u];
+      const float4 b = u >= 2 ? x[u - 2] : win[u + 1];
+      const float4 c = u >= 1 ? x[u - 1] : win[u + 2];
+      y[u].x = silu_fast(w0.x * a.x + w0.y * b.x + w0.z * c.x + w0.w * x[u].x);
+      y[u].y = silu_fast(w1.x * a.y + w1.y * b.y + w1.z * c.y + w1.w * x[u].y);
+      y[u].z = silu_fast(w2.x * a.z + w2.y * b.z + w2.z * c.z + w2.w * x[u].z);
+      y[u].w = silu_fast(w3.x * a.w + w3.y * b.w + w3.z * c.w + w3.w * x[u].w);
     }
-    const __half2 lo = __floats2half2_rn(y.x, y.y), hi = __floats2half2_rn(y.z, y.w);
-    uint2 pk;
-    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(ws + tile + tc::sw128_offset(kC, r_begin + r, lane * 4)) = pk;
+    win[0] = x[1];
+    win[1] = x[2];
+    win[2] = x[3];
+    if (scale != 0.f) {
+      float ss[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        ss[u] = y[u].x * y[u].x + y[u].y * y[u].y + y[u].z * y[u].z + y[u].w * y[u].w;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float rn = scale * rsqrtf(ss[u] + p.l2_eps);
+        y[u].x *= rn;
+        y[u].y *= rn;
+        y[u].z *= rn;
+        y[u].w *= rn;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (r0 + u >= nrows) break;
+      const int row = r_begin + r0 + u;
+      const __half2 lo = __floats2half2_rn(y[u].x, y[u].y), hi = __floats2half2_rn(y[u].z, y[u].w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(dst + row * 128 + ((piece ^ (row & 7)) << 4)) = pk;
+    }
   }
 }
 
