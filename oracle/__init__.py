@@ -61,6 +61,7 @@ class OrcDims(ctypes.Structure):
         ("l2_eps", ctypes.c_double),
         ("norm_eps", ctypes.c_double),
         ("h_fp16", ctypes.c_int32),
+        ("norm_gate", ctypes.c_int32),
     ]
 
 
@@ -75,6 +76,7 @@ class Dims:
     l2_eps: float
     norm_eps: float
     h_fp16: bool = False  # store the state as binary16 after every token
+    norm_gate: int = 0    # 0: y gated by SiLU(z); 1: gated by sigmoid(z)
 
     @property
     def conv_dim(self) -> int:
@@ -82,7 +84,8 @@ class Dims:
 
     def c(self) -> OrcDims:
         return OrcDims(self.n_k_heads, self.n_v_heads, self.d_k, self.d_v, self.d_conv,
-                       self.q_scale, self.l2_eps, self.norm_eps, int(self.h_fp16))
+                       self.q_scale, self.l2_eps, self.norm_eps, int(self.h_fp16),
+                       int(self.norm_gate))
 
 
 _D = ctypes.POINTER(ctypes.c_double)
@@ -106,7 +109,8 @@ def lib():
                                      ctypes.c_double, _D]
         L.orc_recurrence.argtypes = [ctypes.POINTER(OrcDims), _I32, _D, _D, _D, _D, _D, _D,
                                      _D, _D]
-        L.orc_gated_rmsnorm.argtypes = [_I32, _I32, _I32, _D, _D, _D, ctypes.c_double, _D]
+        L.orc_gated_rmsnorm.argtypes = [_I32, _I32, _I32, _D, _D, _D, ctypes.c_double, _I32,
+                                        _D]
         L.orc_mixer.argtypes = [ctypes.POINTER(OrcDims), _I32] + [_D] * 14
         L.orc_chunked.argtypes = [ctypes.POINTER(OrcDims), _I32, _I32, _D, _D, _D, _D, _D,
                                   _D, _D, _I32]
@@ -199,12 +203,13 @@ def recurrence(dims: Dims, qn, kn, v, alpha, beta, H, snapshots: bool = False):
     return Hn, o, snap
 
 
-def gated_rmsnorm(o, z, w, eps: float):
-    """a7: o [T][H_v][d_v], z [T][H_v*d_v], w [d_v] -> y [T][H_v*d_v]."""
+def gated_rmsnorm(o, z, w, eps: float, gate: int = 0):
+    """a7: o [T][H_v][d_v], z [T][H_v*d_v], w [d_v] -> y [T][H_v*d_v]; gate 0 multiplies by
+    SiLU(z), gate 1 by sigmoid(z)."""
     o, z, w = map(_f64, (o, z, w))
     T, Hv, dv = o.shape
     y = np.empty((T, Hv * dv))
-    lib().orc_gated_rmsnorm(T, Hv, dv, _p(o), _p(z), _p(w), float(eps), _p(y))
+    lib().orc_gated_rmsnorm(T, Hv, dv, _p(o), _p(z), _p(w), float(eps), int(gate), _p(y))
     return y
 
 

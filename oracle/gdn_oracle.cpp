@@ -17,7 +17,10 @@
 //           o_t = S_t q_t
 //       (layer_struct.rs, gdn_f32_k);
 //   a7  Z-gated RMSNorm over d_v: y = o / sqrt(mean(o^2) + eps) * w * SiLU(z)
-//       (layer_struct.rs, gated_rms_norm_f32_k).
+//       (layer_struct.rs, gated_rms_norm_f32_k); with OrcDims::norm_gate = 1 the gate is
+//       sigmoid(z) instead of SiLU(z), the reading taken of the gdn_norm_sigmoid models
+//       (layer_struct.rs, the gated_rms_norm_f32_strided_k field), which the pages name
+//       as a model flag without printing the formula.
 // A separate routine, orc_chunked, writes out the chunked (WY / UT-transform) form of
 // the same recurrence (layer_struct.rs, the FLA chunked prefill fields
 // gdn_prefill_fla_recompute_wu_k, gdn_prefill_fla_chunk_delta_h_k,
@@ -74,6 +77,7 @@ struct OrcDims {
   double l2_eps;      // q <- q / sqrt(sum q^2 + l2_eps)
   double norm_eps;    // gated RMSNorm epsilon
   int32_t h_fp16;     // 1: the state is stored as binary16 after every token
+  int32_t norm_gate;  // 0: y gated by SiLU(z); 1: gated by sigmoid(z)
 };
 
 // Rounds x to the nearest IEEE 754 binary16 value, ties to even, returned as a double.
@@ -210,14 +214,18 @@ void orc_recurrence(const OrcDims* d, int32_t T, const double* qn, const double*
 }
 
 // a7: Z-gated RMSNorm.  o: [T][H_v][d_v]; z: [T][H_v*d_v]; w: [d_v]; y: [T][H_v*d_v].
+// gate 0 multiplies by SiLU(z), gate 1 by sigmoid(z).
 void orc_gated_rmsnorm(int32_t T, int32_t n_v_heads, int32_t dv, const double* o,
-                       const double* z, const double* w, double eps, double* y) {
+                       const double* z, const double* w, double eps, int32_t gate, double* y) {
   for (int64_t r = 0; r < (int64_t)T * n_v_heads; ++r) {
     const double* orow = o + r * dv;
     double ss = 0.0;
     for (int32_t j = 0; j < dv; ++j) ss += orow[j] * orow[j];
     const double inv = 1.0 / std::sqrt(ss / dv + eps);
-    for (int32_t j = 0; j < dv; ++j) y[r * dv + j] = orow[j] * inv * w[j] * silu(z[r * dv + j]);
+    for (int32_t j = 0; j < dv; ++j) {
+      const double zj = z[r * dv + j];
+      y[r * dv + j] = orow[j] * inv * w[j] * (gate ? sigmoid(zj) : silu(zj));
+    }
   }
 }
 
@@ -246,7 +254,7 @@ void orc_mixer(const OrcDims* d, int32_t T, const double* qkv, const double* z, 
   orc_gates(T, Hv, a, b, A_log, dt_bias, alpha.data(), beta.data());
   orc_recurrence(d, T, qn.data(), kn.data(), v.data(), alpha.data(), beta.data(), H, out_o,
                  H_snap);
-  orc_gated_rmsnorm(T, Hv, dv, out_o, z, norm_w, d->norm_eps, y);
+  orc_gated_rmsnorm(T, Hv, dv, out_o, z, norm_w, d->norm_eps, d->norm_gate, y);
 }
 
 // Rounds a double to the nearest bfloat16 value (ties to even), returned as double.

@@ -62,7 +62,7 @@ def assert_state_close(H_gpu, H_orc, what="state", tol=STATE_TOL):
 def odims(shape: wl.LayerShape) -> oracle.Dims:
     return oracle.Dims(shape.n_k_heads, shape.n_v_heads, shape.d_k, shape.d_v, shape.d_conv,
                        float(np.float32(shape.q_scale)), float(np.float32(shape.l2_eps)),
-                       float(np.float32(shape.norm_eps)))
+                       float(np.float32(shape.norm_eps)), norm_gate=shape.norm_gate)
 
 
 def oracle_seqs(w: wl.Workload, token_rows: dict, lens, H0=None, conv0=None, idx=None,

@@ -235,6 +235,48 @@ def test_gated_rmsnorm_closed_forms():
     np.testing.assert_allclose(y[0], o[0, 0] / math.sqrt(25 + eps) * w * silu, rtol=1e-14)
 
 
+def test_gated_rmsnorm_sigmoid_gate_closed_forms():
+    """The gdn_norm_sigmoid models' gate (layer_struct.rs, gated_rms_norm_f32_strided_k):
+    sigmoid(z) in place of SiLU(z); with a constant o the norm part is sign(c) up to eps."""
+    dv, eps = 8, 1e-6
+    w = np.linspace(0.5, 1.5, dv)
+    z = np.linspace(-3, 3, dv)
+    for c in (-2.0, 0.5, 3.0):
+        o = np.full((1, 1, dv), c)
+        y = oracle.gated_rmsnorm(o, z[None], w, eps, gate=1)
+        np.testing.assert_allclose(y[0], c / math.sqrt(c * c + eps) * w * scipy.special.expit(z),
+                                   rtol=1e-14)
+    # z = 0 halves the normalised row under the sigmoid gate and zeroes it under SiLU
+    o = np.random.default_rng(5).standard_normal((3, 2, dv))
+    zero = np.zeros((3, 2 * dv))
+    y1 = oracle.gated_rmsnorm(o, zero, w, eps, gate=1).reshape(3, 2, dv)
+    rms = np.sqrt((o * o).mean(-1, keepdims=True) + eps)
+    np.testing.assert_allclose(y1, 0.5 * o / rms * w, rtol=1e-14)
+    assert not oracle.gated_rmsnorm(o, zero, w, eps, gate=0).any()
+
+
+def test_mixer_norm_gate_option_reaches_the_norm():
+    """Through the whole mixer, SiLU(z) = z sigmoid(z) ties the two gates' outputs:
+    y_silu = z * y_sigmoid element by element, with o and the state unchanged."""
+    shape = wl.TINY
+    rng = np.random.default_rng(17)
+    T = 6
+    toks = wl.make_tokens(rng, shape, T, bf16=False)
+    wts = wl.make_weights(rng, shape)
+    conv0 = rng.standard_normal((shape.conv_dim, shape.d_conv))
+    H0 = rng.standard_normal((shape.n_v_heads, shape.d_k, shape.d_v)) * 0.1
+    base = dict(n_k_heads=shape.n_k_heads, n_v_heads=shape.n_v_heads, d_k=shape.d_k,
+                d_v=shape.d_v, d_conv=shape.d_conv, q_scale=shape.q_scale, l2_eps=1e-6,
+                norm_eps=1e-6)
+    r0 = oracle.mixer(oracle.Dims(**base), wts, toks["qkv"], toks["z"], toks["a"], toks["b"],
+                      conv0.copy(), H0.copy())
+    r1 = oracle.mixer(oracle.Dims(**base, norm_gate=1), wts, toks["qkv"], toks["z"], toks["a"],
+                      toks["b"], conv0.copy(), H0.copy())
+    np.testing.assert_array_equal(r0.o, r1.o)
+    np.testing.assert_array_equal(r0.H, r1.H)
+    np.testing.assert_allclose(r0.y, toks["z"] * r1.y, rtol=1e-12, atol=1e-300)
+
+
 # ---------------------------------------------------------------- chunked == loop
 def _prepared(rng, dims, T, alpha_lo=0.05):
     qn = rng.standard_normal((T, dims.n_k_heads, dims.d_k))
