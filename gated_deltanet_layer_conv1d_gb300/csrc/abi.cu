@@ -48,6 +48,8 @@ gdn_status check_dims(const gdn_dims* d) {
   if (!std::isfinite(d->q_scale) || !std::isfinite(d->l2_eps) || !std::isfinite(d->norm_eps) ||
       d->l2_eps < 0.f || d->norm_eps < 0.f)
     return GDN_ERR_INVALID_ARGUMENT;
+  if (d->norm_gate != GDN_NORM_GATE_SILU && d->norm_gate != GDN_NORM_GATE_SIGMOID)
+    return GDN_ERR_INVALID_ARGUMENT;
   return GDN_OK;
 }
 
@@ -113,6 +115,7 @@ void fill_common(RecParams& p, const gdn_dims& d, const gdn_weights& w, const gd
   p.q_scale = d.q_scale;
   p.l2_eps = d.l2_eps;
   p.norm_eps = d.norm_eps;
+  p.norm_gate = d.norm_gate;
   p.conv_w = w.conv_w;
   p.A_log = w.A_log;
   p.dt_bias = w.dt_bias;
@@ -124,6 +127,24 @@ void fill_common(RecParams& p, const gdn_dims& d, const gdn_weights& w, const gd
   p.a = in.a;
   p.b = in.b;
   p.ab_stride = in.ab_stride;
+}
+
+gdn_status gated_rmsnorm_impl(const float* o, const void* z, int64_t z_stride, const float* w,
+                              float eps, int32_t T, int32_t n_v_heads, int32_t d_v,
+                              int32_t dtype, int gate, void* y, gdn_stream_t stream) {
+  if (T < 0 || n_v_heads <= 0 || !std::isfinite(eps) || eps < 0.f)
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (d_v != 16 && d_v != 128) return GDN_ERR_UNSUPPORTED_DIMS;
+  if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return GDN_ERR_INVALID_ARGUMENT;
+  if (T == 0) return GDN_OK;
+  if (!o || !z || !w || !y) return GDN_ERR_NULL_POINTER;
+  if (z_stride < int64_t(n_v_heads) * d_v) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned(o, 16) || !aligned(z, 16) || !aligned(w, 16) || !aligned(y, 16) ||
+      (z_stride * esize(dtype)) % 16 != 0)
+    return GDN_ERR_MISALIGNED;
+  const cudaError_t e = launch_gated_rmsnorm(o, z, z_stride, w, eps, T, n_v_heads, d_v, dtype,
+                                             gate, y, stream);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 }  // namespace
@@ -418,6 +439,7 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* weights,
   p.q_scale = dims->q_scale;
   p.l2_eps = dims->l2_eps;
   p.norm_eps = dims->norm_eps;
+  p.norm_gate = dims->norm_gate;
   p.conv_w = weights->conv_w;
   p.A_log = weights->A_log;
   p.dt_bias = weights->dt_bias;
@@ -460,22 +482,19 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* weights,
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+
 gdn_status gdn_gated_rmsnorm(const float* o, const void* z, int64_t z_stride, const float* w,
                              float eps, int32_t T, int32_t n_v_heads, int32_t d_v,
                              int32_t dtype, void* y, gdn_stream_t stream) {
-  if (T < 0 || n_v_heads <= 0 || !std::isfinite(eps) || eps < 0.f)
-    return GDN_ERR_INVALID_ARGUMENT;
-  if (d_v != 16 && d_v != 128) return GDN_ERR_UNSUPPORTED_DIMS;
-  if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return GDN_ERR_INVALID_ARGUMENT;
-  if (T == 0) return GDN_OK;
-  if (!o || !z || !w || !y) return GDN_ERR_NULL_POINTER;
-  if (z_stride < int64_t(n_v_heads) * d_v) return GDN_ERR_INVALID_ARGUMENT;
-  if (!aligned(o, 16) || !aligned(z, 16) || !aligned(w, 16) || !aligned(y, 16) ||
-      (z_stride * esize(dtype)) % 16 != 0)
-    return GDN_ERR_MISALIGNED;
-  const cudaError_t e = launch_gated_rmsnorm(o, z, z_stride, w, eps, T, n_v_heads, d_v, dtype,
-                                             y, stream);
-  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  return gated_rmsnorm_impl(o, z, z_stride, w, eps, T, n_v_heads, d_v, dtype,
+                            GDN_NORM_GATE_SILU, y, stream);
+}
+
+gdn_status gdn_gated_rmsnorm_sigmoid(const float* o, const void* z, int64_t z_stride,
+                                     const float* w, float eps, int32_t T, int32_t n_v_heads,
+                                     int32_t d_v, int32_t dtype, void* y, gdn_stream_t stream) {
+  return gated_rmsnorm_impl(o, z, z_stride, w, eps, T, n_v_heads, d_v, dtype,
+                            GDN_NORM_GATE_SIGMOID, y, stream);
 }
 
 gdn_status gdn_wy_tables_fill(uint64_t* host_tables, int32_t n, const int32_t* ks,

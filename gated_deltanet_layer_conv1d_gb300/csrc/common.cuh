@@ -64,6 +64,13 @@ __device__ __forceinline__ float silu_f(float x) { return x / (1.f + expf(-x)); 
 // rounding of the outputs it feeds).
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
+// The z gate of the gated RMSNorm: SiLU(z) = z / (1 + e^-z) (kind 0) or sigmoid(z) =
+// 1 / (1 + e^-z) (kind 1); only the numerator differs, so the kind is a select, not a branch.
+__device__ __forceinline__ float zgate(float z, int kind) { return (kind ? 1.f : z) / (1.f + expf(-z)); }
+__device__ __forceinline__ float zgate_fast(float z, int kind) {
+  return __fdividef(kind ? 1.f : z, 1.f + __expf(-z));
+}
+
 // 2^x with the hardware approximation (ex2.approx, relative error below 2^-22; subnormal
 // results flush to zero).
 __device__ __forceinline__ float exp2_fast(float x) {

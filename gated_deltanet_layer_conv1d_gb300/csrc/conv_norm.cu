@@ -15,7 +15,8 @@
 //   raw inputs (exact copies).  Running it as a second launch keeps every read of the
 //   old state ordered before the write of the new one.
 // gdn_gated_rmsnorm_kernel: one warp per (token, value head) (layer_struct.rs,
-//   gated_rms_norm_f32_k / gated_rms_norm_prefill_k).
+//   gated_rms_norm_f32_k / gated_rms_norm_prefill_k); GATE 1 takes sigmoid(z) in place of
+//   SiLU(z) (gated_rms_norm_f32_strided_k of the gdn_norm_sigmoid models).
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -325,7 +326,7 @@ __global__ void gdn_seqlens_check_kernel(const int32_t* cu, int n, int total, in
 
 // kRows rows per warp per pass, all their loads issued before any use, so each warp keeps
 // several independent rows in flight.
-template <typename T, int D>
+template <typename T, int D, int GATE>
 __global__ void gdn_gated_rmsnorm_kernel(const float* __restrict__ o, const T* __restrict__ z,
                                          int64_t z_stride, const float* __restrict__ w,
                                          float eps, int T_, int Hv, T* __restrict__ y) {
@@ -358,10 +359,10 @@ __global__ void gdn_gated_rmsnorm_kernel(const float* __restrict__ o, const T* _
       if (live && r < rows) {
         const float inv = rsqrtf(ss / float(D) + eps);
         float4 yv;
-        yv.x = ov[k].x * inv * w4.x * silu_fast(z4[k].x);
-        yv.y = ov[k].y * inv * w4.y * silu_fast(z4[k].y);
-        yv.z = ov[k].z * inv * w4.z * silu_fast(z4[k].z);
-        yv.w = ov[k].w * inv * w4.w * silu_fast(z4[k].w);
+        yv.x = ov[k].x * inv * w4.x * zgate_fast(z4[k].x, GATE);
+        yv.y = ov[k].y * inv * w4.y * zgate_fast(z4[k].y, GATE);
+        yv.z = ov[k].z * inv * w4.z * zgate_fast(z4[k].z, GATE);
+        yv.w = ov[k].w * inv * w4.w * zgate_fast(z4[k].w, GATE);
         A::store4(y + size_t(t) * Hv * D + h * D + j, yv);
       }
     }
@@ -413,26 +414,38 @@ cudaError_t launch_seqlens_check(const int32_t* cu, int n, int total, int32_t* s
   return cudaGetLastError();
 }
 
+namespace {
+
+template <int GATE>
+void gated_rmsnorm_gate(const float* o, const void* z, int64_t z_stride, const float* w, float eps,
+                        int T, int Hv, int D, int dtype, void* y, int blocks, int threads,
+                        cudaStream_t stream) {
+  if (dtype == GDN_DTYPE_BF16) {
+    auto zp = reinterpret_cast<const __nv_bfloat16*>(z);
+    auto yp = reinterpret_cast<__nv_bfloat16*>(y);
+    if (D == 128) gdn_gated_rmsnorm_kernel<__nv_bfloat16, 128, GATE><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
+    else gdn_gated_rmsnorm_kernel<__nv_bfloat16, 16, GATE><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
+  } else {
+    auto zp = reinterpret_cast<const float*>(z);
+    auto yp = reinterpret_cast<float*>(y);
+    if (D == 128) gdn_gated_rmsnorm_kernel<float, 128, GATE><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
+    else gdn_gated_rmsnorm_kernel<float, 16, GATE><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
+  }
+}
+
+}  // namespace
+
 cudaError_t launch_gated_rmsnorm(const float* o, const void* z, int64_t z_stride,
                                  const float* w, float eps, int T, int Hv, int D, int dtype,
-                                 void* y, cudaStream_t stream) {
+                                 int gate, void* y, cudaStream_t stream) {
   const int rows = T * Hv;
   if (rows == 0) return cudaSuccess;
   const int threads = 256, per_block = threads / 32;
   int blocks = (rows + per_block - 1) / per_block;
   const int cap = sm_count() * 8;
   if (blocks > cap) blocks = cap;
-  if (dtype == GDN_DTYPE_BF16) {
-    auto zp = reinterpret_cast<const __nv_bfloat16*>(z);
-    auto yp = reinterpret_cast<__nv_bfloat16*>(y);
-    if (D == 128) gdn_gated_rmsnorm_kernel<__nv_bfloat16, 128><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
-    else gdn_gated_rmsnorm_kernel<__nv_bfloat16, 16><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
-  } else {
-    auto zp = reinterpret_cast<const float*>(z);
-    auto yp = reinterpret_cast<float*>(y);
-    if (D == 128) gdn_gated_rmsnorm_kernel<float, 128><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
-    else gdn_gated_rmsnorm_kernel<float, 16><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
-  }
+  if (gate) gated_rmsnorm_gate<1>(o, z, z_stride, w, eps, T, Hv, D, dtype, y, blocks, threads, stream);
+  else gated_rmsnorm_gate<0>(o, z, z_stride, w, eps, T, Hv, D, dtype, y, blocks, threads, stream);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@ constexpr int kMaxG = 4;  // value heads per key head a launch supports
 struct RecParams {
   int32_t Hk, Hv, G, conv_dim, n, n_slots;
   float q_scale, l2_eps, norm_eps;
+  int32_t norm_gate;  // 0: SiLU(z), 1: sigmoid(z)
   const float* conv_w;
   const float* A_log;
   const float* dt_bias;
@@ -77,12 +78,13 @@ cudaError_t launch_prefill_prep(const ConvParams& p, cudaStream_t stream);
 
 cudaError_t launch_gated_rmsnorm(const float* o, const void* z, int64_t z_stride,
                                  const float* w, float eps, int T, int Hv, int D, int dtype,
-                                 void* y, cudaStream_t stream);
+                                 int gate, void* y, cudaStream_t stream);
 
 // Chunked prefill.
 struct PrefillParams {
   int32_t Hk, Hv, G, D, conv_dim, n, n_slots, total_tokens, max_seqlen, max_chunks;
   float q_scale, l2_eps, norm_eps;
+  int32_t norm_gate;  // 0: SiLU(z), 1: sigmoid(z)
   const float* conv_w;
   const float* A_log;
   const float* dt_bias;

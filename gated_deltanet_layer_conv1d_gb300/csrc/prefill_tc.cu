@@ -790,7 +790,8 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
               const float2 zf = __bfloat1622float2(z2[e]);
               const int u = 8 * k + 2 * e;
               const __nv_bfloat162 yy = __floats2bfloat162_rn(
-                  v[u] * inv * nw[u] * silu_fast(zf.x), v[u + 1] * inv * nw[u + 1] * silu_fast(zf.y));
+                  v[u] * inv * nw[u] * zgate_fast(zf.x, p.norm_gate),
+                  v[u + 1] * inv * nw[u + 1] * zgate_fast(zf.y, p.norm_gate));
               out[e] = *reinterpret_cast<const uint32_t*>(&yy);
             }
             *reinterpret_cast<uint4*>(yo + 8 * k) = make_uint4(out[0], out[1], out[2], out[3]);
@@ -861,7 +862,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, float* o_work, cudaStream_
   cudaError_t e = launch_spine<64>(q, stream);
   if (e != cudaSuccess) return e;
   return launch_gated_rmsnorm(q.core_out, p.z, p.z_stride, p.norm_w, p.norm_eps,
-                              p.total_tokens, p.Hv, kD, GDN_DTYPE_BF16, p.y, stream);
+                              p.total_tokens, p.Hv, kD, GDN_DTYPE_BF16, p.norm_gate, p.y, stream);
 }
 
 }  // namespace gdn

@@ -215,7 +215,8 @@ __device__ __forceinline__ void l2norm_tokens(float* x, int stride, int k, float
 template <typename T, int D, int NW>
 __device__ __forceinline__ void norm_tokens(const float* o, const float* z, int zstride, int k,
                                             int row0, int h, const float* norm_w, float eps,
-                                            int Hv, T* y, float* core_out, int warp, int lane) {
+                                            int gate, int Hv, T* y, float* core_out, int warp,
+                                            int lane) {
   using A = Act<T>;
   for (int t = warp; t < k; t += NW) {
     const int row = row0 + t;
@@ -228,10 +229,10 @@ __device__ __forceinline__ void norm_tokens(const float* o, const float* z, int 
       const float4 w4 = *reinterpret_cast<const float4*>(norm_w + j);
       const float4 z4 = *reinterpret_cast<const float4*>(z + t * zstride + j);
       float4 yv;
-      yv.x = ov.x * inv * w4.x * silu_f(z4.x);
-      yv.y = ov.y * inv * w4.y * silu_f(z4.y);
-      yv.z = ov.z * inv * w4.z * silu_f(z4.z);
-      yv.w = ov.w * inv * w4.w * silu_f(z4.w);
+      yv.x = ov.x * inv * w4.x * zgate(z4.x, gate);
+      yv.y = ov.y * inv * w4.y * zgate(z4.y, gate);
+      yv.z = ov.z * inv * w4.z * zgate(z4.z, gate);
+      yv.w = ov.w * inv * w4.w * zgate(z4.w, gate);
       A::store4(y + size_t(row) * Hv * D + h * D + j, yv);
       if (core_out) *reinterpret_cast<float4*>(core_out + (size_t(row) * Hv + h) * D + j) = ov;
     }
@@ -461,10 +462,10 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), 1)
           const float inv = rsqrtf(ss / float(D) + p.norm_eps);
           const float4 w4 = *reinterpret_cast<const float4*>(nw_s + j);
           float4 yv;
-          yv.x = ov.x * inv * w4.x * silu_f(z4.x);
-          yv.y = ov.y * inv * w4.y * silu_f(z4.y);
-          yv.z = ov.z * inv * w4.z * silu_f(z4.z);
-          yv.w = ov.w * inv * w4.w * silu_f(z4.w);
+          yv.x = ov.x * inv * w4.x * zgate(z4.x, p.norm_gate);
+          yv.y = ov.y * inv * w4.y * zgate(z4.y, p.norm_gate);
+          yv.z = ov.z * inv * w4.z * zgate(z4.z, p.norm_gate);
+          yv.w = ov.w * inv * w4.w * zgate(z4.w, p.norm_gate);
           A::store4(reinterpret_cast<T*>(p.y) + size_t(it.row0) * p.Hv * D + h * D + j, yv);
           if (p.core_out)
             *reinterpret_cast<float4*>(p.core_out + (size_t(it.row0) * p.Hv + h) * D + j) = ov;
@@ -750,8 +751,8 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), 1)
       } else {
         named_sync(1, NT);  // obuf complete
         norm_tokens<T, D, Map::NW>(obuf, xs + CH + g * D, CHX, k, it.row0, h, nw_s,
-                                   p.norm_eps, p.Hv, reinterpret_cast<T*>(p.y), p.core_out,
-                                   L.warp, L.lane);
+                                   p.norm_eps, p.norm_gate, p.Hv, reinterpret_cast<T*>(p.y),
+                                   p.core_out, L.warp, L.lane);
       }
     }
   }
@@ -883,7 +884,8 @@ __global__ void __launch_bounds__(NT, 1)
     }
     __syncthreads();
     norm_tokens<T, D, Map::NW>(obuf, xs + 3 * D, CHX, k, t_begin + t0, h, p.norm_w, p.norm_eps,
-                               p.Hv, reinterpret_cast<T*>(p.y), p.core_out, L.warp, L.lane);
+                               p.norm_gate, p.Hv, reinterpret_cast<T*>(p.y), p.core_out, L.warp,
+                               L.lane);
     __syncthreads();  // xs, obuf and gate are rewritten by the next segment
   }
   store_tile<D, NT>(Hg, S, L);

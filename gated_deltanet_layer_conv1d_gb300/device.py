@@ -15,7 +15,7 @@ from .workloads import LayerShape, Workload
 
 def dims_of(shape: LayerShape) -> gdn.gdn_dims:
     return gdn.make_dims(shape.n_k_heads, shape.n_v_heads, shape.d_k, shape.d_v, shape.d_conv,
-                         shape.q_scale, shape.l2_eps, shape.norm_eps)
+                         shape.q_scale, shape.l2_eps, shape.norm_eps, shape.norm_gate)
 
 
 def act_dtype(wl: Workload) -> torch.dtype:

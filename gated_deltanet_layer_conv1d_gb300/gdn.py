@@ -20,6 +20,8 @@ GDN_OK = 0
 GDN_DTYPE_F32 = 0
 GDN_DTYPE_BF16 = 1
 GDN_DTYPE_F16 = 2  # h-state pools only
+GDN_NORM_GATE_SILU = 0
+GDN_NORM_GATE_SIGMOID = 1
 MAX_SEQS = 128
 VERIFY_WY_TABLE_SEQS = 128
 VERIFY_WY_TABLES_PER_LAYER = 16
@@ -32,6 +34,7 @@ EXPORTS = ("gdn_decode_batched", "gdn_verify_multi", "gdn_conv_step", "gdn_prefi
            "gdn_prefill_workspace_bytes", "gdn_gated_rmsnorm", "gdn_wy_tables_fill",
            "gdn_status_string", "gdn_version", "gdn_prefill_chunked_noalloc",
            "gdn_fold_accepted", "gdn_decode_batched_h16", "gdn_verify_multi_h16",
+           "gdn_gated_rmsnorm_sigmoid",
            "gdn_state_convert")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -46,7 +49,7 @@ class gdn_dims(ctypes.Structure):
     _fields_ = [("n_k_heads", ctypes.c_int32), ("n_v_heads", ctypes.c_int32),
                 ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32), ("d_conv", ctypes.c_int32),
                 ("q_scale", ctypes.c_float), ("l2_eps", ctypes.c_float),
-                ("norm_eps", ctypes.c_float)]
+                ("norm_eps", ctypes.c_float), ("norm_gate", ctypes.c_int32)]
 
 
 class gdn_weights(ctypes.Structure):
@@ -88,6 +91,7 @@ def lib() -> ctypes.CDLL:
         L.gdn_prefill_workspace_bytes.argtypes = [D, I32, I32, I32, I32]
         L.gdn_prefill_workspace_bytes.restype = SZ
         L.gdn_gated_rmsnorm.argtypes = [P, P, I64, P, ctypes.c_float, I32, I32, I32, I32, P, P]
+        L.gdn_gated_rmsnorm_sigmoid.argtypes = L.gdn_gated_rmsnorm.argtypes
         L.gdn_wy_tables_fill.argtypes = [P, I32, P, P, P]
         L.gdn_status_string.argtypes = [I32]
         L.gdn_status_string.restype = ctypes.c_char_p
@@ -156,8 +160,9 @@ class Inputs:
                           _ptr(self.a), _ptr(self.b), self.a.stride(0), _dtype_code(self.qkv))
 
 
-def make_dims(n_k_heads, n_v_heads, d_k, d_v, d_conv, q_scale, l2_eps, norm_eps) -> gdn_dims:
-    return gdn_dims(n_k_heads, n_v_heads, d_k, d_v, d_conv, q_scale, l2_eps, norm_eps)
+def make_dims(n_k_heads, n_v_heads, d_k, d_v, d_conv, q_scale, l2_eps, norm_eps,
+              norm_gate=GDN_NORM_GATE_SILU) -> gdn_dims:
+    return gdn_dims(n_k_heads, n_v_heads, d_k, d_v, d_conv, q_scale, l2_eps, norm_eps, norm_gate)
 
 
 def gdn_decode_batched(dims: gdn_dims, weights: Weights, inputs: Inputs, n: int, h_pool,
@@ -256,9 +261,10 @@ def gdn_prefill_chunked_noalloc(dims: gdn_dims, weights: Weights, inputs: Inputs
         _ptr(core_out), _ptr(status), _stream(stream)))
 
 
-def gdn_gated_rmsnorm(o, z, w, eps: float, y, stream=None):
+def gdn_gated_rmsnorm(o, z, w, eps: float, y, stream=None, sigmoid=False):
     T, Hv, dv = o.shape
-    _check("gdn_gated_rmsnorm", lib().gdn_gated_rmsnorm(
+    name = "gdn_gated_rmsnorm_sigmoid" if sigmoid else "gdn_gated_rmsnorm"
+    _check(name, getattr(lib(), name)(
         _ptr(o), _ptr(z), z.stride(0), _ptr(w), float(eps), T, Hv, dv, _dtype_code(z), _ptr(y),
         _stream(stream)))
 

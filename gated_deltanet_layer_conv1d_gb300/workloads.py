@@ -42,6 +42,7 @@ class LayerShape:
     q_scale: float
     l2_eps: float = 1e-6
     norm_eps: float = 1e-6
+    norm_gate: int = 0  # 0: SiLU(z) gate, 1: sigmoid(z) gate
 
     @property
     def conv_dim(self) -> int:

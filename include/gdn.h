@@ -112,7 +112,13 @@ typedef struct {
   float q_scale;     /* q <- q / sqrt(sum q^2 + l2_eps) * q_scale */
   float l2_eps;      /* >= 0 */
   float norm_eps;    /* gated RMSNorm epsilon, >= 0 */
+  int32_t norm_gate; /* GDN_NORM_GATE_SILU (0): y = norm(o) w SiLU(z);
+                        GDN_NORM_GATE_SIGMOID (1): y = norm(o) w sigmoid(z), the gate of the
+                        gdn_norm_sigmoid models (layer_struct.rs, gated_rms_norm_f32_strided_k) */
 } gdn_dims;
+
+#define GDN_NORM_GATE_SILU 0
+#define GDN_NORM_GATE_SIGMOID 1
 
 /* Layer parameters, all f32 device memory. */
 typedef struct {
@@ -313,6 +319,14 @@ GDN_API gdn_status gdn_prefill_chunked_noalloc(const gdn_dims* dims, const gdn_w
 GDN_API gdn_status gdn_gated_rmsnorm(const float* o, const void* z, int64_t z_stride, const float* w,
                              float eps, int32_t T, int32_t n_v_heads, int32_t d_v,
                              int32_t dtype, void* y, gdn_stream_t stream);
+
+/* The same with the sigmoid gate: y = o / sqrt(mean o^2 + eps) * w * sigmoid(z) (the
+ * gdn_norm_sigmoid models of layer_struct.rs; gdn_dims.norm_gate selects it in the fused
+ * entry points). */
+GDN_API gdn_status gdn_gated_rmsnorm_sigmoid(const float* o, const void* z, int64_t z_stride,
+                                             const float* w, float eps, int32_t T,
+                                             int32_t n_v_heads, int32_t d_v, int32_t dtype,
+                                             void* y, gdn_stream_t stream);
 
 /* Host helper: fills one layer's WY pointer tables in HOST memory
  * (transformer_layer.rs, the VERIFY_WY_* layout; the engine's upload_verify_wy_tables

@@ -121,7 +121,8 @@ def _decode(g, dims, n=4, inputs=None, h_pool=0x20000, conv_pool=0x30000, slots=
     (dict(d_k=64, d_v=64), 2), (dict(d_k=128, d_v=16), 2), (dict(d_conv=3), 2),
     (dict(n_v_heads=80), 2),           # G = 5 > 4
     (dict(n_v_heads=24), 2),           # not a multiple of n_k_heads
-    (dict(n_k_heads=0), 1), (dict(norm_eps=-1.0), 1), (dict(q_scale=float("nan")), 1)])
+    (dict(n_k_heads=0), 1), (dict(norm_eps=-1.0), 1), (dict(q_scale=float("nan")), 1),
+    (dict(norm_gate=2), 1), (dict(norm_gate=-1), 1)])
 def test_decode_refuses_bad_dims(g, kw, code):
     with pytest.raises(g.GdnError) as e:
         _decode(g, _dims(g, **kw))
@@ -169,8 +170,9 @@ def test_prefill_refuses_bad_chunk_and_workspace(g):
     assert g.gdn_prefill_workspace_bytes(d, 1, 64, 64, chunk=32) == 0
 
 
-def test_gated_rmsnorm_refuses_bad_args(g):
-    st = g.lib().gdn_gated_rmsnorm
+@pytest.mark.parametrize("name", ["gdn_gated_rmsnorm", "gdn_gated_rmsnorm_sigmoid"])
+def test_gated_rmsnorm_refuses_bad_args(g, name):
+    st = getattr(g.lib(), name)
     assert st(0x1000, 0x1000, 4096, 0x1000, ctypes.c_float(1e-6), 4, 32, 64, 1, 0x1000, 0) == 2
     assert st(0x1000, 0x1000, 4096, 0x1000, ctypes.c_float(-1.0), 4, 32, 128, 1, 0x1000, 0) == 1
     assert st(0x1004, 0x1000, 4096, 0x1000, ctypes.c_float(1e-6), 4, 32, 128, 1, 0x1000, 0) == 4
