@@ -117,6 +117,36 @@ class Workload:
         return np.concatenate([[0], np.cumsum(self.lens)]).astype(np.int32)
 
 
+# Residual width of the layer around the mixer (a reading: the pages fix the head counts and
+# dims, 16 key heads and 32 value heads of 128, not the hidden size; 2048 is the width such
+# a layer has in the Qwen3-Next family).
+HIDDEN = 2048
+
+
+def in_proj_width(shape: LayerShape) -> int:
+    """One in_proj output row [Q | K | V | Z | b | a]."""
+    return shape.conv_dim + shape.z_dim + 2 * shape.n_v_heads
+
+
+@dataclass
+class Projections:
+    """Synthetic projection operands, all bf16 values held in float32 arrays."""
+    hidden: np.ndarray  # [T][H] ~ N(0, 1)
+    w_in: np.ndarray    # [in_proj_width][H] ~ N(0, 1/H): in_proj outputs ~ N(0, 1)
+    w_out: np.ndarray   # [H][H_v d_v] ~ N(0, 1/(H_v d_v))
+    y: np.ndarray       # [T][H_v d_v] ~ N(0, 1): a stand-in mixer output for out_proj alone
+
+
+def projections(T: int, shape: LayerShape = FULL, hidden: int = HIDDEN,
+                seed: int = SEED) -> Projections:
+    rng = np.random.default_rng(seed)
+    x = round_bf16(_normal(rng, (T, hidden)))
+    w_in = round_bf16(_normal(rng, (in_proj_width(shape), hidden), 1.0 / hidden))
+    w_out = round_bf16(_normal(rng, (hidden, shape.z_dim), 1.0 / shape.z_dim))
+    y = round_bf16(_normal(rng, (T, shape.z_dim)))
+    return Projections(x, w_in, w_out, y)
+
+
 def tiny_check(q_scale_one: bool = False, prefill_tokens: int = 64, decode_steps: int = 8,
                seed: int = SEED) -> Workload:
     """One sequence, H_k = 1, H_v = 2, d_k = d_v = 16, width 4, float32 throughout:

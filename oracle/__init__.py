@@ -280,6 +280,31 @@ def mixer_batch(dims: Dims, weights: dict, seqs: list[dict], snapshots: bool = F
     return results
 
 
+# ------------------------------------------------------------------ projections
+# layer_struct.rs, Qwen3SsmLayer: the sequential [Q | K | V | Z] QKVZ projection, the b / a
+# gate inputs of ba_gates_k, and out_proj; the dense_gemm fields are the layer's bf16 GEMMs.
+# Plain fp64 products; numpy's matmul is the one step.
+
+def proj(x, w) -> np.ndarray:
+    """x [M][K] times w [N][K] transposed, in fp64: [M][N]."""
+    return _f64(x) @ _f64(w).T
+
+
+def in_proj_width(dims: Dims) -> int:
+    """One in_proj output row: [Q | K | V | Z | b | a]."""
+    return dims.conv_dim + dims.n_v_heads * dims.d_v + 2 * dims.n_v_heads
+
+
+def split_in_proj(dims: Dims, rows) -> dict:
+    """The mixer's inputs as column ranges of in_proj output rows [T][width]:
+    qkv [T][conv_dim], z [T][H_v d_v], b [T][H_v], a [T][H_v] (that order in the row)."""
+    rows = _f64(rows)
+    cd, vd, hv = dims.conv_dim, dims.n_v_heads * dims.d_v, dims.n_v_heads
+    assert rows.shape[1] == cd + vd + 2 * hv
+    return {"qkv": rows[:, :cd], "z": rows[:, cd:cd + vd], "b": rows[:, cd + vd:cd + vd + hv],
+            "a": rows[:, cd + vd + hv:]}
+
+
 def chunked(dims: Dims, chunk: int, qn, kn, v, alpha, beta, H, round_operands: bool = False):
     """The chunked (WY / UT-transform) form of a4.  Returns (H_new, o [T][H_v][d_v])."""
     qn, kn, v, alpha, beta = map(_f64, (qn, kn, v, alpha, beta))

@@ -472,3 +472,38 @@ def test_fp16_state_storage_rounds_every_stored_state_and_stays_close():
     assert 1e-5 < e < 64 * 2.0 ** -11
     # the first output uses the unrounded update, so it equals the exact path's
     np.testing.assert_allclose(o16[0], o[0], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- projections
+def test_proj_against_brute_force_loops():
+    """layer_struct.rs, the bf16 in_proj / out_proj GEMMs: c[m][n] = sum_k x[m][k] w[n][k]
+    (w holds one output feature per row); a non-square case so a transposed operand fails."""
+    rng = np.random.default_rng(61)
+    x = rng.standard_normal((3, 5))
+    w = rng.standard_normal((7, 5))
+    c = oracle.proj(x, w)
+    assert c.shape == (3, 7)
+    for m in range(3):
+        for n in range(7):
+            s = 0.0
+            for k in range(5):
+                s += x[m, k] * w[n, k]
+            assert abs(c[m, n] - s) <= 1e-14 * (1.0 + abs(s))
+    # a selection matrix copies the chosen features
+    sel = np.zeros((2, 5))
+    sel[0, 3] = sel[1, 0] = 1.0
+    np.testing.assert_array_equal(oracle.proj(x, sel), x[:, [3, 0]])
+
+
+def test_split_in_proj_layout():
+    """[Q | K | V | Z | b | a]: every column lands in exactly one piece, in that order."""
+    dims = oracle.Dims(2, 4, 8, 3, 4, 1.0, 1e-6, 1e-6)  # conv_dim 2*2*8 + 4*3 = 44
+    width = oracle.in_proj_width(dims)
+    assert width == 44 + 12 + 2 * 4
+    rows = np.arange(2 * width, dtype=float).reshape(2, width)
+    s = oracle.split_in_proj(dims, rows)
+    assert [s[k].shape[1] for k in ("qkv", "z", "b", "a")] == [44, 12, 4, 4]
+    np.testing.assert_array_equal(
+        np.concatenate([s["qkv"], s["z"], s["b"], s["a"]], axis=1), rows)
+    assert oracle.in_proj_width(dims) == wl.in_proj_width(
+        wl.LayerShape(2, 4, 8, 3, 4, q_scale=1.0))
