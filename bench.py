@@ -449,6 +449,65 @@ def prefill_mode(device, steps, tc_peak, warmup=2):
 PREFILL_FLOPS_PER_TOKEN = prefill_flops(64) / 64
 
 
+def proj_mode(device, steps, tc_peak, hbm_peak, warmup=3):
+    """The bf16 projections around the mixer, hidden width 2048: in_proj (-> [Q|K|V|Z|b|a],
+    12352 outputs) and out_proj (4096 -> 2048) at 8192 tokens (tensor-bound) and at 128
+    tokens (one decode step of 128 sequences: weight-streaming, HBM-bound).  Operand sets
+    rotate so every call reads more than L2 holds; cuBLAS (torch.matmul) on the same
+    operands is timed beside as context."""
+    import torch
+
+    from gated_deltanet_layer_conv1d_gb300 import device as dev
+    from gated_deltanet_layer_conv1d_gb300 import gdn
+    from gated_deltanet_layer_conv1d_gb300 import workloads as wl
+    dims = dev.dims_of(wl.FULL)
+    width = gdn.gdn_in_proj_width(dims)
+    H, vd = wl.HIDDEN, wl.FULL.z_dim
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    g = torch.Generator(device=device).manual_seed(0)
+
+    def rnd(*shape, scale=1.0):
+        return (torch.randn(*shape, generator=g, device=device) * scale).to(torch.bfloat16)
+
+    out = {}
+    for name, T, K, N in (("in_proj", 8192, H, width), ("out_proj", 8192, vd, H),
+                          ("in_proj", 128, H, width), ("out_proj", 128, vd, H)):
+        per_set = (T * K + N * K + T * N) * 2
+        sets = max(1, -(-160 * 2**20 // per_set))
+        a = [rnd(T, K) for _ in range(sets)]
+        b = [rnd(N, K, scale=K ** -0.5) for _ in range(sets)]
+        c = [torch.empty((T, N), dtype=torch.bfloat16, device=device) for _ in range(sets)]
+
+        def ours(i):
+            q = i % sets
+            gdn.gdn_proj_gemm(a[q], b[q], c[q], status, stream)
+
+        def cublas(i):
+            q = i % sets
+            torch.matmul(a[q], b[q].t(), out=c[q])
+
+        ms = time_loop(torch, stream, ours, steps, warmup)
+        assert int(status.item()) == 0
+        ms_cublas = time_loop(torch, stream, cublas, steps, warmup)
+        fl = 2.0 * T * K * N
+        byts = per_set
+        r = {"M": T, "N": N, "K": K, "ms": round(ms, 4), "cublas_ms": round(ms_cublas, 4)}
+        tfs = fl / (ms * 1e-3) / 1e12
+        gbs = byts / (ms * 1e-3) / 1e9
+        if T >= 1024:
+            r["roofline"] = {"bound": "tensor", "achieved": round(tfs, 1), "peak": tc_peak,
+                             "unit": "TFLOP/s", "frac": round(tfs / tc_peak, 4),
+                             "traffic": None, "algorithmic_flops": fl}
+        else:
+            r["roofline"] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                             "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                             "algorithmic_bytes": byts}
+        out[f"{name}_{T}tok"] = r
+    return {"workload": f"bf16 projections, hidden {H}, H_k 16, H_v 32, d 128",
+            "gpu_launches_per_call": 1, "calls": out}
+
+
 def mixed_mode(device, steps, hbm_peak, tc_peak):
     """Mixed serving step: 32 sequences prefilling U{512..4096} tokens on one stream next to
     a 96-sequence ragged verify (k ~ U{2..16}) on another; tokens/s over both."""
@@ -589,7 +648,7 @@ def main():
     ap.add_argument("--no-modes", action="store_true", help="skip the verify / prefill lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--profile", nargs="?", const="decode", default=None,
-                    choices=["decode", "verify", "verify-small", "prefill", "mixed"],
+                    choices=["decode", "verify", "verify-small", "prefill", "mixed", "proj"],
                     help="only one timed loop of one mode (for profiler captures); "
                          "verify-small runs 32 sequences")
     args = ap.parse_args()
@@ -617,6 +676,11 @@ def main():
     gdn.lib()
 
     hbm_peak, tc_peak, peak_src = peaks()
+    if args.profile == "proj":
+        r = proj_mode(device, args.steps, tc_peak, hbm_peak, warmup=args.warmup)
+        if rank == 0:
+            print(json.dumps({"profile_run": "proj", "calls": r["calls"]}))
+        return
     if args.profile in ("verify", "verify-small", "prefill", "mixed"):
         if args.profile == "prefill":
             r = prefill_mode(device, args.steps, tc_peak, warmup=args.warmup)
@@ -688,6 +752,7 @@ def main():
                                                         hbm_peak, h16=True)
         modes["chunked_prefill"] = prefill_mode(device, 5, tc_peak)
         modes["mixed_serving"] = mixed_mode(device, 3, hbm_peak, tc_peak)
+        modes["projections"] = proj_mode(device, 20, tc_peak, hbm_peak)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline_decode()

@@ -497,6 +497,56 @@ gdn_status gdn_gated_rmsnorm_sigmoid(const float* o, const void* z, int64_t z_st
                             GDN_NORM_GATE_SIGMOID, y, stream);
 }
 
+gdn_status gdn_proj_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                         int64_t ldc, int32_t M, int32_t N, int32_t K, int32_t* status_dev,
+                         gdn_stream_t stream) {
+  if (M < 0 || N < 8 || K < 8 || N % 8 != 0 || K % 8 != 0 || lda < K || ldb < K || ldc < N)
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (M == 0) return GDN_OK;
+  if (!A || !B || !C || !status_dev) return GDN_ERR_NULL_POINTER;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(status_dev, 4) ||
+      lda % 8 != 0 || ldb % 8 != 0 || ldc % 8 != 0)
+    return GDN_ERR_MISALIGNED;
+  ProjParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.A = A;
+  p.lda = lda;
+  p.B = B;
+  p.ldb = ldb;
+  p.C = C;
+  p.ldc = ldc;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.status = status_dev;
+  return launch_proj(p, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int32_t gdn_in_proj_width(const gdn_dims* dims) {
+  if (check_dims(dims) != GDN_OK) return 0;
+  return conv_dim_of(*dims) + dims->n_v_heads * dims->d_v + 2 * dims->n_v_heads;
+}
+
+gdn_status gdn_in_proj(const gdn_dims* dims, int32_t hidden_size, const void* hidden,
+                       int64_t hidden_stride, int32_t T, const void* w_in, void* out,
+                       int32_t* status_dev, gdn_stream_t stream) {
+  GDN_TRY(check_dims(dims));
+  if (T < 0) return GDN_ERR_INVALID_ARGUMENT;
+  const int32_t width = gdn_in_proj_width(dims);
+  return gdn_proj_gemm(hidden, hidden_stride, w_in, hidden_size, out, width, T, width,
+                       hidden_size, status_dev, stream);
+}
+
+gdn_status gdn_out_proj(const gdn_dims* dims, int32_t hidden_size, const void* y, int32_t T,
+                        const void* w_out, void* out, int64_t out_stride, int32_t* status_dev,
+                        gdn_stream_t stream) {
+  GDN_TRY(check_dims(dims));
+  if (T < 0) return GDN_ERR_INVALID_ARGUMENT;
+  const int32_t vd = dims->n_v_heads * dims->d_v;
+  return gdn_proj_gemm(y, vd, w_out, vd, out, out_stride, T, hidden_size, vd, status_dev,
+                       stream);
+}
+
 gdn_status gdn_wy_tables_fill(uint64_t* host_tables, int32_t n, const int32_t* ks,
                               const uint64_t* h_ptrs, const uint64_t* inter_ptrs) {
   if (!host_tables) return GDN_ERR_NULL_POINTER;

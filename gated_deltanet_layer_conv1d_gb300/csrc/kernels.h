@@ -123,6 +123,21 @@ struct FoldParams {
 };
 cudaError_t launch_fold(const FoldParams& p, cudaStream_t stream);
 
+// bf16 projection GEMM: C[M][N] = A[M][K] B[N][K]^T (f32 accumulation, bf16 result).
+struct ProjParams {
+  const void* A;
+  int64_t lda;
+  const void* B;
+  int64_t ldb;
+  void* C;
+  int64_t ldc;
+  int32_t M, N, K;
+  int32_t bn;  // output tile width 256 / 128 / 64; 0 picks by the tile count
+  int32_t* status;
+};
+cudaError_t launch_proj(const ProjParams& p, cudaStream_t stream);
+int proj_tile_n(int M, int N);
+
 int sm_count();
 
 }  // namespace gdn

@@ -1,0 +1,306 @@
+// proj.cu -- the bf16 projections on either side of the GDN mixer (sm_103a).
+//
+// layer_struct.rs, Qwen3SsmLayer: the layer projects the hidden row to [Q | K | V | Z]
+// (the sequential QKVZ layout) and to the b, a gate inputs (ba_gates_k reads them), runs
+// the mixer, and projects the gated-norm output y back to the hidden width (out_proj; the
+// dense_gemm / dense_gemm_pipelined fields are the layer's bf16 GEMMs).  Both are one
+// C[M][N] = A[M][K] B[N][K]^T with bf16 operands, f32 accumulation and a bf16 result:
+//   in_proj:  A = hidden [T][H], B = [W_qkvz ; W_ba] [conv_dim + H_v d_v + 2 H_v][H]
+//             -> one row [Q | K | V | Z | b | a] per token, the row layout the mixer's
+//             entry points read (qkv, z, b, a are column offsets of that row);
+//   out_proj: A = y [T][H_v d_v], B = W_out [H][H_v d_v] -> [T][H].
+//
+// gdn_proj_gemm_kernel is persistent (one CTA per SM, tiles strided over the grid) and
+// warp-specialized:
+//   warp 0, one lane   -- TMA producer: 128 x 64 tiles of A and BN x 64 tiles of B into a
+//                         ring of STAGES shared-memory stages (128-byte swizzle, the layout
+//                         the MMA descriptors read), completion on full[s];
+//   warp 1, one lane   -- MMA issuer: four M128 x BN x K16 tcgen05.mma per stage into one
+//                         of two TMEM accumulators, commit -> empty[s] frees the stage,
+//                         commit -> tfull[acc] hands the finished tile to the epilogue;
+//   warps 2..5         -- epilogue: TMEM -> registers (one row per thread), bf16, global
+//                         stores, then tempty[acc] returns the accumulator.
+// With two accumulators the epilogue of one tile runs under the main loop of the next.
+// Rows past M and columns past N of the tiles are zero-filled by TMA and never stored;
+// K past the end is zero-filled too, so K needs only 16-byte rows.
+//
+// Every wait is bounded: a wait that runs out sets a shared abort flag, every role leaves
+// its loop when it sees the flag, the producer waits for the copies it issued, the issuer
+// for its MMAs, and the CTA reports GDN_ERR_TIMEOUT before freeing its tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;                     // one 128-byte swizzle row of bf16
+constexpr int kProjThreads = 192;
+constexpr uint32_t kATileBytes = kBM * kBK * 2;
+
+template <int BN>
+struct ProjCfg {
+  static constexpr uint32_t kBTileBytes = uint32_t(BN) * kBK * 2;
+  static constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr int kStages = int((196u * 1024u) / kStageBytes);
+  static constexpr uint32_t kBar = uint32_t(kStages) * kStageBytes;
+  // full[S], empty[S], tfull[2], tempty[2], drain; then the TMEM slot and the abort flag
+  static constexpr uint32_t kTmemSlot = kBar + 8u * uint32_t(2 * kStages + 5);
+  static constexpr uint32_t kAbort = kTmemSlot + 4;
+  static constexpr uint32_t kBytes = kAbort + 4 + 1024;  // + slack to align the base
+  static constexpr uint32_t kTmemCols = 2u * BN < 32u ? 32u : 2u * BN;
+  static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "M = 128 MMA: N in 16..256, step 16");
+  static_assert((kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation: a power of two");
+};
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+        "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Waits for the phase of `bar` with the given parity; false once the CTA aborts (another
+// role gave up) or this wait runs past the budget (then it raises the abort itself).
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kProjThreads, 1)
+    gdn_proj_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                         const __grid_constant__ CUtensorMap map_b,
+                         const __grid_constant__ ProjParams p) {
+  using C = ProjCfg<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::kBar);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::kTmemSlot);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + C::kAbort);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles_m = (p.M + kBM - 1) / kBM, tiles_n = (p.N + BN - 1) / BN;
+  const int tiles = tiles_m * tiles_n, kblocks = (p.K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);  // one arrive per epilogue warp
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_mbar_init();
+    prefetch_map(&map_a);
+    prefetch_map(&map_b);
+  }
+  if (warp == 1) tc::alloc(tslot, C::kTmemCols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    int s = 0;
+    uint32_t ph = 0;
+    uint32_t issued_mask = 0, issued_par = 0;  // per stage: a copy issued, its phase parity
+    bool ok = true;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      const int m0 = (t % tiles_m) * kBM, n0 = (t / tiles_m) * BN;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!wait_or_abort(&empty[s], ph ^ 1u, abort)) { ok = false; break; }
+        unsigned char* st = sm + uint32_t(s) * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+        tma_load_2d(st, &map_a, kb * kBK, m0, &full[s]);
+        tma_load_2d(st + kATileBytes, &map_b, kb * kBK, n0, &full[s]);
+        issued_mask |= 1u << s;
+        issued_par = (issued_par & ~(1u << s)) | (ph << s);
+        if (++s == S) { s = 0; ph ^= 1u; }
+      }
+    }
+    if (!ok) {
+      // copies still in flight land before this CTA's shared memory is released
+      for (int q = 0; q < S; ++q)
+        if (issued_mask & (1u << q)) mbar_wait_bounded(&full[q], (issued_par >> q) & 1u);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc = tc::idesc_bf16(kBM, BN);
+    int s = 0;
+    uint32_t ph = 0;
+    int acc = 0;
+    uint32_t aph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      if (!wait_or_abort(&tempty[acc], aph ^ 1u, abort)) break;
+      tc::fence_after_sync();
+      const uint32_t d = tmem + uint32_t(acc * BN);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!wait_or_abort(&full[s], ph, abort)) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t a = smem_u32(sm + uint32_t(s) * C::kStageBytes);
+        const uint32_t b = a + kATileBytes;
+#pragma unroll
+        for (int k0 = 0; k0 < kBK; k0 += 16)
+          tc::mma_f16(d, tc::desc_at(a, kBM, k0), tc::desc_at(b, BN, k0), idesc,
+                      kb > 0 || k0 > 0);
+        tc::commit(&empty[s]);
+        if (++s == S) { s = 0; ph ^= 1u; }
+      }
+      if (!ok) break;
+      tc::commit(&tfull[acc]);
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+    // every MMA issued above has completed before the tensor memory is freed
+    tc::commit(drain);
+    mbar_wait_bounded(drain, 0);
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lanes 32q .. 32q + 31
+    int acc = 0;
+    uint32_t aph = 0;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C);
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+      const int m0 = (t % tiles_m) * kBM, n0 = (t / tiles_m) * BN;
+      if (!wait_or_abort(&tfull[acc], aph, abort)) break;
+      tc::fence_after_sync();
+      const int row = m0 + 32 * q + lane;
+      __nv_bfloat16* orow = out + size_t(row) * size_t(p.ldc) + n0;
+      const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc * BN);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tc::ld32(taddr + uint32_t(c0), v);
+        if (row < p.M) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (n0 + c0 + 8 * g < p.N) {
+              const uint4 w = make_uint4(pack_bf16x2(v[8 * g], v[8 * g + 1]),
+                                         pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
+                                         pack_bf16x2(v[8 * g + 4], v[8 * g + 5]),
+                                         pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
+              *reinterpret_cast<uint4*>(orow + c0 + 8 * g) = w;
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort) report(p.status, GDN_ERR_TIMEOUT);
+  if (warp == 1) tc::dealloc(tmem, C::kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// A row-major bf16 matrix [rows][cols] (row stride ld elements) read in boxes of
+// box_rows x 64 with the 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int64_t ld, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(ld) * 2};
+  const cuuint32_t box[2] = {cuuint32_t(kBK), cuuint32_t(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <int BN>
+cudaError_t launch_bn(const ProjParams& p, cudaStream_t stream) {
+  using C = ProjCfg<BN>;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, p.A, p.M, p.K, p.lda, kBM) || !make_map(&mb, p.B, p.N, p.K, p.ldb, BN))
+    return cudaErrorInvalidValue;
+  auto kern = gdn_proj_gemm_kernel<BN>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kBytes));
+  if (e != cudaSuccess) return e;
+  const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  kern<<<grid, kProjThreads, C::kBytes, stream>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int proj_tile_n(int M, int N) {
+  // The widest tile that still gives every SM a tile; narrow tiles when M is one row block
+  // (decode-sized calls stream the weights, and only the tile count spreads them).
+  const int sms = sm_count();
+  const int tm = (M + kBM - 1) / kBM;
+  for (int bn : {256, 128}) {
+    if (tm * ((N + bn - 1) / bn) >= sms) return bn;
+  }
+  return 64;
+}
+
+cudaError_t launch_proj(const ProjParams& p, cudaStream_t stream) {
+  if (p.M == 0 || p.N == 0) return cudaSuccess;
+  switch (p.bn ? p.bn : proj_tile_n(p.M, p.N)) {
+    case 256: return launch_bn<256>(p, stream);
+    case 128: return launch_bn<128>(p, stream);
+    case 64: return launch_bn<64>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gdn

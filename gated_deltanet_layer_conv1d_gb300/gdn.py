@@ -34,7 +34,8 @@ EXPORTS = ("gdn_decode_batched", "gdn_verify_multi", "gdn_conv_step", "gdn_prefi
            "gdn_prefill_workspace_bytes", "gdn_gated_rmsnorm", "gdn_wy_tables_fill",
            "gdn_status_string", "gdn_version", "gdn_prefill_chunked_noalloc",
            "gdn_fold_accepted", "gdn_decode_batched_h16", "gdn_verify_multi_h16",
-           "gdn_gated_rmsnorm_sigmoid",
+           "gdn_gated_rmsnorm_sigmoid", "gdn_proj_gemm", "gdn_in_proj_width", "gdn_in_proj",
+           "gdn_out_proj",
            "gdn_state_convert")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -93,6 +94,11 @@ def lib() -> ctypes.CDLL:
         L.gdn_gated_rmsnorm.argtypes = [P, P, I64, P, ctypes.c_float, I32, I32, I32, I32, P, P]
         L.gdn_gated_rmsnorm_sigmoid.argtypes = L.gdn_gated_rmsnorm.argtypes
         L.gdn_wy_tables_fill.argtypes = [P, I32, P, P, P]
+        L.gdn_proj_gemm.argtypes = [P, I64, P, I64, P, I64, I32, I32, I32, P, P]
+        L.gdn_in_proj_width.argtypes = [D]
+        L.gdn_in_proj_width.restype = I32
+        L.gdn_in_proj.argtypes = [D, I32, P, I64, I32, P, P, P, P]
+        L.gdn_out_proj.argtypes = [D, I32, P, I32, P, P, I64, P, P]
         L.gdn_status_string.argtypes = [I32]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_version.restype = I32
@@ -266,6 +272,60 @@ def gdn_gated_rmsnorm(o, z, w, eps: float, y, stream=None, sigmoid=False):
     name = "gdn_gated_rmsnorm_sigmoid" if sigmoid else "gdn_gated_rmsnorm"
     _check(name, getattr(lib(), name)(
         _ptr(o), _ptr(z), z.stride(0), _ptr(w), float(eps), T, Hv, dv, _dtype_code(z), _ptr(y),
+        _stream(stream)))
+
+
+def _bf16_rows(t, name):
+    assert t.dtype == torch.bfloat16 and t.dim() == 2 and t.stride(1) == 1, \
+        f"{name}: bf16 rows with contiguous columns"
+
+
+def gdn_proj_gemm(a, b, c, status, stream=None):
+    """c[M][N] = a[M][K] b[N][K]^T (bf16 in and out, f32 accumulation)."""
+    for t, nm in ((a, "a"), (b, "b"), (c, "c")):
+        _bf16_rows(t, nm)
+    M, K = a.shape
+    N = b.shape[0]
+    assert b.shape[1] == K and c.shape == (M, N)
+    _check("gdn_proj_gemm", lib().gdn_proj_gemm(
+        _ptr(a), a.stride(0), _ptr(b), b.stride(0), _ptr(c), c.stride(0), M, N, K, _ptr(status),
+        _stream(stream)))
+
+
+def gdn_in_proj_width(dims: gdn_dims) -> int:
+    return int(lib().gdn_in_proj_width(ctypes.byref(dims)))
+
+
+def gdn_in_proj(dims: gdn_dims, hidden, w_in, out, status, stream=None):
+    """out[T][width] = rows [Q | K | V | Z | b | a] of hidden[T][H] w_in[width][H]^T."""
+    _bf16_rows(hidden, "hidden")
+    T, H = hidden.shape
+    width = gdn_in_proj_width(dims)
+    assert w_in.shape == (width, H) and w_in.is_contiguous() and w_in.dtype == torch.bfloat16
+    assert out.shape == (T, width) and out.is_contiguous() and out.dtype == torch.bfloat16
+    _check("gdn_in_proj", lib().gdn_in_proj(
+        ctypes.byref(dims), H, _ptr(hidden), hidden.stride(0), T, _ptr(w_in), _ptr(out),
+        _ptr(status), _stream(stream)))
+
+
+def in_proj_inputs(dims: gdn_dims, out) -> "Inputs":
+    """The mixer's inputs as column ranges of an in_proj output [T][width]."""
+    cd = 2 * dims.n_k_heads * dims.d_k + dims.n_v_heads * dims.d_v
+    vd, hv = dims.n_v_heads * dims.d_v, dims.n_v_heads
+    return Inputs(out[:, :cd], out[:, cd:cd + vd], out[:, cd + vd + hv:cd + vd + 2 * hv],
+                  out[:, cd + vd:cd + vd + hv])
+
+
+def gdn_out_proj(dims: gdn_dims, y, w_out, out, status, stream=None):
+    """out[T][H] = y[T][H_v d_v] w_out[H][H_v d_v]^T."""
+    _bf16_rows(y, "y")
+    _bf16_rows(out, "out")
+    T = y.shape[0]
+    H = w_out.shape[0]
+    assert y.is_contiguous() and w_out.is_contiguous() and w_out.dtype == torch.bfloat16
+    assert w_out.shape[1] == y.shape[1] and out.shape == (T, H)
+    _check("gdn_out_proj", lib().gdn_out_proj(
+        ctypes.byref(dims), H, _ptr(y), T, _ptr(w_out), _ptr(out), out.stride(0), _ptr(status),
         _stream(stream)))
 
 

@@ -328,6 +328,43 @@ GDN_API gdn_status gdn_gated_rmsnorm_sigmoid(const float* o, const void* z, int6
                                              int32_t n_v_heads, int32_t d_v, int32_t dtype,
                                              void* y, gdn_stream_t stream);
 
+/* The bf16 projections on either side of the mixer (layer_struct.rs, Qwen3SsmLayer: the
+ * sequential [Q | K | V | Z] QKVZ projection, the b / a inputs that ba_gates_k reads, and
+ * out_proj; the dense_gemm fields are the layer's bf16 GEMMs).  One GEMM on the tcgen05
+ * tensor cores: C[M][N] = A[M][K] * B[N][K]^T, bf16 operands, f32 accumulation, the result
+ * rounded to the nearest bf16 (ties to even).
+ *   A          : device bf16 [M][lda], lda >= K.
+ *   B          : device bf16 [N][ldb], ldb >= K; row n holds output feature n (the layout
+ *                of a linear layer's weight).
+ *   C          : device bf16 [M][ldc], ldc >= N; must not overlap A or B.
+ *   M >= 0 (0 does nothing, and no pointer is read); N >= 8 and K >= 8, both multiples
+ *   of 8; lda, ldb, ldc multiples of 8 and A, B, C 16-byte aligned (else
+ *   GDN_ERR_MISALIGNED).
+ *   status_dev : device int32; a device-side wait that runs out sets GDN_ERR_TIMEOUT.
+ * Nothing is allocated; the call is asynchronous on `stream`. */
+GDN_API gdn_status gdn_proj_gemm(const void* A, int64_t lda, const void* B, int64_t ldb,
+                                 void* C, int64_t ldc, int32_t M, int32_t N, int32_t K,
+                                 int32_t* status_dev, gdn_stream_t stream);
+
+/* Width of one in_proj output row: conv_dim + H_v d_v + 2 H_v (0 for invalid dims). */
+GDN_API int32_t gdn_in_proj_width(const gdn_dims* dims);
+
+/* in_proj: hidden [T][hidden_size] bf16 (row stride hidden_stride) times
+ * w_in [gdn_in_proj_width(dims)][hidden_size] bf16 -> out [T][width] bf16 with the row
+ * [Q | K | V | Z | b | a] per token.  The mixer's entry points read it directly as
+ * qkv = out, z = out + conv_dim, b = out + conv_dim + H_v d_v, a = b + H_v, every row
+ * stride = width, dtype GDN_DTYPE_BF16.  Same rules as gdn_proj_gemm. */
+GDN_API gdn_status gdn_in_proj(const gdn_dims* dims, int32_t hidden_size, const void* hidden,
+                               int64_t hidden_stride, int32_t T, const void* w_in, void* out,
+                               int32_t* status_dev, gdn_stream_t stream);
+
+/* out_proj: y [T][H_v d_v] bf16 (the mixer's output rows) times
+ * w_out [hidden_size][H_v d_v] bf16 -> out [T][hidden_size] bf16 (row stride out_stride).
+ * Same rules as gdn_proj_gemm. */
+GDN_API gdn_status gdn_out_proj(const gdn_dims* dims, int32_t hidden_size, const void* y,
+                                int32_t T, const void* w_out, void* out, int64_t out_stride,
+                                int32_t* status_dev, gdn_stream_t stream);
+
 /* Host helper: fills one layer's WY pointer tables in HOST memory
  * (transformer_layer.rs, the VERIFY_WY_* layout; the engine's upload_verify_wy_tables
  * stages them only for k in 2..16).  Zero-fills all 16 x 128 entries, then sets

@@ -234,3 +234,27 @@ def test_status_strings(g):
         s = g.status_string(code)
         assert s and s != "unknown status"
     assert g.status_string(12345) == "unknown status"
+
+
+def test_proj_gemm_refuses_bad_arguments(g):
+    f = g.lib().gdn_proj_gemm
+    ok = dict(A=0x10000, lda=64, B=0x20000, ldb=64, C=0x30000, ldc=64, M=4, N=64, K=64,
+              status=0x40000)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["A"], a["lda"], a["B"], a["ldb"], a["C"], a["ldc"], a["M"], a["N"], a["K"],
+                 a["status"], None)
+
+    for kw, code in [(dict(M=-1), 1), (dict(N=4), 1), (dict(K=0), 1), (dict(N=60), 1),
+                     (dict(K=12), 1), (dict(lda=32), 1), (dict(ldc=32), 1), (dict(A=None), 3),
+                     (dict(status=None), 3), (dict(B=0x20008), 4), (dict(C=0x30002), 4),
+                     (dict(lda=68), 4)]:
+        assert call(**kw) == code, kw
+    assert call(M=0) == 0  # nothing to do: no launch
+    assert call(M=0, A=None, C=None) == 0  # an empty tensor's address may be NULL
+
+
+def test_in_proj_width(g):
+    assert g.gdn_in_proj_width(_dims(g)) == 8192 + 4096 + 64
+    assert g.gdn_in_proj_width(_dims(g, d_conv=3)) == 0

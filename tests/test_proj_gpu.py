@@ -1,0 +1,176 @@
+"""GPU parity of the bf16 projections around the mixer (layer_struct.rs, Qwen3SsmLayer: the
+sequential [Q | K | V | Z] QKVZ projection, the b / a inputs of ba_gates_k, out_proj; the
+dense_gemm fields): gdn_proj_gemm at small ragged sizes and at the full in_proj / out_proj
+sizes (the host picks 64-wide output tiles for the 128-token and small calls, 128 for
+2048 x 2048, 256 for the 8000 / 8192-token ones), and one layer chain in_proj -> prefill ->
+decode -> out_proj against the oracle chain.
+
+Tolerance (element by element, from the arithmetic): the kernel accumulates bf16 products
+in f32 and rounds the sum to bf16 once, so |c - c_exact| <= 2^-8 |c_exact| (the final
+rounding, half a bf16 ulp) + K 2^-23 sum_k |x_k w_k| (f32 accumulation, a generous bound),
+and the two bf16 roundings of nearly equal sums can differ by one ulp: the test allows
+2^-7 |c_exact| + K 2^-23 sum_k |x_k w_k|.  In the layer chain the mixer's y keeps the 2e-3
+relative L2 of every bf16 output, and out_proj's output is held to the bound its test
+derives from y's measured error.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_layer_conv1d_gb300 import device as dev
+from gated_deltanet_layer_conv1d_gb300 import gdn
+from gated_deltanet_layer_conv1d_gb300 import workloads as wl
+from tests.gpu_common import (TC_STATE_TOL, assert_state_close, assert_y_close, odims, rel_l2,
+                              require_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def bf16_dev(x) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to("cuda", torch.bfloat16)
+
+
+def assert_gemm_close(c_gpu: torch.Tensor, x, w, rows=None, what="gemm"):
+    """Element-wise bound above on the given rows (default all)."""
+    xs = x if rows is None else x[rows]
+    exact = oracle.proj(xs, w)
+    mag = oracle.proj(np.abs(xs), np.abs(w))
+    got = c_gpu.float().cpu().numpy().astype(np.float64)
+    if rows is not None:
+        got = got[rows]
+    K = x.shape[1]
+    bound = 2.0 ** -7 * np.abs(exact) + K * 2.0 ** -23 * mag
+    err = np.abs(got - exact)
+    bad = np.argwhere(err > bound)
+    assert bad.size == 0, (f"{what}: {len(bad)} elements out of bound, first {bad[0]}: "
+                           f"{got[tuple(bad[0])]} vs {exact[tuple(bad[0])]}")
+
+
+def run_gemm(x, w):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a, b = bf16_dev(x), bf16_dev(w)
+    c = torch.full((x.shape[0], w.shape[0]), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_proj_gemm(a, b, c, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return c
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 64, 64), (100, 200, 72), (129, 136, 8), (300, 2048, 4096),
+                                   (2048, 2048, 2048)])
+def test_gemm_small_and_ragged(M, N, K):
+    rng = np.random.default_rng(M * 7 + N)
+    x = wl.round_bf16(rng.standard_normal((M, K)).astype(np.float32))
+    w = wl.round_bf16((rng.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32))
+    assert_gemm_close(run_gemm(x, w), x, w, what=f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("T", [128, 8000])
+def test_in_proj_full_width(T):
+    """in_proj of the 16/32-head layer: N = 12352 outputs, K = 2048; T = 8000 compares a
+    sample of rows (every 64 x 12352 block boundary region and the ragged tail)."""
+    P = wl.projections(T, seed=71 + T)
+    dims = dev.dims_of(wl.FULL)
+    width = gdn.gdn_in_proj_width(dims)
+    assert width == wl.in_proj_width(wl.FULL) == 12352
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty((T, width), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_in_proj(dims, bf16_dev(P.hidden), bf16_dev(P.w_in), out, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rows = None
+    if T > 1024:
+        rng = np.random.default_rng(72)
+        rows = np.unique(np.concatenate([rng.integers(0, T, 96), np.arange(T - 70, T),
+                                         [0, 127, 128, 4095, 4096]]))
+    assert_gemm_close(out, P.hidden, P.w_in, rows, f"in_proj T={T}")
+
+
+@pytest.mark.parametrize("T", [128, 8192])
+def test_out_proj(T):
+    P = wl.projections(T, seed=73 + T)
+    dims = dev.dims_of(wl.FULL)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty((T, wl.HIDDEN), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_out_proj(dims, bf16_dev(P.y), bf16_dev(P.w_out), out, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rows = None
+    if T > 1024:
+        rows = np.unique(np.concatenate([np.random.default_rng(74).integers(0, T, 96),
+                                         np.arange(T - 40, T)]))
+    assert_gemm_close(out, P.y, P.w_out, rows, f"out_proj T={T}")
+
+
+def test_zero_rows_is_a_no_op():
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    c = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_proj_gemm(a, b, c, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+
+def test_layer_chain_in_proj_prefill_decode_out_proj():
+    """hidden -> in_proj -> prefill of two sequences (the in_proj rows read in place as
+    qkv, z, b, a) -> one decode step each -> out_proj, against the oracle chain (bf16
+    activations between the steps, as the layer stores them)."""
+    lens = [200, 57]
+    T = sum(lens)
+    sh = wl.FULL
+    base = wl.varlen_prefill(lens, seed=75)  # weights and initial states of the mixer
+    P = wl.projections(T + 2, seed=76)      # T prefill rows, then one decode row per sequence
+    d = torch.device("cuda")
+    dims = dev.dims_of(sh)
+    width = gdn.gdn_in_proj_width(dims)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    w_in, w_out = bf16_dev(P.w_in), bf16_dev(P.w_out)
+    weights = dev.weights_to(base, d)
+    h_pool, conv_pool, slots = dev.states_to(base, d)
+
+    rows = torch.empty((T + 2, width), dtype=torch.bfloat16, device=d)
+    gdn.gdn_in_proj(dims, bf16_dev(P.hidden), w_in, rows, status)
+    y = torch.empty((T + 2, sh.z_dim), dtype=torch.bfloat16, device=d)
+    hsz = sh.n_v_heads * sh.d_k * sh.d_v * 4
+    hp = torch.tensor([h_pool.data_ptr() + i * hsz for i in range(2)], dtype=torch.int64, device=d)
+    cu = torch.tensor([0, lens[0], T], dtype=torch.int32, device=d)
+    ws = torch.empty(gdn.gdn_prefill_workspace_bytes(dims, 2, T, max(lens)), dtype=torch.uint8,
+                     device=d)
+    gdn.gdn_prefill_chunked(dims, weights, gdn.in_proj_inputs(dims, rows[:T]), 2, cu, T,
+                            max(lens), hp, conv_pool, 2, slots, y[:T], None, ws, status)
+    gdn.gdn_decode_batched(dims, weights, gdn.in_proj_inputs(dims, rows[T:]), 2, h_pool,
+                           conv_pool, 2, slots, y[T:], None, status)
+    out = torch.empty((T + 2, wl.HIDDEN), dtype=torch.bfloat16, device=d)
+    gdn.gdn_out_proj(dims, y, w_out, out, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+    od = odims(sh)
+    orows = wl.round_bf16(oracle.proj(P.hidden, P.w_in).astype(np.float32))
+    sp = oracle.split_in_proj(od, orows)
+    y_orc = np.empty((T + 2, sh.z_dim))
+    off = [0, lens[0], T]
+    seqs = []
+    for i in range(2):
+        idx = np.r_[off[i]:off[i + 1], T + i]  # the sequence's prefill rows, then its decode row
+        seqs.append({k: sp[k][idx] for k in ("qkv", "z", "a", "b")} |
+                    dict(conv_state=base.conv0[i], H=base.H0[i]))
+    res = oracle.mixer_batch(od, base.weights, seqs)
+    for i, r in enumerate(res):
+        y_orc[off[i]:off[i + 1]] = r.y[:-1]
+        y_orc[T + i] = r.y[-1]
+        assert_state_close(h_pool[i].cpu().numpy(), r.H, f"state seq {i}", TC_STATE_TOL)
+    e_y = assert_y_close(y, y_orc, "mixer y in the chain")
+    # out = bf16(y W^T): the error of y (measured against bf16(y_oracle), the oracle's own
+    # stored y) passes through W_out about unchanged in relative L2 (25 % slack for a random
+    # W), and the final bf16 rounding adds at most 2^-9 relative per element.
+    out_orc = oracle.proj(wl.round_bf16(y_orc.astype(np.float32)), P.w_out)
+    e = rel_l2(out.float().cpu().numpy(), out_orc)
+    assert e <= 1.25 * e_y + 2.0 ** -9, f"out_proj in the chain: {e:.3e} (y {e_y:.3e})"
