@@ -132,11 +132,15 @@ struct ProjParams {
   void* C;
   int64_t ldc;
   int32_t M, N, K;
-  int32_t bn;  // output tile width 256 / 128 / 64; 0 picks by the tile count
+  int32_t bn;      // output tile width 256 / 128 / 64; 0: the launcher picks bn and splits
+  int32_t splits;  // CTAs (one cluster) per tile splitting K, 1..8
   int32_t* status;
 };
+struct ProjShape {
+  int bn, splits;
+};
 cudaError_t launch_proj(const ProjParams& p, cudaStream_t stream);
-int proj_tile_n(int M, int N);
+ProjShape proj_shape(int M, int N, int K);
 
 int sm_count();
 

@@ -24,6 +24,12 @@
 // Rows past M and columns past N of the tiles are zero-filled by TMA and never stored;
 // K past the end is zero-filled too, so K needs only 16-byte rows.
 //
+// Calls with fewer tiles than SMs (a decode step's 128 tokens) split K instead: a cluster
+// of `splits` CTAs per tile, each over its own run of K blocks, leaves its f32 partial
+// tile in shared memory; after a cluster barrier every CTA sums one slice of the tile's
+// rows over all partials (distributed shared memory reads) and stores it, and a second
+// cluster barrier keeps every partial alive until its readers are done.
+//
 // Every wait is bounded: a wait that runs out sets a shared abort flag, every role leaves
 // its loop when it sees the flag, the producer waits for the copies it issued, the issuer
 // for its MMAs, and the CTA reports GDN_ERR_TIMEOUT before freeing its tensor memory.
@@ -53,6 +59,9 @@ struct ProjCfg {
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kBytes = kAbort + 4 + 1024;  // + slack to align the base
   static constexpr uint32_t kTmemCols = 2u * BN < 32u ? 32u : 2u * BN;
+  // split-K partial tile: f32 [128][BN + 4] over the stage ring (drained by then)
+  static constexpr int kRedStride = BN + 4;
+  static_assert(uint32_t(kBM) * kRedStride * 4 <= kBar, "the partial tile fits the ring");
   static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "M = 128 MMA: N in 16..256, step 16");
   static_assert((kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation: a power of two");
 };
@@ -87,6 +96,40 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   return true;
 }
 
+// All threads of all CTAs of the cluster; release / acquire orders shared memory.
+__device__ __forceinline__ void cluster_sync() {
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 16 bytes of CTA `rank`'s shared memory at the offset `local` has in this CTA's.
+__device__ __forceinline__ float4 ld_cluster_f4(const void* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(ra)
+               : "memory");
+  return v;
+}
+
+// The work of one CTA: tiles first, first + stride, ... below end, each over the K blocks
+// [kb0, kb1).  Without a split that is every grid-stride tile over all of K; with one it
+// is tile blockIdx.x / splits over the K run of rank blockIdx.x % splits (the host makes
+// every run non-empty).
+struct Work {
+  int first, stride, end, kb0, kb1, rank;
+};
+__device__ __forceinline__ Work work_of(const ProjParams& p, int tiles, int kblocks) {
+  if (p.splits <= 1) return {int(blockIdx.x), int(gridDim.x), tiles, 0, kblocks, 0};
+  const int r = int(blockIdx.x) % p.splits, t = int(blockIdx.x) / p.splits;
+  const int kc = (kblocks + p.splits - 1) / p.splits;
+  const int kb1 = (r + 1) * kc < kblocks ? (r + 1) * kc : kblocks;
+  return {t, 1, t + 1, r * kc, kb1, r};
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -113,6 +156,8 @@ __global__ void __launch_bounds__(kProjThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles_m = (p.M + kBM - 1) / kBM, tiles_n = (p.N + BN - 1) / BN;
   const int tiles = tiles_m * tiles_n, kblocks = (p.K + kBK - 1) / kBK;
+  const Work wk = work_of(p, tiles, kblocks);
+  const bool split = p.splits > 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -141,9 +186,9 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     uint32_t ph = 0;
     uint32_t issued_mask = 0, issued_par = 0;  // per stage: a copy issued, its phase parity
     bool ok = true;
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+    for (int t = wk.first; t < wk.end && ok; t += wk.stride) {
       const int m0 = (t % tiles_m) * kBM, n0 = (t / tiles_m) * BN;
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
         if (!wait_or_abort(&empty[s], ph ^ 1u, abort)) { ok = false; break; }
         unsigned char* st = sm + uint32_t(s) * C::kStageBytes;
         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
@@ -167,11 +212,11 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+    for (int t = wk.first; t < wk.end && ok; t += wk.stride) {
       if (!wait_or_abort(&tempty[acc], aph ^ 1u, abort)) break;
       tc::fence_after_sync();
       const uint32_t d = tmem + uint32_t(acc * BN);
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
         if (!wait_or_abort(&full[s], ph, abort)) { ok = false; break; }
         tc::fence_after_sync();
         const uint32_t a = smem_u32(sm + uint32_t(s) * C::kStageBytes);
@@ -179,7 +224,7 @@ __global__ void __launch_bounds__(kProjThreads, 1)
 #pragma unroll
         for (int k0 = 0; k0 < kBK; k0 += 16)
           tc::mma_f16(d, tc::desc_at(a, kBM, k0), tc::desc_at(b, BN, k0), idesc,
-                      kb > 0 || k0 > 0);
+                      kb > wk.kb0 || k0 > 0);
         tc::commit(&empty[s]);
         if (++s == S) { s = 0; ph ^= 1u; }
       }
@@ -197,10 +242,25 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     int acc = 0;
     uint32_t aph = 0;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C);
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+    for (int t = wk.first; t < wk.end; t += wk.stride) {
       const int m0 = (t % tiles_m) * kBM, n0 = (t / tiles_m) * BN;
       if (!wait_or_abort(&tfull[acc], aph, abort)) break;
       tc::fence_after_sync();
+      if (split) {
+        // the partial tile, row 32q + lane of this thread, into the (drained) stage ring
+        float* red = reinterpret_cast<float*>(sm) + (32 * q + lane) * C::kRedStride;
+        const uint32_t taddr = tmem + (uint32_t(32 * q) << 16);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float v[32];
+          tc::ld32(taddr + uint32_t(c0), v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(red + c0 + 4 * j) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+        break;  // one tile per CTA
+      }
       const int row = m0 + 32 * q + lane;
       __nv_bfloat16* orow = out + size_t(row) * size_t(p.ldc) + n0;
       const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc * BN);
@@ -229,6 +289,54 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     }
   }
 
+  if (split) {
+    // Every thread of every CTA of the cluster passes both barriers, aborted or not.
+    cluster_sync();  // every partial tile is in its CTA's shared memory
+    if (warp >= 2) {
+      const int t = wk.first, m0 = (t % tiles_m) * kBM, n0 = (t / tiles_m) * BN;
+      const int rows = (kBM + p.splits - 1) / p.splits;
+      const int r0 = wk.rank * rows, r1 = r0 + rows < kBM ? r0 + rows : kBM;
+      const float* red = reinterpret_cast<const float*>(sm);
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C);
+      constexpr int kQ = BN / 4;  // float4 groups per row
+      constexpr int kG = 16;      // groups per thread per pass: 16 remote loads in flight
+      constexpr int kStep = kProjThreads - 64;
+      const int groups = (r1 - r0) * kQ;
+      for (int e0 = int(threadIdx.x) - 64; e0 < groups; e0 += kG * kStep) {
+        float4 acc[kG];
+#pragma unroll
+        for (int g = 0; g < kG; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < p.splits; ++q) {
+          float4 x[kG];
+#pragma unroll
+          for (int g = 0; g < kG; ++g) {
+            const int e = e0 + g * kStep;
+            if (e < groups)
+              x[g] = ld_cluster_f4(red + (r0 + e / kQ) * C::kRedStride + 4 * (e % kQ),
+                                   uint32_t(q));
+          }
+#pragma unroll
+          for (int g = 0; g < kG; ++g) {
+            if (e0 + g * kStep < groups) {
+              acc[g].x += x[g].x;
+              acc[g].y += x[g].y;
+              acc[g].z += x[g].z;
+              acc[g].w += x[g].w;
+            }
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+          const int e = e0 + g * kStep;
+          const int r = r0 + e / kQ, c = 4 * (e % kQ);
+          if (e < groups && m0 + r < p.M && n0 + c < p.N)
+            *reinterpret_cast<uint2*>(out + size_t(m0 + r) * size_t(p.ldc) + n0 + c) =
+                make_uint2(pack_bf16x2(acc[g].x, acc[g].y), pack_bf16x2(acc[g].z, acc[g].w));
+        }
+      }
+    }
+    cluster_sync();  // no CTA leaves while another still reads its partial
+  }
   tc::fence_before_sync();
   __syncthreads();
   if (threadIdx.x == 0 && *abort) report(p.status, GDN_ERR_TIMEOUT);
@@ -275,27 +383,120 @@ cudaError_t launch_bn(const ProjParams& p, cudaStream_t stream) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kBytes));
   if (e != cudaSuccess) return e;
   const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
-  const int grid = tiles < sm_count() ? tiles : sm_count();
-  kern<<<grid, kProjThreads, C::kBytes, stream>>>(ma, mb, p);
-  return cudaGetLastError();
+  if (p.splits <= 1) {
+    const int grid = tiles < sm_count() ? tiles : sm_count();
+    kern<<<grid, kProjThreads, C::kBytes, stream>>>(ma, mb, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(tiles * p.splits));
+  cfg.blockDim = dim3(kProjThreads);
+  cfg.dynamicSmemBytes = C::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(p.splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, p);
+}
+
+// How many clusters of `s` CTAs of the BN-wide kernel the GPU holds at once (a cluster
+// stays inside one GPC, so this is below SMs / s); cached per shape.
+int max_active_clusters(int bn, int s) {
+  static int cache[3][9] = {};
+  const int i = bn == 256 ? 0 : (bn == 128 ? 1 : 2);
+  if (cache[i][s] == 0) {
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(s));
+    cfg.blockDim = dim3(kProjThreads);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(s);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaSuccess;
+    switch (bn) {
+      case 256:
+        cfg.dynamicSmemBytes = ProjCfg<256>::kBytes;
+        e = cudaFuncSetAttribute(gdn_proj_gemm_kernel<256>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(ProjCfg<256>::kBytes));
+        if (e == cudaSuccess)
+          e = cudaOccupancyMaxActiveClusters(&n, gdn_proj_gemm_kernel<256>, &cfg);
+        break;
+      case 128:
+        cfg.dynamicSmemBytes = ProjCfg<128>::kBytes;
+        e = cudaFuncSetAttribute(gdn_proj_gemm_kernel<128>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(ProjCfg<128>::kBytes));
+        if (e == cudaSuccess)
+          e = cudaOccupancyMaxActiveClusters(&n, gdn_proj_gemm_kernel<128>, &cfg);
+        break;
+      default:
+        cfg.dynamicSmemBytes = ProjCfg<64>::kBytes;
+        e = cudaFuncSetAttribute(gdn_proj_gemm_kernel<64>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(ProjCfg<64>::kBytes));
+        if (e == cudaSuccess)
+          e = cudaOccupancyMaxActiveClusters(&n, gdn_proj_gemm_kernel<64>, &cfg);
+        break;
+    }
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    cache[i][s] = n > 0 ? n : -1;  // -1: this split is not available
+  }
+  return cache[i][s];
 }
 
 }  // namespace
 
-int proj_tile_n(int M, int N) {
-  // The widest tile that still gives every SM a tile; narrow tiles when M is one row block
-  // (decode-sized calls stream the weights, and only the tile count spreads them).
+ProjShape proj_shape(int M, int N, int K) {
+  // Cost of a choice, in operand rows x K blocks through the busiest SM: a tile of BN
+  // columns streams 128 + BN rows per K block.  Whole-K tiles run in waves over the SMs;
+  // a split of S (one wave of tiles x S CTAs, at most 8 to a cluster, every K run
+  // non-empty) pays ceil(K blocks / S) blocks plus its partial-tile round trip through
+  // shared memory, about 8 BN; every cluster of it has to be resident at once (a cluster
+  // stays inside one GPC).  Least cost wins; on a tie the wider tile, then no split.
   const int sms = sm_count();
-  const int tm = (M + kBM - 1) / kBM;
-  for (int bn : {256, 128}) {
-    if (tm * ((N + bn - 1) / bn) >= sms) return bn;
+  const int tm = (M + kBM - 1) / kBM, kblocks = (K + kBK - 1) / kBK;
+  ProjShape best{256, 1};
+  long best_cost = -1;
+  auto consider = [&](int bn, int s, long cost) {
+    if (best_cost < 0 || cost < best_cost) {
+      best = {bn, s};
+      best_cost = cost;
+    }
+  };
+  for (int bn : {256, 128, 64}) {
+    const long tiles = long(tm) * ((N + bn - 1) / bn);
+    consider(bn, 1, ((tiles + sms - 1) / sms) * (kBM + bn) * long(kblocks));
+    for (int s = 2; s <= 8 && tiles * s <= sms; ++s) {
+      const int kc = (kblocks + s - 1) / s;
+      if ((s - 1) * kc >= kblocks || tiles > max_active_clusters(bn, s)) continue;
+      consider(bn, s, long(kBM + bn) * kc + 8L * bn);
+    }
   }
-  return 64;
+  return best;
 }
 
-cudaError_t launch_proj(const ProjParams& p, cudaStream_t stream) {
-  if (p.M == 0 || p.N == 0) return cudaSuccess;
-  switch (p.bn ? p.bn : proj_tile_n(p.M, p.N)) {
+cudaError_t launch_proj(const ProjParams& p_in, cudaStream_t stream) {
+  if (p_in.M == 0 || p_in.N == 0) return cudaSuccess;
+  ProjParams p = p_in;
+  if (p.bn == 0) {
+    const ProjShape sh = proj_shape(p.M, p.N, p.K);
+    p.bn = sh.bn;
+    p.splits = sh.splits;
+  }
+  if (p.splits < 1 || p.splits > 8) return cudaErrorInvalidValue;
+  switch (p.bn) {
     case 256: return launch_bn<256>(p, stream);
     case 128: return launch_bn<128>(p, stream);
     case 64: return launch_bn<64>(p, stream);

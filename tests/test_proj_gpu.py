@@ -1,9 +1,11 @@
 """GPU parity of the bf16 projections around the mixer (layer_struct.rs, Qwen3SsmLayer: the
 sequential [Q | K | V | Z] QKVZ projection, the b / a inputs of ba_gates_k, out_proj; the
 dense_gemm fields): gdn_proj_gemm at small ragged sizes and at the full in_proj / out_proj
-sizes (the host picks 64-wide output tiles for the 128-token and small calls, 128 for
-2048 x 2048, 256 for the 8000 / 8192-token ones), and one layer chain in_proj -> prefill ->
-decode -> out_proj against the oracle chain.
+sizes, and one layer chain in_proj -> prefill -> decode -> out_proj against the oracle
+chain.  The shapes cover every launch form the host picks: whole-K persistent tiles 64 wide
+(the small calls) and 256 wide (2048 x 2048, the 8000 / 8192-token calls), and K split over
+a cluster -- 64-wide tiles in 8 (64 x 200 x 1024, ragged M and N), 256-wide in 3 (in_proj
+at 128 tokens) and 6 (300 x 2048 x 4096), 128-wide in 8 (out_proj at 128 tokens).
 
 Tolerance (element by element, from the arithmetic): the kernel accumulates bf16 products
 in f32 and rounds the sum to bf16 once, so |c - c_exact| <= 2^-8 |c_exact| (the final
@@ -62,8 +64,8 @@ def run_gemm(x, w):
     return c
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 64, 64), (100, 200, 72), (129, 136, 8), (300, 2048, 4096),
-                                   (2048, 2048, 2048)])
+@pytest.mark.parametrize("M,N,K", [(1, 64, 64), (100, 200, 72), (129, 136, 8), (64, 200, 1024),
+                                   (300, 2048, 4096), (2048, 2048, 2048)])
 def test_gemm_small_and_ragged(M, N, K):
     rng = np.random.default_rng(M * 7 + N)
     x = wl.round_bf16(rng.standard_normal((M, K)).astype(np.float32))
