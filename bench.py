@@ -508,6 +508,85 @@ def proj_mode(device, steps, tc_peak, hbm_peak, warmup=3):
             "gpu_launches_per_call": 1, "calls": out}
 
 
+def layer_mode(device, steps, warmup=3):
+    """The whole layer around the mixer, hidden width 2048, bf16 between the steps:
+    hidden -> in_proj -> mixer (reading the in_proj rows in place) -> out_proj, as one
+    decode step of 128 sequences (rotating state pools larger than L2) and as the prefill
+    of one 8192-token sequence.  Three launches per decode step; the prefill's are the
+    projections plus the mixer's own."""
+    import torch
+
+    from gated_deltanet_layer_conv1d_gb300 import device as dev
+    from gated_deltanet_layer_conv1d_gb300 import gdn
+    from gated_deltanet_layer_conv1d_gb300 import workloads as wl
+    out = {}
+    stream = torch.cuda.current_stream(device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device, torch.bfloat16)
+
+    # ---- decode: 128 sequences x 1 token
+    w = wl.batched_decode(n=N_SEQ, steps=1)
+    P = wl.projections(N_SEQ * POOLS, seed=5)
+    dims, weights = dev.dims_of(w.shape), dev.weights_to(w, device)
+    width = gdn.gdn_in_proj_width(dims)
+    h_pool, conv_pool, _ = dev.states_to(w, device, n_slots=N_SEQ)
+    h_pool = h_pool.repeat(POOLS, 1, 1, 1).contiguous()
+    conv_pool = conv_pool.repeat(POOLS, 1, 1).contiguous()
+    slots = [torch.arange(q * N_SEQ, (q + 1) * N_SEQ, dtype=torch.int32, device=device)
+             for q in range(POOLS)]
+    hidden = bf(P.hidden).view(POOLS, N_SEQ, wl.HIDDEN)
+    w_in, w_out = bf(P.w_in), bf(P.w_out)
+    rows = torch.empty((N_SEQ, width), dtype=torch.bfloat16, device=device)
+    inputs = gdn.in_proj_inputs(dims, rows)
+    y = torch.empty((N_SEQ, w.shape.z_dim), dtype=torch.bfloat16, device=device)
+    o = torch.empty((N_SEQ, wl.HIDDEN), dtype=torch.bfloat16, device=device)
+
+    def dec(i):
+        q = i % POOLS
+        gdn.gdn_in_proj(dims, hidden[q], w_in, rows, status, stream)
+        gdn.gdn_decode_batched(dims, weights, inputs, N_SEQ, h_pool, conv_pool, POOLS * N_SEQ,
+                               slots[q], y, None, status, stream)
+        gdn.gdn_out_proj(dims, y, w_out, o, status, stream)
+
+    ms = time_loop(torch, stream, dec, steps, warmup)
+    assert int(status.item()) == 0
+    out["decode_128seq_1tok"] = {"ms_per_step": round(ms, 4),
+                                 "value": round(N_SEQ / (ms * 1e-3), 1), "unit": "tokens/s",
+                                 "gpu_launches_per_step": 3}
+    del h_pool, conv_pool
+
+    # ---- prefill: one sequence of 8192 tokens
+    T = 8192
+    w = wl.long_prefill(T)
+    P = wl.projections(T, seed=6)
+    h_pool, conv_pool, slots1 = dev.states_to(w, device)
+    hp = torch.tensor([h_pool.data_ptr()], dtype=torch.int64, device=device)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=device)
+    weights = dev.weights_to(w, device)
+    hidden, w_in, w_out = bf(P.hidden), bf(P.w_in), bf(P.w_out)
+    rows = torch.empty((T, width), dtype=torch.bfloat16, device=device)
+    inputs = gdn.in_proj_inputs(dims, rows)
+    y = torch.empty((T, w.shape.z_dim), dtype=torch.bfloat16, device=device)
+    o = torch.empty((T, wl.HIDDEN), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(gdn.gdn_prefill_workspace_bytes(dims, 1, T, T), dtype=torch.uint8,
+                     device=device)
+
+    def pre(i):
+        gdn.gdn_in_proj(dims, hidden, w_in, rows, status, stream)
+        gdn.gdn_prefill_chunked(dims, weights, inputs, 1, cu, T, T, hp, conv_pool, 1, slots1, y,
+                                None, ws, status, stream)
+        gdn.gdn_out_proj(dims, y, w_out, o, status, stream)
+
+    ms = time_loop(torch, stream, pre, max(3, steps // 20), 2)
+    assert int(status.item()) == 0
+    out["prefill_1x8192tok"] = {"ms_per_step": round(ms, 4), "value": round(T / (ms * 1e-3), 1),
+                                "unit": "tokens/s"}
+    return {"workload": f"GDN layer: in_proj -> mixer -> out_proj, hidden {wl.HIDDEN}, "
+                        "H_k 16, H_v 32, d 128, bf16 activations", "steps": out}
+
+
 def mixed_mode(device, steps, hbm_peak, tc_peak):
     """Mixed serving step: 32 sequences prefilling U{512..4096} tokens on one stream next to
     a 96-sequence ragged verify (k ~ U{2..16}) on another; tokens/s over both."""
@@ -648,7 +727,8 @@ def main():
     ap.add_argument("--no-modes", action="store_true", help="skip the verify / prefill lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--profile", nargs="?", const="decode", default=None,
-                    choices=["decode", "verify", "verify-small", "prefill", "mixed", "proj"],
+                    choices=["decode", "verify", "verify-small", "prefill", "mixed", "proj",
+                             "layer"],
                     help="only one timed loop of one mode (for profiler captures); "
                          "verify-small runs 32 sequences")
     args = ap.parse_args()
@@ -680,6 +760,11 @@ def main():
         r = proj_mode(device, args.steps, tc_peak, hbm_peak, warmup=args.warmup)
         if rank == 0:
             print(json.dumps({"profile_run": "proj", "calls": r["calls"]}))
+        return
+    if args.profile == "layer":
+        r = layer_mode(device, args.steps, warmup=args.warmup)
+        if rank == 0:
+            print(json.dumps({"profile_run": "layer", "steps": r["steps"]}))
         return
     if args.profile in ("verify", "verify-small", "prefill", "mixed"):
         if args.profile == "prefill":
@@ -753,6 +838,7 @@ def main():
         modes["chunked_prefill"] = prefill_mode(device, 5, tc_peak)
         modes["mixed_serving"] = mixed_mode(device, 3, hbm_peak, tc_peak)
         modes["projections"] = proj_mode(device, 20, tc_peak, hbm_peak)
+        modes["layer"] = layer_mode(device, 100)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline_decode()
