@@ -463,8 +463,9 @@ ProjShape proj_shape(int M, int N, int K) {
   // columns streams 128 + BN rows per K block.  Whole-K tiles run in waves over the SMs;
   // a split of S (one wave of tiles x S CTAs, at most 8 to a cluster, every K run
   // non-empty) pays ceil(K blocks / S) blocks plus its partial-tile round trip through
-  // shared memory, about 8 BN; every cluster of it has to be resident at once (a cluster
-  // stays inside one GPC).  Least cost wins; on a tie the wider tile, then no split.
+  // shared memory, measured at about 32 BN; every cluster of it has to be resident at once
+  // (a cluster stays inside one GPC).  Least cost wins; on a tie the wider tile, then no
+  // split.
   const int sms = sm_count();
   const int tm = (M + kBM - 1) / kBM, kblocks = (K + kBK - 1) / kBK;
   ProjShape best{256, 1};
@@ -481,7 +482,7 @@ ProjShape proj_shape(int M, int N, int K) {
     for (int s = 2; s <= 8 && tiles * s <= sms; ++s) {
       const int kc = (kblocks + s - 1) / s;
       if ((s - 1) * kc >= kblocks || tiles > max_active_clusters(bn, s)) continue;
-      consider(bn, s, long(kBM + bn) * kc + 8L * bn);
+      consider(bn, s, long(kBM + bn) * kc + 32L * bn);
     }
   }
   return best;

@@ -2,10 +2,11 @@
 sequential [Q | K | V | Z] QKVZ projection, the b / a inputs of ba_gates_k, out_proj; the
 dense_gemm fields): gdn_proj_gemm at small ragged sizes and at the full in_proj / out_proj
 sizes, and one layer chain in_proj -> prefill -> decode -> out_proj against the oracle
-chain.  The shapes cover every launch form the host picks: whole-K persistent tiles 64 wide
-(the small calls) and 256 wide (2048 x 2048, the 8000 / 8192-token calls), and K split over
-a cluster -- 64-wide tiles in 8 (64 x 200 x 1024, ragged M and N), 256-wide in 3 (in_proj
-at 128 tokens) and 6 (300 x 2048 x 4096), 128-wide in 8 (out_proj at 128 tokens).
+chain.  The shapes cover the launch forms the host picks on a GB300: whole-K persistent
+tiles 64 wide (the small calls), 128 wide (in_proj at 128 tokens) and 256 wide (2048 x 2048,
+the 8000 / 8192-token calls), and K split over a cluster -- 64-wide tiles in 8
+(64 x 200 x 1024, ragged M and N) and in 4 (out_proj at 128 tokens), 128-wide in 3
+(300 x 2048 x 4096, three row blocks).
 
 Tolerance (element by element, from the arithmetic): the kernel accumulates bf16 products
 in f32 and rounds the sum to bf16 once, so |c - c_exact| <= 2^-8 |c_exact| (the final
