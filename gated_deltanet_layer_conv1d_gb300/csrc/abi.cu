@@ -524,7 +524,8 @@ gdn_status gdn_proj_gemm(const void* A, int64_t lda, const void* B, int64_t ldb,
 
 int32_t gdn_in_proj_width(const gdn_dims* dims) {
   if (check_dims(dims) != GDN_OK) return 0;
-  return conv_dim_of(*dims) + dims->n_v_heads * dims->d_v + 2 * dims->n_v_heads;
+  const int32_t w = conv_dim_of(*dims) + dims->n_v_heads * dims->d_v + 2 * dims->n_v_heads;
+  return (w + 7) / 8 * 8;
 }
 
 gdn_status gdn_in_proj(const gdn_dims* dims, int32_t hidden_size, const void* hidden,

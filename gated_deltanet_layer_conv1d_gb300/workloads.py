@@ -124,8 +124,9 @@ HIDDEN = 2048
 
 
 def in_proj_width(shape: LayerShape) -> int:
-    """One in_proj output row [Q | K | V | Z | b | a]."""
-    return shape.conv_dim + shape.z_dim + 2 * shape.n_v_heads
+    """One in_proj output row [Q | K | V | Z | b | a], padded to a multiple of 8 columns
+    (16-byte rows); the padding's weight rows are zero."""
+    return (shape.conv_dim + shape.z_dim + 2 * shape.n_v_heads + 7) // 8 * 8
 
 
 @dataclass
@@ -142,6 +143,7 @@ def projections(T: int, shape: LayerShape = FULL, hidden: int = HIDDEN,
     rng = np.random.default_rng(seed)
     x = round_bf16(_normal(rng, (T, hidden)))
     w_in = round_bf16(_normal(rng, (in_proj_width(shape), hidden), 1.0 / hidden))
+    w_in[shape.conv_dim + shape.z_dim + 2 * shape.n_v_heads:] = 0.0
     w_out = round_bf16(_normal(rng, (hidden, shape.z_dim), 1.0 / shape.z_dim))
     y = round_bf16(_normal(rng, (T, shape.z_dim)))
     return Projections(x, w_in, w_out, y)

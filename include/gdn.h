@@ -346,7 +346,10 @@ GDN_API gdn_status gdn_proj_gemm(const void* A, int64_t lda, const void* B, int6
                                  void* C, int64_t ldc, int32_t M, int32_t N, int32_t K,
                                  int32_t* status_dev, gdn_stream_t stream);
 
-/* Width of one in_proj output row: conv_dim + H_v d_v + 2 H_v (0 for invalid dims). */
+/* Width of one in_proj output row: conv_dim + H_v d_v + 2 H_v rounded up to a multiple of
+ * 8, so that rows start on 16-byte boundaries as the mixer's entry points require (0 for
+ * invalid dims).  Columns past the b / a inputs are padding: their weight rows are the
+ * caller's and nothing reads their outputs.  12352 for H_k = 16, H_v = 32, d = 128. */
 GDN_API int32_t gdn_in_proj_width(const gdn_dims* dims);
 
 /* in_proj: hidden [T][hidden_size] bf16 (row stride hidden_stride) times

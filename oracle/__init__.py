@@ -297,12 +297,13 @@ def in_proj_width(dims: Dims) -> int:
 
 def split_in_proj(dims: Dims, rows) -> dict:
     """The mixer's inputs as column ranges of in_proj output rows [T][width]:
-    qkv [T][conv_dim], z [T][H_v d_v], b [T][H_v], a [T][H_v] (that order in the row)."""
+    qkv [T][conv_dim], z [T][H_v d_v], b [T][H_v], a [T][H_v] (that order in the row);
+    columns past them (row padding) are not inputs."""
     rows = _f64(rows)
     cd, vd, hv = dims.conv_dim, dims.n_v_heads * dims.d_v, dims.n_v_heads
-    assert rows.shape[1] == cd + vd + 2 * hv
+    assert rows.shape[1] >= cd + vd + 2 * hv
     return {"qkv": rows[:, :cd], "z": rows[:, cd:cd + vd], "b": rows[:, cd + vd:cd + vd + hv],
-            "a": rows[:, cd + vd + hv:]}
+            "a": rows[:, cd + vd + hv:cd + vd + 2 * hv]}
 
 
 def chunked(dims: Dims, chunk: int, qn, kn, v, alpha, beta, H, round_operands: bool = False):

@@ -258,3 +258,5 @@ def test_proj_gemm_refuses_bad_arguments(g):
 def test_in_proj_width(g):
     assert g.gdn_in_proj_width(_dims(g)) == 8192 + 4096 + 64
     assert g.gdn_in_proj_width(_dims(g, d_conv=3)) == 0
+    # H_k = 1, H_v = 2, d = 16: 64 + 32 + 4 = 100 columns, padded to 104 (16-byte rows)
+    assert g.gdn_in_proj_width(_dims(g, n_k_heads=1, n_v_heads=2, d_k=16, d_v=16)) == 104

@@ -507,3 +507,8 @@ def test_split_in_proj_layout():
         np.concatenate([s["qkv"], s["z"], s["b"], s["a"]], axis=1), rows)
     assert oracle.in_proj_width(dims) == wl.in_proj_width(
         wl.LayerShape(2, 4, 8, 3, 4, q_scale=1.0))
+    # padding columns after a are not inputs
+    padded = np.concatenate([rows, np.full((2, 8), 7.0)], axis=1)
+    sp = oracle.split_in_proj(dims, padded)
+    for k in ("qkv", "z", "b", "a"):
+        np.testing.assert_array_equal(sp[k], s[k])
