@@ -652,9 +652,30 @@ def mixed_mode(device, steps, hbm_peak, tc_peak):
                                  "frac": round(byts / (ms * 1e-3) / 1e9 / hbm_peak, 4)}}}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
 def cpu_baseline_decode(n_seq=N_SEQ, tokens=4):
     """The fp64 oracle on this host's cores: n_seq sequences x `tokens` decode tokens of
-    the headline workload (one oracle call per sequence, sequences on OpenMP threads)."""
+    the headline workload (one oracle call per sequence, sequences on OpenMP threads), and
+    a quarter of that sample again on one thread."""
     import oracle
     from gated_deltanet_layer_conv1d_gb300 import workloads as wl
     oracle.build()
@@ -668,13 +689,42 @@ def cpu_baseline_decode(n_seq=N_SEQ, tokens=4):
     dims = oracle.Dims(s.n_k_heads, s.n_v_heads, s.d_k, s.d_v, s.d_conv,
                        float(np.float32(s.q_scale)), float(np.float32(s.l2_eps)),
                        float(np.float32(s.norm_eps)))
+    cores = oracle.max_threads()
     t0 = time.perf_counter()
     oracle.mixer_batch(dims, w.weights, seqs)
     dt = time.perf_counter() - t0
-    return {"value": round(n_seq * tokens / dt, 2), "unit": "tokens/s",
-            "cores": oracle.max_threads(), "kind": "oracle",
+    n1 = max(1, n_seq // 4)
+    oracle.set_threads(1)
+    t1 = time.perf_counter()
+    oracle.mixer_batch(dims, w.weights, seqs[:n1])
+    dt1 = time.perf_counter() - t1
+    oracle.set_threads(cores)
+    return {"value": round(n_seq * tokens / dt, 2), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle", "cpu_model": cpu_model(),
+            "single_thread_value": round(n1 * tokens / dt1, 2),
             "sample": f"{n_seq} sequences x {tokens} decode tokens of the 128-sequence "
-                      f"workload (fp64, {dt:.1f} s)"}
+                      f"workload (fp64, {dt:.1f} s on {cores} threads; {n1} of them on one "
+                      f"thread, {dt1:.1f} s)"}
+
+
+def cpu_baseline_prefill(tokens=2048):
+    """The fp64 oracle's token loop over the first `tokens` tokens of the 8192-token
+    prefill workload (one sequence, so one thread)."""
+    import oracle
+    from gated_deltanet_layer_conv1d_gb300 import workloads as wl
+    oracle.build()
+    w = wl.long_prefill(8192)
+    s = w.shape
+    dims = oracle.Dims(s.n_k_heads, s.n_v_heads, s.d_k, s.d_v, s.d_conv,
+                       float(np.float32(s.q_scale)), float(np.float32(s.l2_eps)),
+                       float(np.float32(s.norm_eps)))
+    t0 = time.perf_counter()
+    oracle.mixer(dims, w.weights, *(w.tokens[k][:tokens] for k in ("qkv", "z", "a", "b")),
+                 w.conv0[0], w.H0[0])
+    dt = time.perf_counter() - t0
+    return {"value": round(tokens / dt, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "sample": f"first {tokens} of the 8192 tokens (fp64 token loop, {dt:.1f} s)"}
 
 
 def run_reference(args):
@@ -836,6 +886,8 @@ def main():
         modes["ragged_verify_fp16_state"] = verify_mode(device, max(10, min(200, args.steps // 10)),
                                                         hbm_peak, h16=True)
         modes["chunked_prefill"] = prefill_mode(device, 5, tc_peak)
+        if world == 1 and not args.no_cpu:
+            modes["chunked_prefill"]["cpu_baseline"] = cpu_baseline_prefill()
         modes["mixed_serving"] = mixed_mode(device, 3, hbm_peak, tc_peak)
         modes["projections"] = proj_mode(device, 20, tc_peak, hbm_peak)
         modes["layer"] = layer_mode(device, 100)

@@ -118,6 +118,7 @@ def lib():
                                        ctypes.POINTER(ctypes.c_int32)] + [_PD] * 4 +
                                       [_D] * 4 + [_PD] * 6)
         L.orc_max_threads.restype = _I32
+        L.orc_set_threads.argtypes = [_I32]
         _lib = L
     return _lib
 
@@ -135,6 +136,11 @@ def _p(x):
 
 def max_threads() -> int:
     return int(lib().orc_max_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads mixer_batch uses from now on (OpenMP over sequences)."""
+    lib().orc_set_threads(int(n))
 
 
 def round_fp16(x: float) -> float:

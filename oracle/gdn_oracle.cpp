@@ -398,4 +398,13 @@ int32_t orc_max_threads(void) {
 #endif
 }
 
+// Threads the batch routine uses from now on (n >= 1); no effect without OpenMP.
+void orc_set_threads(int32_t n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 }  // extern "C"
