@@ -672,10 +672,11 @@ def cpu_model() -> str:
     return platform.machine()
 
 
-def cpu_baseline_decode(n_seq=N_SEQ, tokens=4):
+def cpu_baseline_decode(n_seq=N_SEQ, tokens=4, seconds=10.0):
     """The fp64 oracle on this host's cores: n_seq sequences x `tokens` decode tokens of
-    the headline workload (one oracle call per sequence, sequences on OpenMP threads), and
-    a quarter of that sample again on one thread."""
+    the headline workload (one oracle call per sequence, sequences on OpenMP threads),
+    repeated from the same states until `seconds` have passed; then a quarter of the
+    sequences the same way on one thread for half as long."""
     import oracle
     from gated_deltanet_layer_conv1d_gb300 import workloads as wl
     oracle.build()
@@ -690,24 +691,30 @@ def cpu_baseline_decode(n_seq=N_SEQ, tokens=4):
                        float(np.float32(s.q_scale)), float(np.float32(s.l2_eps)),
                        float(np.float32(s.norm_eps)))
     cores = oracle.max_threads()
-    t0 = time.perf_counter()
-    oracle.mixer_batch(dims, w.weights, seqs)
-    dt = time.perf_counter() - t0
+
+    def run(batch, budget):
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle.mixer_batch(dims, w.weights, batch)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= budget:
+                return reps, dt
+
+    reps, dt = run(seqs, seconds)
     n1 = max(1, n_seq // 4)
     oracle.set_threads(1)
-    t1 = time.perf_counter()
-    oracle.mixer_batch(dims, w.weights, seqs[:n1])
-    dt1 = time.perf_counter() - t1
+    reps1, dt1 = run(seqs[:n1], seconds / 2)
     oracle.set_threads(cores)
-    return {"value": round(n_seq * tokens / dt, 2), "unit": "tokens/s", "cores": cores,
+    return {"value": round(reps * n_seq * tokens / dt, 2), "unit": "tokens/s", "cores": cores,
             "kind": "oracle", "cpu_model": cpu_model(),
-            "single_thread_value": round(n1 * tokens / dt1, 2),
+            "single_thread_value": round(reps1 * n1 * tokens / dt1, 2),
             "sample": f"{n_seq} sequences x {tokens} decode tokens of the 128-sequence "
-                      f"workload (fp64, {dt:.1f} s on {cores} threads; {n1} of them on one "
-                      f"thread, {dt1:.1f} s)"}
+                      f"workload, {reps} times ({dt:.1f} s on {cores} threads); {n1} of them "
+                      f"{reps1} times on one thread ({dt1:.1f} s); fp64"}
 
 
-def cpu_baseline_prefill(tokens=2048):
+def cpu_baseline_prefill(tokens=8192):
     """The fp64 oracle's token loop over the first `tokens` tokens of the 8192-token
     prefill workload (one sequence, so one thread)."""
     import oracle
@@ -724,7 +731,7 @@ def cpu_baseline_prefill(tokens=2048):
     dt = time.perf_counter() - t0
     return {"value": round(tokens / dt, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "cpu_model": cpu_model(),
-            "sample": f"first {tokens} of the 8192 tokens (fp64 token loop, {dt:.1f} s)"}
+            "sample": f"{tokens} of the 8192 tokens (fp64 token loop, {dt:.1f} s)"}
 
 
 def run_reference(args):

@@ -548,6 +548,15 @@ gdn_status gdn_out_proj(const gdn_dims* dims, int32_t hidden_size, const void* y
                        stream);
 }
 
+gdn_status gdn_selftest_wait(int64_t budget_ns, int32_t* status_dev, gdn_stream_t stream) {
+  if (budget_ns < 1 || budget_ns > 1000000000LL) return GDN_ERR_INVALID_ARGUMENT;
+  if (!status_dev) return GDN_ERR_NULL_POINTER;
+  if (!aligned(status_dev, 4)) return GDN_ERR_MISALIGNED;
+  return launch_wait_selftest(uint64_t(budget_ns), status_dev, stream) == cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
+}
+
 gdn_status gdn_wy_tables_fill(uint64_t* host_tables, int32_t n, const int32_t* ks,
                               const uint64_t* h_ptrs, const uint64_t* inter_ptrs) {
   if (!host_tables) return GDN_ERR_NULL_POINTER;

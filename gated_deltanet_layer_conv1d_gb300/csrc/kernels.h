@@ -142,6 +142,8 @@ struct ProjShape {
 cudaError_t launch_proj(const ProjParams& p, cudaStream_t stream);
 ProjShape proj_shape(int M, int N, int K);
 
+cudaError_t launch_wait_selftest(uint64_t budget_ns, int32_t* status, cudaStream_t stream);
+
 int sm_count();
 
 }  // namespace gdn

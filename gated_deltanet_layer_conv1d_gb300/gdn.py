@@ -35,7 +35,7 @@ EXPORTS = ("gdn_decode_batched", "gdn_verify_multi", "gdn_conv_step", "gdn_prefi
            "gdn_status_string", "gdn_version", "gdn_prefill_chunked_noalloc",
            "gdn_fold_accepted", "gdn_decode_batched_h16", "gdn_verify_multi_h16",
            "gdn_gated_rmsnorm_sigmoid", "gdn_proj_gemm", "gdn_in_proj_width", "gdn_in_proj",
-           "gdn_out_proj",
+           "gdn_out_proj", "gdn_selftest_wait",
            "gdn_state_convert")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -99,6 +99,7 @@ def lib() -> ctypes.CDLL:
         L.gdn_in_proj_width.restype = I32
         L.gdn_in_proj.argtypes = [D, I32, P, I64, I32, P, P, P, P]
         L.gdn_out_proj.argtypes = [D, I32, P, I32, P, P, I64, P, P]
+        L.gdn_selftest_wait.argtypes = [I64, P, P]
         L.gdn_status_string.argtypes = [I32]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_version.restype = I32
@@ -327,6 +328,12 @@ def gdn_out_proj(dims: gdn_dims, y, w_out, out, status, stream=None):
     _check("gdn_out_proj", lib().gdn_out_proj(
         ctypes.byref(dims), H, _ptr(y), T, _ptr(w_out), _ptr(out), out.stride(0), _ptr(status),
         _stream(stream)))
+
+
+def gdn_selftest_wait(budget_ns: int, status, stream=None):
+    """One bounded wait that nothing completes: sets status to GDN_ERR_TIMEOUT (19)."""
+    _check("gdn_selftest_wait", lib().gdn_selftest_wait(int(budget_ns), _ptr(status),
+                                                        _stream(stream)))
 
 
 def gdn_wy_tables_fill(ks, h_ptrs, inter_ptrs):

@@ -376,6 +376,13 @@ GDN_API gdn_status gdn_out_proj(const gdn_dims* dims, int32_t hidden_size, const
 GDN_API gdn_status gdn_wy_tables_fill(uint64_t* host_tables, int32_t n, const int32_t* ks,
                               const uint64_t* h_ptrs, const uint64_t* inter_ptrs);
 
+/* Self-test of the bounded device-side wait every kernel uses: one thread waits, for at
+ * most budget_ns (1 .. 1e9 ns), on an mbarrier that nothing arrives on, then writes
+ * GDN_ERR_TIMEOUT to *status_dev (first error wins) and returns.  The context stays usable;
+ * nothing faults or traps.  Used by the tests to show that a wait which never completes
+ * ends with a status the host can read. */
+GDN_API gdn_status gdn_selftest_wait(int64_t budget_ns, int32_t* status_dev, gdn_stream_t stream);
+
 /* A static, human-readable name of a status code. */
 GDN_API const char* gdn_status_string(gdn_status status);
 

@@ -260,3 +260,11 @@ def test_in_proj_width(g):
     assert g.gdn_in_proj_width(_dims(g, d_conv=3)) == 0
     # H_k = 1, H_v = 2, d = 16: 64 + 32 + 4 = 100 columns, padded to 104 (16-byte rows)
     assert g.gdn_in_proj_width(_dims(g, n_k_heads=1, n_v_heads=2, d_k=16, d_v=16)) == 104
+
+
+def test_selftest_wait_refuses_bad_arguments(g):
+    f = g.lib().gdn_selftest_wait
+    assert f(0, 0x60000, None) == 1
+    assert f(2_000_000_000, 0x60000, None) == 1
+    assert f(1000, None, None) == 3
+    assert f(1000, 0x60002, None) == 4
