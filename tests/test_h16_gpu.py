@@ -81,6 +81,25 @@ def test_decode_h16_tiny_f32_activations():
         np.testing.assert_array_equal(conv_pool[sl][i].cpu().numpy(), r.conv_state)
 
 
+@pytest.mark.parametrize("G", [1, 3, 4])
+def test_decode_h16_head_groupings(G):
+    """fp16-pool decode takes an item's value heads two at a time: G = 3 mixes a pair and a
+    single head, G = 4 two pairs, G = 1 only the single-head path."""
+    shape = wl.LayerShape(2, 2 * G, 16, 16, 4, q_scale=16 ** -0.5)
+    w = wl.batched_decode(n=6, steps=5, shape=shape, seed=20 + G)
+    ys, cores, h16, conv_pool, sl, H0 = run_decode_h16(w, w.extra["slot_perm"])
+    steps = [w.tokens] + w.steps
+    rows = {k: np.stack([s[k] for s in steps], axis=1).reshape(w.n * len(steps), -1)
+            for k in ("qkv", "z", "a", "b")}
+    res = oracle_h16(w, rows, [len(steps)] * w.n, H0)
+    y_orc = np.stack([r.y for r in res])
+    for s in range(len(steps)):
+        assert_y_close(ys[s], y_orc[:, s], f"G={G} y step {s}")
+    H = h16[sl].double().cpu().numpy()
+    for i, r in enumerate(res):
+        assert_state_close(H[i], r.H, f"G={G} fp16 state seq {i}", H16_TOL)
+
+
 def test_decode_h16_128_sequences_64_steps():
     w = wl.batched_decode(n=128, steps=64, seed=3)
     ys, cores, h16, conv_pool, sl, H0 = run_decode_h16(w, w.extra["slot_perm"])
