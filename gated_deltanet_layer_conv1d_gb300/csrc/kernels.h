@@ -134,6 +134,7 @@ struct ProjParams {
   int32_t M, N, K;
   int32_t bn;      // output tile width 256 / 128 / 64; 0: the launcher picks bn and splits
   int32_t splits;  // CTAs (one cluster) per tile splitting K, 1..8
+  int32_t n_fast;  // tile order: 1 walks N fastest, 0 walks M fastest
   int32_t* status;
 };
 struct ProjShape {

@@ -130,6 +130,16 @@ __device__ __forceinline__ Work work_of(const ProjParams& p, int tiles, int kblo
   return {t, 1, t + 1, r * kc, kb1, r};
 }
 
+// Tile t's row and column block.  Tiles are walked M-fastest (the CTAs in flight share a
+// weight tile and the activations stay in L2) unless the activation operand is the larger
+// one (n_fast: the CTAs in flight share an activation tile and the weights stay in L2).
+__device__ __forceinline__ int tile_m(const ProjParams& p, int t, int tiles_m, int tiles_n) {
+  return p.n_fast ? t / tiles_n : t % tiles_m;
+}
+__device__ __forceinline__ int tile_n(const ProjParams& p, int t, int tiles_m, int tiles_n) {
+  return p.n_fast ? t % tiles_n : t / tiles_m;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -187,7 +197,8 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     uint32_t issued_mask = 0, issued_par = 0;  // per stage: a copy issued, its phase parity
     bool ok = true;
     for (int t = wk.first; t < wk.end && ok; t += wk.stride) {
-      const int m0 = (t % tiles_m) * kBM, n0 = (t / tiles_m) * BN;
+      const int m0 = tile_m(p, t, tiles_m, tiles_n) * kBM;
+      const int n0 = tile_n(p, t, tiles_m, tiles_n) * BN;
       for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
         if (!wait_or_abort(&empty[s], ph ^ 1u, abort)) { ok = false; break; }
         unsigned char* st = sm + uint32_t(s) * C::kStageBytes;
@@ -243,7 +254,8 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     uint32_t aph = 0;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C);
     for (int t = wk.first; t < wk.end; t += wk.stride) {
-      const int m0 = (t % tiles_m) * kBM, n0 = (t / tiles_m) * BN;
+      const int m0 = tile_m(p, t, tiles_m, tiles_n) * kBM;
+      const int n0 = tile_n(p, t, tiles_m, tiles_n) * BN;
       if (!wait_or_abort(&tfull[acc], aph, abort)) break;
       tc::fence_after_sync();
       if (split) {
@@ -293,7 +305,9 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     // Every thread of every CTA of the cluster passes both barriers, aborted or not.
     cluster_sync();  // every partial tile is in its CTA's shared memory
     if (warp >= 2) {
-      const int t = wk.first, m0 = (t % tiles_m) * kBM, n0 = (t / tiles_m) * BN;
+      const int t = wk.first;
+      const int m0 = tile_m(p, t, tiles_m, tiles_n) * kBM;
+      const int n0 = tile_n(p, t, tiles_m, tiles_n) * BN;
       const int rows = (kBM + p.splits - 1) / p.splits;
       const int r0 = wk.rank * rows, r1 = r0 + rows < kBM ? r0 + rows : kBM;
       const float* red = reinterpret_cast<const float*>(sm);
@@ -497,6 +511,7 @@ cudaError_t launch_proj(const ProjParams& p_in, cudaStream_t stream) {
     p.splits = sh.splits;
   }
   if (p.splits < 1 || p.splits > 8) return cudaErrorInvalidValue;
+  p.n_fast = p.M > p.N ? 1 : 0;  // A (M x K) larger than B (N x K)
   switch (p.bn) {
     case 256: return launch_bn<256>(p, stream);
     case 128: return launch_bn<128>(p, stream);
