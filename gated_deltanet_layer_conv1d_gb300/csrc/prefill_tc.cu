@@ -502,6 +502,8 @@ struct SpineSmem {
   static_assert(NCOL == 64 || NCOL == 128, "whole 64-column blocks of the MN-major operands");
 };
 
+constexpr int kOrderMax = 512;  // sequences the spine orders by length (more: call order)
+
 template <int NCOL>
 __global__ void __launch_bounds__(4 * NCOL, 1)
     gdn_prefill_spine_kernel(const __grid_constant__ PrefillParams p) {
@@ -512,7 +514,23 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
   // (neither is in an output warp, whose work trails the chain)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int slice = blockIdx.x % kNS, unit = blockIdx.x / kNS;
-  const int seq = unit / p.Hv, h = unit % p.Hv, kh = h / p.G;
+  // Units are handed out longest sequence first (ties: lower index first): CTAs start in
+  // block order, so the long chains start early and the short ones fill in behind them.
+  __shared__ int len_s[kOrderMax], order_s[kOrderMax];
+  int seq = unit / p.Hv;
+  if (p.n > 1 && p.n <= kOrderMax) {
+    for (int i = tid; i < p.n; i += blockDim.x) len_s[i] = p.cu_seqlens[i + 1] - p.cu_seqlens[i];
+    __syncthreads();
+    for (int i = tid; i < p.n; i += blockDim.x) {
+      const int li = len_s[i];
+      int r = 0;
+      for (int j = 0; j < p.n; ++j) r += (len_s[j] > li) || (len_s[j] == li && j < i);
+      order_s[r] = i;
+    }
+    __syncthreads();
+    seq = order_s[seq];
+  }
+  const int h = unit % p.Hv, kh = h / p.G;
   const int t_begin = p.cu_seqlens[seq], t_end = p.cu_seqlens[seq + 1];
   const uint64_t hp = p.h_ptrs[seq];
   {
