@@ -119,6 +119,21 @@ def test_varlen_prefill_full_f32_sequential():
     check_prefill(w, run_prefill(w))
 
 
+def test_prefill_many_short_sequences():
+    """520 sequences of 0..4 tokens on the tensor-core path: more sequences than the
+    spine orders by length (512), so its units go in call order; empty sequences keep
+    their states."""
+    rng = np.random.default_rng(17)
+    lens = rng.integers(0, 5, size=520)
+    lens[:3] = [0, 4, 1]
+    w = wl.varlen_prefill(lens, seed=17)
+    assert tensor_core_path(w)
+    r = run_prefill(w)
+    check_prefill(w, r)
+    for i in np.flatnonzero(lens == 0)[:5]:
+        np.testing.assert_array_equal(r["h_pool"][i].cpu().numpy(), w.H0[i])
+
+
 def test_prefill_zero_length_sequence_keeps_state():
     w = wl.varlen_prefill([65, 0, 3], seed=16)
     r = run_prefill(w)
