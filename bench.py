@@ -785,7 +785,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--profile", nargs="?", const="decode", default=None,
                     choices=["decode", "verify", "verify-small", "prefill", "mixed", "proj",
-                             "layer"],
+                             "layer", "fold", "decode16"],
                     help="only one timed loop of one mode (for profiler captures); "
                          "verify-small runs 32 sequences")
     args = ap.parse_args()
@@ -817,6 +817,14 @@ def main():
         r = proj_mode(device, args.steps, tc_peak, hbm_peak, warmup=args.warmup)
         if rank == 0:
             print(json.dumps({"profile_run": "proj", "calls": r["calls"]}))
+        return
+    if args.profile in ("fold", "decode16"):
+        if args.profile == "fold":
+            r = fold_mode(device, args.steps, hbm_peak, warmup=args.warmup)
+        else:
+            r = decode_h16_mode(device, args.steps, hbm_peak, warmup=args.warmup)
+        if rank == 0:
+            print(json.dumps({"profile_run": args.profile, "ms_per_step": r["ms_per_step"]}))
         return
     if args.profile == "layer":
         r = layer_mode(device, args.steps, warmup=args.warmup)
