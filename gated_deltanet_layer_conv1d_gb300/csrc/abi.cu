@@ -142,8 +142,8 @@ gdn_status gated_rmsnorm_impl(const float* o, const void* z, int64_t z_stride, c
   if (!aligned(o, 16) || !aligned(z, 16) || !aligned(w, 16) || !aligned(y, 16) ||
       (z_stride * esize(dtype)) % 16 != 0)
     return GDN_ERR_MISALIGNED;
-  const cudaError_t e = launch_gated_rmsnorm(o, z, z_stride, w, eps, T, n_v_heads, d_v, dtype,
-                                             gate, y, stream);
+  const cudaError_t e = launch_gated_rmsnorm(o, false, z, z_stride, w, eps, T, n_v_heads, d_v,
+                                             dtype, gate, y, stream);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

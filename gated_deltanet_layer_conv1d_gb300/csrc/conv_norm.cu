@@ -326,8 +326,18 @@ __global__ void gdn_seqlens_check_kernel(const int32_t* cu, int n, int total, in
 
 // kRows rows per warp per pass, all their loads issued before any use, so each warp keeps
 // several independent rows in flight.
-template <typename T, int D, int GATE>
-__global__ void gdn_gated_rmsnorm_kernel(const float* __restrict__ o, const T* __restrict__ z,
+__device__ __forceinline__ float4 load_o4(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+__device__ __forceinline__ float4 load_o4(const __half* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <typename T, int D, int GATE, typename OT = float>
+__global__ void gdn_gated_rmsnorm_kernel(const OT* __restrict__ o, const T* __restrict__ z,
                                          int64_t z_stride, const float* __restrict__ w,
                                          float eps, int T_, int Hv, T* __restrict__ y) {
   using A = Act<T>;
@@ -347,7 +357,7 @@ __global__ void gdn_gated_rmsnorm_kernel(const float* __restrict__ o, const T* _
       ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       z4[k] = ov[k];
       if (live && r < rows) {
-        ov[k] = *reinterpret_cast<const float4*>(o + size_t(r) * D + j);
+        ov[k] = load_o4(o + size_t(r) * D + j);
         z4[k] = A::load4(z + size_t(t) * z_stride + h * D + j);
       }
     }
@@ -416,26 +426,26 @@ cudaError_t launch_seqlens_check(const int32_t* cu, int n, int total, int32_t* s
 
 namespace {
 
-template <int GATE>
-void gated_rmsnorm_gate(const float* o, const void* z, int64_t z_stride, const float* w, float eps,
+template <int GATE, typename OT>
+void gated_rmsnorm_gate(const OT* o, const void* z, int64_t z_stride, const float* w, float eps,
                         int T, int Hv, int D, int dtype, void* y, int blocks, int threads,
                         cudaStream_t stream) {
   if (dtype == GDN_DTYPE_BF16) {
     auto zp = reinterpret_cast<const __nv_bfloat16*>(z);
     auto yp = reinterpret_cast<__nv_bfloat16*>(y);
-    if (D == 128) gdn_gated_rmsnorm_kernel<__nv_bfloat16, 128, GATE><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
-    else gdn_gated_rmsnorm_kernel<__nv_bfloat16, 16, GATE><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
+    if (D == 128) gdn_gated_rmsnorm_kernel<__nv_bfloat16, 128, GATE, OT><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
+    else gdn_gated_rmsnorm_kernel<__nv_bfloat16, 16, GATE, OT><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
   } else {
     auto zp = reinterpret_cast<const float*>(z);
     auto yp = reinterpret_cast<float*>(y);
-    if (D == 128) gdn_gated_rmsnorm_kernel<float, 128, GATE><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
-    else gdn_gated_rmsnorm_kernel<float, 16, GATE><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
+    if (D == 128) gdn_gated_rmsnorm_kernel<float, 128, GATE, OT><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
+    else gdn_gated_rmsnorm_kernel<float, 16, GATE, OT><<<blocks, threads, 0, stream>>>(o, zp, z_stride, w, eps, T, Hv, yp);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_gated_rmsnorm(const float* o, const void* z, int64_t z_stride,
+cudaError_t launch_gated_rmsnorm(const void* o, bool o_half, const void* z, int64_t z_stride,
                                  const float* w, float eps, int T, int Hv, int D, int dtype,
                                  int gate, void* y, cudaStream_t stream) {
   const int rows = T * Hv;
@@ -444,8 +454,15 @@ cudaError_t launch_gated_rmsnorm(const float* o, const void* z, int64_t z_stride
   int blocks = (rows + per_block - 1) / per_block;
   const int cap = sm_count() * 8;
   if (blocks > cap) blocks = cap;
-  if (gate) gated_rmsnorm_gate<1>(o, z, z_stride, w, eps, T, Hv, D, dtype, y, blocks, threads, stream);
-  else gated_rmsnorm_gate<0>(o, z, z_stride, w, eps, T, Hv, D, dtype, y, blocks, threads, stream);
+  if (o_half) {
+    const __half* oh = reinterpret_cast<const __half*>(o);
+    if (gate) gated_rmsnorm_gate<1>(oh, z, z_stride, w, eps, T, Hv, D, dtype, y, blocks, threads, stream);
+    else gated_rmsnorm_gate<0>(oh, z, z_stride, w, eps, T, Hv, D, dtype, y, blocks, threads, stream);
+  } else {
+    const float* of = reinterpret_cast<const float*>(o);
+    if (gate) gated_rmsnorm_gate<1>(of, z, z_stride, w, eps, T, Hv, D, dtype, y, blocks, threads, stream);
+    else gated_rmsnorm_gate<0>(of, z, z_stride, w, eps, T, Hv, D, dtype, y, blocks, threads, stream);
+  }
   return cudaGetLastError();
 }
 

@@ -76,13 +76,15 @@ cudaError_t launch_conv_step(const ConvParams& p, int dtype, cudaStream_t stream
 // the workspace tiles (bf16 activations, d = 128).
 cudaError_t launch_prefill_prep(const ConvParams& p, cudaStream_t stream);
 
-cudaError_t launch_gated_rmsnorm(const float* o, const void* z, int64_t z_stride,
+// o: f32, or fp16 when o_half (the prefill's internal hand-off of O to the norm).
+cudaError_t launch_gated_rmsnorm(const void* o, bool o_half, const void* z, int64_t z_stride,
                                  const float* w, float eps, int T, int Hv, int D, int dtype,
                                  int gate, void* y, cudaStream_t stream);
 
 // Chunked prefill.
 struct PrefillParams {
   int32_t Hk, Hv, G, D, conv_dim, n, n_slots, total_tokens, max_seqlen, max_chunks;
+  void* o_half;  // internal: fp16 [T][Hv][128] room for O when no f32 core output is wanted
   float q_scale, l2_eps, norm_eps;
   int32_t norm_gate;  // 0: SiLU(z), 1: sigmoid(z)
   const float* conv_w;

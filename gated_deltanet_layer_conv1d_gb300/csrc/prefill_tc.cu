@@ -777,7 +777,11 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
 #pragma unroll
       for (int u = 0; u < 32; ++u) v[u] = eg * X[u] + v[u];
       const size_t orow = size_t(t_begin + t0 + row) * p.Hv + h;
-      if (p.core_out && row < L) {
+      if (p.o_half && row < L) {  // the norm kernel's fp16 copy of O
+        __half* o = reinterpret_cast<__half*>(p.o_half) + orow * kD + col0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(o + 8 * q) = pack8_h(v + 8 * q);
+      } else if (p.core_out && row < L) {
         float* o = p.core_out + orow * kD + col0;
 #pragma unroll
         for (int u = 0; u < 32; u += 4)
@@ -875,11 +879,14 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, float* o_work, cudaStream_
   // to its own kernel.
   const int units = p.n * p.Hv, sms = sm_count();
   if (units * 2 > sms) return launch_spine<128>(p, stream);
+  // Without an f32 core output to fill, O reaches the norm kernel as fp16 (2^-11 relative,
+  // far below the bf16 rounding of y), which halves that hand-off's bytes.
   PrefillParams q = p;
-  if (!q.core_out) q.core_out = o_work;
+  q.o_half = p.core_out ? nullptr : static_cast<void*>(o_work);
   cudaError_t e = launch_spine<64>(q, stream);
   if (e != cudaSuccess) return e;
-  return launch_gated_rmsnorm(q.core_out, p.z, p.z_stride, p.norm_w, p.norm_eps,
+  return launch_gated_rmsnorm(q.o_half ? q.o_half : static_cast<const void*>(q.core_out),
+                              q.o_half != nullptr, p.z, p.z_stride, p.norm_w, p.norm_eps,
                               p.total_tokens, p.Hv, kD, GDN_DTYPE_BF16, p.norm_gate, p.y, stream);
 }
 
