@@ -680,6 +680,25 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     bad |= !mbar_wait_bounded(&full[c & 1], uint32_t(c >> 1) & 1u);
     consumed = c;
     const float* gd = reinterpret_cast<const float*>(sm + st + S::kGd);
+    // U rows of this thread (W-row lanes 64..127) into registers: while MMA_a runs when U
+    // came with the chunk's operands (two-slice spine), else once its own copy has landed
+    float X[32];
+    auto read_u = [&]() {
+      const int r = row - kC;
+      if (!S::kUInStage) bad |= !mbar_wait_bounded(ufull, uint32_t(c) & 1u);
+      const float* Us = reinterpret_cast<const float*>(
+                            sm + (S::kUInStage ? st + S::kUst : S::kUs)) +
+                        cg * (kC * 32) + r * 32;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 x = *reinterpret_cast<const float4*>(Us + ((k ^ (r & 7)) << 2));
+        X[4 * k] = x.x;
+        X[4 * k + 1] = x.y;
+        X[4 * k + 2] = x.z;
+        X[4 * k + 3] = x.w;
+      }
+    };
+    if (S::kUInStage && q4 >= 2) read_u();
 
     // ---- MMA_a: [Q;W] H0
     if (tid == kIssuer) {
@@ -697,24 +716,12 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     // ---- Delta = U - W H0 (fp16 Delta^T for MMA_b); the Q H0 rows stay in registers
     float eg = 0.f;
     const float eL = exp2_fast(gd[kC - 1]);
-    float X[32];
     {
       float v[32];
       tc::ld32(tmem + tl + kTA + jl0, v);
       if (q4 >= 2) {
         const int r = row - kC;
-        if (!S::kUInStage) bad |= !mbar_wait_bounded(ufull, uint32_t(c) & 1u);
-        const float* Us = reinterpret_cast<const float*>(
-                              sm + (S::kUInStage ? st + S::kUst : S::kUs)) +
-                          cg * (kC * 32) + r * 32;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float4 x = *reinterpret_cast<const float4*>(Us + ((k ^ (r & 7)) << 2));
-          X[4 * k] = x.x;
-          X[4 * k + 1] = x.y;
-          X[4 * k + 2] = x.z;
-          X[4 * k + 3] = x.w;
-        }
+        if (!S::kUInStage) read_u();
 #pragma unroll
         for (int u = 0; u < 32; ++u) v[u] = X[u] - v[u];
 #pragma unroll
