@@ -36,6 +36,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
@@ -358,17 +360,20 @@ __global__ void __launch_bounds__(kProjThreads, 1)
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
+  // the driver's entry point, looked up once per process (calls may come from any thread)
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+  if (!f) {
+    void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess)
       return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    fn.store(f, std::memory_order_release);
   }
-  return fn;
+  return f;
 }
 
 // A row-major bf16 matrix [rows][cols] (row stride ld elements) read in boxes of
@@ -417,12 +422,16 @@ cudaError_t launch_bn(const ProjParams& p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kern, ma, mb, p);
 }
 
-// How many clusters of `s` CTAs of the BN-wide kernel the GPU holds at once (a cluster
-// stays inside one GPC, so this is below SMs / s); cached per shape.
+// How many clusters of `s` CTAs of the BN-wide kernel the current GPU holds at once (a
+// cluster stays inside one GPC, so this is below SMs / s); cached per device and shape.
+constexpr int kProjMaxDevices = 64;
 int max_active_clusters(int bn, int s) {
-  static int cache[3][9] = {};
+  static std::atomic<int> cache[kProjMaxDevices][3][9];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kProjMaxDevices) return -1;
   const int i = bn == 256 ? 0 : (bn == 128 ? 1 : 2);
-  if (cache[i][s] == 0) {
+  int cached = cache[dev][i][s].load(std::memory_order_relaxed);
+  if (cached == 0) {
     int n = 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(s));
@@ -465,9 +474,10 @@ int max_active_clusters(int bn, int s) {
       (void)cudaGetLastError();
       n = 0;
     }
-    cache[i][s] = n > 0 ? n : -1;  // -1: this split is not available
+    cached = n > 0 ? n : -1;  // -1: this split is not available
+    cache[dev][i][s].store(cached, std::memory_order_relaxed);
   }
-  return cache[i][s];
+  return cached;
 }
 
 }  // namespace
