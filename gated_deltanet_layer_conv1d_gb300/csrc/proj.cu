@@ -359,6 +359,234 @@ __global__ void __launch_bounds__(kProjThreads, 1)
   if (warp == 1) tc::dealloc(tmem, C::kTmemCols);
 }
 
+// ------------------------------------------------------------------ SM pairs
+// Large calls (two row blocks or more, 256-wide tiles) run on SM pairs: a cluster of two
+// CTAs computes one 256 x 256 tile with tcgen05.mma.cta_group::2.  CTA r of the pair loads
+// rows r*128 .. r*128+127 of the tile's A block and of its B block into its own shared
+// memory; both copies complete on the even (leader) CTA's full barrier, the leader's one
+// thread issues the M = 256 MMAs that read both CTAs' halves, and its commits arrive on
+// the stage and accumulator barriers of both CTAs at once.  Each CTA's TMEM holds its 128
+// rows of the 256 x 256 accumulator, which its own epilogue warps store; they report back
+// to the leader's tempty barrier.  Per SM and K block that is 32 KB of operands for a
+// 128 x 256 x 64 product instead of 48 KB, and six stages fit where four did.
+struct PairCfg {
+  static constexpr uint32_t kHalfTile = 128u * kBK * 2;      // 128 rows x 64 bf16
+  static constexpr uint32_t kStageBytes = 2 * kHalfTile;     // this CTA's A and B halves
+  static constexpr int kStages = 6;
+  static constexpr uint32_t kBar = uint32_t(kStages) * kStageBytes;
+  static constexpr uint32_t kTmemSlot = kBar + 8u * uint32_t(2 * kStages + 5);
+  static constexpr uint32_t kAbort = kTmemSlot + 4;
+  static constexpr uint32_t kBytes = kAbort + 4 + 1024;
+  static constexpr int kAccs = 2;             // 256-column accumulators in TMEM
+  static constexpr uint32_t kTmemCols = 256u * kAccs;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t peer_addr(const void* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  return ra;
+}
+// A tile into this CTA's shared memory, completing on a barrier of either CTA of the pair
+// (bar: a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2 [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+// Arrives on the barrier at this offset in both CTAs of the pair once the MMAs issued
+// before have completed.
+__device__ __forceinline__ void commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)), "h"(uint16_t(3))
+      : "memory");
+}
+__device__ __forceinline__ void commit_pair_local(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+      ::"r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void arrive_remote(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kProjThreads, 1)
+    gdn_proj_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a,
+                              const __grid_constant__ CUtensorMap map_b,
+                              const __grid_constant__ ProjParams p) {
+  using C = PairCfg;
+  constexpr int S = C::kStages;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::kBar);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::kTmemSlot);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + C::kAbort);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int tiles_m = (p.M + 255) / 256, tiles_n = (p.N + 255) / 256;
+  const int tiles = tiles_m * tiles_n, kblocks = (p.K + kBK - 1) / kBK;
+  const int pair = int(blockIdx.x) >> 1, pairs = int(gridDim.x) >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 8);  // the four epilogue warps of each CTA of the pair
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_mbar_init();
+    prefetch_map(&map_a);
+    prefetch_map(&map_b);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(tslot)), "r"(C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before either signals the other's
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = pair; t < tiles && ok; t += pairs) {
+      const int mb = p.n_fast ? t / tiles_n : t % tiles_m;
+      const int nb = p.n_fast ? t % tiles_n : t / tiles_m;
+      const int m0 = mb * 256 + int(rank) * 128, n0 = nb * 256 + int(rank) * 128;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!wait_or_abort(&empty[s], ph ^ 1u, abort)) { ok = false; break; }
+        unsigned char* st = sm + uint32_t(s) * C::kStageBytes;
+        if (leader) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
+        const uint32_t fb = peer_addr(&full[s], 0);
+        tma_load_2d_pair(st, &map_a, kb * kBK, m0, fb);
+        tma_load_2d_pair(st + C::kHalfTile, &map_b, kb * kBK, n0, fb);
+        if (++s == S) { s = 0; ph ^= 1u; }
+      }
+    }
+    if (!ok && leader) {
+      // the pair's copies still in flight land before shared memory is released
+      for (int q = 0; q < S; ++q) mbar_wait_bounded(&full[q], 0, kWaitBudgetNs / 8);
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ---------------------------------------------------------------- MMA issuer (leader)
+    constexpr uint32_t idesc = tc::idesc_bf16(256, 256);
+    int s = 0;
+    uint32_t ph = 0;
+    int acc = 0;
+    uint32_t aph = 0;
+    bool ok = true;
+    for (int t = pair; t < tiles && ok; t += pairs) {
+      if (!wait_or_abort(&tempty[acc], aph ^ 1u, abort)) break;
+      tc::fence_after_sync();
+      const uint32_t d = tmem + uint32_t(acc * 256);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!wait_or_abort(&full[s], ph, abort)) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t a = smem_u32(sm + uint32_t(s) * C::kStageBytes);
+        const uint32_t b = a + C::kHalfTile;
+#pragma unroll
+        for (int k0 = 0; k0 < kBK; k0 += 16)
+          mma_pair(d, tc::desc_at(a, 128, k0), tc::desc_at(b, 128, k0), idesc, kb > 0 || k0 > 0);
+        commit_pair(&empty[s]);
+        if (++s == S) { s = 0; ph ^= 1u; }
+      }
+      if (!ok) break;
+      commit_pair(&tfull[acc]);
+      if (++acc == C::kAccs) {
+        acc = 0;
+        aph ^= 1u;
+      }
+    }
+    commit_pair_local(drain);
+    mbar_wait_bounded(drain, 0);
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lanes 32q .. 32q + 31 of this CTA's 128 rows
+    int acc = 0;
+    uint32_t aph = 0;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C);
+    for (int t = pair; t < tiles; t += pairs) {
+      const int mb = p.n_fast ? t / tiles_n : t % tiles_m;
+      const int nb = p.n_fast ? t % tiles_n : t / tiles_m;
+      const int n0 = nb * 256;
+      if (!wait_or_abort(&tfull[acc], aph, abort)) break;
+      tc::fence_after_sync();
+      const int row = mb * 256 + int(rank) * 128 + 32 * q + lane;
+      __nv_bfloat16* orow = out + size_t(row) * size_t(p.ldc) + n0;
+      const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc * 256);
+#pragma unroll 1
+      for (int c0 = 0; c0 < 256; c0 += 32) {
+        float v[32];
+        tc::ld32(taddr + uint32_t(c0), v);
+        if (row < p.M) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (n0 + c0 + 8 * g < p.N) {
+              const uint4 w = make_uint4(pack_bf16x2(v[8 * g], v[8 * g + 1]),
+                                         pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
+                                         pack_bf16x2(v[8 * g + 4], v[8 * g + 5]),
+                                         pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
+              *reinterpret_cast<uint4*>(orow + c0 + 8 * g) = w;
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) arrive_remote(peer_addr(&tempty[acc], 0));
+      if (++acc == C::kAccs) {
+        acc = 0;
+        aph ^= 1u;
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // the pair's MMAs, copies and remote arrivals are done
+  tc::fence_after_sync();
+  if (threadIdx.x == 0 && *abort) report(p.status, GDN_ERR_TIMEOUT);
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(C::kTmemCols)
+                 : "memory");
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   // the driver's entry point, looked up once per process (calls may come from any thread)
   static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
@@ -480,6 +708,67 @@ int max_active_clusters(int bn, int s) {
   return cached;
 }
 
+// How many SM pairs of the pair kernel the current GPU holds at once; cached per device.
+int max_active_pairs() {
+  static std::atomic<int> cache[kProjMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kProjMaxDevices) return -1;
+  int cached = cache[dev].load(std::memory_order_relaxed);
+  if (cached == 0) {
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kProjThreads);
+    cfg.dynamicSmemBytes = PairCfg::kBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaFuncSetAttribute(gdn_proj_gemm_pair_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(PairCfg::kBytes));
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, gdn_proj_gemm_pair_kernel, &cfg);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    cached = n > 0 ? n : -1;
+    cache[dev].store(cached, std::memory_order_relaxed);
+  }
+  return cached;
+}
+
+cudaError_t launch_pair(const ProjParams& p, cudaStream_t stream) {
+  using C = PairCfg;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, p.A, p.M, p.K, p.lda, 128) || !make_map(&mb, p.B, p.N, p.K, p.ldb, 128))
+    return cudaErrorInvalidValue;
+  auto kern = gdn_proj_gemm_pair_kernel;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kBytes));
+  if (e != cudaSuccess) return e;
+  const int tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
+  const int max_pairs = max_active_pairs();
+  if (max_pairs <= 0) return cudaErrorInvalidConfiguration;
+  const int pairs = tiles < max_pairs ? tiles : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(2 * pairs));
+  cfg.blockDim = dim3(kProjThreads);
+  cfg.dynamicSmemBytes = C::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, p);
+}
+
 }  // namespace
 
 ProjShape proj_shape(int M, int N, int K) {
@@ -522,6 +811,8 @@ cudaError_t launch_proj(const ProjParams& p_in, cudaStream_t stream) {
   }
   if (p.splits < 1 || p.splits > 8) return cudaErrorInvalidValue;
   p.n_fast = p.M > p.N ? 1 : 0;  // A (M x K) larger than B (N x K)
+  if (p.bn == 256 && p.splits == 1 && p.M > kBM && max_active_pairs() > 0)
+    return launch_pair(p, stream);
   switch (p.bn) {
     case 256: return launch_bn<256>(p, stream);
     case 128: return launch_bn<128>(p, stream);
