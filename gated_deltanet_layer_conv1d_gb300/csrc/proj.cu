@@ -24,6 +24,9 @@
 // Rows past M and columns past N of the tiles are zero-filled by TMA and never stored;
 // K past the end is zero-filled too, so K needs only 16-byte rows.
 //
+// Calls with two row blocks or more that take 256-wide tiles run on SM pairs instead (the
+// pair kernel further down: 256 x 256 tiles, tcgen05.mma.cta_group::2).
+//
 // Calls with fewer tiles than SMs (a decode step's 128 tokens) split K instead: a cluster
 // of `splits` CTAs per tile, each over its own run of K blocks, leaves its f32 partial
 // tile in shared memory; after a cluster barrier every CTA sums one slice of the tile's
