@@ -76,6 +76,26 @@ def test_gemm_small_and_ragged(M, N, K):
     assert_gemm_close(run_gemm(x, w), x, w, what=f"{M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(200, 12352, 2048), (2048, 2048, 2048), (100, 200, 72)])
+def test_gemm_strided_operands(M, N, K):
+    """A read from a wider buffer (lda > K) and C written into one (ldc > N), on the pair
+    kernel with a single 256-row block (the odd CTA's rows partly past M), on the pair
+    kernel with full blocks, and on the one-SM kernel."""
+    rng = np.random.default_rng(M + K)
+    x = wl.round_bf16(rng.standard_normal((M, K)).astype(np.float32))
+    w = wl.round_bf16((rng.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a_big = torch.zeros((M, K + 24), dtype=torch.bfloat16, device="cuda")
+    a_big[:, 8:8 + K] = bf16_dev(x)
+    c_big = torch.full((M, N + 40), 7.0, dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_proj_gemm(a_big[:, 8:8 + K], bf16_dev(w), c_big[:, 16:16 + N], status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_gemm_close(c_big[:, 16:16 + N], x, w, what=f"strided {M}x{N}x{K}")
+    # columns outside the view are untouched
+    assert (c_big[:, :16] == 7.0).all() and (c_big[:, 16 + N:] == 7.0).all()
+
+
 @pytest.mark.parametrize("T", [128, 8000])
 def test_in_proj_full_width(T):
     """in_proj of the 16/32-head layer: N = 12352 outputs, K = 2048; T = 8000 compares a
