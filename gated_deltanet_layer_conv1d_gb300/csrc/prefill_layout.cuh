@@ -35,7 +35,7 @@ struct PrefillLayout {
   static constexpr size_t kPTile = size_t(64) * 64 * 2;  // one fp16 [64][64] tile
   static constexpr size_t kGate = size_t(2) * kC * 4;    // log(alpha), beta
   static constexpr size_t kDecay = size_t(kC) * 4;       // g
-  static constexpr size_t kU = size_t(kC) * 128 * 4;     // U, f32
+  static constexpr size_t kU = size_t(kC) * 128 * 2;     // U, fp16
   // per value head: W | K~ | P | g | U  (every part 256-byte aligned)
   static constexpr size_t kHeadPrep = kTile + kTile + kPTile + kDecay + kU;
   int Hk, Hv;

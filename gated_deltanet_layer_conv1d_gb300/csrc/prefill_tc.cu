@@ -424,12 +424,14 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
         *reinterpret_cast<__half*>(sm + S::kWi + tc::sw128_offset(64, 32 * half + u, i)) =
             __float2half_rn(v[u]);
       tc::ld32(tmem + tl + kTU + 32 * half, v);
-      // U column group q4 (= i / 32), row r, column i % 32 = lane, in its swizzled place
-      float* Ug = reinterpret_cast<float*>(ws + lay.u(cs, h)) + q4 * (kC * 32);
+      // U (fp16) column group q4 (= i / 32), row r, column i % 32 = lane: 16-byte piece
+      // lane / 8 of the row at piece (lane / 8) ^ ((r / 2) % 4), so that the spine's
+      // row-per-thread reads of a piece are free of bank conflicts
+      __half* Ug = reinterpret_cast<__half*>(ws + lay.u(cs, h)) + q4 * (kC * 32);
 #pragma unroll
       for (int u = 0; u < 32; ++u) {
         const int r = 32 * half + u;
-        Ug[r * 32 + ((((lane >> 2) ^ (r & 7))) << 2) + (lane & 3)] = v[u];
+        Ug[r * 32 + (((lane >> 3) ^ ((r >> 1) & 3)) << 3) + (lane & 7)] = __float2half_rn(v[u]);
       }
     }
     for (int idx = tid; idx < kC * 16; idx += kPrepThreads) {
@@ -484,15 +486,15 @@ struct SpineSmem {
   // The two-slice spine also keeps U in each buffer (one chunk ahead, like the rest); the
   // whole-row spine has room for one U buffer only, refilled after each chunk's read.
   static constexpr bool kUInStage = NCOL == 64;
-  static constexpr uint32_t kUst = 58368;  // [NCOL / 32][64][32] f32 U (swizzled), kUInStage
-  static constexpr uint32_t kStage = kUInStage ? kUst + NCOL * 256 : 58368;
-  static constexpr uint32_t kTx = 4 * 8192 + 8192 + 16384 + 256 + (kUInStage ? NCOL * 256 : 0);
+  static constexpr uint32_t kUst = 58368;  // [NCOL / 32][64][32] fp16 U (swizzled), kUInStage
+  static constexpr uint32_t kStage = kUInStage ? kUst + NCOL * 128 : 58368;
+  static constexpr uint32_t kTx = 4 * 8192 + 8192 + 16384 + 256 + (kUInStage ? NCOL * 128 : 0);
   static constexpr uint32_t kHT = 2 * kStage;          // [128][NCOL] f16 H slice (MN-major B)
   static constexpr uint32_t kDT = kHT + NCOL * 256;    // [64][NCOL] f16 Delta (MN-major B)
   static constexpr uint32_t kUs = kDT + NCOL * 128;    // the single U buffer, !kUInStage
   // Gated norm in the spine (whole rows, NCOL = 128 only):
   static constexpr bool kNorm = NCOL == 128;
-  static constexpr uint32_t kZ = kUs + (kUInStage ? 0 : NCOL * 256);  // [64][128] bf16 z rows
+  static constexpr uint32_t kZ = kUs + (kUInStage ? 0 : NCOL * 128);  // [64][128] bf16 z rows
   static constexpr uint32_t kRed = kZ + (kNorm ? 16384 : 0);   // [4][64] f32 partial sums
   static constexpr uint32_t kNW = kRed + (kNorm ? 1024 : 0);   // [128] f32 norm weight
   static constexpr uint32_t kMisc = kNW + (kNorm ? 512 : 0);   // bars, tmem slot
@@ -617,7 +619,7 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     bulk_g2s(st + S::kQW + 24576, wimg + 8192, 8192, &full[c & 1]);
     bulk_g2s(st + S::kGd, ws + lay.g(cs, h), 256, &full[c & 1]);
     if constexpr (S::kUInStage)
-      bulk_g2s(st + S::kUst, ws + lay.u(cs, h) + size_t(slice) * NCOL * 256, NCOL * 256,
+      bulk_g2s(st + S::kUst, ws + lay.u(cs, h) + size_t(slice) * NCOL * 128, NCOL * 128,
                &full[c & 1]);
     mbar_arrive_expect_tx(&fullB[c & 1], 8192 + 16384);
     bulk_g2s(st + S::kP, ws + lay.p(cs, h), 8192, &fullB[c & 1]);
@@ -625,9 +627,9 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
   };
   // Chunk c's U columns of this slice into the single U buffer (completing on ufull).
   auto issue_u = [&](int c) {
-    mbar_arrive_expect_tx(ufull, NCOL * 256);
-    bulk_g2s(sm + S::kUs, ws + lay.u(slot0 + size_t(c), h) + size_t(slice) * NCOL * 256,
-             NCOL * 256, ufull);
+    mbar_arrive_expect_tx(ufull, NCOL * 128);
+    bulk_g2s(sm + S::kUs, ws + lay.u(slot0 + size_t(c), h) + size_t(slice) * NCOL * 128,
+             NCOL * 128, ufull);
   };
   if (tid == kLoader) {
     issue_loads(0);
@@ -686,16 +688,19 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     auto read_u = [&]() {
       const int r = row - kC;
       if (!S::kUInStage) bad |= !mbar_wait_bounded(ufull, uint32_t(c) & 1u);
-      const float* Us = reinterpret_cast<const float*>(
-                            sm + (S::kUInStage ? st + S::kUst : S::kUs)) +
-                        cg * (kC * 32) + r * 32;
+      const __half* Us = reinterpret_cast<const __half*>(
+                             sm + (S::kUInStage ? st + S::kUst : S::kUs)) +
+                         cg * (kC * 32) + r * 32;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float4 x = *reinterpret_cast<const float4*>(Us + ((k ^ (r & 7)) << 2));
-        X[4 * k] = x.x;
-        X[4 * k + 1] = x.y;
-        X[4 * k + 2] = x.z;
-        X[4 * k + 3] = x.w;
+      for (int k = 0; k < 4; ++k) {
+        const uint4 x = *reinterpret_cast<const uint4*>(Us + ((k ^ ((r >> 1) & 3)) << 3));
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          X[8 * k + 2 * e] = f.x;
+          X[8 * k + 2 * e + 1] = f.y;
+        }
       }
     };
     if (S::kUInStage && q4 >= 2) read_u();

@@ -291,8 +291,8 @@ GDN_API size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t n, int3
  * GPU that loads the library until the process exits.  It calls no allocator.
  *   - Sizes: a call whose gdn_prefill_workspace_bytes(...) exceeds the scratch returns
  *     GDN_ERR_SCRATCH_TOO_SMALL and launches nothing.  At H_k = 16, H_v = 32, d = 128 each
- *     64-token chunk slot takes 3.3 MiB (tiles, W, K~, P, U) and each token 16 KiB of f32
- *     core output, so the scratch holds one sequence of up to 895 tokens, or several
+ *     64-token chunk slot takes 2.8 MiB (tiles, W, K~, P, U) and each token 16 KiB of
+ *     core output, so the scratch holds one sequence of up to 1,023 tokens, or several
  *     shorter ones.
  *   - Set-up: the first call on a device, with that device current, looks up the scratch's
  *     device address (cudaGetSymbolAddress); make that first call before any stream capture.

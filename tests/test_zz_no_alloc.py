@@ -76,7 +76,7 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
 def test_noalloc_refuses_a_problem_larger_than_its_scratch():
     w = wl.varlen_prefill([64], seed=23)
     dims = dev.dims_of(w.shape)
-    too_many = 8192  # 130 chunk slots of about 3.3 MiB each: more than the 64 MiB scratch
+    too_many = 8192  # 130 chunk slots of about 2.8 MiB each: more than the 64 MiB scratch
     assert gdn.gdn_prefill_workspace_bytes(dims, 1, too_many, too_many) > gdn.NOALLOC_SCRATCH_BYTES
     d = torch.device("cuda")
     h_pool, conv_pool, slots = dev.states_to(w, d)
