@@ -39,6 +39,8 @@
 // the tensor-core chunked prefill does not take.
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -78,6 +80,22 @@ struct Lane {
   __device__ __forceinline__ int row(int m) const { return rowb + Map::RS * m; }
 };
 
+// A thread's four state elements of one tile row in registers: f32 (float4), or packed
+// fp16 (uint2) where the tile is read from and written back to an fp16 pool after a single
+// token, so holding it at storage width rounds exactly where the store would.
+__device__ __forceinline__ float4 sr_get(const float4& s) { return s; }
+__device__ __forceinline__ float4 sr_get(const uint2& s) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&s.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&s.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void sr_set(float4& s, float4 v) { s = v; }
+__device__ __forceinline__ void sr_set(uint2& s, float4 v) {
+  const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+  s.x = *reinterpret_cast<const uint32_t*>(&a);
+  s.y = *reinterpret_cast<const uint32_t*>(&b);
+}
+
 // One token of the gated delta rule on the register tile S (rows L.row(m), columns
 // L.col0..+3).  xq, xk: the normalised q, k of the token in shared memory; xv: its v;
 // red: this token's reduction buffer [2][RB][D] (alternate per token); orow: where the
@@ -86,8 +104,8 @@ struct Lane {
 // NAMED selects the barrier: named barrier 1 over the NT compute threads (kernels with a
 // separate producer warp) or __syncthreads.  `flag` is OR-reduced by that barrier; if any
 // thread raised it, every thread gets true back and the update is not applied.
-template <int D, int NT, bool NAMED = false>
-__device__ __forceinline__ bool token_update(float4 (&S)[RecMap<D, NT>::M], const Lane<D, NT>& L,
+template <int D, int NT, bool NAMED = false, typename SR = float4>
+__device__ __forceinline__ bool token_update(SR (&S)[RecMap<D, NT>::M], const Lane<D, NT>& L,
                                              const float* xq, const float* xk, const float* xv,
                                              float al, float be, float kq, float* red,
                                              float* orow, bool flag = false) {
@@ -98,9 +116,10 @@ __device__ __forceinline__ bool token_update(float4 (&S)[RecMap<D, NT>::M], cons
   for (int m = 0; m < Map::M; ++m) {
     const int i = L.row(m);
     const float ki = xk[i], qi = xq[i];
+    const float4 sm = sr_get(S[m]);
     kr[m] = ki;
-    u.x += S[m].x * ki; u.y += S[m].y * ki; u.z += S[m].z * ki; u.w += S[m].w * ki;
-    pp.x += S[m].x * qi; pp.y += S[m].y * qi; pp.z += S[m].z * qi; pp.w += S[m].w * qi;
+    u.x += sm.x * ki; u.y += sm.y * ki; u.z += sm.z * ki; u.w += sm.w * ki;
+    pp.x += sm.x * qi; pp.y += sm.y * qi; pp.z += sm.z * qi; pp.w += sm.w * qi;
   }
 #pragma unroll
   for (int off = Map::CQ; off < 32; off <<= 1) {
@@ -141,12 +160,17 @@ __device__ __forceinline__ bool token_update(float4 (&S)[RecMap<D, NT>::M], cons
     o.w = al * PP.w + dl.w * kq;
     *reinterpret_cast<float4*>(orow + L.col0) = o;
   }
+  // packed tiles run at a tighter register budget: k is read again rather than kept
+  constexpr bool kReloadK = std::is_same<SR, uint2>::value;
 #pragma unroll
   for (int m = 0; m < Map::M; ++m) {
-    S[m].x = al * S[m].x + kr[m] * dl.x;
-    S[m].y = al * S[m].y + kr[m] * dl.y;
-    S[m].z = al * S[m].z + kr[m] * dl.z;
-    S[m].w = al * S[m].w + kr[m] * dl.w;
+    const float ki = kReloadK ? xk[L.row(m)] : kr[m];
+    float4 sm = sr_get(S[m]);
+    sm.x = al * sm.x + ki * dl.x;
+    sm.y = al * sm.y + ki * dl.y;
+    sm.z = al * sm.z + ki * dl.z;
+    sm.w = al * sm.w + ki * dl.w;
+    sr_set(S[m], sm);
   }
   return false;
 }
@@ -173,11 +197,23 @@ __device__ __forceinline__ void store_state4(__half* p, float4 v) {
   *reinterpret_cast<uint2*>(p) = u;
 }
 
-template <int D, int NT, typename SH = float>
-__device__ __forceinline__ void store_tile(SH* dst, const float4 (&S)[RecMap<D, NT>::M],
+// Tile element (row, col0..+3) into a register of either kind, and back out.
+__device__ __forceinline__ void load_sr(float4& r, const float* p) { r = load_state4(p); }
+__device__ __forceinline__ void load_sr(float4& r, const __half* p) { r = load_state4(p); }
+__device__ __forceinline__ void load_sr(uint2& r, const __half* p) {
+  r = *reinterpret_cast<const uint2*>(p);
+}
+__device__ __forceinline__ void store_sr(float* p, const float4& r) { store_state4(p, r); }
+__device__ __forceinline__ void store_sr(__half* p, const float4& r) { store_state4(p, r); }
+__device__ __forceinline__ void store_sr(__half* p, const uint2& r) {
+  *reinterpret_cast<uint2*>(p) = r;
+}
+
+template <int D, int NT, typename SH = float, typename SR = float4>
+__device__ __forceinline__ void store_tile(SH* dst, const SR (&S)[RecMap<D, NT>::M],
                                            const Lane<D, NT>& L) {
 #pragma unroll
-  for (int m = 0; m < RecMap<D, NT>::M; ++m) store_state4(dst + L.row(m) * D + L.col0, S[m]);
+  for (int m = 0; m < RecMap<D, NT>::M; ++m) store_sr(dst + L.row(m) * D + L.col0, S[m]);
 }
 
 // L2-normalises q and k of `k` tokens held in shared memory (q at x + t*stride, k right
@@ -357,9 +393,15 @@ template <int NT, int KMAX>
 __host__ __device__ constexpr int rec_threads() {
   return NT + (KMAX == 1 ? 64 : 32);
 }
+// Decode on fp16 pools holds its tile packed (half the registers) and runs two CTAs per
+// SM, so one CTA's per-head chain (reduction, barrier, update) overlaps the other's.
+template <int KMAX, typename SH>
+__host__ __device__ constexpr int rec_min_blocks() {
+  return (KMAX == 1 && sizeof(SH) == 2) ? 2 : 1;
+}
 
 template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY, typename SH>
-__global__ void __launch_bounds__(rec_threads<NT, KMAX>(), 1)
+__global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX, SH>()))
     gdn_recurrent_kernel(const __grid_constant__ RecParams p) {
   using Map = RecMap<D, NT>;
   using SL = RecSmem<D, NT, KMAX, STAGES, T, SH>;
@@ -720,16 +762,17 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), 1)
       // decode: obuf slot hq & 1 is free once the norm warp has taken head hq - 2
       if (SL::kNormWarp && hq >= 2)
         ok &= mbar_wait_bounded(&nfree[hq & 1], uint32_t((hq - 2) >> 1) & 1u);
-      float4 S[Map::M];
+      using SR = std::conditional_t<(KMAX == 1 && sizeof(SH) == 2), uint2, float4>;
+      SR S[Map::M];
       const SH* tile = reinterpret_cast<const SH*>(stage + size_t(s) * SL::kTile);
 #pragma unroll
-      for (int mm = 0; mm < Map::M; ++mm) S[mm] = load_state4(tile + L.row(mm) * D + L.col0);
+      for (int mm = 0; mm < Map::M; ++mm) load_sr(S[mm], tile + L.row(mm) * D + L.col0);
       __syncwarp();
       if (L.lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
       ++q;
       for (int t = 0; t < k; ++t) {
         const float* xq = xs + t * CHX;
-        if (token_update<D, NT, true>(S, L, xq, xq + D, xq + (2 + g) * D,
+        if (token_update<D, NT, true, SR>(S, L, xq, xq + D, xq + (2 + g) * D,
                                       gate[(t * kMaxG + g) * 2 + 0],
                                       gate[(t * kMaxG + g) * 2 + 1], kq_s[t],
                                       // decode alternates by head: no barrier separates
@@ -741,7 +784,7 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), 1)
           return;
         }
         if (VERIFY || t == k - 1)
-          store_tile<D, NT, SH>(state_dst<D, VERIFY, SH>(p, it, tab_item, h, t), S, L);
+          store_tile<D, NT, SH, SR>(state_dst<D, VERIFY, SH>(p, it, tab_item, h, t), S, L);
       }
       if constexpr (SL::kNormWarp) {
         if (L.rb == 0) {  // this warp wrote part of o
@@ -767,7 +810,18 @@ cudaError_t launch_rec(const RecParams& p, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  const int P = p.n_items < sm_count() ? p.n_items : sm_count();
+  // persistent: as many CTAs as fit at once (every CTA's producer and consumers wait only
+  // on one another, so a CTA that had to wait for a free SM would still finish)
+  int per_sm = 1;
+  if (rec_min_blocks<KMAX, SH>() > 1) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, rec_threads<NT, KMAX>(),
+                                                      smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    if (per_sm > rec_min_blocks<KMAX, SH>()) per_sm = rec_min_blocks<KMAX, SH>();
+  }
+  const int cap = sm_count() * per_sm;
+  const int P = p.n_items < cap ? p.n_items : cap;
   kern<<<P, rec_threads<NT, KMAX>(), smem, stream>>>(p);
   return cudaGetLastError();
 }
@@ -779,8 +833,10 @@ cudaError_t launch_rec_typed(const RecParams& p, int D, bool verify, cudaStream_
     // with eight, each thread holding sixteen rows of the tile: half as many warps meet at
     // each head's barrier (measured: f32 pools 0.0997 -> 0.0968 ms, fp16 0.0772 -> 0.0735
     // ms per 128-sequence step; verify with eight 0.469 -> 0.523 ms).
+    // Decode on fp16 pools: two stages of 32 KiB tiles, so two CTAs share an SM.
+    constexpr int kDecodeStages = sizeof(SH) == 2 ? 2 : 3;
     if (verify) return launch_rec<T, 128, 512, GDN_VERIFY_K_MAX, 2, true, SH>(p, stream);
-    return launch_rec<T, 128, 256, 1, 3, false, SH>(p, stream);
+    return launch_rec<T, 128, 256, 1, kDecodeStages, false, SH>(p, stream);
   }
   if (verify) return launch_rec<T, 16, 64, GDN_VERIFY_K_MAX, 2, true, SH>(p, stream);
   return launch_rec<T, 16, 64, 1, 3, false, SH>(p, stream);
