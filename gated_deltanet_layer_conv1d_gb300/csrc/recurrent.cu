@@ -104,11 +104,14 @@ __device__ __forceinline__ void sr_set(uint2& s, float4 v) {
 // NAMED selects the barrier: named barrier 1 over the NT compute threads (kernels with a
 // separate producer warp) or __syncthreads.  `flag` is OR-reduced by that barrier; if any
 // thread raised it, every thread gets true back and the update is not applied.
+// rq, rk: the L2 scales of q and k when xq, xk hold them unnormalised (decode), else 1:
+// S k_hat = rk (S k), S q_hat = rq (S q), and k_hat delta^T = k (rk delta)^T.
 template <int D, int NT, bool NAMED = false, typename SR = float4>
 __device__ __forceinline__ bool token_update(SR (&S)[RecMap<D, NT>::M], const Lane<D, NT>& L,
                                              const float* xq, const float* xk, const float* xv,
                                              float al, float be, float kq, float* red,
-                                             float* orow, bool flag = false) {
+                                             float* orow, bool flag = false, float rq = 1.f,
+                                             float rk = 1.f) {
   using Map = RecMap<D, NT>;
   float kr[Map::M];
   float4 u = make_float4(0.f, 0.f, 0.f, 0.f), pp = u;
@@ -146,6 +149,8 @@ __device__ __forceinline__ bool token_update(SR (&S)[RecMap<D, NT>::M], const La
     U.x += a4.x; U.y += a4.y; U.z += a4.z; U.w += a4.w;
     PP.x += p4.x; PP.y += p4.y; PP.z += p4.z; PP.w += p4.w;
   }
+  U.x *= rk; U.y *= rk; U.z *= rk; U.w *= rk;
+  PP.x *= rq; PP.y *= rq; PP.z *= rq; PP.w *= rq;
   const float4 v4 = *reinterpret_cast<const float4*>(xv + L.col0);
   float4 dl;
   dl.x = be * (v4.x - al * U.x);
@@ -160,6 +165,7 @@ __device__ __forceinline__ bool token_update(SR (&S)[RecMap<D, NT>::M], const La
     o.w = al * PP.w + dl.w * kq;
     *reinterpret_cast<float4*>(orow + L.col0) = o;
   }
+  dl.x *= rk; dl.y *= rk; dl.z *= rk; dl.w *= rk;
   // packed tiles run at a tighter register budget: k is read again rather than kept
   constexpr bool kReloadK = std::is_same<SR, uint2>::value;
 #pragma unroll
@@ -302,7 +308,9 @@ struct RecSmem {
   // Per-launch staging so no global load sits on the per-head critical path:
   // slot of each sequence, whether its item can run (0 = yes, else the GDN_ERR_* code),
   // its table-0 pointer (verify), and the current item's 16 table entries (verify).
-  static constexpr size_t kSlots = kKq + ((size_t(KMAX) * 4 + 15) / 16) * 16;  // [128] i32
+  // decode: per-warp partial sums q.q, k.k, q.k of the item's q and k, [D / 32][3]
+  static constexpr size_t kL2 = kKq + ((size_t(KMAX) * 4 + 15) / 16) * 16;
+  static constexpr size_t kSlots = kL2 + ((size_t(D + 31) / 32 * 12 + 15) / 16) * 16;  // [128] i32
   static constexpr size_t kValid = kSlots + GDN_MAX_SEQS * 4;                  // [128] i32
   static constexpr size_t kTab0 = kValid + GDN_MAX_SEQS * 4;                   // [128] u64
   static constexpr size_t kTabItem = kTab0 + GDN_MAX_SEQS * 8;                 // [16] u64
@@ -422,6 +430,7 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
   volatile int32_t* issued_s = reinterpret_cast<volatile int32_t*>(smem + SL::kIssued);
   float* gate = reinterpret_cast<float*>(smem + SL::kGate);
   float* kq_s = reinterpret_cast<float*>(smem + SL::kKq);
+  float* l2_s = reinterpret_cast<float*>(smem + SL::kL2);
   float* xs = reinterpret_cast<float*>(smem + SL::kXs);
   int32_t* slots_s = reinterpret_cast<int32_t*>(smem + SL::kSlots);
   int32_t* valid_s = reinterpret_cast<int32_t*>(smem + SL::kValid);
@@ -668,33 +677,42 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
         drain(q);
         return;
       }
-      for (int lc = tid; lc < CHX; lc += NT) {
-        if (lc >= CH) {
-          const int zc = lc - CH;
-          for (int t = 0; t < k; ++t) xs[t * CHX + lc] = A::to_f(raw_z[t * G * D + zc]);
-          continue;
-        }
+      // One token per item: conv + SiLU of channel lc into xs, the conv state shifted by
+      // the new raw input (exact copies); returns the channel's output.
+      auto conv_channel = [&](int lc) -> float {
         const float4 w4 = *reinterpret_cast<const float4*>(raw_w + size_t(lc) * kW);
         const float4 s4 = A::load4(raw_cs + size_t(lc) * kW);
-        float buf[kW + KMAX];
-        buf[0] = s4.x; buf[1] = s4.y; buf[2] = s4.z; buf[3] = s4.w;
-#pragma unroll
-        for (int t = 0; t < KMAX; ++t)
-          if (t < k) buf[kW + t] = A::to_f(raw_x[t * CH + lc]);
-#pragma unroll
-        for (int t = 0; t < KMAX; ++t)
-          if (t < k)
-            xs[t * CHX + lc] = silu_f(w4.x * buf[t + 1] + w4.y * buf[t + 2] + w4.z * buf[t + 3] +
-                                      w4.w * buf[t + 4]);
-        float4 ns = s4;
-#pragma unroll
-        for (int t = 1; t <= KMAX; ++t)
-          if (t == k) ns = make_float4(buf[t], buf[t + 1], buf[t + 2], buf[t + 3]);
+        const float x = A::to_f(raw_x[lc]);
+        const float y = silu_f(w4.x * s4.y + w4.y * s4.z + w4.z * s4.w + w4.w * x);
+        xs[lc] = y;
         T* cs = reinterpret_cast<T*>(p.conv_pool) +
                 (size_t(it.slot) * p.conv_dim + global_channel(it.kh, lc)) * kW;
-        A::store4(cs, ns);  // exact copies of raw inputs
+        A::store4(cs, make_float4(s4.y, s4.z, s4.w, x));
+        return y;
+      };
+      // Threads below D take q_i and k_i together and sum q.q, k.k and q.k for the L2
+      // norms, which the head updates apply as scales (no normalising pass, no barrier
+      // for it); the others take the v channels; everyone stages one z channel.
+      float sq = 0.f, sk = 0.f, sqk = 0.f;
+      for (int i = tid; i < D; i += NT) {
+        const float qv = conv_channel(i), kv = conv_channel(D + i);
+        sq += qv * qv;
+        sk += kv * kv;
+        sqk += qv * kv;
       }
-      named_sync(1, NT);  // raw block consumed
+      for (int vi = tid - D; vi >= 0 && vi < G * D; vi += NT - D) conv_channel(2 * D + vi);
+      for (int zi = tid; zi < G * D; zi += NT) xs[CH + zi] = A::to_f(raw_z[zi]);
+      if (L.warp < (D + 31) / 32) {
+        sq = warp_sum(sq);
+        sk = warp_sum(sk);
+        sqk = warp_sum(sqk);
+        if (L.lane == 0) {
+          l2_s[3 * L.warp + 0] = sq;
+          l2_s[3 * L.warp + 1] = sk;
+          l2_s[3 * L.warp + 2] = sqk;
+        }
+      }
+      named_sync(1, NT);  // raw block consumed; xs and the sums complete
       if (tid == 0) mbar_arrive(raw_empty);
       if (r_next < rounds) load_scalars(nxt);
     } else {
@@ -750,8 +768,22 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
       named_sync(1, NT);
     }
     ++m;
-    l2norm_tokens<D, Map::NW>(xs, CHX, k, p.q_scale, p.l2_eps, kq_s, L.warp, L.lane);
-    named_sync(1, NT);
+    float rq = 1.f, rk = 1.f, kq1 = 0.f;  // decode: L2 scales of q and k, q_hat.k_hat
+    if constexpr (SL::kPrefetch) {
+      float sq = 0.f, sk = 0.f, sqk = 0.f;
+#pragma unroll
+      for (int w = 0; w < (D + 31) / 32; ++w) {
+        sq += l2_s[3 * w];
+        sk += l2_s[3 * w + 1];
+        sqk += l2_s[3 * w + 2];
+      }
+      rq = p.q_scale * rsqrtf(sq + p.l2_eps);
+      rk = rsqrtf(sk + p.l2_eps);
+      kq1 = rq * rk * sqk;
+    } else {
+      l2norm_tokens<D, Map::NW>(xs, CHX, k, p.q_scale, p.l2_eps, kq_s, L.warp, L.lane);
+      named_sync(1, NT);
+    }
 
     // ---------------- value heads of the item
     for (int g = 0; g < G; ++g) {
@@ -774,12 +806,13 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
         const float* xq = xs + t * CHX;
         if (token_update<D, NT, true, SR>(S, L, xq, xq + D, xq + (2 + g) * D,
                                       gate[(t * kMaxG + g) * 2 + 0],
-                                      gate[(t * kMaxG + g) * 2 + 1], kq_s[t],
+                                      gate[(t * kMaxG + g) * 2 + 1],
+                                      SL::kPrefetch ? kq1 : kq_s[t],
                                       // decode alternates by head: no barrier separates
                                       // one head's reduction reads from the next's writes
                                       red + ((SL::kNormWarp ? hq : t) & 1) * 2 * Map::RB * D,
                                       obuf + (SL::kNormWarp ? (hq & 1) : t) * D,
-                                      t == 0 && !ok)) {
+                                      t == 0 && !ok, rq, rk)) {
           drain(q - 1);
           return;
         }
