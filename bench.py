@@ -76,11 +76,16 @@ def peaks():
 
 
 def _kernel_sources_hash() -> str:
+    """Hash of the decode kernel's sources without their comments and blank lines, so
+    that a comment edit does not disown the counters captured on the same code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_deltanet_layer_conv1d_gb300", "csrc")
     for name in ("recurrent.cu", "common.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            for line in f:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -15,23 +15,29 @@
 // pool instead of table 0 and no intermediates.
 //
 // Design (HBM-bound: the state tile is read once, and written once per token kept):
-//   * persistent grid, one CTA of 512 threads per SM; items are dealt to CTAs in a
-//     zig-zag over the item list (most tokens first), so ragged k balances;
-//   * one elected thread streams the 64 KiB state tile of each (item, value head) into
+//   * persistent grid: one CTA per SM (two on fp16 decode pools); items are dealt to CTAs
+//     in a zig-zag over the item list (most tokens first), so ragged k balances;
+//   * threads: NT compute threads (16 warps for verify, 8 for decode), one producer warp,
+//     and for decode one norm warp;
+//   * one elected producer thread streams the state tile of each (item, value head) into
 //     a shared-memory ring with bulk async copies completing on mbarriers; the tile is
-//     moved to registers (32 floats per thread) and its stage refilled at once, so
-//     STAGES tiles are in flight while one is computed;
-//   * thread (warp w, lane l) owns rows rb*32 + (l/8) + 4m (m < 8) and columns
+//     moved to registers and its stage refilled at once, so STAGES tiles are in flight
+//     while one is computed; decode also prefetches the next item's raw prologue inputs;
+//   * thread (warp w, lane l) owns rows rb*RS*M + (l/8) + 4m and columns
 //     cb*32 + (l%8)*4 .. +3 of the [d_k][d_v] tile (rb = w/4, cb = w%4): every
 //     shared-memory read is conflict-free and every 128-bit global store of a warp
-//     covers four whole 128-byte lines;
+//     covers four whole 128-byte lines; fp16 decode holds its tile packed, two values
+//     per register;
 //   * per token, the column sums u = S k and p = S q are reduced in registers, across
 //     the row-lanes with warp shuffles and across the row-block warps through shared
 //     memory (one barrier per token), then
 //       delta = beta (v - alpha u),  S <- alpha S + k delta^T,  o = alpha p + delta (k.q)
 //     which is S_t = alpha S (I - beta k k^T) + beta v k^T, o = S_t q regrouped;
-//   * the gated RMSNorm of a head's outputs runs one warp per token, with z staged in
-//     shared memory by the item prologue.
+//     decode applies the L2 norms of q and k there as scales (their sums come from the
+//     conv pass);
+//   * the gated RMSNorm of a head's outputs: decode hands o to the norm warp through a
+//     two-slot buffer; verify runs it one warp per token after each head, with z staged
+//     in shared memory by the item prologue.
 //
 // gdn_prefill_seq_kernel is the same per-token update run over a whole sequence, one CTA
 // per (sequence, value head), in segments of 16 tokens (layer_struct.rs,
@@ -389,7 +395,8 @@ __device__ __forceinline__ const SH* state_src(const RecParams& p, const Item& i
   return reinterpret_cast<const SH*>(p.h_pool) + (size_t(it.slot) * p.Hv + h) * D * D;
 }
 
-// Thread roles: threads [0, NT) compute (16 warps at d = 128), the next warp produces.
+// Thread roles: threads [0, NT) compute (at d = 128, 16 warps for verify and 8 for
+// decode), the next warp produces.
 // Lane 0 of the producer warp streams every state tile into the stage ring (full/empty
 // mbarriers per stage) and, for decode, each item's raw prologue inputs into a staging
 // block (raw_full/raw_empty), with bulk async copies.  Compute threads synchronise only
