@@ -25,8 +25,11 @@
 //     MMA_a [Q;W] H0             (M 128 = 64 query rows + 64 W rows, N NCOL, K 128)
 //     MMA_b K~^T Delta and [P;*] Delta  (M 128, N NCOL, K 64; rows past P are ignored)
 //   with Delta and the new H written back between them as fp16 MN-major operands (each
-//   thread stores its own row, 16 bytes at a time); it writes the core output O.  The next chunk's operands arrive by bulk copy into the other of two
-//   buffers meanwhile.  The gated RMSNorm of O follows as its own kernel.
+//   thread stores its own row, 16 bytes at a time).  The next chunk's operands arrive by
+//   bulk copy into the other of two buffers meanwhile.  With whole rows (NCOL = 128) the
+//   spine applies the gated RMSNorm to O itself and writes y; with two column slices it
+//   writes O (fp16 unless the caller asked for the f32 core output) and the gated norm
+//   follows as its own kernel.
 //
 // Operands are fp16 (kind::f16, f32 accumulation): every operand here is bounded
 // (normalised q and k, O(1) v, T, P, Delta and state), and fp16's 11-bit significand
