@@ -813,7 +813,7 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
         named_sync(1, 8 * 32);
         ss = red[row] + red[kC + row] + red[2 * kC + row] + red[3 * kC + row];
         const float inv = rsqrtf(ss / float(kD) + p.norm_eps);
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        cp_async_wait_all();
         if (row < L) {
           __nv_bfloat16* yo = reinterpret_cast<__nv_bfloat16*>(p.y) + orow * kD + jl0;
 #pragma unroll
@@ -837,7 +837,7 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
       }
     }
   }
-  if (S::kNorm) asm volatile("cp.async.wait_group 0;" ::: "memory");
+  if (S::kNorm) cp_async_wait_all();
 
   if (aborted) {
     if (tid == kLoader) {
