@@ -641,11 +641,26 @@ def mixed_mode(device, steps, hbm_peak, tc_peak):
             done.record(st)
             main.wait_event(done)
 
+    def prefill_alone(i):
+        gdn.gdn_prefill_chunked(dims, weights, pin, pre.n, cu, T, Lmax, php, pc, pre.n, ps, py,
+                                None, ws, status[0:1], main)
+
+    def verify_alone(i):
+        gdn.gdn_verify_multi(dims, weights, vin, ver.n, ks, tables, vc, ver.n, vs, None, vy,
+                             None, status[1:2], main)
+
     ms = time_loop(torch, main, fn, steps, 2)
+    ms_pre = time_loop(torch, main, prefill_alone, steps, 2)
+    ms_ver = time_loop(torch, main, verify_alone, steps, 2)
     assert int(status.abs().sum().item()) == 0
     tokens = T + sum(ks)
     fl = PREFILL_FLOPS_PER_TOKEN * T
-    byts = verify_bytes(ks) + prefill_bytes(T)
+    b_pre, b_ver = prefill_bytes(T), verify_bytes(ks)
+    byts = b_ver + b_pre
+
+    def frac(work, ms_, peak, scale):
+        return round(work / (ms_ * 1e-3) / scale / peak, 4)
+
     return {"workload": "mixed_32prefill_U512to4096_96verify_k2to16", "tokens_per_step": tokens,
             "prefill_tokens": T, "verify_tokens": sum(ks), "ms_per_step": round(ms, 4),
             "value": round(tokens / (ms * 1e-3), 1), "unit": "tokens/s", "streams": 2,
@@ -654,7 +669,15 @@ def mixed_mode(device, steps, hbm_peak, tc_peak):
                                     "frac": round(fl / (ms * 1e-3) / 1e12 / tc_peak, 4)},
                          "hbm": {"achieved": round(byts / (ms * 1e-3) / 1e9, 1),
                                  "peak": hbm_peak, "unit": "GB/s",
-                                 "frac": round(byts / (ms * 1e-3) / 1e9 / hbm_peak, 4)}}}
+                                 "frac": round(byts / (ms * 1e-3) / 1e9 / hbm_peak, 4)}},
+            # each part alone on one stream, same calls and sizes: the step's time against
+            # their sum shows what running them side by side saves
+            "parts": {"prefill": {"ms": round(ms_pre, 4), "tokens": T,
+                                  "tensor_frac": frac(fl, ms_pre, tc_peak, 1e12),
+                                  "hbm_frac": frac(b_pre, ms_pre, hbm_peak, 1e9)},
+                      "verify": {"ms": round(ms_ver, 4), "tokens": sum(ks),
+                                 "hbm_frac": frac(b_ver, ms_ver, hbm_peak, 1e9)},
+                      "sum_ms": round(ms_pre + ms_ver, 4)}}
 
 
 def cpu_model() -> str:
@@ -850,7 +873,10 @@ def main():
             r = verify_mode(device, args.steps, hbm_peak, warmup=args.warmup,
                             n=32 if args.profile == "verify-small" else N_SEQ)
         if rank == 0:
-            print(json.dumps({"profile_run": args.profile, "ms_per_step": r["ms_per_step"]}))
+            out = {"profile_run": args.profile, "ms_per_step": r["ms_per_step"]}
+            if "parts" in r:
+                out["parts"] = r["parts"]
+            print(json.dumps(out))
         return
     bench = DecodeBench(device)
     for i in range(args.warmup):
