@@ -6,7 +6,8 @@ chain.  The shapes cover the launch forms the host picks on a GB300: whole-K per
 tiles 64 wide (the small calls), 128 wide (in_proj at 128 tokens) and 256 wide (2048 x 2048,
 the 8000 / 8192-token calls), and K split over a cluster -- 64-wide tiles in 8
 (64 x 200 x 1024, ragged M and N) and in 4 (out_proj at 128 tokens), 128-wide in 3
-(300 x 2048 x 4096, three row blocks) -- and the SM-pair kernel (256 x 256 tiles on two
+(300 x 2048 x 4096, three row blocks), 256-wide in 3 (100 x 9856 x 6144: a wide, deep
+call of few rows, ragged M and a half-filled last tile) -- and the SM-pair kernel (256 x 256 tiles on two
 SMs) for every 256-wide call of two row blocks or more: 2048 x 2048, the 8000 / 8192-token
 calls, in_proj in the layer chain (259 rows) and 4000 x 1000 x 520 (ragged M, N and K).
 
@@ -68,7 +69,8 @@ def run_gemm(x, w):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 64, 64), (100, 200, 72), (129, 136, 8), (64, 200, 1024),
-                                   (300, 2048, 4096), (2048, 2048, 2048), (4000, 1000, 520)])
+                                   (300, 2048, 4096), (2048, 2048, 2048), (4000, 1000, 520),
+                                   (100, 9856, 6144)])
 def test_gemm_small_and_ragged(M, N, K):
     rng = np.random.default_rng(M * 7 + N)
     x = wl.round_bf16(rng.standard_normal((M, K)).astype(np.float32))
