@@ -808,6 +808,27 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def mode_summary(modes: dict) -> dict:
+    """{mode: [ms per step, throughput, roofline fraction]} for every mode that ran (the
+    projections and the layer steps by call)."""
+    out = {}
+    for name, m in modes.items():
+        if "ms_per_step" in m:
+            rf = m.get("roofline", {})
+            frac = rf.get("frac") if "frac" in rf else rf.get("tensor", {}).get("frac")
+            out[name] = [m["ms_per_step"], m.get("value"), frac]
+        for part, pm in m.get("parts", {}).items():
+            if isinstance(pm, dict) and "ms" in pm:
+                tok = pm.get("tokens")
+                out[f"{name}.{part}"] = [pm["ms"], round(tok / pm["ms"] * 1e3, 1) if tok else None,
+                                         pm.get("tensor_frac", pm.get("hbm_frac"))]
+        for sub in ("calls", "steps"):
+            for cname, c in m.get(sub, {}).items():
+                ms = c.get("ms", c.get("ms_per_step"))
+                out[cname] = [ms, c.get("value"), c.get("roofline", {}).get("frac")]
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -968,6 +989,9 @@ def main():
             "cpu_baseline": cpu,
             "modes": modes,
         }
+        # One compact line per mode at the very end, so that the last few hundred bytes of the
+        # output carry every mode's time, throughput and roofline fraction.
+        line["summary"] = mode_summary(modes)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

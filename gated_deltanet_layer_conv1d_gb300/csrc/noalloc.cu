@@ -14,12 +14,17 @@ constexpr size_t kScratchBytes = GDN_NOALLOC_SCRATCH_BYTES;
 
 // The scratch: one array per device that loads the library, kept until the process exits.
 // Host code must not use the name as a device address; it looks the address up below.
+// This file's module holds no kernel, so under CUDA's lazy module loading (the default) the
+// array is reserved when the address is first looked up, not when the library loads: the
+// first call per device (a call with n = 0 does only that) must come before the caller
+// reserves the rest of the device's memory.
 static __device__ __align__(256) unsigned char g_prefill_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::atomic<uintptr_t> g_scratch_addr[kMaxDevices];
 
-// Device address of the scratch on the current device, looked up once per device.
+// Device address of the scratch on the current device, looked up once per device and kept
+// for the life of the process (a cudaDeviceReset would leave it stale).
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -49,8 +54,10 @@ extern "C" gdn_status gdn_prefill_chunked_noalloc(
   if (!dims) return GDN_ERR_NULL_POINTER;
   const size_t need = gdn_prefill_workspace_bytes(dims, n, total_tokens, max_seqlen, chunk);
   if (need > gdn::kScratchBytes) return GDN_ERR_SCRATCH_TOO_SMALL;
+  // The look-up runs on every call, n = 0 included, so that a call with nothing to do is
+  // the set-up call: it reserves the array (lazy module loading) and caches its address.
   void* scratch = nullptr;
-  if (need > 0 && gdn::scratch_address(&scratch) != cudaSuccess) return GDN_ERR_CUDA;
+  if (gdn::scratch_address(&scratch) != cudaSuccess) return GDN_ERR_CUDA;
   return gdn_prefill_chunked(dims, weights, inputs, n, cu_seqlens_dev, total_tokens, max_seqlen,
                              chunk, h_state_ptrs_dev, conv_pool, n_slots, slots_dev, y,
                              core_out, scratch, need, status_dev, stream);

@@ -13,9 +13,10 @@
 //                         P  = lower_incl(Q K^T e^{g_r - g_s})   (swizzled [64][64])
 //                         g  = cumulative log2 decay [64]        (f32; rows past the end
 //                                                                 repeat the last value)
-//                         U  = T diag(beta) V                    (f32, [4][64][32]: the
+//                         U  = T diag(beta) V                    (fp16, [4][64][32]: the
 //                               value columns in groups of 32, each group [r][32] with its
-//                               16-byte pieces swizzled, piece p of row r at p ^ (r % 8))
+//                               16-byte pieces swizzled, piece p of row r at
+//                               p ^ ((r / 2) % 4))
 // Sequence s owns slots base(s) .. base(s) + ceil(len_s / 64) - 1 with
 // base(s) = floor(cu_seqlens[s] / 64) + s, which never overlap and need at most
 // floor(total_tokens / 64) + n + 1 slots.  Rows of a slot past the end of its sequence are

@@ -228,3 +228,33 @@ def mixed_serving(n_prefill: int = 32, n_verify: int = 96, len_lo: int = 512,
     ver = Workload("mixed_verify", shape, True, w, Hv_, cv, ks, tv,
                    extra={"slot_perm": np.arange(n_verify, dtype=np.int32)})
     return pre, ver
+
+
+# Extreme gate and gate-input rows for the edge cases of the method: logits of +-30 are exact
+# in bf16 and drive each gate to its limit (the decay gate's softplus(a + dt_bias) is 30, past
+# the point where softplus(x) = x to f32 precision).
+#   "reset"       a = +30            decay alpha = exp(-exp(A_log) * 30) ~ 1e-5 .. 1e-35
+#   "hold"        a = -30, b = -30   alpha = 1 and beta = 0 to f32 precision: state unchanged
+#   "write"       b = +30            beta = 1 to f32 precision
+#   "reset_write" a = +30, b = +30   the state becomes the one rank-1 write
+#   "zbig"        z = +-30           the output gate at both ends (SiLU(30) = 30, SiLU(-30) ~ 0)
+EXTREME = ("reset", "hold", "write", "reset_write", "zbig")
+
+
+def set_extreme(tokens: dict, rows, kind: str) -> None:
+    """Overwrites the given token rows of a tokens dict (in place) with one extreme pattern."""
+    rows = np.atleast_1d(np.asarray(rows, np.int64))
+    if rows.size == 0 or kind == "normal":
+        return
+    if kind in ("reset", "reset_write"):
+        tokens["a"][rows] = 30.0
+    if kind == "hold":
+        tokens["a"][rows] = -30.0
+        tokens["b"][rows] = -30.0
+    if kind in ("write", "reset_write"):
+        tokens["b"][rows] = 30.0
+    if kind == "zbig":
+        z = tokens["z"][rows]
+        tokens["z"][rows] = np.where(z >= 0, np.float32(30.0), np.float32(-30.0))
+    if kind not in EXTREME:
+        raise ValueError(kind)

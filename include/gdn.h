@@ -296,7 +296,12 @@ GDN_API size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t n, int3
  *     shorter ones.
  *   - Set-up: the first call on a device, with that device current, looks up the scratch's
  *     device address (cudaGetSymbolAddress); make that first call before any stream capture.
- *     Its failure returns GDN_ERR_CUDA.
+ *     Its failure returns GDN_ERR_CUDA.  Under CUDA's lazy module loading (the default since
+ *     CUDA 12.2; CUDA_MODULE_LOADING=EAGER changes it) the array is reserved by that first
+ *     call, not when the library loads, so make it before reserving the rest of the device's
+ *     memory: a call with n = 0 and total_tokens = 0 (valid dims and weights, every other
+ *     pointer may be NULL) does only this set-up.  The cached address does not survive a
+ *     cudaDeviceReset of that device; do not use this entry point after one.
  *   - Sharing: every call on a device uses the same array and leaves its contents behind;
  *     nothing in it needs to start at zero.  Calls that overlap on the GPU (other streams,
  *     other host threads) race on it: serialise them.

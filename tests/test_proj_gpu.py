@@ -27,8 +27,8 @@ import oracle
 from gated_deltanet_layer_conv1d_gb300 import device as dev
 from gated_deltanet_layer_conv1d_gb300 import gdn
 from gated_deltanet_layer_conv1d_gb300 import workloads as wl
-from tests.gpu_common import (TC_STATE_TOL, assert_state_close, assert_y_close, odims, rel_l2,
-                              require_gpu)
+from tests.gpu_common import (ROW_FACTOR, TC_ELEM_FACTOR, TC_STATE_TOL, assert_state_close,
+                              assert_y_close, check_rows, odims, require_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -182,7 +182,17 @@ def test_layer_chain_in_proj_prefill_decode_out_proj():
     od = odims(sh)
     orows = wl.round_bf16(oracle.proj(P.hidden, P.w_in).astype(np.float32))
     sp = oracle.split_in_proj(od, orows)
+    # The GPU's in_proj rows equal the oracle's bf16-rounded rows except where the f32 sum and
+    # the exact one round to different bf16 values (one step apart, or more where the sum
+    # cancels: the f32 accumulation error is relative to sum |x w|), and that is rare.
+    got_rows = rows.float().cpu().numpy()[:, :orows.shape[1]]
+    ne = got_rows != orows
+    acc = np.abs(P.hidden.astype(np.float64)) @ np.abs(P.w_in.astype(np.float64)).T
+    step = np.abs(orows) * 2.0 ** -7 + P.hidden.shape[1] * 2.0 ** -23 * acc[:, :orows.shape[1]]
+    assert (np.abs(got_rows - orows)[ne] <= step[ne]).all()
+    assert ne.mean() < 1e-2, ne.mean()
     y_orc = np.empty((T + 2, sh.z_dim))
+    o_orc = np.empty((T + 2, sh.n_v_heads, sh.d_v))
     off = [0, lens[0], T]
     seqs = []
     for i in range(2):
@@ -193,11 +203,27 @@ def test_layer_chain_in_proj_prefill_decode_out_proj():
     for i, r in enumerate(res):
         y_orc[off[i]:off[i + 1]] = r.y[:-1]
         y_orc[T + i] = r.y[-1]
-        assert_state_close(h_pool[i].cpu().numpy(), r.H, f"state seq {i}", TC_STATE_TOL)
-    e_y = assert_y_close(y, y_orc, "mixer y in the chain")
+        o_orc[off[i]:off[i + 1]] = r.o[:-1]
+        o_orc[T + i] = r.o[-1]
+        # The mixer's inputs are the GPU's in_proj rows, a few elements of which round to
+        # the neighbouring bf16 value of the oracle's (their f32 sums straddle a rounding
+        # boundary); a state row that such a b or a gate logit feeds carries that input
+        # difference, so rows and elements here get four times the common factors.
+        assert_state_close(h_pool[i].cpu().numpy(), r.H, f"state seq {i}", TC_STATE_TOL,
+                           row_factor=4 * ROW_FACTOR, elem_factor=4 * TC_ELEM_FACTOR)
+    e_y = assert_y_close(y, y_orc, "mixer y in the chain", o_orc=o_orc)
     # out = bf16(y W^T): the error of y (measured against bf16(y_oracle), the oracle's own
     # stored y) passes through W_out about unchanged in relative L2 (25 % slack for a random
     # W), and the final bf16 rounding adds at most 2^-9 relative per element.
     out_orc = oracle.proj(wl.round_bf16(y_orc.astype(np.float32)), P.w_out)
-    e = rel_l2(out.float().cpu().numpy(), out_orc)
-    assert e <= 1.25 * e_y + 2.0 ** -9, f"out_proj in the chain: {e:.3e} (y {e_y:.3e})"
+    # Each out row mixes the 32 head rows of its token's y, so its floor carries theirs:
+    # ||out_t|| * sqrt(sum_h max(||y_th||, floor_th)^2) / ||y_t||, with the y floors of
+    # assert_y_close (a y row of a tiny core-output row may carry a larger relative error).
+    yr = wl.round_bf16(y_orc.astype(np.float32)).astype(np.float64).reshape(T + 2, -1, sh.d_v)
+    yn = np.linalg.norm(yr, axis=2)
+    on = np.linalg.norm(o_orc, axis=2)
+    yfl = np.maximum(yn, yn * np.median(on) / np.where(on > 0, on, np.inf))
+    out_floor = (np.linalg.norm(out_orc, axis=1) * np.linalg.norm(yfl, axis=1) /
+                 np.linalg.norm(yn, axis=1))
+    e = check_rows(out.float().cpu().numpy(), out_orc, wl.HIDDEN, 1.25 * e_y + 2.0 ** -9,
+                   f"out_proj in the chain (y {e_y:.3e})", 2.0 ** -7, out_floor)[0]

@@ -8,8 +8,8 @@ import torch
 from gated_deltanet_layer_conv1d_gb300 import device as dev
 from gated_deltanet_layer_conv1d_gb300 import gdn
 from gated_deltanet_layer_conv1d_gb300 import workloads as wl
-from tests.gpu_common import (assert_state_close, assert_y_close, oracle_seqs, require_gpu,
-                              rel_l2, F32_TOL)
+from tests.gpu_common import (assert_core_close, assert_state_close, assert_y_close,
+                              oracle_seqs, require_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -60,9 +60,8 @@ def check(w, r, snap_seqs):
     res = oracle_seqs(w, w.tokens, ks)
     y_orc = np.concatenate([x.y for x in res])
     o_orc = np.concatenate([x.o for x in res])
-    assert_y_close(r["y"], y_orc, "verify y")
-    e = rel_l2(r["core"].cpu().numpy(), o_orc)
-    assert e <= F32_TOL, f"core o: {e:.3e}"
+    assert_y_close(r["y"], y_orc, "verify y", o_orc=o_orc)
+    assert_core_close(r["core"], o_orc, "verify core o")
     for i, x in enumerate(res):
         assert_state_close(r["H"][i], x.H, f"final state seq {i}")
         np.testing.assert_array_equal(r["conv"][i], x.conv_state)
