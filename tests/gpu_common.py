@@ -133,7 +133,7 @@ def _d_of(cols: int) -> int:
 
 
 def assert_y_close(y_gpu: torch.Tensor, y_orc: np.ndarray, what="y", tol=None, d=None,
-                   o_orc=None):
+                   o_orc=None, row_factor=ROW_FACTOR, elem_factor=ELEM_FACTOR):
     """y (bf16 or f32 rows [T][H_v * d_v]) against the oracle's y; per tensor, per
     (token, head) row and per element.  o_orc: the oracle's core output of the same rows
     ([T][H_v][d_v]), which sets each row's floor (module docstring); without it the floor is
@@ -154,7 +154,7 @@ def assert_y_close(y_gpu: torch.Tensor, y_orc: np.ndarray, what="y", tol=None, d
         on = np.linalg.norm(np.asarray(o_orc, np.float64).reshape(-1, d), axis=1)
         yn = np.linalg.norm(ref.reshape(-1, d), axis=1)
         floor = yn * np.median(on) / np.where(on > 0, on, np.inf)
-    return check_rows(y, ref, d, tol, what, ulp, floor)[0]
+    return check_rows(y, ref, d, tol, what, ulp, floor, row_factor, elem_factor)[0]
 
 
 def assert_core_close(core_gpu, o_orc, what="core o", tol=F32_TOL, elem_factor=ELEM_FACTOR):
