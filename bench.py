@@ -416,6 +416,73 @@ def fold_mode(device, steps, hbm_peak, warmup=3, n=N_SEQ):
                          "algorithmic_bytes": byts}}
 
 
+def woa_mode(device, steps, hbm_peak, warmup=3, n=N_SEQ):
+    """A speculative step of 128 sequences (k ~ U{2..16} drafts, m ~ U{1..k} accepted) in
+    the two forms: the write-on-accept verify, its fold and the flag clear, against the
+    verify that writes every intermediate state plus the copy fold."""
+    import torch
+
+    from gated_deltanet_layer_conv1d_gb300 import device as dev
+    from gated_deltanet_layer_conv1d_gb300 import gdn
+    from gated_deltanet_layer_conv1d_gb300 import workloads as wl
+    w = wl.ragged_verify(n=n)
+    ks = [int(k) for k in w.lens]
+    rng = np.random.default_rng(1)
+    m = [int(rng.integers(1, k + 1)) for k in ks]
+    h_pool, conv_pool, slots = dev.states_to(w, device)
+    inter = torch.empty((n, 15, 32, 128, 128), dtype=torch.float32, device=device)
+    ci = torch.empty((n, 15, 8192, 4), dtype=torch.bfloat16, device=device)
+    hsz = 32 * 128 * 128 * 4
+    tables = dev.wy_tables_to(ks, [h_pool.data_ptr() + i * hsz for i in range(n)],
+                              [[inter[i, t].data_ptr() for t in range(15)] for i in range(n)],
+                              device)
+    inp = dev.tokens_to(w.tokens, torch.bfloat16, device)
+    y = torch.empty((sum(ks), 4096), dtype=torch.bfloat16, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    dims, weights = dev.dims_of(w.shape), dev.weights_to(w, device)
+    stream = torch.cuda.current_stream(device)
+    words = gdn.gdn_woa_stash_seq_floats(dims, gdn.GDN_DTYPE_BF16)
+    stash = torch.empty((n, words), dtype=torch.float32, device=device)
+    flag = torch.zeros(1, dtype=torch.int32, device=device)
+    acc = torch.tensor(m, dtype=torch.int32, device=device)
+
+    def woa(i):
+        gdn.gdn_verify_woa(dims, weights, inp, n, ks, tables, conv_pool, n, slots, stash, n,
+                           flag, y, None, status, stream)
+        gdn.gdn_woa_fold(dims, n, acc, tables, conv_pool, n, slots, stash, flag,
+                         gdn.GDN_DTYPE_BF16, status, stream)
+        gdn.gdn_woa_clear(flag, stream)
+
+    def copy(i):
+        gdn.gdn_verify_multi(dims, weights, inp, n, ks, tables, conv_pool, n, slots, ci, y,
+                             None, status, stream)
+        gdn.gdn_fold_accepted(dims, n, ks, acc, tables, conv_pool, n, slots, ci,
+                              gdn.GDN_DTYPE_BF16, status, stream)
+
+    ms_woa = time_loop(torch, stream, woa, steps, warmup)
+    assert int(status.item()) == 0
+    ms_copy = time_loop(torch, stream, copy, steps, warmup)
+    assert int(status.item()) == 0
+    # algorithmic bytes of the write-on-accept step, per sequence: the verify reads the state
+    # and conv state, its inputs and outputs, and writes the stash (per token alpha, k_hat,
+    # delta, the raw row); the fold reads the state, the accepted tokens' factors and raw
+    # rows, the conv state, and writes the state and conv state
+    state, conv_b, io = 2 * 1024 * 1024, 8192 * 4 * 2, 32896
+    per_tok = 32 * 4 + 16 * 128 * 4 + 32 * 128 * 4 + 8192 * 2
+    byts = sum(state + conv_b + k * io + k * per_tok +
+               2 * state + a * (per_tok - 8192 * 2) + min(a, 4) * 8192 * 2 + 2 * conv_b
+               for k, a in zip(ks, m))
+    gbs = byts / (ms_woa * 1e-3) / 1e9
+    return {"workload": f"speculative_step_{n}seq_k2to16_write_on_accept",
+            "tokens_per_step": sum(ks), "ms_per_step": round(ms_woa, 4),
+            "value": round(sum(ks) / (ms_woa * 1e-3), 1), "unit": "tokens/s",
+            "gpu_launches_per_step": 3,
+            "copy_form_ms_per_step": round(ms_copy, 4),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                         "algorithmic_bytes": byts}}
+
+
 def prefill_mode(device, steps, tc_peak, warmup=2):
     import torch
 
@@ -839,7 +906,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--profile", nargs="?", const="decode", default=None,
                     choices=["decode", "verify", "verify-small", "prefill", "mixed", "proj",
-                             "layer", "fold", "decode16"],
+                             "layer", "fold", "decode16", "woa"],
                     help="only one timed loop of one mode (for profiler captures); "
                          "verify-small runs 32 sequences")
     args = ap.parse_args()
@@ -872,9 +939,11 @@ def main():
         if rank == 0:
             print(json.dumps({"profile_run": "proj", "calls": r["calls"]}))
         return
-    if args.profile in ("fold", "decode16"):
+    if args.profile in ("fold", "decode16", "woa"):
         if args.profile == "fold":
             r = fold_mode(device, args.steps, hbm_peak, warmup=args.warmup)
+        elif args.profile == "woa":
+            r = woa_mode(device, args.steps, hbm_peak, warmup=args.warmup)
         else:
             r = decode_h16_mode(device, args.steps, hbm_peak, warmup=args.warmup)
         if rank == 0:
@@ -954,6 +1023,7 @@ def main():
     if not args.no_modes and rank == 0:
         modes["ragged_verify"] = verify_mode(device, max(10, min(200, args.steps // 10)), hbm_peak)
         modes["accepted_fold"] = fold_mode(device, 50, hbm_peak)
+        modes["speculative_step_write_on_accept"] = woa_mode(device, 50, hbm_peak)
         modes["decode_fp16_state"] = decode_h16_mode(device, 200, hbm_peak)
         modes["ragged_verify_fp16_state"] = verify_mode(device, max(10, min(200, args.steps // 10)),
                                                         hbm_peak, h16=True)

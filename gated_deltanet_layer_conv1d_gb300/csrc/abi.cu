@@ -230,7 +230,8 @@ static gdn_status verify_impl(const gdn_dims* dims, const gdn_weights* weights,
                             const uint64_t* wy_tables_dev, void* conv_pool, int32_t n_slots,
                             const int32_t* slots_dev, void* conv_inter, void* y,
                             float* core_out, int32_t* status_dev, gdn_stream_t stream,
-                              bool h16) {
+                              bool h16, void* woa_stash = nullptr, int32_t woa_seqs = 0,
+                              uint32_t* woa_flag = nullptr) {
   GDN_TRY(check_dims(dims));
   GDN_TRY(check_weights(weights));
   if (n <= 0) return GDN_ERR_INVALID_ARGUMENT;
@@ -247,8 +248,24 @@ static gdn_status verify_impl(const gdn_dims* dims, const gdn_weights* weights,
   if (!wy_tables_dev) return GDN_ERR_NULL_POINTER;
   if (!aligned(wy_tables_dev, 8) || (conv_inter && !aligned(conv_inter, 16)))
     return GDN_ERR_MISALIGNED;
+  if (woa_stash) {
+    if (!woa_flag) return GDN_ERR_NULL_POINTER;
+    if (!aligned(woa_stash, 16) || !aligned(woa_flag, 4)) return GDN_ERR_MISALIGNED;
+    if (woa_seqs < n) return GDN_ERR_INVALID_ARGUMENT;
+  }
   RecParams p;
   fill_common(p, *dims, *weights, *inputs);
+  if (woa_stash) {
+    const WoaLayout l = woa_layout(dims->n_k_heads, dims->n_v_heads, dims->d_k, dims->d_v,
+                                   conv_dim_of(*dims), int(esize(inputs->dtype)));
+    p.woa_stash = static_cast<unsigned char*>(woa_stash);
+    p.woa_flag = woa_flag;
+    p.woa_seq_bytes = l.seq_bytes;
+    p.woa_alpha = int32_t(l.alpha);
+    p.woa_khat = int32_t(l.khat);
+    p.woa_delta = int32_t(l.delta);
+    p.woa_raw = int32_t(l.raw);
+  }
   p.n = n;
   p.n_slots = n_slots;
   p.tables = wy_tables_dev;
@@ -281,6 +298,66 @@ gdn_status gdn_verify_multi(const gdn_dims* dims, const gdn_weights* weights,
                             float* core_out, int32_t* status_dev, gdn_stream_t stream) {
   return verify_impl(dims, weights, inputs, n, ks_host, wy_tables_dev, conv_pool, n_slots,
                      slots_dev, conv_inter, y, core_out, status_dev, stream, false);
+}
+
+size_t gdn_woa_stash_seq_floats(const gdn_dims* dims, int32_t dtype) {
+  if (check_dims(dims) != GDN_OK) return 0;
+  if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return 0;
+  const WoaLayout l = woa_layout(dims->n_k_heads, dims->n_v_heads, dims->d_k, dims->d_v,
+                                 conv_dim_of(*dims), int(esize(dtype)));
+  return size_t(l.seq_bytes / 4);
+}
+
+gdn_status gdn_verify_woa(const gdn_dims* dims, const gdn_weights* weights,
+                          const gdn_inputs* inputs, int32_t n, const int32_t* ks_host,
+                          const uint64_t* wy_tables_dev, void* conv_pool, int32_t n_slots,
+                          const int32_t* slots_dev, void* stash, int32_t stash_seqs,
+                          uint32_t* flag_dev, void* y, float* core_out, int32_t* status_dev,
+                          gdn_stream_t stream) {
+  if (!stash) return GDN_ERR_NULL_POINTER;
+  return verify_impl(dims, weights, inputs, n, ks_host, wy_tables_dev, conv_pool, n_slots,
+                     slots_dev, nullptr, y, core_out, status_dev, stream, false, stash,
+                     stash_seqs, flag_dev);
+}
+
+gdn_status gdn_woa_fold(const gdn_dims* dims, int32_t n, const int32_t* accepted_dev,
+                        const uint64_t* wy_tables_dev, void* conv_pool, int32_t n_slots,
+                        const int32_t* slots_dev, const void* stash, const uint32_t* flag_dev,
+                        int32_t dtype, int32_t* status_dev, gdn_stream_t stream) {
+  GDN_TRY(check_dims(dims));
+  if (n <= 0) return GDN_ERR_INVALID_ARGUMENT;
+  if (n > GDN_MAX_SEQS) return GDN_ERR_TOO_MANY_SEQS;
+  if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return GDN_ERR_INVALID_ARGUMENT;
+  if (!accepted_dev || !wy_tables_dev || !stash || !flag_dev || !status_dev)
+    return GDN_ERR_NULL_POINTER;
+  GDN_TRY(check_pools(conv_pool, n_slots, slots_dev));
+  if (!aligned(accepted_dev, 4) || !aligned(wy_tables_dev, 8) || !aligned(stash, 16) ||
+      !aligned(flag_dev, 4) || !aligned(status_dev, 4))
+    return GDN_ERR_MISALIGNED;
+  WoaFoldParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.Hk = dims->n_k_heads;
+  p.Hv = dims->n_v_heads;
+  p.d = dims->d_k;
+  p.conv_dim = conv_dim_of(*dims);
+  p.esize = int32_t(esize(dtype));
+  p.n = n;
+  p.n_slots = n_slots;
+  p.accepted = accepted_dev;
+  p.tables = wy_tables_dev;
+  p.conv_pool = conv_pool;
+  p.slots = slots_dev;
+  p.stash = static_cast<const unsigned char*>(stash);
+  p.flag = flag_dev;
+  p.status = status_dev;
+  p.lay = woa_layout(p.Hk, p.Hv, dims->d_k, dims->d_v, p.conv_dim, p.esize);
+  return status_of(launch_woa_fold(p, stream));
+}
+
+gdn_status gdn_woa_clear(uint32_t* flag_dev, gdn_stream_t stream) {
+  if (!flag_dev) return GDN_ERR_NULL_POINTER;
+  if (!aligned(flag_dev, 4)) return GDN_ERR_MISALIGNED;
+  return status_of(launch_woa_clear(flag_dev, stream));
 }
 
 gdn_status gdn_verify_multi_h16(const gdn_dims* dims, const gdn_weights* weights,

@@ -36,6 +36,13 @@ struct RecParams {
   float* core_out;
   int32_t* status;
   int32_t n_items;         // n * Hk
+  // Write-on-accept verify (woa_stash non-null): no state is written; sequence i's stash
+  // at woa_stash + i * woa_seq_bytes receives k, and per token alpha, k_hat, delta and the
+  // raw qkv row (byte offsets below); every CTA sets *woa_flag to 1 at its end.
+  unsigned char* woa_stash;
+  uint32_t* woa_flag;
+  int64_t woa_seq_bytes;
+  int32_t woa_alpha, woa_khat, woa_delta, woa_raw;
   uint8_t ks[GDN_MAX_SEQS];       // tokens of sequence i (original index)
   uint8_t order[GDN_MAX_SEQS];    // sequence indices, most tokens first
   uint16_t row_off[GDN_MAX_SEQS]; // first token row of sequence i
@@ -124,6 +131,30 @@ struct FoldParams {
   uint8_t ks[GDN_MAX_SEQS];
 };
 cudaError_t launch_fold(const FoldParams& p, cudaStream_t stream);
+
+// Write-on-accept stash of one sequence (byte offsets; see RecParams), sized for
+// GDN_VERIFY_K_MAX tokens.
+struct WoaLayout {
+  int64_t alpha, khat, delta, raw, seq_bytes;
+};
+WoaLayout woa_layout(int Hk, int Hv, int dk, int dv, int conv_dim, int esize);
+
+// The deferred fold of a write-on-accept verify: sequence i's state (table 0 entry i) takes
+// the first accepted[i] tokens' updates from its stash, and its conv state the last d_conv
+// raw inputs up to that token; nothing happens while *flag is 0.
+struct WoaFoldParams {
+  int32_t Hk, Hv, d, conv_dim, esize, n, n_slots;
+  const int32_t* accepted;   // [n] device
+  const uint64_t* tables;    // [16][128]; table 0 only
+  void* conv_pool;
+  const int32_t* slots;
+  const unsigned char* stash;
+  const uint32_t* flag;
+  int32_t* status;
+  WoaLayout lay;
+};
+cudaError_t launch_woa_fold(const WoaFoldParams& p, cudaStream_t stream);
+cudaError_t launch_woa_clear(uint32_t* flag, cudaStream_t stream);
 
 // bf16 projection GEMM: C[M][N] = A[M][K] B[N][K]^T (f32 accumulation, bf16 result).
 struct ProjParams {

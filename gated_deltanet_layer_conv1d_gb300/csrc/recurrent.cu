@@ -117,7 +117,7 @@ __device__ __forceinline__ bool token_update(SR (&S)[RecMap<D, NT>::M], const La
                                              const float* xq, const float* xk, const float* xv,
                                              float al, float be, float kq, float* red,
                                              float* orow, bool flag = false, float rq = 1.f,
-                                             float rk = 1.f) {
+                                             float rk = 1.f, float* drow = nullptr) {
   using Map = RecMap<D, NT>;
   float kr[Map::M];
   float4 u = make_float4(0.f, 0.f, 0.f, 0.f), pp = u;
@@ -170,6 +170,8 @@ __device__ __forceinline__ bool token_update(SR (&S)[RecMap<D, NT>::M], const La
     o.z = al * PP.z + dl.z * kq;
     o.w = al * PP.w + dl.w * kq;
     *reinterpret_cast<float4*>(orow + L.col0) = o;
+    // write-on-accept: the token's update is k_hat delta^T (k normalised when drow is used)
+    if (drow) *reinterpret_cast<float4*>(drow + L.col0) = dl;
   }
   dl.x *= rk; dl.y *= rk; dl.z *= rk; dl.w *= rk;
   // packed tiles run at a tighter register budget: k is read again rather than kept
@@ -352,7 +354,7 @@ __device__ __forceinline__ int seq_check(const RecParams& p, int seq) {
   const int slot = p.slots[seq];
   if (slot < 0 || slot >= p.n_slots) return GDN_ERR_BAD_SLOT;
   if (VERIFY) {
-    const int k = p.ks[seq];
+    const int k = p.woa_stash ? 1 : p.ks[seq];  // write-on-accept reads table 0 only
     for (int t = 0; t < k; ++t) {
       const uint64_t e = p.tables[t * GDN_VERIFY_WY_TABLE_SEQS + seq];
       if (e == 0 || (e & 15u) != 0) return GDN_ERR_BAD_TABLE_ENTRY;
@@ -415,7 +417,8 @@ __host__ __device__ constexpr int rec_min_blocks() {
   return (KMAX == 1 && sizeof(SH) == 2) ? 2 : 1;
 }
 
-template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY, typename SH>
+template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY, typename SH,
+          bool WOA = false>
 __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX, SH>()))
     gdn_recurrent_kernel(const __grid_constant__ RecParams p) {
   using Map = RecMap<D, NT>;
@@ -665,6 +668,9 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
   while (r_next < rounds) {
     const Item it = nxt;
     const int k = it.k;
+    // write-on-accept (a verify built for it): the stash of this item's sequence
+    constexpr bool woa = VERIFY && WOA;
+    unsigned char* woa_seq = woa ? p.woa_stash + size_t(it.seq) * p.woa_seq_bytes : nullptr;
     r_next = next_valid(r_next + 1, nxt);
 
     // ---------------- item prologue: conv + SiLU (+ state update), z, gates, L2 norms
@@ -750,6 +756,9 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
             const int t = t0 + u;
             if (t < k) {
               win = make_float4(win.y, win.z, win.w, xg[u]);
+              if (VERIFY && woa)  // the raw input, an exact copy, for the deferred fold
+                reinterpret_cast<T*>(woa_seq + p.woa_raw)[size_t(t) * p.conv_dim + gc] =
+                    A::from_f(xg[u]);
               xs[t * CHX + lc] =
                   silu_f(w4.x * win.x + w4.y * win.y + w4.z * win.z + w4.w * win.w);
               if (VERIFY && p.conv_inter && t < k - 1) {
@@ -760,7 +769,7 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
             }
           }
         }
-        A::store4(cs, win);  // exact copies of the last kW raw inputs
+        if (!woa) A::store4(cs, win);  // exact copies of the last kW raw inputs
       }
       for (int idx = tid; idx < k * G; idx += NT) {
         const int t = idx / G, g = idx - t * G;
@@ -771,6 +780,7 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
                 A::to_f(reinterpret_cast<const T*>(p.b)[ro]), p.A_log[h], p.dt_bias[h], &al, &be);
         gate[(t * kMaxG + g) * 2 + 0] = al;
         gate[(t * kMaxG + g) * 2 + 1] = be;
+        if (VERIFY && woa) reinterpret_cast<float*>(woa_seq + p.woa_alpha)[t * p.Hv + h] = al;
       }
       named_sync(1, NT);
     }
@@ -790,6 +800,14 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
     } else {
       l2norm_tokens<D, Map::NW>(xs, CHX, k, p.q_scale, p.l2_eps, kq_s, L.warp, L.lane);
       named_sync(1, NT);
+      if (VERIFY && woa) {  // k, and the normalised k of every token, for the deferred fold
+        float* kh_out = reinterpret_cast<float*>(woa_seq + p.woa_khat);
+        for (int idx = tid; idx < k * D; idx += NT) {
+          const int t = idx / D, i = idx - t * D;
+          kh_out[(size_t(t) * p.Hk + it.kh) * D + i] = xs[t * CHX + D + i];
+        }
+        if (tid == 0 && it.kh == 0) *reinterpret_cast<int32_t*>(woa_seq) = k;
+      }
     }
 
     // ---------------- value heads of the item
@@ -819,11 +837,14 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
                                       // one head's reduction reads from the next's writes
                                       red + ((SL::kNormWarp ? hq : t) & 1) * 2 * Map::RB * D,
                                       obuf + (SL::kNormWarp ? (hq & 1) : t) * D,
-                                      t == 0 && !ok, rq, rk)) {
+                                      t == 0 && !ok, rq, rk,
+                                      (VERIFY && woa) ? reinterpret_cast<float*>(woa_seq + p.woa_delta) +
+                                                            (size_t(t) * p.Hv + h) * D
+                                                      : nullptr)) {
           drain(q - 1);
           return;
         }
-        if (VERIFY || t == k - 1)
+        if (!woa && (VERIFY || t == k - 1))
           store_tile<D, NT, SH, SR>(state_dst<D, VERIFY, SH>(p, it, tab_item, h, t), S, L);
       }
       if constexpr (SL::kNormWarp) {
@@ -839,12 +860,15 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
       }
     }
   }
+  // write-on-accept: the stash holds a verify the fold has not applied yet
+  if (VERIFY && WOA && tid == 0) *p.woa_flag = 1u;
 }
 
-template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY, typename SH>
+template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY, typename SH,
+          bool WOA = false>
 cudaError_t launch_rec(const RecParams& p, cudaStream_t stream) {
   using SL = RecSmem<D, NT, KMAX, STAGES, T, SH>;
-  auto kern = gdn_recurrent_kernel<T, D, NT, KMAX, STAGES, VERIFY, SH>;
+  auto kern = gdn_recurrent_kernel<T, D, NT, KMAX, STAGES, VERIFY, SH, WOA>;
   const size_t smem = SL::bytes(p.G);
   if (smem > kMaxSmemPerBlock) return cudaErrorInvalidConfiguration;  // shape not supported
   cudaError_t e =
@@ -880,6 +904,13 @@ cudaError_t launch_rec_typed(const RecParams& p, int D, bool verify, cudaStream_
   }
   if (verify) return launch_rec<T, 16, 64, GDN_VERIFY_K_MAX, 2, true, SH>(p, stream);
   return launch_rec<T, 16, 64, 1, 3, false, SH>(p, stream);
+}
+
+// The write-on-accept verify (f32 state pools only).
+template <typename T>
+cudaError_t launch_rec_woa(const RecParams& p, int D, cudaStream_t stream) {
+  if (D == 128) return launch_rec<T, 128, 512, GDN_VERIFY_K_MAX, 2, true, float, true>(p, stream);
+  return launch_rec<T, 16, 64, GDN_VERIFY_K_MAX, 2, true, float, true>(p, stream);
 }
 
 // ======================================================================================
@@ -1006,6 +1037,11 @@ cudaError_t launch_seq(const PrefillParams& p, cudaStream_t stream) {
 
 cudaError_t launch_recurrent(const RecParams& p, int dtype, int D, bool verify, bool h16,
                              cudaStream_t stream) {
+  if (verify && p.woa_stash) {
+    if (h16) return cudaErrorInvalidConfiguration;  // write-on-accept keeps f32 pools only
+    return dtype == GDN_DTYPE_BF16 ? launch_rec_woa<__nv_bfloat16>(p, D, stream)
+                                   : launch_rec_woa<float>(p, D, stream);
+  }
   if (h16) {
     if (dtype == GDN_DTYPE_BF16)
       return launch_rec_typed<__nv_bfloat16, __half>(p, D, verify, stream);

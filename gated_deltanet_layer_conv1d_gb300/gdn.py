@@ -36,7 +36,8 @@ EXPORTS = ("gdn_decode_batched", "gdn_verify_multi", "gdn_conv_step", "gdn_prefi
            "gdn_fold_accepted", "gdn_decode_batched_h16", "gdn_verify_multi_h16",
            "gdn_gated_rmsnorm_sigmoid", "gdn_proj_gemm", "gdn_in_proj_width", "gdn_in_proj",
            "gdn_out_proj", "gdn_selftest_wait",
-           "gdn_state_convert")
+           "gdn_state_convert", "gdn_woa_stash_seq_floats", "gdn_verify_woa", "gdn_woa_fold",
+           "gdn_woa_clear")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -82,6 +83,11 @@ def lib() -> ctypes.CDLL:
         L.gdn_verify_multi.argtypes = [D, W, IN, I32, P, P, P, I32, P, P, P, P, P, P]
         L.gdn_conv_step.argtypes = [D, W, IN, I32, P, I32, P, I32, P, P, P, P]
         L.gdn_fold_accepted.argtypes = [D, I32, P, P, P, P, I32, P, P, I32, I32, P, P]
+        L.gdn_woa_stash_seq_floats.argtypes = [D, I32]
+        L.gdn_woa_stash_seq_floats.restype = SZ
+        L.gdn_verify_woa.argtypes = [D, W, IN, I32, P, P, P, I32, P, P, I32, P, P, P, P, P]
+        L.gdn_woa_fold.argtypes = [D, I32, P, P, P, I32, P, P, P, I32, P, P]
+        L.gdn_woa_clear.argtypes = [P, P]
         L.gdn_decode_batched_h16.argtypes = L.gdn_decode_batched.argtypes
         L.gdn_verify_multi_h16.argtypes = L.gdn_verify_multi.argtypes
         L.gdn_state_convert.argtypes = [P, I32, P, I32, I64, P]
@@ -200,6 +206,34 @@ def gdn_fold_accepted(dims: gdn_dims, n: int, ks_host, accepted, wy_tables, conv
         ctypes.byref(dims), n, ctypes.cast(ks, ctypes.c_void_p), _ptr(accepted), _ptr(wy_tables),
         _ptr(conv_pool), n_slots, _ptr(slots), _ptr(conv_inter), int(dtype), int(h_dtype),
         _ptr(status), _stream(stream)))
+
+
+def gdn_woa_stash_seq_floats(dims: gdn_dims, dtype: int) -> int:
+    """4-byte words of write-on-accept stash per sequence."""
+    return int(lib().gdn_woa_stash_seq_floats(ctypes.byref(dims), int(dtype)))
+
+
+def gdn_verify_woa(dims: gdn_dims, weights: Weights, inputs: Inputs, n: int, ks_host,
+                   wy_tables, conv_pool, n_slots: int, slots, stash, stash_seqs: int, flag, y,
+                   core_out=None, status=None, stream=None):
+    """gdn_verify_multi that leaves the states alone and stashes each token's update."""
+    ks = (ctypes.c_int32 * len(ks_host))(*[int(k) for k in ks_host])
+    w, i = weights.c(), inputs.c()
+    _check("gdn_verify_woa", lib().gdn_verify_woa(
+        ctypes.byref(dims), ctypes.byref(w), ctypes.byref(i), n, ctypes.cast(ks, ctypes.c_void_p),
+        _ptr(wy_tables), _ptr(conv_pool), n_slots, _ptr(slots), _ptr(stash), int(stash_seqs),
+        _ptr(flag), _ptr(y), _ptr(core_out), _ptr(status), _stream(stream)))
+
+
+def gdn_woa_fold(dims: gdn_dims, n: int, accepted, wy_tables, conv_pool, n_slots: int, slots,
+                 stash, flag, dtype: int, status=None, stream=None):
+    _check("gdn_woa_fold", lib().gdn_woa_fold(
+        ctypes.byref(dims), n, _ptr(accepted), _ptr(wy_tables), _ptr(conv_pool), n_slots,
+        _ptr(slots), _ptr(stash), _ptr(flag), int(dtype), _ptr(status), _stream(stream)))
+
+
+def gdn_woa_clear(flag, stream=None):
+    _check("gdn_woa_clear", lib().gdn_woa_clear(_ptr(flag), _stream(stream)))
 
 
 def gdn_decode_batched_h16(dims: gdn_dims, weights: Weights, inputs: Inputs, n: int, h_pool,

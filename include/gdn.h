@@ -213,6 +213,44 @@ GDN_API gdn_status gdn_fold_accepted(const gdn_dims* dims, int32_t n, const int3
                                      const void* conv_inter, int32_t dtype, int32_t h_dtype,
                                      int32_t* status_dev, gdn_stream_t stream);
 
+/* Write-on-accept verify and its deferred fold (trait_layer.rs, LayerWriteOnAccept:
+ * gdn_woa_stash_seq_floats and gdn_woa_bind; layer_struct.rs, the gdn_wy4_woa_k,
+ * gdn_wy4_fold_k and gdn_wy4_clear_k handles and the woa_flag / woa_stash bindings).
+ * gdn_verify_woa computes the same outputs as gdn_verify_multi but writes no state: the
+ * state (table 0 entry i) and the conv state stay as they were, and sequence i's stash
+ * receives k_i and, for each draft token t, the factors of its state update
+ * (S_t = alpha_t S_{t-1} + delta_t k_hat_t^T, with delta_t = beta_t (v_t - alpha_t S_{t-1}
+ * k_hat_t)) and its raw qkv row; then the engaged word is set to 1.  Once the caller knows
+ * how many drafts m_i it accepts, gdn_woa_fold replays tokens 0 .. m_i - 1 on the state in
+ * one pass and moves the conv state to the last d_conv raw inputs up to token m_i - 1, and
+ * gdn_woa_clear zeroes the engaged word (a fold while it is 0 changes nothing).  The
+ * verify writes k_i x (a few KiB) per sequence instead of k_i - 1 intermediate states of
+ * H_v d_k d_v floats each; the fold reads and writes each state once.  f32 state pools only.
+ *   gdn_woa_stash_seq_floats: 4-byte words of stash per sequence (room for
+ *     GDN_VERIFY_K_MAX tokens) for these dims and activation dtype; 0 on invalid input.
+ *   stash      : device, [stash_seqs][gdn_woa_stash_seq_floats] 4-byte words, 16-B aligned,
+ *                caller-owned; sequence i (the verify's i) uses row i; stash_seqs >= n.
+ *   flag_dev   : device uint32, the engaged word (4-B aligned).
+ * gdn_verify_woa: the arguments and errors of gdn_verify_multi without conv_inter; only
+ *   table 0 is read (the intermediate tables may be zero).
+ * gdn_woa_fold: n, accepted_dev, wy_tables_dev, conv_pool, n_slots, slots_dev as for
+ *   gdn_fold_accepted (1 <= accepted_dev[i] <= k_i, else GDN_ERR_BAD_ACCEPTED and that
+ *   sequence is left as it is); stash and flag_dev as passed to gdn_verify_woa; dtype is
+ *   the verify's activation dtype. */
+GDN_API size_t gdn_woa_stash_seq_floats(const gdn_dims* dims, int32_t dtype);
+GDN_API gdn_status gdn_verify_woa(const gdn_dims* dims, const gdn_weights* weights,
+                                  const gdn_inputs* inputs, int32_t n, const int32_t* ks_host,
+                                  const uint64_t* wy_tables_dev, void* conv_pool,
+                                  int32_t n_slots, const int32_t* slots_dev, void* stash,
+                                  int32_t stash_seqs, uint32_t* flag_dev, void* y,
+                                  float* core_out, int32_t* status_dev, gdn_stream_t stream);
+GDN_API gdn_status gdn_woa_fold(const gdn_dims* dims, int32_t n, const int32_t* accepted_dev,
+                                const uint64_t* wy_tables_dev, void* conv_pool,
+                                int32_t n_slots, const int32_t* slots_dev, const void* stash,
+                                const uint32_t* flag_dev, int32_t dtype, int32_t* status_dev,
+                                gdn_stream_t stream);
+GDN_API gdn_status gdn_woa_clear(uint32_t* flag_dev, gdn_stream_t stream);
+
 /* Half-width h-state pools (layer_struct.rs: the FP16 h-state variants gdn_f16_norm_k,
  * gdn_f16_strided_norm_half_k and gdn_wyn_f16_table_k, and the width converters
  * ssm_h_f16_to_f32_k / ssm_h_f32_to_f16_k).  The same mixer on states stored as fp16

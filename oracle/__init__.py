@@ -322,3 +322,42 @@ def chunked(dims: Dims, chunk: int, qn, kn, v, alpha, beta, H, round_operands: b
     lib().orc_chunked(ctypes.byref(d), T, int(chunk), _p(qn), _p(kn), _p(v), _p(alpha),
                       _p(beta), _p(Hn), _p(o), 1 if round_operands else 0)
     return Hn, o
+
+
+# ------------------------------------------------------------------ write-on-accept
+# trait_layer.rs, LayerWriteOnAccept (gdn_woa_stash_seq_floats, gdn_woa_bind); layer_struct.rs,
+# the gdn_wy4_woa_k / gdn_wy4_fold_k handles.  The pages name a verify that leaves the state
+# alone and stashes what a later fold needs; the reading taken: each token's update of the
+# delta rule is rank one, S_t = alpha_t S_{t-1} + delta_t k_hat_t^T with
+# delta_t = beta_t (v_t - alpha_t S_{t-1} k_hat_t), so the stash holds (alpha_t, k_hat_t,
+# delta_t) per token and the fold replays the accepted ones.
+
+def woa_factors(dims: Dims, weights: dict, qkv, a, b, conv_state, H):
+    """Per-token factors of the k draft rows of one sequence, from the recurrence itself:
+    alpha [k][H_v], k_hat [k][H_k][d_k], delta [k][H_v][d_v] (H stored [H_v][d_k][d_v])."""
+    qkv, a, b = map(_f64, (qkv, a, b))
+    xc, _, _ = conv(weights["conv_w"], conv_state, qkv)
+    qn, kn, v = l2norm_split(dims, xc)
+    alpha, beta = gates(a, b, weights["A_log"], weights["dt_bias"])
+    G = dims.n_v_heads // dims.n_k_heads
+    Hs = _f64(H).copy()
+    T = qkv.shape[0]
+    delta = np.empty((T, dims.n_v_heads, dims.d_v))
+    for t in range(T):
+        for h in range(dims.n_v_heads):
+            k = kn[t, h // G]
+            u = Hs[h].T @ k                      # S_{t-1} k_hat (S = H^T)
+            d = beta[t, h] * (v[t, h] - alpha[t, h] * u)
+            Hs[h] = alpha[t, h] * Hs[h] + np.outer(k, d)
+            delta[t, h] = d
+    return alpha, kn, delta
+
+
+def woa_fold(dims: Dims, H, alpha, k_hat, delta, m: int):
+    """The deferred fold: H [H_v][d_k][d_v] after replaying tokens 0 .. m-1."""
+    Hn = _f64(H).copy()
+    G = dims.n_v_heads // dims.n_k_heads
+    for t in range(m):
+        for h in range(dims.n_v_heads):
+            Hn[h] = alpha[t, h] * Hn[h] + np.outer(k_hat[t, h // G], delta[t, h])
+    return Hn

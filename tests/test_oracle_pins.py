@@ -512,3 +512,29 @@ def test_split_in_proj_layout():
     sp = oracle.split_in_proj(dims, padded)
     for k in ("qkv", "z", "b", "a"):
         np.testing.assert_array_equal(sp[k], s[k])
+
+
+@pytest.mark.parametrize("shape", [wl.TINY, wl.LayerShape(2, 4, 16, 16, 4, q_scale=0.25)])
+def test_woa_fold_of_the_stash_equals_the_state_after_m_tokens(shape):
+    """Write-on-accept reading: replaying the stashed per-token factors of the first m draft
+    tokens gives the state the token loop reaches after m tokens (the copy fold's state), for
+    every m; the factors satisfy S_t = alpha_t S_{t-1} + delta_t k_hat_t^T exactly."""
+    rng = np.random.default_rng(81)
+    w = wl.make_weights(rng, shape)
+    k = 9
+    tok = wl.make_tokens(rng, shape, k, bf16=True)
+    conv0 = wl.round_bf16(rng.standard_normal((shape.conv_dim, 4)).astype(np.float32) * 0.3)
+    H0 = rng.standard_normal((shape.n_v_heads, shape.d_k, shape.d_v)) * 0.3
+    d = oracle.Dims(shape.n_k_heads, shape.n_v_heads, shape.d_k, shape.d_v, 4,
+                    float(np.float32(shape.q_scale)), 1e-6, 1e-6)
+    r = oracle.mixer(d, w, tok["qkv"], tok["z"], tok["a"], tok["b"], conv0, H0, snapshots=True)
+    alpha, k_hat, delta = oracle.woa_factors(d, w, tok["qkv"], tok["a"], tok["b"], conv0, H0)
+    np.testing.assert_allclose(np.linalg.norm(k_hat, axis=-1), 1.0, rtol=1e-5)
+    for m in range(1, k + 1):
+        got = oracle.woa_fold(d, H0, alpha, k_hat, delta, m)
+        np.testing.assert_allclose(got, r.H_snap[m - 1], rtol=1e-12, atol=1e-12)
+    assert np.array_equal(oracle.woa_fold(d, H0, alpha, k_hat, delta, 0), H0)
+    # a wrong sign or a dropped decay in the replay fails: replaying with alpha = 1 does not
+    # reach the state after two tokens
+    assert not np.allclose(oracle.woa_fold(d, H0, np.ones_like(alpha), k_hat, delta, 2),
+                           r.H_snap[1], rtol=1e-6)
