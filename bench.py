@@ -483,7 +483,9 @@ def woa_mode(device, steps, hbm_peak, warmup=3, n=N_SEQ):
                          "algorithmic_bytes": byts}}
 
 
-def prefill_mode(device, steps, tc_peak, warmup=2):
+def prefill_mode(device, steps, tc_peak, warmup=2, f32=False):
+    """The 1 x 8192-token prefill; f32: the token-sequential f32 option (the 1e-4 class),
+    timed beside the tensor-core form."""
     import torch
 
     from gated_deltanet_layer_conv1d_gb300 import device as dev
@@ -495,6 +497,8 @@ def prefill_mode(device, steps, tc_peak, warmup=2):
     hp = torch.tensor([h_pool.data_ptr()], dtype=torch.int64, device=device)
     cu = torch.tensor([0, T], dtype=torch.int32, device=device)
     dims, weights = dev.dims_of(w.shape), dev.weights_to(w, device)
+    if f32:
+        dims.prefill_precision = gdn.GDN_PREFILL_F32
     inp = dev.tokens_to(w.tokens, torch.bfloat16, device)
     y = torch.empty((T, 4096), dtype=torch.bfloat16, device=device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
@@ -510,6 +514,10 @@ def prefill_mode(device, steps, tc_peak, warmup=2):
     assert int(status.item()) == 0
     fl = prefill_flops(T)
     tfs = fl / (ms * 1e-3) / 1e12
+    if f32:
+        return {"workload": f"long_prefill_{T}tok_f32_token_sequential", "tokens_per_step": T,
+                "ms_per_step": round(ms, 4), "value": round(T / (ms * 1e-3), 1),
+                "unit": "tokens/s", "state_error_class": "1e-4"}
     return {"workload": f"long_prefill_{T}tok_chunk64", "tokens_per_step": T,
             "ms_per_step": round(ms, 4), "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s",
             "roofline": {"bound": "tensor", "achieved": round(tfs, 2), "peak": tc_peak,
@@ -1028,6 +1036,7 @@ def main():
         modes["ragged_verify_fp16_state"] = verify_mode(device, max(10, min(200, args.steps // 10)),
                                                         hbm_peak, h16=True)
         modes["chunked_prefill"] = prefill_mode(device, 5, tc_peak)
+        modes["prefill_f32_option"] = prefill_mode(device, 3, tc_peak, f32=True)
         if world == 1 and not args.no_cpu:
             modes["chunked_prefill"]["cpu_baseline"] = cpu_baseline_prefill()
         modes["mixed_serving"] = mixed_mode(device, 3, hbm_peak, tc_peak)

@@ -50,6 +50,8 @@ gdn_status check_dims(const gdn_dims* d) {
     return GDN_ERR_INVALID_ARGUMENT;
   if (d->norm_gate != GDN_NORM_GATE_SILU && d->norm_gate != GDN_NORM_GATE_SIGMOID)
     return GDN_ERR_INVALID_ARGUMENT;
+  if (d->prefill_precision != GDN_PREFILL_TENSOR_FP16 && d->prefill_precision != GDN_PREFILL_F32)
+    return GDN_ERR_INVALID_ARGUMENT;
   return GDN_OK;
 }
 
@@ -471,6 +473,7 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t n, int32_t tota
   if (check_dims(dims) != GDN_OK || n < 0 || total_tokens < 0 || max_seqlen < 0 ||
       chunk != GDN_PREFILL_CHUNK)
     return 0;
+  if (dims->prefill_precision == GDN_PREFILL_F32) return 0;  // the sequential form needs none
   return prefill_workspace_bytes(dims->n_k_heads, dims->n_v_heads, dims->d_k, n, total_tokens,
                                  max_seqlen);
 }
@@ -494,8 +497,10 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* weights,
   GDN_TRY(check_pools(conv_pool, n_slots, slots_dev));
   if (!cu_seqlens_dev || !h_state_ptrs_dev) return GDN_ERR_NULL_POINTER;
   if (!aligned(cu_seqlens_dev, 4) || !aligned(h_state_ptrs_dev, 8)) return GDN_ERR_MISALIGNED;
-  const size_t need = prefill_workspace_bytes(dims->n_k_heads, dims->n_v_heads, dims->d_k, n,
-                                              total_tokens, max_seqlen);
+  const size_t need = dims->prefill_precision == GDN_PREFILL_F32
+                          ? 0
+                          : prefill_workspace_bytes(dims->n_k_heads, dims->n_v_heads, dims->d_k,
+                                                    n, total_tokens, max_seqlen);
   if (need > 0) {
     if (!workspace) return GDN_ERR_NULL_POINTER;
     if (!aligned(workspace, 256)) return GDN_ERR_MISALIGNED;
@@ -517,6 +522,7 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* weights,
   p.l2_eps = dims->l2_eps;
   p.norm_eps = dims->norm_eps;
   p.norm_gate = dims->norm_gate;
+  p.f32_path = dims->prefill_precision == GDN_PREFILL_F32;
   p.conv_w = weights->conv_w;
   p.A_log = weights->A_log;
   p.dt_bias = weights->dt_bias;

@@ -94,6 +94,7 @@ struct PrefillParams {
   void* o_half;  // internal: fp16 [T][Hv][128] room for O when no f32 core output is wanted
   float q_scale, l2_eps, norm_eps;
   int32_t norm_gate;  // 0: SiLU(z), 1: sigmoid(z)
+  int32_t f32_path;   // 1: the token-sequential f32 form even where the tensor-core form runs
   const float* conv_w;
   const float* A_log;
   const float* dt_bias;

@@ -4,8 +4,8 @@
 // (conv, SiLU, L2 norms, gates of every token into the workspace tiles), the chunk kernel
 // (every chunk's W, U, P and K~ at once), the state spine (chunk after chunk per sequence
 // and value head, writing the core output O) and the gated RMSNorm of O.  Every other
-// shape or dtype: the token-sequential kernel.  The conv-state update runs after either
-// (see abi.cu).
+// shape or dtype, and any call whose dims ask for GDN_PREFILL_F32: the token-sequential
+// kernel, f32 throughout.  The conv-state update runs after either (see abi.cu).
 #include "common.cuh"
 #include "kernels.h"
 #include "prefill_layout.cuh"
@@ -23,7 +23,7 @@ size_t prefill_workspace_bytes(int Hk, int Hv, int D, int n, int total_tokens, i
 }
 
 cudaError_t launch_prefill(const PrefillParams& p, int dtype, cudaStream_t stream) {
-  if (p.D == 128 && dtype == GDN_DTYPE_BF16) {
+  if (p.D == 128 && dtype == GDN_DTYPE_BF16 && !p.f32_path) {
     ConvParams c{};
     c.Hk = p.Hk;
     c.Hv = p.Hv;

@@ -22,6 +22,8 @@ GDN_DTYPE_BF16 = 1
 GDN_DTYPE_F16 = 2  # h-state pools only
 GDN_NORM_GATE_SILU = 0
 GDN_NORM_GATE_SIGMOID = 1
+GDN_PREFILL_TENSOR_FP16 = 0
+GDN_PREFILL_F32 = 1
 MAX_SEQS = 128
 VERIFY_WY_TABLE_SEQS = 128
 VERIFY_WY_TABLES_PER_LAYER = 16
@@ -51,7 +53,8 @@ class gdn_dims(ctypes.Structure):
     _fields_ = [("n_k_heads", ctypes.c_int32), ("n_v_heads", ctypes.c_int32),
                 ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32), ("d_conv", ctypes.c_int32),
                 ("q_scale", ctypes.c_float), ("l2_eps", ctypes.c_float),
-                ("norm_eps", ctypes.c_float), ("norm_gate", ctypes.c_int32)]
+                ("norm_eps", ctypes.c_float), ("norm_gate", ctypes.c_int32),
+                ("prefill_precision", ctypes.c_int32)]
 
 
 class gdn_weights(ctypes.Structure):
@@ -174,8 +177,9 @@ class Inputs:
 
 
 def make_dims(n_k_heads, n_v_heads, d_k, d_v, d_conv, q_scale, l2_eps, norm_eps,
-              norm_gate=GDN_NORM_GATE_SILU) -> gdn_dims:
-    return gdn_dims(n_k_heads, n_v_heads, d_k, d_v, d_conv, q_scale, l2_eps, norm_eps, norm_gate)
+              norm_gate=GDN_NORM_GATE_SILU, prefill_precision=0) -> gdn_dims:
+    return gdn_dims(n_k_heads, n_v_heads, d_k, d_v, d_conv, q_scale, l2_eps, norm_eps, norm_gate,
+                    prefill_precision)
 
 
 def gdn_decode_batched(dims: gdn_dims, weights: Weights, inputs: Inputs, n: int, h_pool,

@@ -115,10 +115,18 @@ typedef struct {
   int32_t norm_gate; /* GDN_NORM_GATE_SILU (0): y = norm(o) w SiLU(z);
                         GDN_NORM_GATE_SIGMOID (1): y = norm(o) w sigmoid(z), the gate of the
                         gdn_norm_sigmoid models (layer_struct.rs, gated_rms_norm_f32_strided_k) */
+  int32_t prefill_precision; /* gdn_prefill_chunked at d = 128 with bf16 activations:
+                        GDN_PREFILL_TENSOR_FP16 (0): the chunked WY form on the tensor cores,
+                        fp16 operands (state error ~4e-4 relative);
+                        GDN_PREFILL_F32 (1): the token-sequential f32 form on CUDA cores (the
+                        1e-4 class of the decode and verify paths; no workspace), far slower.
+                        Every other entry point ignores it. */
 } gdn_dims;
 
 #define GDN_NORM_GATE_SILU 0
 #define GDN_NORM_GATE_SIGMOID 1
+#define GDN_PREFILL_TENSOR_FP16 0
+#define GDN_PREFILL_F32 1
 
 /* Layer parameters, all f32 device memory. */
 typedef struct {
