@@ -17,12 +17,13 @@
 // Design (HBM-bound: the state tile is read once, and written once per token kept):
 //   * persistent grid: one CTA per SM (two on fp16 decode pools); items are dealt to CTAs
 //     in a zig-zag over the item list (most tokens first), so ragged k balances;
-//   * threads: NT compute threads (16 warps for verify, 8 for decode), one producer warp,
-//     and for decode one norm warp;
-//   * one elected producer thread streams the state tile of each (item, value head) into
-//     a shared-memory ring with bulk async copies completing on mbarriers; the tile is
-//     moved to registers and its stage refilled at once, so STAGES tiles are in flight
-//     while one is computed; decode also prefetches the next item's raw prologue inputs;
+//   * threads: NT compute threads (16 warps for verify, 8 for decode); decode adds one
+//     producer warp and one norm warp;
+//   * the state tile of each (item, value head) streams into a shared-memory ring with
+//     bulk async copies completing on mbarriers; the tile is moved to registers and its
+//     stage refilled -- by decode's producer thread at once, by verify's thread 0 after
+//     the head's first barrier -- so STAGES tiles are in flight while one is computed;
+//     decode also prefetches the next item's raw prologue inputs;
 //   * thread (warp w, lane l) owns rows rb*RS*M + (l/8) + 4m and columns
 //     cb*32 + (l%8)*4 .. +3 of the [d_k][d_v] tile (rb = w/4, cb = w%4): every
 //     shared-memory read is conflict-free and every 128-bit global store of a warp
@@ -30,11 +31,13 @@
 //     per register;
 //   * per token, the column sums u = S k and p = S q are reduced in registers, across
 //     the row-lanes with warp shuffles and across the row-block warps through shared
-//     memory (one barrier per token), then
+//     memory, then
 //       delta = beta (v - alpha u),  S <- alpha S + k delta^T,  o = alpha p + delta (k.q)
-//     which is S_t = alpha S (I - beta k k^T) + beta v k^T, o = S_t q regrouped;
-//     decode applies the L2 norms of q and k there as scales (their sums come from the
-//     conv pass);
+//     which is S_t = alpha S (I - beta k k^T) + beta v k^T, o = S_t q regrouped; decode
+//     does this once (one barrier) and applies the L2 norms of q and k there as scales
+//     (their sums come from the conv pass); verify takes its tokens in pairs, one barrier
+//     per pair, the second token seeing the first's update through k_0.k_1 and k_0.q_1
+//     (verify_head);
 //   * the gated RMSNorm of a head's outputs: decode hands o to the norm warp through a
 //     two-slot buffer; verify runs it one warp per token after each head, with z staged
 //     in shared memory by the item prologue.
@@ -117,7 +120,7 @@ __device__ __forceinline__ bool token_update(SR (&S)[RecMap<D, NT>::M], const La
                                              const float* xq, const float* xk, const float* xv,
                                              float al, float be, float kq, float* red,
                                              float* orow, bool flag = false, float rq = 1.f,
-                                             float rk = 1.f, float* drow = nullptr) {
+                                             float rk = 1.f) {
   using Map = RecMap<D, NT>;
   float kr[Map::M];
   float4 u = make_float4(0.f, 0.f, 0.f, 0.f), pp = u;
@@ -170,8 +173,6 @@ __device__ __forceinline__ bool token_update(SR (&S)[RecMap<D, NT>::M], const La
     o.z = al * PP.z + dl.z * kq;
     o.w = al * PP.w + dl.w * kq;
     *reinterpret_cast<float4*>(orow + L.col0) = o;
-    // write-on-accept: the token's update is k_hat delta^T (k normalised when drow is used)
-    if (drow) *reinterpret_cast<float4*>(drow + L.col0) = dl;
   }
   dl.x *= rk; dl.y *= rk; dl.z *= rk; dl.w *= rk;
   // packed tiles run at a tighter register budget: k is read again rather than kept
@@ -301,10 +302,15 @@ struct RecSmem {
   static constexpr size_t kTile = size_t(D) * D * sizeof(SH);
   static constexpr size_t kStage = 0;
   static constexpr size_t kRed = kStage + STAGES * kTile;                  // [2][2][RB][D]
+  // Verify reduces a head's column sums two tokens at a time: red is then two buffers of
+  // [RB][4][D] (the k and q sums of a pair of tokens).
+  static constexpr bool kPairs = (KMAX > 1);
+  static constexpr size_t kRedBytes =
+      kPairs ? size_t(2) * Map::RB * 4 * D * 4 : size_t(2) * 2 * Map::RB * D * 4;
   // Decode hands each head's output to a norm warp through a two-slot obuf.
   static constexpr bool kNormWarp = (KMAX == 1);
   static constexpr int kObufRows = KMAX > 2 ? KMAX : 2;
-  static constexpr size_t kObuf = kRed + size_t(2) * 2 * Map::RB * D * 4;  // [kObufRows][D]
+  static constexpr size_t kObuf = kRed + kRedBytes;                        // [kObufRows][D]
   static constexpr size_t kNw = kObuf + size_t(kObufRows) * D * 4;         // [D] norm_w
   // mbarriers: full[STAGES] | empty[STAGES] | raw_full | raw_empty | nfull[2] | nfree[2],
   // then two counters (tiles and raw blocks the producer has started), read only when a
@@ -317,7 +323,9 @@ struct RecSmem {
   // slot of each sequence, whether its item can run (0 = yes, else the GDN_ERR_* code),
   // its table-0 pointer (verify), and the current item's 16 table entries (verify).
   // decode: per-warp partial sums q.q, k.k, q.k of the item's q and k, [D / 32][3]
-  static constexpr size_t kL2 = kKq + ((size_t(KMAX) * 4 + 15) / 16) * 16;
+  // verify: (k_t0.k_t1, k_t0.q_t1) of each pair of tokens [KMAX/2][2]
+  static constexpr size_t kPair = kKq + ((size_t(KMAX) * 4 + 15) / 16) * 16;
+  static constexpr size_t kL2 = kPair + (kPairs ? ((size_t(KMAX) * 4 + 15) / 16) * 16 : 0);
   static constexpr size_t kSlots = kL2 + ((size_t(D + 31) / 32 * 12 + 15) / 16) * 16;  // [128] i32
   static constexpr size_t kValid = kSlots + GDN_MAX_SEQS * 4;                  // [128] i32
   static constexpr size_t kTab0 = kValid + GDN_MAX_SEQS * 4;                   // [128] u64
@@ -397,18 +405,192 @@ __device__ __forceinline__ const SH* state_src(const RecParams& p, const Item& i
   return reinterpret_cast<const SH*>(p.h_pool) + (size_t(it.slot) * p.Hv + h) * D * D;
 }
 
+__device__ __forceinline__ void fma4(float4& acc, const float4& s, float x) {
+  acc.x += s.x * x;
+  acc.y += s.y * x;
+  acc.z += s.z * x;
+  acc.w += s.w * x;
+}
+// acc += the value of `send` held by lane (lane ^ off)
+__device__ __forceinline__ void add_xor4(float4& acc, const float4& send, int off) {
+  const float4 r = make_float4(__shfl_xor_sync(0xffffffffu, send.x, off),
+                               __shfl_xor_sync(0xffffffffu, send.y, off),
+                               __shfl_xor_sync(0xffffffffu, send.z, off),
+                               __shfl_xor_sync(0xffffffffu, send.w, off));
+  acc.x += r.x;
+  acc.y += r.y;
+  acc.z += r.z;
+  acc.w += r.w;
+}
+
+// One value head of a verify item, two tokens per barrier: the column sums of a pair are
+// taken from the state before the pair, and the pair's second token sees the first's
+// update through two scalars.  In the tile's orientation (H = S^T: rows d_k, columns d_v),
+// with A_t = H^T k_t and B_t = H^T q_t of the state H before the pair (t0, t1):
+//   delta_0 = beta_0 (v_0 - alpha_0 A_0),       o_0 = alpha_0 B_0 + (q_0.k_0) delta_0
+//   H' = alpha_0 H + k_0 delta_0^T,  so  H'^T k_1 = alpha_0 A_1 + (k_0.k_1) delta_0  and
+//   H'^T q_1 = alpha_0 B_1 + (k_0.q_1) delta_0, which give delta_1 and o_1 by the same rule
+// (the token-by-token delta rule, Gated DeltaNet paper, the gated delta rule's recurrence;
+// the pair is its chunkwise form with chunks of two).  The four sums of a pair come out of
+// the register tile in one pass: each warp reduce-scatters them over its rows (lane bits 4
+// and 3 pick the vector a lane keeps), the warps' partials go through one of two buffers
+// [RB][4][D] in turn, and every thread adds the RB partials of its own four columns.  The
+// state updates and stores follow in the same step, so stores go out between reductions.
+// After the barrier each lane adds up only the vector it kept (RB loads) and takes the
+// other three from its neighbours by shuffles.
+// pair_s: [KMAX/2][2] = (k_0.k_1, k_0.q_1) of each pair; kq_s: q_t.k_t.  after_first()
+// runs once, on every thread, after the head's first barrier (every thread holds the tile
+// in registers by then).
+// Returns true if the first barrier saw `abort` raised by any thread (nothing written).
+template <typename T, int D, int NT, int KMAX, typename SH, typename SR, bool WOA, typename F>
+__device__ __forceinline__ bool verify_head(const RecParams& p, const Item& it, int h, int g,
+                                            int k, SR (&S)[RecMap<D, NT>::M],
+                                            const Lane<D, NT>& L, const float* xs, int CHX,
+                                            const float* gate, const float* kq_s,
+                                            const float* pair_s, float* red, float* obuf,
+                                            const uint64_t* tab_item, unsigned char* woa_seq,
+                                            bool abort, F&& after_first) {
+  using Map = RecMap<D, NT>;
+  static_assert(Map::CQ == 4 || Map::CQ == 8, "the reduce-scatter splits lane bits 3 and 4");
+  // after the reduce-scatter a lane holds vector 2 hi + mid of (A_0, B_0, A_1, B_1)
+  const bool hi = (L.lane >> 4) & 1, mid = (L.lane >> 3) & 1;
+  const bool writer = ((L.lane / Map::CQ) & (8 / Map::CQ - 1)) == 0;
+  const bool o_writer = L.rb == 0 && L.rs == 0;
+  float* woa_d = WOA ? reinterpret_cast<float*>(woa_seq + p.woa_delta) + size_t(h) * D + L.col0
+                     : nullptr;
+  // The state after a pair's second token is stored row by row inside the next pair's
+  // partial sums (which read the same registers), and the state after its first token row
+  // by row inside the second token's update, so stores leave between arithmetic rather
+  // than in bursts.  pend: where the registers' state still has to go (null: nowhere).
+  SH* pend = nullptr;
+  for (int t0 = 0; t0 < k; t0 += 2) {
+    const bool has1 = t0 + 1 < k;
+    const int t1 = has1 ? t0 + 1 : t0;  // odd k: the last pair's second token is a copy
+    const float* x0 = xs + t0 * CHX;
+    const float* x1 = xs + t1 * CHX;
+    float4 K0, K1;  // the k sums of the pair, then its q sums, each halved across lane bit 4
+#pragma unroll
+    for (int qk = 0; qk < 2; ++qk) {
+      const int off = qk ? 0 : D;
+      float4 Pa = make_float4(0.f, 0.f, 0.f, 0.f), Pb = Pa;
+#pragma unroll
+      for (int m = 0; m < Map::M; ++m) {
+        const int i = L.row(m);
+        const float4 sm = sr_get(S[m]);
+        if (!WOA && qk == 0 && pend) store_sr(pend + i * D + L.col0, S[m]);
+        fma4(Pa, sm, x0[off + i]);
+        fma4(Pb, sm, x1[off + i]);
+      }
+      float4 Kx = hi ? Pb : Pa;
+      add_xor4(Kx, hi ? Pa : Pb, 16);
+      if (qk) K1 = Kx; else K0 = Kx;
+    }
+    float4 R = mid ? K1 : K0;
+    add_xor4(R, mid ? K0 : K1, 8);
+#pragma unroll
+    for (int off = Map::CQ; off < 8; off <<= 1) {
+      const float4 mine = R;
+      add_xor4(R, mine, off);
+    }
+    float* rbuf = red + ((t0 >> 1) & 1) * Map::RB * 4 * D;
+    if (writer)
+      *reinterpret_cast<float4*>(rbuf + (L.rb * 4 + 2 * hi + mid) * D + L.col0) = R;
+    if (t0 == 0) {
+      if (named_sync_or(1, NT, abort)) return true;
+      after_first();
+    } else {
+      named_sync(1, NT);
+    }
+    // each lane adds the RB partials of the vector it holds, for its four columns; the
+    // others come from the lanes that hold them
+    float4 V = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int b = 0; b < Map::RB; ++b) {
+      const float4 a = *reinterpret_cast<const float4*>(rbuf + (b * 4 + 2 * hi + mid) * D + L.col0);
+      V.x += a.x; V.y += a.y; V.z += a.z; V.w += a.w;
+    }
+    auto vec_of = [&](int v) {  // the lane with this lane's columns holding vector v
+      const int src = (L.lane & 7) | ((v & 1) << 3) | ((v >> 1) << 4);
+      return make_float4(__shfl_sync(0xffffffffu, V.x, src), __shfl_sync(0xffffffffu, V.y, src),
+                         __shfl_sync(0xffffffffu, V.z, src), __shfl_sync(0xffffffffu, V.w, src));
+    };
+    const float4 A0 = vec_of(0), A1 = vec_of(2);
+    const float al0 = gate[(t0 * kMaxG + g) * 2], be0 = gate[(t0 * kMaxG + g) * 2 + 1];
+    const float al1 = gate[(t1 * kMaxG + g) * 2], be1 = gate[(t1 * kMaxG + g) * 2 + 1];
+    const float kk = pair_s[t0], kq01 = pair_s[t0 + 1];
+    const float kq0 = kq_s[t0], kq1 = kq_s[t1];
+    const float4 v0 = *reinterpret_cast<const float4*>(x0 + (2 + g) * D + L.col0);
+    const float4 v1 = *reinterpret_cast<const float4*>(x1 + (2 + g) * D + L.col0);
+    float4 d0, d1;
+    d0.x = be0 * (v0.x - al0 * A0.x);
+    d0.y = be0 * (v0.y - al0 * A0.y);
+    d0.z = be0 * (v0.z - al0 * A0.z);
+    d0.w = be0 * (v0.w - al0 * A0.w);
+    d1.x = be1 * (v1.x - al1 * (al0 * A1.x + kk * d0.x));
+    d1.y = be1 * (v1.y - al1 * (al0 * A1.y + kk * d0.y));
+    d1.z = be1 * (v1.z - al1 * (al0 * A1.z + kk * d0.z));
+    d1.w = be1 * (v1.w - al1 * (al0 * A1.w + kk * d0.w));
+    if (L.rb == 0) {  // warp-uniform: the warps whose rs == 0 lanes write o
+      const float4 B0 = vec_of(1), B1 = vec_of(3);
+      float4 o0, o1;
+      o0.x = al0 * B0.x + kq0 * d0.x;
+      o0.y = al0 * B0.y + kq0 * d0.y;
+      o0.z = al0 * B0.z + kq0 * d0.z;
+      o0.w = al0 * B0.w + kq0 * d0.w;
+      o1.x = al1 * (al0 * B1.x + kq01 * d0.x) + kq1 * d1.x;
+      o1.y = al1 * (al0 * B1.y + kq01 * d0.y) + kq1 * d1.y;
+      o1.z = al1 * (al0 * B1.z + kq01 * d0.z) + kq1 * d1.z;
+      o1.w = al1 * (al0 * B1.w + kq01 * d0.w) + kq1 * d1.w;
+      if (o_writer) {
+        *reinterpret_cast<float4*>(obuf + t0 * D + L.col0) = o0;
+        if (has1) *reinterpret_cast<float4*>(obuf + t1 * D + L.col0) = o1;
+        if (WOA) {  // the update of token t is k_hat_t delta_t^T
+          *reinterpret_cast<float4*>(woa_d + size_t(t0) * p.Hv * D) = d0;
+          if (has1) *reinterpret_cast<float4*>(woa_d + size_t(t1) * p.Hv * D) = d1;
+        }
+      }
+    }
+    SH* dst0 = WOA ? nullptr : state_dst<D, true, SH>(p, it, tab_item, h, t0);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (u == 1 && !has1) break;
+      const float al = u ? al1 : al0;
+      const float4 dd = u ? d1 : d0;
+      const float* xk = (u ? x1 : x0) + D;
+#pragma unroll
+      for (int m = 0; m < Map::M; ++m) {
+        const int i = L.row(m);
+        const float ki = xk[i];
+        float4 sm = sr_get(S[m]);
+        if (!WOA && u == 1) store_sr(dst0 + i * D + L.col0, S[m]);  // the state after t0
+        sm.x = al * sm.x + ki * dd.x;
+        sm.y = al * sm.y + ki * dd.y;
+        sm.z = al * sm.z + ki * dd.z;
+        sm.w = al * sm.w + ki * dd.w;
+        sr_set(S[m], sm);
+      }
+    }
+    if (!WOA) pend = has1 ? state_dst<D, true, SH>(p, it, tab_item, h, t1) : dst0;
+  }
+  if (!WOA && pend) store_tile<D, NT, SH, SR>(pend, S, L);
+  return false;
+}
+
 // Thread roles: threads [0, NT) compute (at d = 128, 16 warps for verify and 8 for
-// decode), the next warp produces.
-// Lane 0 of the producer warp streams every state tile into the stage ring (full/empty
-// mbarriers per stage) and, for decode, each item's raw prologue inputs into a staging
-// block (raw_full/raw_empty), with bulk async copies.  Compute threads synchronise only
-// with named barrier 1; a stage is released by one mbarrier arrive per compute warp.
+// decode).  State tiles stream into a ring of stages by bulk async copies, each landing on
+// the stage's full mbarrier.  Decode has a producer warp after the compute threads: its
+// lane 0 issues the tiles (a stage is released by one mbarrier arrive per compute warp on
+// its empty mbarrier) and each item's raw prologue inputs into a staging block
+// (raw_full/raw_empty).  Verify has no producer warp: once every compute thread has a
+// head's tile in registers (its first barrier), thread 0 issues the tile STAGES heads
+// ahead into the stage it came from -- sixteen warps, so 128 registers a thread.  Compute
+// threads synchronise only with named barrier 1.
 // Decode has one more warp, which applies the gated RMSNorm to each head's output: the
 // compute warps that write a head's o arrive on nfull[slot], the norm warp copies o and z
 // to registers and arrives on nfree[slot], so the norm never sits on the chain of heads.
 template <int NT, int KMAX>
 __host__ __device__ constexpr int rec_threads() {
-  return NT + (KMAX == 1 ? 64 : 32);
+  return NT + (KMAX == 1 ? 64 : 0);
 }
 // Decode on fp16 pools holds its tile packed (half the registers) and runs two CTAs per
 // SM, so one CTA's per-head chain (reduction, barrier, update) overlaps the other's.
@@ -440,6 +622,7 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
   volatile int32_t* issued_s = reinterpret_cast<volatile int32_t*>(smem + SL::kIssued);
   float* gate = reinterpret_cast<float*>(smem + SL::kGate);
   float* kq_s = reinterpret_cast<float*>(smem + SL::kKq);
+  float* pair_s = reinterpret_cast<float*>(smem + SL::kPair);
   float* l2_s = reinterpret_cast<float*>(smem + SL::kL2);
   float* xs = reinterpret_cast<float*>(smem + SL::kXs);
   int32_t* slots_s = reinterpret_cast<int32_t*>(smem + SL::kSlots);
@@ -497,6 +680,26 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
     return rounds;
   };
 
+  // Tile of value head g of item `it` into stage s (one thread).
+  auto issue_tile = [&](int s, const Item& it, int g) {
+    const SH* src = state_src<D, VERIFY, SH>(p, it, tab0_s, it.kh * G + g);
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&full[s], uint32_t(SL::kTile));
+    constexpr uint32_t kPiece = SL::kTile >= 16384 ? 16384u : uint32_t(SL::kTile);
+#pragma unroll
+    for (uint32_t off = 0; off < SL::kTile; off += kPiece)
+      bulk_g2s(stage + s * SL::kTile + off,
+               reinterpret_cast<const unsigned char*>(src) + off, kPiece, &full[s]);
+    issued_s[0] = issued_s[0] + 1;
+  };
+  // The next (item, head) after (r, g).
+  auto advance = [&](int& r, int& g, Item& it) {
+    if (++g == G) {
+      g = 0;
+      r = next_valid(r + 1, it);
+    }
+  };
+
   // =========================================================================== norm (decode)
   if (SL::kNormWarp && tid >= NT + 32) {
     using A = Act<T>;
@@ -539,17 +742,6 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
   // =========================================================================== producer
   if (tid >= NT) {
     if (tid != NT) return;
-    auto issue_tile = [&](int s, const Item& it, int g) {
-      const SH* src = state_src<D, VERIFY, SH>(p, it, tab0_s, it.kh * G + g);
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&full[s], uint32_t(SL::kTile));
-      constexpr uint32_t kPiece = SL::kTile >= 16384 ? 16384u : uint32_t(SL::kTile);
-#pragma unroll
-      for (uint32_t off = 0; off < SL::kTile; off += kPiece)
-        bulk_g2s(stage + s * SL::kTile + off,
-                 reinterpret_cast<const unsigned char*>(src) + off, kPiece, &full[s]);
-      issued_s[0] = issued_s[0] + 1;
-    };
     // The raw prologue inputs of one item as contiguous blocks: conv state, conv
     // weights and raw qkv of its q | k | v channel ranges, and z of its value heads.
     auto issue_raw = [&](const Item& it) {
@@ -577,12 +769,6 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
                  reinterpret_cast<const T*>(p.z) + size_t(it.row0 + t) * p.z_stride + it.kh * G * D,
                  uint32_t(G) * D * sizeof(T), raw_full);
       issued_s[1] = issued_s[1] + 1;
-    };
-    auto advance = [&](int& r, int& g, Item& it) {
-      if (++g == G) {
-        g = 0;
-        r = next_valid(r + 1, it);
-      }
     };
     Item it_raw, it_i, it_x;
     int r_raw = next_valid(0, it_raw);
@@ -639,6 +825,16 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
     }
   }
   int q = 0, m = 0;  // tiles and items consumed by this CTA
+  // verify: thread 0 issues the tiles, the first STAGES now and then one per finished head
+  Item it_i;
+  int r_i = rounds, g_i = 0;  // next tile to issue
+  if (SL::kPairs && tid == 0) {
+    r_i = next_valid(0, it_i);
+    for (int s = 0; s < STAGES && r_i < rounds; ++s) {
+      issue_tile(s, it_i, g_i);
+      advance(r_i, g_i, it_i);
+    }
+  }
   // A bounded wait gave up: let this CTA's copies still in flight land, then stop.
   auto drain = [&](int q_from) {
     if (tid != 0) return;
@@ -730,57 +926,101 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
       if (r_next < rounds) load_scalars(nxt);
     } else {
       named_sync(1, NT);  // every warp is done with the previous item's xs, gates, tables
-      if (VERIFY && tid < k) tab_item[tid] = p.tables[tid * GDN_VERIFY_WY_TABLE_SEQS + it.seq];
-      for (int lc = tid; lc < CHX; lc += NT) {
-        if (lc >= CH) {  // z channel: staged as f32
-          const int zc = lc - CH;
-          const T* zp = reinterpret_cast<const T*>(p.z) + size_t(it.row0) * p.z_stride +
-                        it.kh * G * D + zc;
-          for (int t = 0; t < k; ++t) xs[t * CHX + lc] = A::to_f(zp[size_t(t) * p.z_stride]);
-          continue;
+      // Every load of the prologue is issued before any of its results is used: the
+      // item's table entries and gate inputs, then a thread's channels two at a time.
+      static_assert(NT >= KMAX * kMaxG, "one thread per (token, value head) for the gates");
+      uint64_t tab_v = 0;
+      if (VERIFY && tid < k) tab_v = p.tables[tid * GDN_VERIFY_WY_TABLE_SEQS + it.seq];
+      float g_a = 0.f, g_b = 0.f, g_Al = 0.f, g_Dt = 0.f;
+      if (tid < k * G) {
+        const int t = tid / G, h = it.kh * G + (tid - t * G);
+        const size_t ro = size_t(it.row0 + t) * p.ab_stride + h;
+        g_a = A::to_f(reinterpret_cast<const T*>(p.a)[ro]);
+        g_b = A::to_f(reinterpret_cast<const T*>(p.b)[ro]);
+        g_Al = p.A_log[h];
+        g_Dt = p.dt_bias[h];
+      }
+      // Pass 1, loads: a thread's channels two at a time, every raw input of both (z
+      // inputs for lc >= CH; else the k raw conv inputs, the conv state -- the last kW raw
+      // inputs, oldest first -- and the weights) in registers before any is stored; the raw
+      // values are parked in xs.  Pass 2 runs the conv + SiLU of each conv channel over
+      // xs in place, each token shifting its raw input into the window; the window after
+      // the last token is the new conv state.
+      constexpr int kG = KMAX < 8 ? KMAX : 8;  // tokens per round of loads
+      auto channel_src = [&](int lc, size_t& stride) -> const T* {
+        if (lc >= CH) {
+          stride = p.z_stride;
+          return reinterpret_cast<const T*>(p.z) + size_t(it.row0) * p.z_stride +
+                 it.kh * G * D + (lc - CH);
         }
+        stride = p.qkv_stride;
+        return reinterpret_cast<const T*>(p.qkv) + size_t(it.row0) * p.qkv_stride +
+               global_channel(it.kh, lc);
+      };
+      auto load_state = [&](int lc, float4& win, float4& w4) {
+        if (lc >= CH) return;
         const int gc = global_channel(it.kh, lc);
-        T* cs = reinterpret_cast<T*>(p.conv_pool) + (size_t(it.slot) * p.conv_dim + gc) * kW;
-        const float4 w4 = *reinterpret_cast<const float4*>(p.conv_w + size_t(gc) * kW);
-        // win: the last kW raw inputs, oldest first; each token shifts its input in.
-        float4 win = A::load4(cs);
-        const T* xrow = reinterpret_cast<const T*>(p.qkv) + size_t(it.row0) * p.qkv_stride + gc;
-        constexpr int kGrp = KMAX < 4 ? KMAX : 4;  // raw loads in flight together
-        for (int t0 = 0; t0 < k; t0 += kGrp) {
-          float xg[kGrp];
-#pragma unroll
-          for (int u = 0; u < kGrp; ++u)
-            if (t0 + u < k) xg[u] = A::to_f(xrow[size_t(t0 + u) * p.qkv_stride]);
-#pragma unroll
-          for (int u = 0; u < kGrp; ++u) {
-            const int t = t0 + u;
-            if (t < k) {
-              win = make_float4(win.y, win.z, win.w, xg[u]);
-              if (VERIFY && woa)  // the raw input, an exact copy, for the deferred fold
-                reinterpret_cast<T*>(woa_seq + p.woa_raw)[size_t(t) * p.conv_dim + gc] =
-                    A::from_f(xg[u]);
-              xs[t * CHX + lc] =
-                  silu_f(w4.x * win.x + w4.y * win.y + w4.z * win.z + w4.w * win.w);
-              if (VERIFY && p.conv_inter && t < k - 1) {
-                T* ci = reinterpret_cast<T*>(p.conv_inter) +
-                        ((size_t(it.seq) * (GDN_VERIFY_WY_TABLES_PER_LAYER - 1) + t) * p.conv_dim + gc) * kW;
-                A::store4(ci, win);
-              }
-            }
+        win = A::load4(reinterpret_cast<const T*>(p.conv_pool) +
+                       (size_t(it.slot) * p.conv_dim + gc) * kW);
+        w4 = *reinterpret_cast<const float4*>(p.conv_w + size_t(gc) * kW);
+      };
+      auto conv_channel = [&](int lc, float4 win, const float4& w4) {
+        const int gc = global_channel(it.kh, lc);
+        for (int t = 0; t < k; ++t) {
+          const float x = xs[t * CHX + lc];
+          win = make_float4(win.y, win.z, win.w, x);
+          if (VERIFY && woa)  // the raw input, an exact copy, for the deferred fold
+            reinterpret_cast<T*>(woa_seq + p.woa_raw)[size_t(t) * p.conv_dim + gc] = A::from_f(x);
+          xs[t * CHX + lc] = silu_f(w4.x * win.x + w4.y * win.y + w4.z * win.z + w4.w * win.w);
+          if (VERIFY && p.conv_inter && t < k - 1) {
+            T* ci = reinterpret_cast<T*>(p.conv_inter) +
+                    ((size_t(it.seq) * (GDN_VERIFY_WY_TABLES_PER_LAYER - 1) + t) * p.conv_dim + gc) * kW;
+            A::store4(ci, win);
           }
         }
-        if (!woa) A::store4(cs, win);  // exact copies of the last kW raw inputs
+        if (!woa)  // exact copies of the last kW raw inputs
+          A::store4(reinterpret_cast<T*>(p.conv_pool) + (size_t(it.slot) * p.conv_dim + gc) * kW,
+                    win);
+      };
+      for (int lc = tid; lc < CHX; lc += 2 * NT) {
+        const int lc1 = lc + NT;
+        const bool two = lc1 < CHX;
+        float4 wina, w4a, winb, w4b;
+        size_t sa, sb = 0;
+        const T* pa = channel_src(lc, sa);
+        const T* pb = two ? channel_src(lc1, sb) : pa;
+        load_state(lc, wina, w4a);
+        if (two) load_state(lc1, winb, w4b);
+        for (int t0 = 0; t0 < k; t0 += kG) {
+          float xa[kG], xb[kG];
+#pragma unroll
+          for (int u = 0; u < kG; ++u)
+            if (t0 + u < k) xa[u] = A::to_f(pa[size_t(t0 + u) * sa]);
+          if (two) {
+#pragma unroll
+            for (int u = 0; u < kG; ++u)
+              if (t0 + u < k) xb[u] = A::to_f(pb[size_t(t0 + u) * sb]);
+          }
+#pragma unroll
+          for (int u = 0; u < kG; ++u)
+            if (t0 + u < k) xs[(t0 + u) * CHX + lc] = xa[u];
+          if (two) {
+#pragma unroll
+            for (int u = 0; u < kG; ++u)
+              if (t0 + u < k) xs[(t0 + u) * CHX + lc1] = xb[u];
+          }
+        }
+        if (lc < CH) conv_channel(lc, wina, w4a);
+        if (two && lc1 < CH) conv_channel(lc1, winb, w4b);
       }
-      for (int idx = tid; idx < k * G; idx += NT) {
-        const int t = idx / G, g = idx - t * G;
-        const int h = it.kh * G + g;
-        const size_t ro = size_t(it.row0 + t) * p.ab_stride + h;
+      if (VERIFY && tid < k) tab_item[tid] = tab_v;
+      if (tid < k * G) {
+        const int t = tid / G, g = tid - t * G;
         float al, be;
-        gates_f(A::to_f(reinterpret_cast<const T*>(p.a)[ro]),
-                A::to_f(reinterpret_cast<const T*>(p.b)[ro]), p.A_log[h], p.dt_bias[h], &al, &be);
+        gates_f(g_a, g_b, g_Al, g_Dt, &al, &be);
         gate[(t * kMaxG + g) * 2 + 0] = al;
         gate[(t * kMaxG + g) * 2 + 1] = be;
-        if (VERIFY && woa) reinterpret_cast<float*>(woa_seq + p.woa_alpha)[t * p.Hv + h] = al;
+        if (VERIFY && woa) reinterpret_cast<float*>(woa_seq + p.woa_alpha)[t * p.Hv + it.kh * G + g] = al;
       }
       named_sync(1, NT);
     }
@@ -800,6 +1040,21 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
     } else {
       l2norm_tokens<D, Map::NW>(xs, CHX, k, p.q_scale, p.l2_eps, kq_s, L.warp, L.lane);
       named_sync(1, NT);
+      if constexpr (SL::kPairs) {
+        // k_t0.k_t1 and k_t0.q_t1 of each pair (t0 even): one warp per dot product; the
+        // heads read them after their first barrier
+        for (int e = L.warp; e < k - 1; e += Map::NW) {
+          if (e & 1) continue;
+          for (int which = 0; which < 2; ++which) {
+            const float* xa = xs + e * CHX + D;
+            const float* xb = xs + (e + 1) * CHX + (which ? 0 : D);
+            float acc = 0.f;
+            for (int i = L.lane; i < D; i += 32) acc += xa[i] * xb[i];
+            acc = warp_sum(acc);
+            if (L.lane == 0) pair_s[e + which] = acc;
+          }
+        }
+      }
       if (VERIFY && woa) {  // k, and the normalised k of every token, for the deferred fold
         float* kh_out = reinterpret_cast<float*>(woa_seq + p.woa_khat);
         for (int idx = tid; idx < k * D; idx += NT) {
@@ -824,39 +1079,46 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
       const SH* tile = reinterpret_cast<const SH*>(stage + size_t(s) * SL::kTile);
 #pragma unroll
       for (int mm = 0; mm < Map::M; ++mm) load_sr(S[mm], tile + L.row(mm) * D + L.col0);
-      __syncwarp();
-      if (L.lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
+      if constexpr (!SL::kPairs) {
+        __syncwarp();
+        if (L.lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
+      }
       ++q;
-      for (int t = 0; t < k; ++t) {
-        const float* xq = xs + t * CHX;
-        if (token_update<D, NT, true, SR>(S, L, xq, xq + D, xq + (2 + g) * D,
-                                      gate[(t * kMaxG + g) * 2 + 0],
-                                      gate[(t * kMaxG + g) * 2 + 1],
-                                      SL::kPrefetch ? kq1 : kq_s[t],
-                                      // decode alternates by head: no barrier separates
-                                      // one head's reduction reads from the next's writes
-                                      red + ((SL::kNormWarp ? hq : t) & 1) * 2 * Map::RB * D,
-                                      obuf + (SL::kNormWarp ? (hq & 1) : t) * D,
-                                      t == 0 && !ok, rq, rk,
-                                      (VERIFY && woa) ? reinterpret_cast<float*>(woa_seq + p.woa_delta) +
-                                                            (size_t(t) * p.Hv + h) * D
-                                                      : nullptr)) {
+      if constexpr (SL::kPairs) {
+        // stage s is free once every thread has its tile in registers: after the first
+        // barrier of the head, thread 0 issues the tile STAGES heads ahead into it
+        auto refill = [&]() {
+          if (tid == 0 && r_i < rounds) {
+            issue_tile(s, it_i, g_i);
+            advance(r_i, g_i, it_i);
+          }
+        };
+        if (verify_head<T, D, NT, KMAX, SH, SR, VERIFY && WOA>(p, it, h, g, k, S, L, xs, CHX,
+                                                               gate, kq_s, pair_s, red, obuf,
+                                                               tab_item, woa_seq, !ok, refill)) {
           drain(q - 1);
           return;
         }
-        if (!woa && (VERIFY || t == k - 1))
-          store_tile<D, NT, SH, SR>(state_dst<D, VERIFY, SH>(p, it, tab_item, h, t), S, L);
-      }
-      if constexpr (SL::kNormWarp) {
-        if (L.rb == 0) {  // this warp wrote part of o
-          __syncwarp();
-          if (L.lane == 0) mbar_arrive(&nfull[hq & 1]);
-        }
-      } else {
         named_sync(1, NT);  // obuf complete
         norm_tokens<T, D, Map::NW>(obuf, xs + CH + g * D, CHX, k, it.row0, h, nw_s,
                                    p.norm_eps, p.norm_gate, p.Hv, reinterpret_cast<T*>(p.y),
                                    p.core_out, L.warp, L.lane);
+      } else {  // decode: one token; the norm warp takes o from obuf slot hq & 1
+        static_assert(KMAX == 1 && !VERIFY, "verify runs in pairs of tokens");
+        // slots alternate by head: no barrier separates one head's reduction reads from
+        // the next's writes
+        if (token_update<D, NT, true, SR>(S, L, xs, xs + D, xs + (2 + g) * D, gate[g * 2],
+                                          gate[g * 2 + 1], kq1,
+                                          red + (hq & 1) * 2 * Map::RB * D,
+                                          obuf + (hq & 1) * D, !ok, rq, rk)) {
+          drain(q - 1);
+          return;
+        }
+        store_tile<D, NT, SH, SR>(state_dst<D, VERIFY, SH>(p, it, tab_item, h, 0), S, L);
+        if (L.rb == 0) {  // this warp wrote part of o
+          __syncwarp();
+          if (L.lane == 0) mbar_arrive(&nfull[hq & 1]);
+        }
       }
     }
   }
