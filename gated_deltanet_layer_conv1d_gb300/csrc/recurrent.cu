@@ -85,9 +85,43 @@ struct Lane {
     rs = lane / Map::CQ;
     col0 = cb * 4 * Map::CQ + cq * 4;
     rowb = rb * (Map::RS * Map::M) + rs;  // row of m = 0; row m is rowb + RS*m
+    xrow = rb * (Map::RS * Map::M) + rs * Map::M;
   }
   __device__ __forceinline__ int row(int m) const { return rowb + Map::RS * m; }
+  // xrow: where the thread's M rows start in a vector held in qk_pos order
+  int xrow;
 };
+
+// Position of element i of a d_k vector held in shared memory in "row-block order": each
+// thread's M rows (rowb + RS*m, strided so that a warp's 128-bit stores cover whole
+// lines of consecutive rows) sit at xrow .. xrow + M - 1, so it reads them with vector
+// loads.  q and k of the verify and decode prologues are staged this way.
+template <int D, int NT>
+__device__ __forceinline__ int qk_pos(int i) {
+  using Map = RecMap<D, NT>;
+  constexpr int B = Map::RS * Map::M;
+  const int b = i / B, r = i - b * B;
+  return b * B + (r % Map::RS) * Map::M + r / Map::RS;
+}
+
+// The thread's M elements x[0 .. M - 1] of a shared-memory vector in row-block order
+// (x = vector + xrow, 16-byte aligned when M is a multiple of 4).
+template <int M>
+__device__ __forceinline__ void load_rows(const float* x, float (&out)[M]) {
+  if constexpr (M % 4 == 0) {
+#pragma unroll
+    for (int m = 0; m < M; m += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(x + m);
+      out[m] = v.x;
+      out[m + 1] = v.y;
+      out[m + 2] = v.z;
+      out[m + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int m = 0; m < M; ++m) out[m] = x[m];
+  }
+}
 
 // A thread's four state elements of one tile row in registers: f32 (float4), or packed
 // fp16 (uint2) where the tile is read from and written back to an fp16 pool after a single
@@ -113,21 +147,30 @@ __device__ __forceinline__ void sr_set(uint2& s, float4 v) {
 // NAMED selects the barrier: named barrier 1 over the NT compute threads (kernels with a
 // separate producer warp) or __syncthreads.  `flag` is OR-reduced by that barrier; if any
 // thread raised it, every thread gets true back and the update is not applied.
+// PERM: xq and xk hold q and k in row-block order (qk_pos), else in natural order.
 // rq, rk: the L2 scales of q and k when xq, xk hold them unnormalised (decode), else 1:
 // S k_hat = rk (S k), S q_hat = rq (S q), and k_hat delta^T = k (rk delta)^T.
-template <int D, int NT, bool NAMED = false, typename SR = float4>
+template <int D, int NT, bool NAMED = false, typename SR = float4, bool PERM = false>
 __device__ __forceinline__ bool token_update(SR (&S)[RecMap<D, NT>::M], const Lane<D, NT>& L,
                                              const float* xq, const float* xk, const float* xv,
                                              float al, float be, float kq, float* red,
                                              float* orow, bool flag = false, float rq = 1.f,
                                              float rk = 1.f) {
   using Map = RecMap<D, NT>;
-  float kr[Map::M];
+  // packed tiles run at a tighter register budget: k is read again rather than kept, and
+  // q and k are read one element at a time
+  constexpr bool kReloadK = std::is_same<SR, uint2>::value;
+  constexpr bool kVecLoad = PERM && !kReloadK;
+  auto at = [&](const float* x, int m) { return PERM ? x[L.xrow + m] : x[L.row(m)]; };
+  float kr[Map::M], qr[Map::M];
+  if constexpr (kVecLoad) {
+    load_rows(xk + L.xrow, kr);
+    load_rows(xq + L.xrow, qr);
+  }
   float4 u = make_float4(0.f, 0.f, 0.f, 0.f), pp = u;
 #pragma unroll
   for (int m = 0; m < Map::M; ++m) {
-    const int i = L.row(m);
-    const float ki = xk[i], qi = xq[i];
+    const float ki = kVecLoad ? kr[m] : at(xk, m), qi = kVecLoad ? qr[m] : at(xq, m);
     const float4 sm = sr_get(S[m]);
     kr[m] = ki;
     u.x += sm.x * ki; u.y += sm.y * ki; u.z += sm.z * ki; u.w += sm.w * ki;
@@ -175,11 +218,9 @@ __device__ __forceinline__ bool token_update(SR (&S)[RecMap<D, NT>::M], const La
     *reinterpret_cast<float4*>(orow + L.col0) = o;
   }
   dl.x *= rk; dl.y *= rk; dl.z *= rk; dl.w *= rk;
-  // packed tiles run at a tighter register budget: k is read again rather than kept
-  constexpr bool kReloadK = std::is_same<SR, uint2>::value;
 #pragma unroll
   for (int m = 0; m < Map::M; ++m) {
-    const float ki = kReloadK ? xk[L.row(m)] : kr[m];
+    const float ki = kReloadK ? at(xk, m) : kr[m];
     float4 sm = sr_get(S[m]);
     sm.x = al * sm.x + ki * dl.x;
     sm.y = al * sm.y + ki * dl.y;
@@ -473,13 +514,15 @@ __device__ __forceinline__ bool verify_head(const RecParams& p, const Item& it, 
     for (int qk = 0; qk < 2; ++qk) {
       const int off = qk ? 0 : D;
       float4 Pa = make_float4(0.f, 0.f, 0.f, 0.f), Pb = Pa;
+      float xa[Map::M], xb[Map::M];
+      load_rows(x0 + off + L.xrow, xa);
+      load_rows(x1 + off + L.xrow, xb);
 #pragma unroll
       for (int m = 0; m < Map::M; ++m) {
-        const int i = L.row(m);
         const float4 sm = sr_get(S[m]);
-        if (!WOA && qk == 0 && pend) store_sr(pend + i * D + L.col0, S[m]);
-        fma4(Pa, sm, x0[off + i]);
-        fma4(Pb, sm, x1[off + i]);
+        if (!WOA && qk == 0 && pend) store_sr(pend + L.row(m) * D + L.col0, S[m]);
+        fma4(Pa, sm, xa[m]);
+        fma4(Pb, sm, xb[m]);
       }
       float4 Kx = hi ? Pb : Pa;
       add_xor4(Kx, hi ? Pa : Pb, 16);
@@ -556,13 +599,13 @@ __device__ __forceinline__ bool verify_head(const RecParams& p, const Item& it, 
       if (u == 1 && !has1) break;
       const float al = u ? al1 : al0;
       const float4 dd = u ? d1 : d0;
-      const float* xk = (u ? x1 : x0) + D;
+      float kr[Map::M];
+      load_rows((u ? x1 : x0) + D + L.xrow, kr);
 #pragma unroll
       for (int m = 0; m < Map::M; ++m) {
-        const int i = L.row(m);
-        const float ki = xk[i];
+        const float ki = kr[m];
         float4 sm = sr_get(S[m]);
-        if (!WOA && u == 1) store_sr(dst0 + i * D + L.col0, S[m]);  // the state after t0
+        if (!WOA && u == 1) store_sr(dst0 + L.row(m) * D + L.col0, S[m]);  // the state after t0
         sm.x = al * sm.x + ki * dd.x;
         sm.y = al * sm.y + ki * dd.y;
         sm.z = al * sm.z + ki * dd.z;
@@ -670,6 +713,12 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
     if (lc < D) return kh * D + lc;
     if (lc < 2 * D) return Hk * D + kh * D + (lc - D);
     return 2 * Hk * D + kh * G * D + (lc - 2 * D);
+  };
+  // Position in a token's row of xs of item-local channel lc: q and k in row-block order.
+  auto xpos = [&](int lc) -> int {
+    if (lc < D) return qk_pos<D, NT>(lc);
+    if (lc < 2 * D) return D + qk_pos<D, NT>(lc - D);
+    return lc;
   };
   // First round at or after r whose item can run (rounds if none).
   auto next_valid = [&](int r, Item& it) -> int {
@@ -893,7 +942,7 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
         const float4 s4 = A::load4(raw_cs + size_t(lc) * kW);
         const float x = A::to_f(raw_x[lc]);
         const float y = silu_f(w4.x * s4.y + w4.y * s4.z + w4.z * s4.w + w4.w * x);
-        xs[lc] = y;
+        xs[xpos(lc)] = y;
         T* cs = reinterpret_cast<T*>(p.conv_pool) +
                 (size_t(it.slot) * p.conv_dim + global_channel(it.kh, lc)) * kW;
         A::store4(cs, make_float4(s4.y, s4.z, s4.w, x));
@@ -966,12 +1015,13 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
       };
       auto conv_channel = [&](int lc, float4 win, const float4& w4) {
         const int gc = global_channel(it.kh, lc);
+        const int xl = xpos(lc);
         for (int t = 0; t < k; ++t) {
-          const float x = xs[t * CHX + lc];
+          const float x = xs[t * CHX + xl];
           win = make_float4(win.y, win.z, win.w, x);
           if (VERIFY && woa)  // the raw input, an exact copy, for the deferred fold
             reinterpret_cast<T*>(woa_seq + p.woa_raw)[size_t(t) * p.conv_dim + gc] = A::from_f(x);
-          xs[t * CHX + lc] = silu_f(w4.x * win.x + w4.y * win.y + w4.z * win.z + w4.w * win.w);
+          xs[t * CHX + xl] = silu_f(w4.x * win.x + w4.y * win.y + w4.z * win.z + w4.w * win.w);
           if (VERIFY && p.conv_inter && t < k - 1) {
             T* ci = reinterpret_cast<T*>(p.conv_inter) +
                     ((size_t(it.seq) * (GDN_VERIFY_WY_TABLES_PER_LAYER - 1) + t) * p.conv_dim + gc) * kW;
@@ -991,6 +1041,7 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
         const T* pb = two ? channel_src(lc1, sb) : pa;
         load_state(lc, wina, w4a);
         if (two) load_state(lc1, winb, w4b);
+        const int xla = xpos(lc), xlb = xpos(lc1);
         for (int t0 = 0; t0 < k; t0 += kG) {
           float xa[kG], xb[kG];
 #pragma unroll
@@ -1003,11 +1054,11 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
           }
 #pragma unroll
           for (int u = 0; u < kG; ++u)
-            if (t0 + u < k) xs[(t0 + u) * CHX + lc] = xa[u];
+            if (t0 + u < k) xs[(t0 + u) * CHX + xla] = xa[u];
           if (two) {
 #pragma unroll
             for (int u = 0; u < kG; ++u)
-              if (t0 + u < k) xs[(t0 + u) * CHX + lc1] = xb[u];
+              if (t0 + u < k) xs[(t0 + u) * CHX + xlb] = xb[u];
           }
         }
         if (lc < CH) conv_channel(lc, wina, w4a);
@@ -1059,7 +1110,7 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
         float* kh_out = reinterpret_cast<float*>(woa_seq + p.woa_khat);
         for (int idx = tid; idx < k * D; idx += NT) {
           const int t = idx / D, i = idx - t * D;
-          kh_out[(size_t(t) * p.Hk + it.kh) * D + i] = xs[t * CHX + D + i];
+          kh_out[(size_t(t) * p.Hk + it.kh) * D + i] = xs[t * CHX + D + qk_pos<D, NT>(i)];
         }
         if (tid == 0 && it.kh == 0) *reinterpret_cast<int32_t*>(woa_seq) = k;
       }
@@ -1107,7 +1158,7 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
         static_assert(KMAX == 1 && !VERIFY, "verify runs in pairs of tokens");
         // slots alternate by head: no barrier separates one head's reduction reads from
         // the next's writes
-        if (token_update<D, NT, true, SR>(S, L, xs, xs + D, xs + (2 + g) * D, gate[g * 2],
+        if (token_update<D, NT, true, SR, true>(S, L, xs, xs + D, xs + (2 + g) * D, gate[g * 2],
                                           gate[g * 2 + 1], kq1,
                                           red + (hq & 1) * 2 * Map::RB * D,
                                           obuf + (hq & 1) * D, !ok, rq, rk)) {
