@@ -334,7 +334,8 @@ __device__ __forceinline__ void norm_tokens(const float* o, const float* z, int 
 // ======================================================================================
 // decode / verify
 // ======================================================================================
-template <int D, int NT, int KMAX, int STAGES, typename T, typename SH = float>
+template <int D, int NT, int KMAX, int STAGES, typename T, typename SH = float,
+          bool RAWPF = false>
 struct RecSmem {
   using Map = RecMap<D, NT>;
   // Decode prefetches the next item's raw inputs into shared memory while the current
@@ -374,14 +375,20 @@ struct RecSmem {
   static constexpr size_t kXs = kTabItem + GDN_VERIFY_WY_TABLES_PER_LAYER * 8;
   // xs: [KMAX][(2 + 2G) D] f32 = q | k | v of G heads | z of G heads, per token
   __host__ __device__ static size_t xs_bytes(int G) { return size_t(KMAX) * (2 + 2 * G) * D * 4; }
-  // raw (prefetch only): conv state [CH][4] T | conv_w [CH][4] f32 | x [KMAX][CH] T |
-  // z [KMAX][G D] T, CH = (2 + G) D
+  // RAWPF: verify prefetches each next item's raw inputs as decode does (where shared memory
+  // has room: fp16 pools, whose stages are half the size), without the conv weights (read
+  // from global, where every item of a key head finds them in L2).
+  static constexpr bool kRawPF = (KMAX > 1) && RAWPF;
+  // raw (decode, kRawPF): conv state [CH][4] T | conv_w [CH][4] f32 (decode) |
+  // x [KMAX][CH] T | z [KMAX][G D] T, CH = (2 + G) D
   __host__ __device__ static size_t raw_cs(int) { return 0; }
   __host__ __device__ static size_t raw_w(int G) { return raw_cs(G) + size_t(2 + G) * D * 4 * sizeof(T); }
-  __host__ __device__ static size_t raw_x(int G) { return raw_w(G) + size_t(2 + G) * D * 4 * 4; }
+  __host__ __device__ static size_t raw_x(int G) {
+    return raw_w(G) + (kPrefetch ? size_t(2 + G) * D * 4 * 4 : 0);
+  }
   __host__ __device__ static size_t raw_z(int G) { return raw_x(G) + size_t(KMAX) * (2 + G) * D * sizeof(T); }
   __host__ __device__ static size_t raw_bytes(int G) {
-    return kPrefetch ? raw_z(G) + size_t(KMAX) * G * D * sizeof(T) : 0;
+    return (kPrefetch || kRawPF) ? raw_z(G) + size_t(KMAX) * G * D * sizeof(T) : 0;
   }
   __host__ __device__ static size_t kRaw(int G) { return kXs + xs_bytes(G); }
   __host__ __device__ static size_t bytes(int G) { return kRaw(G) + raw_bytes(G); }
@@ -643,11 +650,11 @@ __host__ __device__ constexpr int rec_min_blocks() {
 }
 
 template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY, typename SH,
-          bool WOA = false>
+          bool WOA = false, bool RAWPF = false>
 __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX, SH>()))
     gdn_recurrent_kernel(const __grid_constant__ RecParams p) {
   using Map = RecMap<D, NT>;
-  using SL = RecSmem<D, NT, KMAX, STAGES, T, SH>;
+  using SL = RecSmem<D, NT, KMAX, STAGES, T, SH, RAWPF>;
   using A = Act<T>;
   constexpr int NWC = NT / 32;  // compute warps
   extern __shared__ __align__(128) unsigned char smem[];
@@ -746,6 +753,39 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
     if (++g == G) {
       g = 0;
       r = next_valid(r + 1, it);
+    }
+  };
+
+  // Verify with kRawPF: the raw inputs of item `it` into the raw block -- its conv state
+  // and, per token, its q | k | v raw channel ranges and its z row range -- issued by the
+  // lanes of warp 0 (lane t: token t; lanes 16..18: the three conv-state ranges).
+  auto issue_raw_verify = [&](const Item& it) {
+    static_assert(KMAX <= 16, "one lane per token");
+    const int lane = tid & 31, k = it.k;
+    // channel range seg: q [0, D), k [D, 2D), v [2D, (2 + G) D)
+    auto len = [&](int seg) { return seg < 2 ? D : G * D; };
+    if (lane == 0) {
+      mbar_arrive_expect_tx(raw_full, uint32_t(CH) * kW * sizeof(T) +
+                                          uint32_t(k) * (CH + G * D) * sizeof(T));
+      issued_s[1] = issued_s[1] + 1;
+    }
+    __syncwarp();
+    fence_proxy_async_smem();
+    if (lane < k) {
+      const T* row = reinterpret_cast<const T*>(p.qkv) + size_t(it.row0 + lane) * p.qkv_stride;
+#pragma unroll
+      for (int seg = 0; seg < 3; ++seg)
+        bulk_g2s(raw_x + size_t(lane) * CH + seg * D, row + global_channel(it.kh, seg * D),
+                 uint32_t(len(seg)) * sizeof(T), raw_full);
+      bulk_g2s(raw_z + size_t(lane) * G * D,
+               reinterpret_cast<const T*>(p.z) + size_t(it.row0 + lane) * p.z_stride + it.kh * G * D,
+               uint32_t(G) * D * sizeof(T), raw_full);
+    } else if (lane >= 16 && lane < 19) {
+      const int seg = lane - 16;
+      bulk_g2s(raw_cs + size_t(seg) * D * kW,
+               reinterpret_cast<const T*>(p.conv_pool) +
+                   (size_t(it.slot) * p.conv_dim + global_channel(it.kh, seg * D)) * kW,
+               uint32_t(len(seg)) * kW * sizeof(T), raw_full);
     }
   };
 
@@ -910,6 +950,7 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
   Item nxt;
   int r_next = next_valid(0, nxt);
   if (SL::kPrefetch && r_next < rounds) load_scalars(nxt);
+  if (SL::kRawPF && L.warp == 0 && r_next < rounds) issue_raw_verify(nxt);
   while (r_next < rounds) {
     const Item it = nxt;
     const int k = it.k;
@@ -974,7 +1015,13 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
       if (tid == 0) mbar_arrive(raw_empty);
       if (r_next < rounds) load_scalars(nxt);
     } else {
-      named_sync(1, NT);  // every warp is done with the previous item's xs, gates, tables
+      // every warp is done with the previous item's xs, gates, tables (and, kRawPF, this
+      // item's raw block has landed)
+      const bool rok = !SL::kRawPF || mbar_wait_bounded(raw_full, uint32_t(m) & 1u);
+      if (named_sync_or(1, NT, !rok)) {
+        drain(q);
+        return;
+      }
       // Every load of the prologue is issued before any of its results is used: the
       // item's table entries and gate inputs, then a thread's channels two at a time.
       static_assert(NT >= KMAX * kMaxG, "one thread per (token, value head) for the gates");
@@ -1032,6 +1079,22 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
           A::store4(reinterpret_cast<T*>(p.conv_pool) + (size_t(it.slot) * p.conv_dim + gc) * kW,
                     win);
       };
+      if constexpr (SL::kRawPF) {
+        // the raw inputs are in the raw block: z staged as f32; each conv channel's raw
+        // column parked in xs, then run with the weights (global, L2) and its conv state
+        for (int lc = tid; lc < CHX; lc += NT) {
+          if (lc >= CH) {
+            for (int t = 0; t < k; ++t) xs[t * CHX + lc] = A::to_f(raw_z[t * G * D + (lc - CH)]);
+            continue;
+          }
+          const float4 w4 =
+              *reinterpret_cast<const float4*>(p.conv_w + size_t(global_channel(it.kh, lc)) * kW);
+          const float4 win = A::load4(raw_cs + size_t(lc) * kW);
+          const int xl = xpos(lc);
+          for (int t = 0; t < k; ++t) xs[t * CHX + xl] = A::to_f(raw_x[t * CH + lc]);
+          conv_channel(lc, win, w4);
+        }
+      } else
       for (int lc = tid; lc < CHX; lc += 2 * NT) {
         const int lc1 = lc + NT;
         const bool two = lc1 < CHX;
@@ -1074,6 +1137,9 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
         if (VERIFY && woa) reinterpret_cast<float*>(woa_seq + p.woa_alpha)[t * p.Hv + it.kh * G + g] = al;
       }
       named_sync(1, NT);
+      // kRawPF: every thread is done with the raw block; the next item's inputs stream in
+      // while this item's heads run
+      if (SL::kRawPF && L.warp == 0 && r_next < rounds) issue_raw_verify(nxt);
     }
     ++m;
     float rq = 1.f, rk = 1.f, kq1 = 0.f;  // decode: L2 scales of q and k, q_hat.k_hat
@@ -1178,10 +1244,10 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
 }
 
 template <typename T, int D, int NT, int KMAX, int STAGES, bool VERIFY, typename SH,
-          bool WOA = false>
+          bool WOA = false, bool RAWPF = false>
 cudaError_t launch_rec(const RecParams& p, cudaStream_t stream) {
-  using SL = RecSmem<D, NT, KMAX, STAGES, T, SH>;
-  auto kern = gdn_recurrent_kernel<T, D, NT, KMAX, STAGES, VERIFY, SH, WOA>;
+  using SL = RecSmem<D, NT, KMAX, STAGES, T, SH, RAWPF>;
+  auto kern = gdn_recurrent_kernel<T, D, NT, KMAX, STAGES, VERIFY, SH, WOA, RAWPF>;
   const size_t smem = SL::bytes(p.G);
   if (smem > kMaxSmemPerBlock) return cudaErrorInvalidConfiguration;  // shape not supported
   cudaError_t e =
@@ -1203,6 +1269,16 @@ cudaError_t launch_rec(const RecParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// Verify prefetches raw inputs on fp16 pools where the raw block fits beside the rest.
+template <typename T, int D, int NT, typename SH>
+cudaError_t launch_verify(const RecParams& p, cudaStream_t stream) {
+  if constexpr (sizeof(SH) == 2) {
+    if (RecSmem<D, NT, GDN_VERIFY_K_MAX, 2, T, SH, true>::bytes(p.G) <= kMaxSmemPerBlock)
+      return launch_rec<T, D, NT, GDN_VERIFY_K_MAX, 2, true, SH, false, true>(p, stream);
+  }
+  return launch_rec<T, D, NT, GDN_VERIFY_K_MAX, 2, true, SH>(p, stream);
+}
+
 template <typename T, typename SH>
 cudaError_t launch_rec_typed(const RecParams& p, int D, bool verify, cudaStream_t stream) {
   if (D == 128) {
@@ -1212,10 +1288,10 @@ cudaError_t launch_rec_typed(const RecParams& p, int D, bool verify, cudaStream_
     // ms per 128-sequence step; verify with eight 0.469 -> 0.523 ms).
     // Decode on fp16 pools: two stages of 32 KiB tiles, so two CTAs share an SM.
     constexpr int kDecodeStages = sizeof(SH) == 2 ? 2 : 3;
-    if (verify) return launch_rec<T, 128, 512, GDN_VERIFY_K_MAX, 2, true, SH>(p, stream);
+    if (verify) return launch_verify<T, 128, 512, SH>(p, stream);
     return launch_rec<T, 128, 256, 1, kDecodeStages, false, SH>(p, stream);
   }
-  if (verify) return launch_rec<T, 16, 64, GDN_VERIFY_K_MAX, 2, true, SH>(p, stream);
+  if (verify) return launch_verify<T, 16, 64, SH>(p, stream);
   return launch_rec<T, 16, 64, 1, 3, false, SH>(p, stream);
 }
 
