@@ -376,8 +376,8 @@ struct RecSmem {
   // xs: [KMAX][(2 + 2G) D] f32 = q | k | v of G heads | z of G heads, per token
   __host__ __device__ static size_t xs_bytes(int G) { return size_t(KMAX) * (2 + 2 * G) * D * 4; }
   // RAWPF: verify prefetches each next item's raw inputs as decode does (where shared memory
-  // has room: fp16 pools, whose stages are half the size), without the conv weights (read
-  // from global, where every item of a key head finds them in L2).
+  // has room beside the stages), without the conv weights (read from global, where every
+  // item of a key head finds them in L2).
   static constexpr bool kRawPF = (KMAX > 1) && RAWPF;
   // raw (decode, kRawPF): conv state [CH][4] T | conv_w [CH][4] f32 (decode) |
   // x [KMAX][CH] T | z [KMAX][G D] T, CH = (2 + G) D
@@ -1269,12 +1269,17 @@ cudaError_t launch_rec(const RecParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// Verify prefetches raw inputs on fp16 pools where the raw block fits beside the rest.
+// Verify prefetches raw inputs where the raw block fits beside the rest: fp16 pools with
+// two stages; f32 pools with one (its tile is issued a whole head ahead, after the
+// previous head's first barrier, which measured as enough).
 template <typename T, int D, int NT, typename SH>
 cudaError_t launch_verify(const RecParams& p, cudaStream_t stream) {
   if constexpr (sizeof(SH) == 2) {
     if (RecSmem<D, NT, GDN_VERIFY_K_MAX, 2, T, SH, true>::bytes(p.G) <= kMaxSmemPerBlock)
       return launch_rec<T, D, NT, GDN_VERIFY_K_MAX, 2, true, SH, false, true>(p, stream);
+  } else {
+    if (RecSmem<D, NT, GDN_VERIFY_K_MAX, 1, T, SH, true>::bytes(p.G) <= kMaxSmemPerBlock)
+      return launch_rec<T, D, NT, GDN_VERIFY_K_MAX, 1, true, SH, false, true>(p, stream);
   }
   return launch_rec<T, D, NT, GDN_VERIFY_K_MAX, 2, true, SH>(p, stream);
 }
@@ -1298,7 +1303,11 @@ cudaError_t launch_rec_typed(const RecParams& p, int D, bool verify, cudaStream_
 // The write-on-accept verify (f32 state pools only).
 template <typename T>
 cudaError_t launch_rec_woa(const RecParams& p, int D, cudaStream_t stream) {
-  if (D == 128) return launch_rec<T, 128, 512, GDN_VERIFY_K_MAX, 2, true, float, true>(p, stream);
+  if (D == 128) {
+    if (RecSmem<128, 512, GDN_VERIFY_K_MAX, 1, T, float, true>::bytes(p.G) <= kMaxSmemPerBlock)
+      return launch_rec<T, 128, 512, GDN_VERIFY_K_MAX, 1, true, float, true, true>(p, stream);
+    return launch_rec<T, 128, 512, GDN_VERIFY_K_MAX, 2, true, float, true>(p, stream);
+  }
   return launch_rec<T, 16, 64, GDN_VERIFY_K_MAX, 2, true, float, true>(p, stream);
 }
 
