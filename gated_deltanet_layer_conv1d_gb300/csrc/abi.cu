@@ -580,9 +580,12 @@ gdn_status gdn_gated_rmsnorm_sigmoid(const float* o, const void* z, int64_t z_st
                             GDN_NORM_GATE_SIGMOID, y, stream);
 }
 
-gdn_status gdn_proj_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
-                         int64_t ldc, int32_t M, int32_t N, int32_t K, int32_t* status_dev,
-                         gdn_stream_t stream) {
+namespace {
+// b_weights: B is a weight matrix no kernel writes (in_proj / out_proj), which the GEMM
+// fetches before the previous kernel in the stream has finished.
+gdn_status proj_gemm_impl(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                          int64_t ldc, int32_t M, int32_t N, int32_t K, int32_t* status_dev,
+                          gdn_stream_t stream, bool b_weights) {
   if (M < 0 || N < 8 || K < 8 || N % 8 != 0 || K % 8 != 0 || lda < K || ldb < K || ldc < N)
     return GDN_ERR_INVALID_ARGUMENT;
   if (M == 0) return GDN_OK;
@@ -601,8 +604,16 @@ gdn_status gdn_proj_gemm(const void* A, int64_t lda, const void* B, int64_t ldb,
   p.M = M;
   p.N = N;
   p.K = K;
+  p.b_weights = b_weights ? 1 : 0;
   p.status = status_dev;
   return launch_proj(p, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+}  // namespace
+
+gdn_status gdn_proj_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                         int64_t ldc, int32_t M, int32_t N, int32_t K, int32_t* status_dev,
+                         gdn_stream_t stream) {
+  return proj_gemm_impl(A, lda, B, ldb, C, ldc, M, N, K, status_dev, stream, false);
 }
 
 int32_t gdn_in_proj_width(const gdn_dims* dims) {
@@ -617,8 +628,8 @@ gdn_status gdn_in_proj(const gdn_dims* dims, int32_t hidden_size, const void* hi
   GDN_TRY(check_dims(dims));
   if (T < 0) return GDN_ERR_INVALID_ARGUMENT;
   const int32_t width = gdn_in_proj_width(dims);
-  return gdn_proj_gemm(hidden, hidden_stride, w_in, hidden_size, out, width, T, width,
-                       hidden_size, status_dev, stream);
+  return proj_gemm_impl(hidden, hidden_stride, w_in, hidden_size, out, width, T, width,
+                        hidden_size, status_dev, stream, true);
 }
 
 gdn_status gdn_out_proj(const gdn_dims* dims, int32_t hidden_size, const void* y, int32_t T,
@@ -627,8 +638,8 @@ gdn_status gdn_out_proj(const gdn_dims* dims, int32_t hidden_size, const void* y
   GDN_TRY(check_dims(dims));
   if (T < 0) return GDN_ERR_INVALID_ARGUMENT;
   const int32_t vd = dims->n_v_heads * dims->d_v;
-  return gdn_proj_gemm(y, vd, w_out, vd, out, out_stride, T, hidden_size, vd, status_dev,
-                       stream);
+  return proj_gemm_impl(y, vd, w_out, vd, out, out_stride, T, hidden_size, vd, status_dev,
+                        stream, true);
 }
 
 gdn_status gdn_selftest_wait(int64_t budget_ns, int32_t* status_dev, gdn_stream_t stream) {

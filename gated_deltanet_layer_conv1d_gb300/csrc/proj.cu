@@ -28,10 +28,11 @@
 // pair kernel further down: 256 x 256 tiles, tcgen05.mma.cta_group::2).
 //
 // Calls with fewer tiles than SMs (a decode step's 128 tokens) split K instead: a cluster
-// of `splits` CTAs per tile, each over its own run of K blocks, leaves its f32 partial
-// tile in shared memory; after a cluster barrier every CTA sums one slice of the tile's
-// rows over all partials (distributed shared memory reads) and stores it, and a second
-// cluster barrier keeps every partial alive until its readers are done.
+// of `splits` CTAs per tile, each over its own run of K blocks.  Once every CTA of the
+// cluster is past its main loop (a cluster barrier), each writes every row of its f32
+// partial tile from TMEM straight into the shared memory of the CTA that owns that row's
+// slice (distributed shared memory stores, no round trip); after a second cluster barrier
+// every CTA sums its slice over the partials locally and stores it.
 //
 // Every wait is bounded: a wait that runs out sets a shared abort flag, every role leaves
 // its loop when it sees the flag, the producer waits for the copies it issued, the issuer
@@ -64,9 +65,10 @@ struct ProjCfg {
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kBytes = kAbort + 4 + 1024;  // + slack to align the base
   static constexpr uint32_t kTmemCols = 2u * BN < 32u ? 32u : 2u * BN;
-  // split-K partial tile: f32 [128][BN + 4] over the stage ring (drained by then)
+  // split-K partial rows: f32 [splits][rows][BN + 4] (splits * rows <= 128 + 7) over the
+  // stage ring (drained by then)
   static constexpr int kRedStride = BN + 4;
-  static_assert(uint32_t(kBM) * kRedStride * 4 <= kBar, "the partial tile fits the ring");
+  static_assert(uint32_t(kBM + 7) * kRedStride * 4 <= kBar, "the partial rows fit the ring");
   static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "M = 128 MMA: N in 16..256, step 16");
   static_assert((kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation: a power of two");
 };
@@ -106,18 +108,6 @@ __device__ __forceinline__ void cluster_sync() {
   __syncwarp();
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// 16 bytes of CTA `rank`'s shared memory at the offset `local` has in this CTA's.
-__device__ __forceinline__ float4 ld_cluster_f4(const void* local, uint32_t rank) {
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(ra)
-               : "memory");
-  return v;
 }
 
 // The work of one CTA: tiles first, first + stride, ... below end, each over the K blocks
@@ -194,22 +184,51 @@ __global__ void __launch_bounds__(kProjThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
+  // Every thread but the producer waits for the previous kernel in the stream at once (the
+  // epilogue's stores must not overtake its reads); the producer first fetches weights.
+  const bool producer = warp == 0 && lane == 0;
+  if (!producer) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 
-  if (warp == 0 && lane == 0) {
+  if (producer) {
     // ---------------------------------------------------------------- TMA producer
     int s = 0;
     uint32_t ph = 0;
     uint32_t issued_mask = 0, issued_par = 0;  // per stage: a copy issued, its phase parity
     bool ok = true;
+    // A weight operand: the B tiles of the first `pre` stages are on their way before the
+    // wait (their stages expect both halves); every A tile waits.
+    int pre = 0;
+    if (p.b_weights) {
+      int t = wk.first, kb = wk.kb0;
+      for (; pre < S && t < wk.end; ++pre) {
+        mbar_arrive_expect_tx(&full[pre], C::kStageBytes);
+        tma_load_2d(sm + uint32_t(pre) * C::kStageBytes + kATileBytes, &map_b, kb * kBK,
+                    tile_n(p, t, tiles_m, tiles_n) * BN, &full[pre]);
+        if (++kb == wk.kb1) {
+          kb = wk.kb0;
+          t += wk.stride;
+        }
+      }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    int idx = 0;  // loads issued, in order
     for (int t = wk.first; t < wk.end && ok; t += wk.stride) {
       const int m0 = tile_m(p, t, tiles_m, tiles_n) * kBM;
       const int n0 = tile_n(p, t, tiles_m, tiles_n) * BN;
-      for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
-        if (!wait_or_abort(&empty[s], ph ^ 1u, abort)) { ok = false; break; }
+      for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++idx) {
         unsigned char* st = sm + uint32_t(s) * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-        tma_load_2d(st, &map_a, kb * kBK, m0, &full[s]);
-        tma_load_2d(st + kATileBytes, &map_b, kb * kBK, n0, &full[s]);
+        if (idx < pre) {  // stage s = idx: fresh, its B half already issued
+          tma_load_2d(st, &map_a, kb * kBK, m0, &full[s]);
+        } else {
+          if (!wait_or_abort(&empty[s], ph ^ 1u, abort)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+          tma_load_2d(st, &map_a, kb * kBK, m0, &full[s]);
+          tma_load_2d(st + kATileBytes, &map_b, kb * kBK, n0, &full[s]);
+        }
         issued_mask |= 1u << s;
         issued_par = (issued_par & ~(1u << s)) | (ph << s);
         if (++s == S) { s = 0; ph ^= 1u; }
@@ -220,6 +239,7 @@ __global__ void __launch_bounds__(kProjThreads, 1)
       for (int q = 0; q < S; ++q)
         if (issued_mask & (1u << q)) mbar_wait_bounded(&full[q], (issued_par >> q) & 1u);
     }
+
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc = tc::idesc_bf16(kBM, BN);
@@ -263,21 +283,7 @@ __global__ void __launch_bounds__(kProjThreads, 1)
       const int n0 = tile_n(p, t, tiles_m, tiles_n) * BN;
       if (!wait_or_abort(&tfull[acc], aph, abort)) break;
       tc::fence_after_sync();
-      if (split) {
-        // the partial tile, row 32q + lane of this thread, into the (drained) stage ring
-        float* red = reinterpret_cast<float*>(sm) + (32 * q + lane) * C::kRedStride;
-        const uint32_t taddr = tmem + (uint32_t(32 * q) << 16);
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          float v[32];
-          tc::ld32(taddr + uint32_t(c0), v);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<float4*>(red + c0 + 4 * j) =
-                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        }
-        break;  // one tile per CTA
-      }
+      if (split) break;  // one tile per CTA: its partial stays in TMEM for now
       const int row = m0 + 32 * q + lane;
       __nv_bfloat16* orow = out + size_t(row) * size_t(p.ldc) + n0;
       const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc * BN);
@@ -308,53 +314,56 @@ __global__ void __launch_bounds__(kProjThreads, 1)
 
   if (split) {
     // Every thread of every CTA of the cluster passes both barriers, aborted or not.
-    cluster_sync();  // every partial tile is in its CTA's shared memory
+    // Rows are dealt to the CTAs in slices of `rows`; each CTA's partial row goes straight
+    // from TMEM into the shared memory of the CTA that sums its slice, at [from rank][row
+    // in slice] of a buffer over that CTA's (drained) stage ring.
+    const int rows = (kBM + p.splits - 1) / p.splits;
+    float* buf = reinterpret_cast<float*>(sm);
+    cluster_sync();  // every CTA is past its main loop: every stage ring is free
+    if (warp >= 2) {
+      const int q = warp & 3, row = 32 * q + lane, owner = row / rows;
+      uint32_t dst = 0;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                   : "=r"(dst)
+                   : "r"(smem_u32(buf + (wk.rank * rows + (row - owner * rows)) * C::kRedStride)),
+                     "r"(uint32_t(owner)));
+      tc::fence_after_sync();
+      const uint32_t taddr = tmem + (uint32_t(32 * q) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tc::ld32(taddr + uint32_t(c0), v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
+                       ::"r"(dst + uint32_t(4 * (c0 + 4 * j))), "f"(v[4 * j]), "f"(v[4 * j + 1]),
+                         "f"(v[4 * j + 2]), "f"(v[4 * j + 3])
+                       : "memory");
+      }
+    }
+    cluster_sync();  // every slice has all its partial rows
     if (warp >= 2) {
       const int t = wk.first;
       const int m0 = tile_m(p, t, tiles_m, tiles_n) * kBM;
       const int n0 = tile_n(p, t, tiles_m, tiles_n) * BN;
-      const int rows = (kBM + p.splits - 1) / p.splits;
-      const int r0 = wk.rank * rows, r1 = r0 + rows < kBM ? r0 + rows : kBM;
-      const float* red = reinterpret_cast<const float*>(sm);
+      const int r0 = wk.rank * rows, nr = (r0 + rows < kBM ? r0 + rows : kBM) - r0;
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C);
       constexpr int kQ = BN / 4;  // float4 groups per row
-      constexpr int kG = 16;      // groups per thread per pass: 16 remote loads in flight
-      constexpr int kStep = kProjThreads - 64;
-      const int groups = (r1 - r0) * kQ;
-      for (int e0 = int(threadIdx.x) - 64; e0 < groups; e0 += kG * kStep) {
-        float4 acc[kG];
-#pragma unroll
-        for (int g = 0; g < kG; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q = 0; q < p.splits; ++q) {
-          float4 x[kG];
-#pragma unroll
-          for (int g = 0; g < kG; ++g) {
-            const int e = e0 + g * kStep;
-            if (e < groups)
-              x[g] = ld_cluster_f4(red + (r0 + e / kQ) * C::kRedStride + 4 * (e % kQ),
-                                   uint32_t(q));
-          }
-#pragma unroll
-          for (int g = 0; g < kG; ++g) {
-            if (e0 + g * kStep < groups) {
-              acc[g].x += x[g].x;
-              acc[g].y += x[g].y;
-              acc[g].z += x[g].z;
-              acc[g].w += x[g].w;
-            }
-          }
+      for (int e = int(threadIdx.x) - 64; e < nr * kQ; e += kProjThreads - 64) {
+        const int lr = e / kQ, c = 4 * (e % kQ);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int f = 0; f < p.splits; ++f) {
+          const float4 x = *reinterpret_cast<const float4*>(buf + (f * rows + lr) * C::kRedStride + c);
+          acc.x += x.x;
+          acc.y += x.y;
+          acc.z += x.z;
+          acc.w += x.w;
         }
-#pragma unroll
-        for (int g = 0; g < kG; ++g) {
-          const int e = e0 + g * kStep;
-          const int r = r0 + e / kQ, c = 4 * (e % kQ);
-          if (e < groups && m0 + r < p.M && n0 + c < p.N)
-            *reinterpret_cast<uint2*>(out + size_t(m0 + r) * size_t(p.ldc) + n0 + c) =
-                make_uint2(pack_bf16x2(acc[g].x, acc[g].y), pack_bf16x2(acc[g].z, acc[g].w));
-        }
+        if (m0 + r0 + lr < p.M && n0 + c < p.N)
+          *reinterpret_cast<uint2*>(out + size_t(m0 + r0 + lr) * size_t(p.ldc) + n0 + c) =
+              make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
       }
     }
-    cluster_sync();  // no CTA leaves while another still reads its partial
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -481,6 +490,8 @@ __global__ void __launch_bounds__(kProjThreads, 1)
   cluster_sync();  // both CTAs' barriers exist before either signals the other's
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
+  pdl_wait();  // everything below may read what the previous kernel in the stream wrote
+  pdl_launch_dependents();
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -635,22 +646,11 @@ cudaError_t launch_bn(const ProjParams& p, cudaStream_t stream) {
   const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
   if (p.splits <= 1) {
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    kern<<<grid, kProjThreads, C::kBytes, stream>>>(ma, mb, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(unsigned(grid)), dim3(kProjThreads), C::kBytes, stream, 1u, ma,
+                      mb, p);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(tiles * p.splits));
-  cfg.blockDim = dim3(kProjThreads);
-  cfg.dynamicSmemBytes = C::kBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(p.splits);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, p);
+  return launch_pdl(kern, dim3(unsigned(tiles * p.splits)), dim3(kProjThreads), C::kBytes,
+                    stream, unsigned(p.splits), ma, mb, p);
 }
 
 // How many clusters of `s` CTAs of the BN-wide kernel the current GPU holds at once (a
@@ -757,19 +757,8 @@ cudaError_t launch_pair(const ProjParams& p, cudaStream_t stream) {
   const int max_pairs = max_active_pairs();
   if (max_pairs <= 0) return cudaErrorInvalidConfiguration;
   const int pairs = tiles < max_pairs ? tiles : max_pairs;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(2 * pairs));
-  cfg.blockDim = dim3(kProjThreads);
-  cfg.dynamicSmemBytes = C::kBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, p);
+  return launch_pdl(kern, dim3(unsigned(2 * pairs)), dim3(kProjThreads), C::kBytes, stream, 2u,
+                    ma, mb, p);
 }
 
 }  // namespace

@@ -707,7 +707,11 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
     issued_s[1] = 0;
     fence_mbar_init();
   }
-  for (int j = tid; j < D; j += kThreads) nw_s[j] = p.norm_w[j];
+  for (int j = tid; j < D; j += kThreads) nw_s[j] = p.norm_w[j];  // weights: no kernel writes them
+  // Everything below may read what the previous kernel in the stream wrote (slots, tables,
+  // states, inputs); once past that, the next kernel may start on SMs this grid leaves.
+  pdl_wait();
+  pdl_launch_dependents();
   for (int i = tid; i < p.n; i += kThreads) {
     slots_s[i] = p.slots[i];
     valid_s[i] = seq_check<VERIFY>(p, i);
@@ -1265,8 +1269,8 @@ cudaError_t launch_rec(const RecParams& p, cudaStream_t stream) {
   }
   const int cap = sm_count() * per_sm;
   const int P = p.n_items < cap ? p.n_items : cap;
-  kern<<<P, rec_threads<NT, KMAX>(), smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(unsigned(P)), dim3(unsigned(rec_threads<NT, KMAX>())), smem, stream,
+                    1u, p);
 }
 
 // Verify prefetches raw inputs where the raw block fits beside the rest: fp16 pools with

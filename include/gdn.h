@@ -23,6 +23,15 @@
  *     caller's device status word `*status_dev` -- the first error wins, the kernel
  *     skips the affected work and returns normally; it never traps.  The caller zeroes
  *     the word before the call and reads it afterwards.
+ *   - Stream order: the decode / verify kernels and the projection GEMMs are launched with
+ *     programmatic stream serialization.  Each one lets the next kernel in the stream
+ *     start on the SMs it leaves once it has itself waited for the kernel before it, and
+ *     reads nothing another kernel may have written until that kernel has finished --
+ *     except read-only weights: the gated-norm weight (decode / verify) and the weight
+ *     operand of gdn_in_proj / gdn_out_proj, which may be fetched while the previous
+ *     kernel in the stream is still running.  A caller that rewrites those weights does so
+ *     with a kernel or copy that is not the last work before the call (any kernel of its
+ *     own does: it does not trigger early) -- in practice nothing changes for a caller.
  *   - Pointers marked "device" are CUDA device (or managed) memory; "host" is host memory.
  *   - Row strides are in ELEMENTS of the activation dtype.
  *   - Supported shapes: (d_k, d_v) in {(16, 16), (128, 128)}, d_conv = 4,
