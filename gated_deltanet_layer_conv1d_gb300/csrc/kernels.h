@@ -166,7 +166,7 @@ struct ProjParams {
   void* C;
   int64_t ldc;
   int32_t M, N, K;
-  int32_t bn;      // output tile width 256 / 128 / 64; 0: the launcher picks bn and splits
+  int32_t bn;      // output tile width 256 / 128 / 96 / 64; 0: the launcher picks bn and splits
   int32_t splits;  // CTAs (one cluster) per tile splitting K, 1..8
   int32_t n_fast;  // tile order: 1 walks N fastest, 0 walks M fastest
   // 1: B is a weight matrix that no kernel writes, so its first tiles are fetched before

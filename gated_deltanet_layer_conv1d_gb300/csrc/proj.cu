@@ -64,7 +64,9 @@ struct ProjCfg {
   static constexpr uint32_t kTmemSlot = kBar + 8u * uint32_t(2 * kStages + 5);
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kBytes = kAbort + 4 + 1024;  // + slack to align the base
-  static constexpr uint32_t kTmemCols = 2u * BN < 32u ? 32u : 2u * BN;
+  // two accumulators of BN columns, rounded up to the power of two TMEM allocates
+  static constexpr uint32_t kTmemCols =
+      2u * BN <= 32u ? 32u : (2u * BN <= 64u ? 64u : (2u * BN <= 128u ? 128u : (2u * BN <= 256u ? 256u : 512u)));
   // split-K partial rows: f32 [splits][rows][BN + 4] (splits * rows <= 128 + 7) over the
   // stage ring (drained by then)
   static constexpr int kRedStride = BN + 4;
@@ -657,10 +659,10 @@ cudaError_t launch_bn(const ProjParams& p, cudaStream_t stream) {
 // cluster stays inside one GPC, so this is below SMs / s); cached per device and shape.
 constexpr int kProjMaxDevices = 64;
 int max_active_clusters(int bn, int s) {
-  static std::atomic<int> cache[kProjMaxDevices][3][9];
+  static std::atomic<int> cache[kProjMaxDevices][4][9];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kProjMaxDevices) return -1;
-  const int i = bn == 256 ? 0 : (bn == 128 ? 1 : 2);
+  const int i = bn == 256 ? 0 : (bn == 128 ? 1 : (bn == 96 ? 3 : 2));
   int cached = cache[dev][i][s].load(std::memory_order_relaxed);
   if (cached == 0) {
     int n = 0;
@@ -691,6 +693,14 @@ int max_active_clusters(int bn, int s) {
                                  int(ProjCfg<128>::kBytes));
         if (e == cudaSuccess)
           e = cudaOccupancyMaxActiveClusters(&n, gdn_proj_gemm_kernel<128>, &cfg);
+        break;
+      case 96:
+        cfg.dynamicSmemBytes = ProjCfg<96>::kBytes;
+        e = cudaFuncSetAttribute(gdn_proj_gemm_kernel<96>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(ProjCfg<96>::kBytes));
+        if (e == cudaSuccess)
+          e = cudaOccupancyMaxActiveClusters(&n, gdn_proj_gemm_kernel<96>, &cfg);
         break;
       default:
         cfg.dynamicSmemBytes = ProjCfg<64>::kBytes;
@@ -781,7 +791,7 @@ ProjShape proj_shape(int M, int N, int K) {
       best_cost = cost;
     }
   };
-  for (int bn : {256, 128, 64}) {
+  for (int bn : {256, 128, 96, 64}) {
     const long tiles = long(tm) * ((N + bn - 1) / bn);
     consider(bn, 1, ((tiles + sms - 1) / sms) * (kBM + bn) * long(kblocks));
     for (int s = 2; s <= 8 && tiles * s <= sms; ++s) {
@@ -808,6 +818,7 @@ cudaError_t launch_proj(const ProjParams& p_in, cudaStream_t stream) {
   switch (p.bn) {
     case 256: return launch_bn<256>(p, stream);
     case 128: return launch_bn<128>(p, stream);
+    case 96: return launch_bn<96>(p, stream);
     case 64: return launch_bn<64>(p, stream);
     default: return cudaErrorInvalidValue;
   }
