@@ -913,10 +913,10 @@ def main():
     ap.add_argument("--no-modes", action="store_true", help="skip the verify / prefill lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--profile", nargs="?", const="decode", default=None,
-                    choices=["decode", "verify", "verify-small", "prefill", "mixed", "proj",
-                             "layer", "fold", "decode16", "woa"],
+                    choices=["decode", "verify", "verify-small", "verify16", "verify16-small",
+                             "prefill", "mixed", "proj", "layer", "fold", "decode16", "woa"],
                     help="only one timed loop of one mode (for profiler captures); "
-                         "verify-small runs 32 sequences")
+                         "verify-small runs 32 sequences; verify16 runs on fp16 state pools")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -962,14 +962,16 @@ def main():
         if rank == 0:
             print(json.dumps({"profile_run": "layer", "steps": r["steps"]}))
         return
-    if args.profile in ("verify", "verify-small", "prefill", "mixed"):
+    if args.profile in ("verify", "verify-small", "verify16", "verify16-small", "prefill",
+                        "mixed"):
         if args.profile == "prefill":
             r = prefill_mode(device, args.steps, tc_peak, warmup=args.warmup)
         elif args.profile == "mixed":
             r = mixed_mode(device, args.steps, hbm_peak, tc_peak)
         else:
             r = verify_mode(device, args.steps, hbm_peak, warmup=args.warmup,
-                            n=32 if args.profile == "verify-small" else N_SEQ)
+                            n=32 if args.profile.endswith("-small") else N_SEQ,
+                            h16=args.profile.startswith("verify16"))
         if rank == 0:
             out = {"profile_run": args.profile, "ms_per_step": r["ms_per_step"]}
             if "parts" in r:

@@ -28,11 +28,12 @@
 // pair kernel further down: 256 x 256 tiles, tcgen05.mma.cta_group::2).
 //
 // Calls with fewer tiles than SMs (a decode step's 128 tokens) split K instead: a cluster
-// of `splits` CTAs per tile, each over its own run of K blocks.  Once every CTA of the
-// cluster is past its main loop (a cluster barrier), each writes every row of its f32
-// partial tile from TMEM straight into the shared memory of the CTA that owns that row's
-// slice (distributed shared memory stores, no round trip); after a second cluster barrier
-// every CTA sums its slice over the partials locally and stores it.
+// of `splits` CTAs per tile, each over its own run of K blocks.  Each CTA keeps an inbox
+// beside its stage ring for the partial rows of the slice of the tile it sums; as soon as
+// its accumulator is complete it writes every row of its f32 partial tile from TMEM into
+// the inbox of the CTA that owns the row (remote async stores that complete on that CTA's
+// inbox barrier; its own rows with plain stores), and every CTA sums its slice once its
+// barrier has counted every peer's bytes -- no cluster barrier after the main loop.
 //
 // Every wait is bounded: a wait that runs out sets a shared abort flag, every role leaves
 // its loop when it sees the flag, the producer waits for the copies it issued, the issuer
@@ -54,23 +55,27 @@ constexpr int kBK = 64;                     // one 128-byte swizzle row of bf16
 constexpr int kProjThreads = 192;
 constexpr uint32_t kATileBytes = kBM * kBK * 2;
 
-template <int BN>
+template <int BN, bool SPLIT = false>
 struct ProjCfg {
   static constexpr uint32_t kBTileBytes = uint32_t(BN) * kBK * 2;
   static constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
-  static constexpr int kStages = int((196u * 1024u) / kStageBytes);
-  static constexpr uint32_t kBar = uint32_t(kStages) * kStageBytes;
-  // full[S], empty[S], tfull[2], tempty[2], drain; then the TMEM slot and the abort flag
-  static constexpr uint32_t kTmemSlot = kBar + 8u * uint32_t(2 * kStages + 5);
+  // split-K inbox: f32 [splits][rows][BN + 4] (splits * rows <= 128 + 7): the partial rows
+  // of this CTA's slice from every CTA of the cluster, its own included
+  static constexpr int kRedStride = BN + 4;
+  static constexpr uint32_t kInbox =
+      SPLIT ? ((uint32_t(kBM + 7) * kRedStride * 4 + 1023u) / 1024u) * 1024u : 0u;
+  static constexpr int kStages = int((196u * 1024u - kInbox) / kStageBytes);
+  static constexpr uint32_t kRing = uint32_t(kStages) * kStageBytes;
+  static constexpr uint32_t kBar = kRing + kInbox;
+  // full[S], empty[S], tfull[2], tempty[2], drain, inbox; then the TMEM slot and the abort
+  // flag
+  static constexpr uint32_t kTmemSlot = kBar + 8u * uint32_t(2 * kStages + 6);
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kBytes = kAbort + 4 + 1024;  // + slack to align the base
   // two accumulators of BN columns, rounded up to the power of two TMEM allocates
   static constexpr uint32_t kTmemCols =
       2u * BN <= 32u ? 32u : (2u * BN <= 64u ? 64u : (2u * BN <= 128u ? 128u : (2u * BN <= 256u ? 256u : 512u)));
-  // split-K partial rows: f32 [splits][rows][BN + 4] (splits * rows <= 128 + 7) over the
-  // stage ring (drained by then)
-  static constexpr int kRedStride = BN + 4;
-  static_assert(uint32_t(kBM + 7) * kRedStride * 4 <= kBar, "the partial rows fit the ring");
+  static_assert(kStages >= 3, "a ring of at least three stages");
   static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "M = 128 MMA: N in 16..256, step 16");
   static_assert((kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation: a power of two");
 };
@@ -142,12 +147,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int BN>
+template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(kProjThreads, 1)
     gdn_proj_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                          const __grid_constant__ CUtensorMap map_b,
                          const __grid_constant__ ProjParams p) {
-  using C = ProjCfg<BN>;
+  using C = ProjCfg<BN, SPLIT>;
   constexpr int S = C::kStages;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -157,6 +162,8 @@ __global__ void __launch_bounds__(kProjThreads, 1)
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
+  uint64_t* inbox_full = drain + 1;
+  float* inbox = reinterpret_cast<float*>(sm + C::kRing);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::kTmemSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + C::kAbort);
 
@@ -164,7 +171,9 @@ __global__ void __launch_bounds__(kProjThreads, 1)
   const int tiles_m = (p.M + kBM - 1) / kBM, tiles_n = (p.N + BN - 1) / BN;
   const int tiles = tiles_m * tiles_n, kblocks = (p.K + kBK - 1) / kBK;
   const Work wk = work_of(p, tiles, kblocks);
-  const bool split = p.splits > 1;
+  constexpr bool split = SPLIT;  // launched with p.splits > 1 in clusters of p.splits
+  const int rows = (kBM + p.splits - 1) / p.splits;  // split: rows per CTA's slice
+  const int r0 = wk.rank * rows, nr = (r0 + rows < kBM ? r0 + rows : kBM) - r0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -176,6 +185,9 @@ __global__ void __launch_bounds__(kProjThreads, 1)
       mbar_init(&tempty[b], 4);  // one arrive per epilogue warp
     }
     mbar_init(drain, 1);
+    mbar_init(inbox_full, 1);
+    // split: every other CTA of the cluster sends this CTA's nr rows of its partial tile
+    if (split) mbar_arrive_expect_tx(inbox_full, uint32_t(p.splits - 1) * nr * BN * 4);
     *abort = 0;
     fence_mbar_init();
     prefetch_map(&map_a);
@@ -186,6 +198,9 @@ __global__ void __launch_bounds__(kProjThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
+  // split: this CTA's barriers are initialised; a CTA sends to a peer only after the
+  // cluster barrier this arrive belongs to has completed
+  if (split) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   // Every thread but the producer waits for the previous kernel in the stream at once (the
   // epilogue's stores must not overtake its reads); the producer first fetches weights.
   const bool producer = warp == 0 && lane == 0;
@@ -315,55 +330,66 @@ __global__ void __launch_bounds__(kProjThreads, 1)
   }
 
   if (split) {
-    // Every thread of every CTA of the cluster passes both barriers, aborted or not.
-    // Rows are dealt to the CTAs in slices of `rows`; each CTA's partial row goes straight
-    // from TMEM into the shared memory of the CTA that sums its slice, at [from rank][row
-    // in slice] of a buffer over that CTA's (drained) stage ring.
-    const int rows = (kBM + p.splits - 1) / p.splits;
-    float* buf = reinterpret_cast<float*>(sm);
-    cluster_sync();  // every CTA is past its main loop: every stage ring is free
+    // Rows are dealt to the CTAs of the cluster in slices of `rows`.  Each epilogue thread
+    // sends its row of the partial tile from TMEM to the CTA that owns the row's slice --
+    // into slot [this rank] of that CTA's inbox, by remote async stores that complete on
+    // the owner's inbox barrier, or by plain stores into its own inbox -- and then every
+    // CTA sums its slice over the slots once its barrier says every peer's rows landed.
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // peers initialised
     if (warp >= 2) {
       const int q = warp & 3, row = 32 * q + lane, owner = row / rows;
-      uint32_t dst = 0;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-                   : "=r"(dst)
-                   : "r"(smem_u32(buf + (wk.rank * rows + (row - owner * rows)) * C::kRedStride)),
-                     "r"(uint32_t(owner)));
-      tc::fence_after_sync();
+      float* dst = inbox + (wk.rank * rows + (row - owner * rows)) * C::kRedStride;
+      const bool mine = owner == wk.rank;
+      uint32_t rdst = 0, rbar = 0;
+      if (!mine) {
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                     : "=r"(rdst) : "r"(smem_u32(dst)), "r"(uint32_t(owner)));
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                     : "=r"(rbar) : "r"(smem_u32(inbox_full)), "r"(uint32_t(owner)));
+      }
+      const bool have = !*abort;  // the accumulator is complete unless the CTA aborted
       const uint32_t taddr = tmem + (uint32_t(32 * q) << 16);
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = 0; c0 < BN && have; c0 += 32) {
         float v[32];
         tc::ld32(taddr + uint32_t(c0), v);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
-                       ::"r"(dst + uint32_t(4 * (c0 + 4 * j))), "f"(v[4 * j]), "f"(v[4 * j + 1]),
-                         "f"(v[4 * j + 2]), "f"(v[4 * j + 3])
-                       : "memory");
-      }
-    }
-    cluster_sync();  // every slice has all its partial rows
-    if (warp >= 2) {
-      const int t = wk.first;
-      const int m0 = tile_m(p, t, tiles_m, tiles_n) * kBM;
-      const int n0 = tile_n(p, t, tiles_m, tiles_n) * BN;
-      const int r0 = wk.rank * rows, nr = (r0 + rows < kBM ? r0 + rows : kBM) - r0;
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C);
-      constexpr int kQ = BN / 4;  // float4 groups per row
-      for (int e = int(threadIdx.x) - 64; e < nr * kQ; e += kProjThreads - 64) {
-        const int lr = e / kQ, c = 4 * (e % kQ);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int f = 0; f < p.splits; ++f) {
-          const float4 x = *reinterpret_cast<const float4*>(buf + (f * rows + lr) * C::kRedStride + c);
-          acc.x += x.x;
-          acc.y += x.y;
-          acc.z += x.z;
-          acc.w += x.w;
+        for (int j = 0; j < 8; ++j) {
+          if (mine) {
+            *reinterpret_cast<float4*>(dst + c0 + 4 * j) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          } else {
+            asm volatile(
+                "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], "
+                "{%1, %2, %3, %4}, [%5];"
+                ::"r"(rdst + uint32_t(4 * (c0 + 4 * j))), "f"(v[4 * j]), "f"(v[4 * j + 1]),
+                  "f"(v[4 * j + 2]), "f"(v[4 * j + 3]), "r"(rbar)
+                : "memory");
+          }
         }
-        if (m0 + r0 + lr < p.M && n0 + c < p.N)
-          *reinterpret_cast<uint2*>(out + size_t(m0 + r0 + lr) * size_t(p.ldc) + n0 + c) =
-              make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      }
+      named_sync(1, 128);  // this CTA's own rows are in its inbox
+      if (wait_or_abort(inbox_full, 0u, abort)) {
+        const int t = wk.first;
+        const int m0 = tile_m(p, t, tiles_m, tiles_n) * kBM;
+        const int n0 = tile_n(p, t, tiles_m, tiles_n) * BN;
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C);
+        constexpr int kQ = BN / 4;  // float4 groups per row
+        for (int e = int(threadIdx.x) - 64; e < nr * kQ; e += kProjThreads - 64) {
+          const int lr = e / kQ, c = 4 * (e % kQ);
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int f = 0; f < p.splits; ++f) {
+            const float4 x =
+                *reinterpret_cast<const float4*>(inbox + (f * rows + lr) * C::kRedStride + c);
+            acc.x += x.x;
+            acc.y += x.y;
+            acc.z += x.z;
+            acc.w += x.w;
+          }
+          if (m0 + r0 + lr < p.M && n0 + c < p.N)
+            *reinterpret_cast<uint2*>(out + size_t(m0 + r0 + lr) * size_t(p.ldc) + n0 + c) =
+                make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+        }
       }
     }
   }
@@ -635,18 +661,18 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int64_t ld, 
          CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, bool SPLIT>
 cudaError_t launch_bn(const ProjParams& p, cudaStream_t stream) {
-  using C = ProjCfg<BN>;
+  using C = ProjCfg<BN, SPLIT>;
   CUtensorMap ma, mb;
   if (!make_map(&ma, p.A, p.M, p.K, p.lda, kBM) || !make_map(&mb, p.B, p.N, p.K, p.ldb, BN))
     return cudaErrorInvalidValue;
-  auto kern = gdn_proj_gemm_kernel<BN>;
+  auto kern = gdn_proj_gemm_kernel<BN, SPLIT>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kBytes));
   if (e != cudaSuccess) return e;
   const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
-  if (p.splits <= 1) {
+  if (!SPLIT) {
     const int grid = tiles < sm_count() ? tiles : sm_count();
     return launch_pdl(kern, dim3(unsigned(grid)), dim3(kProjThreads), C::kBytes, stream, 1u, ma,
                       mb, p);
@@ -655,66 +681,46 @@ cudaError_t launch_bn(const ProjParams& p, cudaStream_t stream) {
                     stream, unsigned(p.splits), ma, mb, p);
 }
 
-// How many clusters of `s` CTAs of the BN-wide kernel the current GPU holds at once (a
-// cluster stays inside one GPC, so this is below SMs / s); cached per device and shape.
+// Clusters of s CTAs of the split kernel of width BN the current GPU holds at once.
+template <int BN>
+int query_active_clusters(int s) {
+  int n = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(s));
+  cfg.blockDim = dim3(kProjThreads);
+  cfg.dynamicSmemBytes = ProjCfg<BN, true>::kBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(s);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaFuncSetAttribute(gdn_proj_gemm_kernel<BN, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(ProjCfg<BN, true>::kBytes));
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, gdn_proj_gemm_kernel<BN, true>, &cfg);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  return n;
+}
+
+// How many clusters of `s` CTAs of the BN-wide split kernel the current GPU holds at once
+// (a cluster stays inside one GPC, so this is below SMs / s); cached per device and shape.
+// Splits run at widths 128, 96 and 64 (a 256-wide split leaves no room for a ring).
 constexpr int kProjMaxDevices = 64;
 int max_active_clusters(int bn, int s) {
-  static std::atomic<int> cache[kProjMaxDevices][4][9];
+  static std::atomic<int> cache[kProjMaxDevices][3][9];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kProjMaxDevices) return -1;
-  const int i = bn == 256 ? 0 : (bn == 128 ? 1 : (bn == 96 ? 3 : 2));
+  if (bn != 128 && bn != 96 && bn != 64) return -1;
+  const int i = bn == 128 ? 0 : (bn == 96 ? 1 : 2);
   int cached = cache[dev][i][s].load(std::memory_order_relaxed);
   if (cached == 0) {
-    int n = 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(s));
-    cfg.blockDim = dim3(kProjThreads);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(s);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaSuccess;
-    switch (bn) {
-      case 256:
-        cfg.dynamicSmemBytes = ProjCfg<256>::kBytes;
-        e = cudaFuncSetAttribute(gdn_proj_gemm_kernel<256>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(ProjCfg<256>::kBytes));
-        if (e == cudaSuccess)
-          e = cudaOccupancyMaxActiveClusters(&n, gdn_proj_gemm_kernel<256>, &cfg);
-        break;
-      case 128:
-        cfg.dynamicSmemBytes = ProjCfg<128>::kBytes;
-        e = cudaFuncSetAttribute(gdn_proj_gemm_kernel<128>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(ProjCfg<128>::kBytes));
-        if (e == cudaSuccess)
-          e = cudaOccupancyMaxActiveClusters(&n, gdn_proj_gemm_kernel<128>, &cfg);
-        break;
-      case 96:
-        cfg.dynamicSmemBytes = ProjCfg<96>::kBytes;
-        e = cudaFuncSetAttribute(gdn_proj_gemm_kernel<96>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(ProjCfg<96>::kBytes));
-        if (e == cudaSuccess)
-          e = cudaOccupancyMaxActiveClusters(&n, gdn_proj_gemm_kernel<96>, &cfg);
-        break;
-      default:
-        cfg.dynamicSmemBytes = ProjCfg<64>::kBytes;
-        e = cudaFuncSetAttribute(gdn_proj_gemm_kernel<64>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(ProjCfg<64>::kBytes));
-        if (e == cudaSuccess)
-          e = cudaOccupancyMaxActiveClusters(&n, gdn_proj_gemm_kernel<64>, &cfg);
-        break;
-    }
-    if (e != cudaSuccess) {
-      (void)cudaGetLastError();
-      n = 0;
-    }
+    const int n = bn == 128 ? query_active_clusters<128>(s)
+                            : (bn == 96 ? query_active_clusters<96>(s) : query_active_clusters<64>(s));
     cached = n > 0 ? n : -1;  // -1: this split is not available
     cache[dev][i][s].store(cached, std::memory_order_relaxed);
   }
@@ -815,11 +821,19 @@ cudaError_t launch_proj(const ProjParams& p_in, cudaStream_t stream) {
   p.n_fast = p.M > p.N ? 1 : 0;  // A (M x K) larger than B (N x K)
   if (p.bn == 256 && p.splits == 1 && p.M > kBM && max_active_pairs() > 0)
     return launch_pair(p, stream);
+  if (p.splits > 1) {
+    switch (p.bn) {
+      case 128: return launch_bn<128, true>(p, stream);
+      case 96: return launch_bn<96, true>(p, stream);
+      case 64: return launch_bn<64, true>(p, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (p.bn) {
-    case 256: return launch_bn<256>(p, stream);
-    case 128: return launch_bn<128>(p, stream);
-    case 96: return launch_bn<96>(p, stream);
-    case 64: return launch_bn<64>(p, stream);
+    case 256: return launch_bn<256, false>(p, stream);
+    case 128: return launch_bn<128, false>(p, stream);
+    case 96: return launch_bn<96, false>(p, stream);
+    case 64: return launch_bn<64, false>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
