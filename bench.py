@@ -292,6 +292,35 @@ def time_loop(torch, stream, fn, steps, warmup):
     return e0.elapsed_time(e1) / steps
 
 
+def time_graph(torch, stream, fn, calls=50, reps=4):
+    """GPU time per call of `fn(i, st)`, from `calls` calls captured in one CUDA graph (on a
+    side stream, as capture requires) and replayed `reps` times on `stream`: no host launch
+    overhead in the timed region, which for a 10 us GEMM launched from Python would
+    otherwise dominate."""
+    side = torch.cuda.Stream(stream.device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for i in range(3):
+            fn(i, side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for i in range(calls):
+            fn(i, side)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (calls * reps)
+
+
 def verify_mode(device, steps, hbm_peak, warmup=3, n=N_SEQ, h16=False):
     """The 128-sequence ragged verify; h16: on fp16 state pools and intermediates."""
     import torch
@@ -533,8 +562,11 @@ def proj_mode(device, steps, tc_peak, hbm_peak, warmup=3):
     """The bf16 projections around the mixer, hidden width 2048: in_proj (-> [Q|K|V|Z|b|a],
     12352 outputs) and out_proj (4096 -> 2048) at 8192 tokens (tensor-bound) and at 128
     tokens (one decode step of 128 sequences: weight-streaming, HBM-bound).  Operand sets
-    rotate so every call reads more than L2 holds; cuBLAS (torch.matmul) on the same
-    operands is timed beside as context."""
+    rotate so every call reads more than L2 holds.  `ms` is the library call as a caller
+    makes it (back-to-back calls on one stream); `graph_ms` the same calls replayed from a
+    CUDA graph; cuBLAS (torch.matmul) on the same operands is timed beside from a CUDA
+    graph too (`cublas_ms`), since at 128 tokens its eager loop times Python's dispatch,
+    not the GPU."""
     import torch
 
     from gated_deltanet_layer_conv1d_gb300 import device as dev
@@ -559,20 +591,23 @@ def proj_mode(device, steps, tc_peak, hbm_peak, warmup=3):
         b = [rnd(N, K, scale=K ** -0.5) for _ in range(sets)]
         c = [torch.empty((T, N), dtype=torch.bfloat16, device=device) for _ in range(sets)]
 
-        def ours(i):
+        def ours(i, st=stream):
             q = i % sets
-            gdn.gdn_proj_gemm(a[q], b[q], c[q], status, stream)
+            gdn.gdn_proj_gemm(a[q], b[q], c[q], status, st)
 
-        def cublas(i):
+        def cublas(i, st=None):
             q = i % sets
-            torch.matmul(a[q], b[q].t(), out=c[q])
+            torch.matmul(a[q], b[q].t(), out=c[q])  # on the current stream
 
         ms = time_loop(torch, stream, ours, steps, warmup)
         assert int(status.item()) == 0
-        ms_cublas = time_loop(torch, stream, cublas, steps, warmup)
+        ms_graph = time_graph(torch, stream, ours, calls=20 if T >= 1024 else 50)
+        assert int(status.item()) == 0
+        ms_cublas = time_graph(torch, stream, cublas, calls=20 if T >= 1024 else 50)
         fl = 2.0 * T * K * N
         byts = per_set
-        r = {"M": T, "N": N, "K": K, "ms": round(ms, 4), "cublas_ms": round(ms_cublas, 4)}
+        r = {"M": T, "N": N, "K": K, "ms": round(ms, 4), "graph_ms": round(ms_graph, 4),
+             "cublas_ms": round(ms_cublas, 4), "cublas_timing": "cuda_graph_replay"}
         tfs = fl / (ms * 1e-3) / 1e12
         gbs = byts / (ms * 1e-3) / 1e9
         if T >= 1024:
@@ -586,6 +621,30 @@ def proj_mode(device, steps, tc_peak, hbm_peak, warmup=3):
         out[f"{name}_{T}tok"] = r
     return {"workload": f"bf16 projections, hidden {H}, H_k 16, H_v 32, d 128",
             "gpu_launches_per_call": 1, "calls": out}
+
+
+def proj128_profile(device, steps, warmup=3):
+    """Only the two 128-token projection calls of proj_mode, eager: warmup + steps calls
+    of in_proj, then of out_proj (for profiler captures)."""
+    import torch
+
+    from gated_deltanet_layer_conv1d_gb300 import device as dev
+    from gated_deltanet_layer_conv1d_gb300 import gdn
+    from gated_deltanet_layer_conv1d_gb300 import workloads as wl
+    dims = dev.dims_of(wl.FULL)
+    width = gdn.gdn_in_proj_width(dims)
+    H, vd = wl.HIDDEN, wl.FULL.z_dim
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    g = torch.Generator(device=device).manual_seed(0)
+    for K, N in ((H, width), (vd, H)):
+        a = (torch.randn(128, K, generator=g, device=device)).to(torch.bfloat16)
+        b = (torch.randn(N, K, generator=g, device=device) * K ** -0.5).to(torch.bfloat16)
+        c = torch.empty((128, N), dtype=torch.bfloat16, device=device)
+        for _ in range(warmup + steps):
+            gdn.gdn_proj_gemm(a, b, c, status, stream)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
 
 
 def layer_mode(device, steps, warmup=3):
@@ -914,7 +973,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--profile", nargs="?", const="decode", default=None,
                     choices=["decode", "verify", "verify-small", "verify16", "verify16-small",
-                             "prefill", "mixed", "proj", "layer", "fold", "decode16", "woa"],
+                             "prefill", "mixed", "proj", "proj128", "layer", "fold", "decode16",
+                             "woa"],
                     help="only one timed loop of one mode (for profiler captures); "
                          "verify-small runs 32 sequences; verify16 runs on fp16 state pools")
     args = ap.parse_args()
@@ -942,6 +1002,11 @@ def main():
     gdn.lib()
 
     hbm_peak, tc_peak, peak_src = peaks()
+    if args.profile == "proj128":
+        proj128_profile(device, args.steps, warmup=args.warmup)
+        if rank == 0:
+            print(json.dumps({"profile_run": "proj128"}))
+        return
     if args.profile == "proj":
         r = proj_mode(device, args.steps, tc_peak, hbm_peak, warmup=args.warmup)
         if rank == 0:
