@@ -301,6 +301,52 @@ __device__ __forceinline__ void l2norm_tokens(float* x, int stride, int k, float
   }
 }
 
+// Verify: for each token t (one warp each) the sums q.q, k.k and q.k of its q and k as
+// staged (not normalised) and, for the second token of a pair (t odd), k_{t-1}.k_t and
+// k_{t-1}.q_t.  The L2 scales r_q = q_scale / |q| and r_k = 1 / |k| go to scl_s[t][2],
+// q_hat.k_hat to kq_s[t], the unscaled pair dots to pair_s[t-1], pair_s[t] (the pair loop
+// scales them: k_hat_0.k_hat_1 = r_k0 r_k1 k_0.k_1, ...).  Order-independent, so it reads
+// q and k in their staged (row-block) order.
+template <int D, int NW>
+__device__ __forceinline__ void qk_scales_tokens(const float* x, int stride, int k, float q_scale,
+                                                 float eps, float* kq_s, float* scl_s,
+                                                 float* pair_s, int warp, int lane) {
+  for (int t = warp; t < k; t += NW) {
+    const float* xq = x + t * stride;
+    const float* xk = xq + D;
+    const bool second = (t & 1) != 0;  // warp-uniform
+    float sq = 0.f, sk = 0.f, sqk = 0.f, skk = 0.f, skq = 0.f;
+    for (int i = lane; i < D; i += 32) {
+      const float qv = xq[i], kv = xk[i];
+      sq += qv * qv;
+      sk += kv * kv;
+      sqk += qv * kv;
+      if (second) {
+        const float pv = xk[i - stride];  // k of token t - 1
+        skk += pv * kv;
+        skq += pv * qv;
+      }
+    }
+    sq = warp_sum(sq);
+    sk = warp_sum(sk);
+    sqk = warp_sum(sqk);
+    if (second) {
+      skk = warp_sum(skk);
+      skq = warp_sum(skq);
+    }
+    if (lane == 0) {
+      const float rq = q_scale * rsqrtf(sq + eps), rk = rsqrtf(sk + eps);
+      scl_s[2 * t] = rq;
+      scl_s[2 * t + 1] = rk;
+      kq_s[t] = rq * rk * sqk;
+      if (second) {
+        pair_s[t - 1] = skk;
+        pair_s[t] = skq;
+      }
+    }
+  }
+}
+
 // Gated RMSNorm of one value head's outputs for `k` tokens, one warp per token.
 // o: [k][D] f32 in shared memory; z: [k][zstride] f32 in shared memory (this head's
 // slice); y row r = row0 + t.
@@ -365,9 +411,11 @@ struct RecSmem {
   // slot of each sequence, whether its item can run (0 = yes, else the GDN_ERR_* code),
   // its table-0 pointer (verify), and the current item's 16 table entries (verify).
   // decode: per-warp partial sums q.q, k.k, q.k of the item's q and k, [D / 32][3]
-  // verify: (k_t0.k_t1, k_t0.q_t1) of each pair of tokens [KMAX/2][2]
+  // verify: (k_t0.k_t1, k_t0.q_t1) of each pair of tokens [KMAX/2][2], unscaled; the L2
+  // scales (r_q, r_k) of every token [KMAX][2]
   static constexpr size_t kPair = kKq + ((size_t(KMAX) * 4 + 15) / 16) * 16;
-  static constexpr size_t kL2 = kPair + (kPairs ? ((size_t(KMAX) * 4 + 15) / 16) * 16 : 0);
+  static constexpr size_t kScl = kPair + (kPairs ? ((size_t(KMAX) * 4 + 15) / 16) * 16 : 0);
+  static constexpr size_t kL2 = kScl + (kPairs ? size_t(KMAX) * 2 * 4 : 0);
   static constexpr size_t kSlots = kL2 + ((size_t(D + 31) / 32 * 12 + 15) / 16) * 16;  // [128] i32
   static constexpr size_t kValid = kSlots + GDN_MAX_SEQS * 4;                  // [128] i32
   static constexpr size_t kTab0 = kValid + GDN_MAX_SEQS * 4;                   // [128] u64
@@ -486,7 +534,9 @@ __device__ __forceinline__ void add_xor4(float4& acc, const float4& send, int of
 // state updates and stores follow in the same step, so stores go out between reductions.
 // After the barrier each lane adds up only the vector it kept (RB loads) and takes the
 // other three from its neighbours by shuffles.
-// pair_s: [KMAX/2][2] = (k_0.k_1, k_0.q_1) of each pair; kq_s: q_t.k_t.  after_first()
+// q and k are staged unnormalised; scl_s: [KMAX][2] their L2 scales (r_q with the q
+// scale); pair_s: [KMAX/2][2] = (k_0.k_1, k_0.q_1) of each pair, unscaled; kq_s:
+// q_hat_t.k_hat_t.  after_first()
 // runs once, on every thread, after the head's first barrier (every thread holds the tile
 // in registers by then).
 // Returns true if the first barrier saw `abort` raised by any thread (nothing written).
@@ -495,7 +545,8 @@ __device__ __forceinline__ bool verify_head(const RecParams& p, const Item& it, 
                                             int k, SR (&S)[RecMap<D, NT>::M],
                                             const Lane<D, NT>& L, const float* xs, int CHX,
                                             const float* gate, const float* kq_s,
-                                            const float* pair_s, float* red, float* obuf,
+                                            const float* pair_s, const float* scl_s,
+                                            float* red, float* obuf,
                                             const uint64_t* tab_item, unsigned char* woa_seq,
                                             bool abort, F&& after_first) {
   using Map = RecMap<D, NT>;
@@ -503,7 +554,6 @@ __device__ __forceinline__ bool verify_head(const RecParams& p, const Item& it, 
   // after the reduce-scatter a lane holds vector 2 hi + mid of (A_0, B_0, A_1, B_1)
   const bool hi = (L.lane >> 4) & 1, mid = (L.lane >> 3) & 1;
   const bool writer = ((L.lane / Map::CQ) & (8 / Map::CQ - 1)) == 0;
-  const bool o_writer = L.rb == 0 && L.rs == 0;
   float* woa_d = WOA ? reinterpret_cast<float*>(woa_seq + p.woa_delta) + size_t(h) * D + L.col0
                      : nullptr;
   // The state after a pair's second token is stored row by row inside the next pair's
@@ -564,10 +614,16 @@ __device__ __forceinline__ bool verify_head(const RecParams& p, const Item& it, 
       return make_float4(__shfl_sync(0xffffffffu, V.x, src), __shfl_sync(0xffffffffu, V.y, src),
                          __shfl_sync(0xffffffffu, V.z, src), __shfl_sync(0xffffffffu, V.w, src));
     };
-    const float4 A0 = vec_of(0), A1 = vec_of(2);
+    // q and k are staged unnormalised: the sums and the pair dots take their L2 scales here,
+    // and k_hat delta^T = k (r_k delta)^T in the updates
+    const float rq0 = scl_s[2 * t0], rk0 = scl_s[2 * t0 + 1];
+    const float rq1 = scl_s[2 * t1], rk1 = scl_s[2 * t1 + 1];
+    float4 A0 = vec_of(0), A1 = vec_of(2);
+    A0.x *= rk0; A0.y *= rk0; A0.z *= rk0; A0.w *= rk0;
+    A1.x *= rk1; A1.y *= rk1; A1.z *= rk1; A1.w *= rk1;
     const float al0 = gate[(t0 * kMaxG + g) * 2], be0 = gate[(t0 * kMaxG + g) * 2 + 1];
     const float al1 = gate[(t1 * kMaxG + g) * 2], be1 = gate[(t1 * kMaxG + g) * 2 + 1];
-    const float kk = pair_s[t0], kq01 = pair_s[t0 + 1];
+    const float kk = pair_s[t0] * rk0 * rk1, kq01 = pair_s[t0 + 1] * rk0 * rq1;
     const float kq0 = kq_s[t0], kq1 = kq_s[t1];
     const float4 v0 = *reinterpret_cast<const float4*>(x0 + (2 + g) * D + L.col0);
     const float4 v1 = *reinterpret_cast<const float4*>(x1 + (2 + g) * D + L.col0);
@@ -580,24 +636,29 @@ __device__ __forceinline__ bool verify_head(const RecParams& p, const Item& it, 
     d1.y = be1 * (v1.y - al1 * (al0 * A1.y + kk * d0.y));
     d1.z = be1 * (v1.z - al1 * (al0 * A1.z + kk * d0.z));
     d1.w = be1 * (v1.w - al1 * (al0 * A1.w + kk * d0.w));
-    if (L.rb == 0) {  // warp-uniform: the warps whose rs == 0 lanes write o
-      const float4 B0 = vec_of(1), B1 = vec_of(3);
-      float4 o0, o1;
+    if (L.rb == 0) {  // warp-uniform: o of t0 on row block 0, of t1 on row block 1
+      float4 B0 = vec_of(1);
+      B0.x *= rq0; B0.y *= rq0; B0.z *= rq0; B0.w *= rq0;
+      float4 o0;
       o0.x = al0 * B0.x + kq0 * d0.x;
       o0.y = al0 * B0.y + kq0 * d0.y;
       o0.z = al0 * B0.z + kq0 * d0.z;
       o0.w = al0 * B0.w + kq0 * d0.w;
+      if (L.rs == 0) {
+        *reinterpret_cast<float4*>(obuf + t0 * D + L.col0) = o0;
+        if (WOA) *reinterpret_cast<float4*>(woa_d + size_t(t0) * p.Hv * D) = d0;
+      }
+    } else if (L.rb == 1 && has1) {
+      float4 B1 = vec_of(3);
+      B1.x *= rq1; B1.y *= rq1; B1.z *= rq1; B1.w *= rq1;
+      float4 o1;
       o1.x = al1 * (al0 * B1.x + kq01 * d0.x) + kq1 * d1.x;
       o1.y = al1 * (al0 * B1.y + kq01 * d0.y) + kq1 * d1.y;
       o1.z = al1 * (al0 * B1.z + kq01 * d0.z) + kq1 * d1.z;
       o1.w = al1 * (al0 * B1.w + kq01 * d0.w) + kq1 * d1.w;
-      if (o_writer) {
-        *reinterpret_cast<float4*>(obuf + t0 * D + L.col0) = o0;
-        if (has1) *reinterpret_cast<float4*>(obuf + t1 * D + L.col0) = o1;
-        if (WOA) {  // the update of token t is k_hat_t delta_t^T
-          *reinterpret_cast<float4*>(woa_d + size_t(t0) * p.Hv * D) = d0;
-          if (has1) *reinterpret_cast<float4*>(woa_d + size_t(t1) * p.Hv * D) = d1;
-        }
+      if (L.rs == 0) {
+        *reinterpret_cast<float4*>(obuf + t1 * D + L.col0) = o1;
+        if (WOA) *reinterpret_cast<float4*>(woa_d + size_t(t1) * p.Hv * D) = d1;
       }
     }
     SH* dst0 = WOA ? nullptr : state_dst<D, true, SH>(p, it, tab_item, h, t0);
@@ -605,7 +666,9 @@ __device__ __forceinline__ bool verify_head(const RecParams& p, const Item& it, 
     for (int u = 0; u < 2; ++u) {
       if (u == 1 && !has1) break;
       const float al = u ? al1 : al0;
-      const float4 dd = u ? d1 : d0;
+      const float rk = u ? rk1 : rk0;
+      const float4 dd = u ? make_float4(d1.x * rk, d1.y * rk, d1.z * rk, d1.w * rk)
+                          : make_float4(d0.x * rk, d0.y * rk, d0.z * rk, d0.w * rk);
       float kr[Map::M];
       load_rows((u ? x1 : x0) + D + L.xrow, kr);
 #pragma unroll
@@ -673,6 +736,7 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
   float* gate = reinterpret_cast<float*>(smem + SL::kGate);
   float* kq_s = reinterpret_cast<float*>(smem + SL::kKq);
   float* pair_s = reinterpret_cast<float*>(smem + SL::kPair);
+  float* scl_s = reinterpret_cast<float*>(smem + SL::kScl);
   float* l2_s = reinterpret_cast<float*>(smem + SL::kL2);
   float* xs = reinterpret_cast<float*>(smem + SL::kXs);
   int32_t* slots_s = reinterpret_cast<int32_t*>(smem + SL::kSlots);
@@ -1159,28 +1223,15 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
       rk = rsqrtf(sk + p.l2_eps);
       kq1 = rq * rk * sqk;
     } else {
-      l2norm_tokens<D, Map::NW>(xs, CHX, k, p.q_scale, p.l2_eps, kq_s, L.warp, L.lane);
+      qk_scales_tokens<D, Map::NW>(xs, CHX, k, p.q_scale, p.l2_eps, kq_s, scl_s, pair_s,
+                                   L.warp, L.lane);
       named_sync(1, NT);
-      if constexpr (SL::kPairs) {
-        // k_t0.k_t1 and k_t0.q_t1 of each pair (t0 even): one warp per dot product; the
-        // heads read them after their first barrier
-        for (int e = L.warp; e < k - 1; e += Map::NW) {
-          if (e & 1) continue;
-          for (int which = 0; which < 2; ++which) {
-            const float* xa = xs + e * CHX + D;
-            const float* xb = xs + (e + 1) * CHX + (which ? 0 : D);
-            float acc = 0.f;
-            for (int i = L.lane; i < D; i += 32) acc += xa[i] * xb[i];
-            acc = warp_sum(acc);
-            if (L.lane == 0) pair_s[e + which] = acc;
-          }
-        }
-      }
       if (VERIFY && woa) {  // k, and the normalised k of every token, for the deferred fold
         float* kh_out = reinterpret_cast<float*>(woa_seq + p.woa_khat);
         for (int idx = tid; idx < k * D; idx += NT) {
           const int t = idx / D, i = idx - t * D;
-          kh_out[(size_t(t) * p.Hk + it.kh) * D + i] = xs[t * CHX + D + qk_pos<D, NT>(i)];
+          kh_out[(size_t(t) * p.Hk + it.kh) * D + i] =
+              xs[t * CHX + D + qk_pos<D, NT>(i)] * scl_s[2 * t + 1];
         }
         if (tid == 0 && it.kh == 0) *reinterpret_cast<int32_t*>(woa_seq) = k;
       }
@@ -1215,7 +1266,8 @@ __global__ void __launch_bounds__(rec_threads<NT, KMAX>(), (rec_min_blocks<KMAX,
           }
         };
         if (verify_head<T, D, NT, KMAX, SH, SR, VERIFY && WOA>(p, it, h, g, k, S, L, xs, CHX,
-                                                               gate, kq_s, pair_s, red, obuf,
+                                                               gate, kq_s, pair_s, scl_s, red,
+                                                               obuf,
                                                                tab_item, woa_seq, !ok, refill)) {
           drain(q - 1);
           return;
