@@ -92,6 +92,7 @@ cudaError_t launch_gated_rmsnorm(const void* o, bool o_half, const void* z, int6
 struct PrefillParams {
   int32_t Hk, Hv, G, D, conv_dim, n, n_slots, total_tokens, max_seqlen, max_chunks;
   void* o_half;  // internal: fp16 [T][Hv][128] room for O when no f32 core output is wanted
+  int32_t* counts;  // internal: [n][Hv][2] chunks of O each column slice has stored
   float q_scale, l2_eps, norm_eps;
   int32_t norm_gate;  // 0: SiLU(z), 1: sigmoid(z)
   int32_t f32_path;   // 1: the token-sequential f32 form even where the tensor-core form runs

@@ -49,9 +49,12 @@ cudaError_t launch_prefill(const PrefillParams& p, int dtype, cudaStream_t strea
     c.workspace = p.workspace;
     cudaError_t e = launch_prefill_prep(c, stream);
     if (e != cudaSuccess) return e;
-    float* o_work = reinterpret_cast<float*>(static_cast<unsigned char*>(p.workspace) +
-                                             PrefillLayout{p.Hk, p.Hv}.o_offset(p.n, p.total_tokens));
-    return launch_prefill_tc(p, o_work, stream);
+    const PrefillLayout lay{p.Hk, p.Hv};
+    unsigned char* ws = static_cast<unsigned char*>(p.workspace);
+    PrefillParams q = p;
+    q.counts = reinterpret_cast<int32_t*>(ws + lay.count_offset(p.n, p.total_tokens));
+    return launch_prefill_tc(q, reinterpret_cast<float*>(ws + lay.o_offset(p.n, p.total_tokens)),
+                             stream);
   }
   return launch_prefill_sequential(p, dtype, stream);
 }

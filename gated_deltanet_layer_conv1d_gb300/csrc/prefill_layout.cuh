@@ -76,8 +76,12 @@ struct PrefillLayout {
   size_t o_offset(int n, int total_tokens) const {
     return (slots(n, total_tokens) * slot_bytes() + 255) / 256 * 256;
   }
+  // byte offset of the two-slice spine's progress counters: int32 [n][Hv][2], after O
+  size_t count_offset(int n, int total_tokens) const {
+    return o_offset(n, total_tokens) + (size_t(total_tokens) * Hv * 128 * 4 + 255) / 256 * 256;
+  }
   size_t total_bytes(int n, int total_tokens) const {
-    return o_offset(n, total_tokens) + size_t(total_tokens) * Hv * 128 * 4;
+    return count_offset(n, total_tokens) + size_t(n) * Hv * 2 * 4;
   }
 };
 

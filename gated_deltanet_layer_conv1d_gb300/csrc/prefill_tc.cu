@@ -28,8 +28,9 @@
 //   thread stores its own row, 16 bytes at a time).  The next chunk's operands arrive by
 //   bulk copy into the other of two buffers meanwhile.  With whole rows (NCOL = 128) the
 //   spine applies the gated RMSNorm to O itself and writes y; with two column slices it
-//   writes O (fp16 unless the caller asked for the f32 core output) and the gated norm
-//   follows as its own kernel.
+//   writes O (fp16 unless the caller asked for the f32 core output), counts the chunks it
+//   has stored, and the launch's remaining CTAs (a cooperative launch over the SMs the
+//   chains leave free) apply the gated norm to each chunk behind the chains.
 //
 // Operands are fp16 (kind::f16, f32 accumulation): every operand here is bounded
 // (normalised q and k, O(1) v, T, P, Delta and state), and fp16's 11-bit significand
@@ -132,6 +133,9 @@ constexpr uint32_t kPrepTmem = 128;
 __global__ void __launch_bounds__(kPrepThreads, 3)
     gdn_prefill_chunk_kernel(const __grid_constant__ PrefillParams p) {
   using S = PrepSmem;
+  // the two-slice spine's progress counters start from zero on every call
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < 2 * p.n * p.Hv; i += blockDim.x) p.counts[i] = 0;
   const int cs = blockIdx.x / p.Hv, h = blockIdx.x % p.Hv, kh = h / p.G;
   // The sequence that owns chunk slot cs: the last s with base(s) <= cs.
   int seq = 0;
@@ -497,6 +501,9 @@ struct SpineSmem {
   static constexpr uint32_t kUs = kDT + NCOL * 128;    // the single U buffer, !kUInStage
   // Gated norm in the spine (whole rows, NCOL = 128 only):
   static constexpr bool kNorm = NCOL == 128;
+  // Two column slices: O goes out as it is, counted per chunk, and the launch's last CTAs
+  // apply the norm.
+  static constexpr bool kCounted = NCOL == 64;
   static constexpr uint32_t kZ = kUs + (kUInStage ? 0 : NCOL * 128);  // [64][128] bf16 z rows
   static constexpr uint32_t kRed = kZ + (kNorm ? 16384 : 0);   // [4][64] f32 partial sums
   static constexpr uint32_t kNW = kRed + (kNorm ? 1024 : 0);   // [128] f32 norm weight
@@ -508,15 +515,173 @@ struct SpineSmem {
 };
 
 constexpr int kOrderMax = 512;  // sequences the spine orders by length (more: call order)
+constexpr int kCountStop = 1 << 30;  // counted by a chain that stopped early
+
+// A column slice's count of stored chunks of O: written after a CTA barrier that follows
+// the stores, behind a device-scope fence (so it releases every thread's stores); read
+// relaxed and followed by a fence before the reader's CTA barrier.
+__device__ __forceinline__ void publish_count(int32_t* cnt, int v) {
+  __threadfence();
+  asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(cnt), "r"(v) : "memory");
+}
+__device__ __forceinline__ int load_count(const int32_t* cnt) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+  return v;
+}
+
+// The gated RMSNorm behind the two-slice spine, y = O / rms(O) * w * gate(z), run by the
+// launch's last CTAs on the SMs the chains leave free (the launch is cooperative, so the
+// chains they wait for are resident; it has at least two such CTAs per head).  Units of
+// work are (sequence, head, 8-row part of a chunk); norm CTA k follows units k, k + nr, ...
+// (at most kNormUnits of them) chunk by chunk.  Each round waits until both column slices
+// of every one of its heads have stored past the next chunk, then normalises every chunk
+// that has become ready, so a CTA that falls behind catches up in one round.  Warp w of NW
+// takes rows w, w + NW, ... of the round, eight at a time, lane l columns 4l .. 4l + 3.
+constexpr int kNormUnits = 4;
+constexpr int kNormRows = 8;  // rows of a chunk per unit
+
+__device__ void spine_norm_ctas(const PrefillParams& p, int k, int nr) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+  constexpr int kParts = kC / kNormRows;
+  const int units = p.n * p.Hv * kParts;
+  const int nwu = k < units ? (units - 1 - k) / nr + 1 : 0;
+  if (nwu == 0 || nwu > kNormUnits) return;  // the launch keeps nwu <= kNormUnits
+  __shared__ int uh_s[kNormUnits], r0_s[kNormUnits], tb_s[kNormUnits], len_s[kNormUnits],
+      upto_s;
+  if (tid < nwu) {
+    const int w = k + tid * nr, u = w / kParts, seq = u / p.Hv;
+    const int tb = p.cu_seqlens[seq], te = p.cu_seqlens[seq + 1];
+    uh_s[tid] = u;                         // (sequence, head)
+    r0_s[tid] = (w % kParts) * kNormRows;  // first row of the part within a chunk
+    tb_s[tid] = tb;
+    // the chains skip what this skips: a bad range or state pointer
+    len_s[tid] = check_seq(p, tb, te, p.h_ptrs[seq]) != 0 ? 0 : te - tb;
+  }
+  __syncthreads();
+  int ncmax = 0;
+  for (int i = 0; i < nwu; ++i) ncmax = max(ncmax, (len_s[i] + kC - 1) / kC);
+  // floor(q / nwu) as (q * ceil(2^32 / nwu)) >> 32, exact for q < 2^32 / nwu
+  const uint64_t inv_nwu = (0x100000000ull + nwu - 1) / nwu;
+  const float4 w4 = *reinterpret_cast<const float4*>(p.norm_w + 4 * lane);
+  const __nv_bfloat16* zg = reinterpret_cast<const __nv_bfloat16*>(p.z);
+  __nv_bfloat16* yg = reinterpret_cast<__nv_bfloat16*>(p.y);
+  int c0 = 0;
+  while (c0 < ncmax) {
+    if (tid == 0) {
+      // chunks below `ready` are stored in both slices of every head still running
+      int ready = 0;
+      const uint64_t t0 = globaltimer_ns();
+      for (;;) {
+        ready = ncmax;
+        for (int i = 0; i < nwu; ++i) {
+          const int nc = (len_s[i] + kC - 1) / kC;
+          if (nc <= c0) continue;
+          const int32_t* cnt = p.counts + 2 * uh_s[i];
+          const int v = min(load_count(cnt), load_count(cnt + 1));
+          if (v < nc) ready = min(ready, v);
+        }
+        if (ready > c0) break;
+        if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+          report(p.status, GDN_ERR_TIMEOUT);
+          ready = -1;
+          break;
+        }
+        __nanosleep(128);
+      }
+      __threadfence();
+      upto_s = ready;
+    }
+    __syncthreads();
+    const int c1 = upto_s;
+    __syncthreads();  // upto_s is rewritten next round
+    if (c1 < 0) return;
+    // rows of this round in (chunk, unit, row) order
+    const int X = (c1 - c0) * nwu * kNormRows;
+    for (int x0 = warp; x0 < X; x0 += 8 * nw) {
+      // eight rows' addresses (a dead row reads row 0, which exists: X > 0 means some
+      // sequence has tokens), then every load before any use
+      size_t orow[8], zrow[8];
+      bool live[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int x = x0 + j * nw, q = x / kNormRows;
+        const int cc = int((uint64_t(q) * inv_nwu) >> 32), i = q - cc * nwu;
+        const int r = (c0 + cc) * kC + r0_s[i] + x % kNormRows;  // row within the sequence
+        live[j] = x < X && r < len_s[i];
+        const int t = tb_s[i] + r, h = uh_s[i] % p.Hv;
+        orow[j] = live[j] ? size_t(t) * p.Hv + h : 0;
+        zrow[j] = live[j] ? size_t(t) * p.z_stride + size_t(h) * kD : 0;
+      }
+      float4 ov[8];
+      uint2 zr[8];
+      if (p.o_half) {
+        const __half* oh = reinterpret_cast<const __half*>(p.o_half) + 4 * lane;
+        uint2 oraw[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) oraw[j] = __ldcg(reinterpret_cast<const uint2*>(oh + orow[j] * kD));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) zr[j] = __ldg(reinterpret_cast<const uint2*>(zg + zrow[j] + 4 * lane));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&oraw[j].x));
+          const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&oraw[j].y));
+          ov[j] = make_float4(a.x, a.y, b.x, b.y);
+        }
+      } else {
+        const float* of = p.core_out + 4 * lane;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ov[j] = __ldcg(reinterpret_cast<const float4*>(of + orow[j] * kD));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) zr[j] = __ldg(reinterpret_cast<const uint2*>(zg + zrow[j] + 4 * lane));
+      }
+      // the eight rows side by side (dead rows too; only their stores are skipped)
+      float ss[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        ss[j] = ov[j].x * ov[j].x + ov[j].y * ov[j].y + ov[j].z * ov[j].z + ov[j].w * ov[j].w;
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], m);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 o = ov[j];
+        const float inv = rsqrtf(ss[j] / float(kD) + p.norm_eps);
+        const float2 za = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zr[j].x));
+        const float2 zb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zr[j].y));
+        const __nv_bfloat162 y01 =
+            __floats2bfloat162_rn(o.x * inv * w4.x * zgate_fast(za.x, p.norm_gate),
+                                  o.y * inv * w4.y * zgate_fast(za.y, p.norm_gate));
+        const __nv_bfloat162 y23 =
+            __floats2bfloat162_rn(o.z * inv * w4.z * zgate_fast(zb.x, p.norm_gate),
+                                  o.w * inv * w4.w * zgate_fast(zb.y, p.norm_gate));
+        if (live[j])
+          *reinterpret_cast<uint2*>(yg + orow[j] * kD + 4 * lane) =
+              make_uint2(*reinterpret_cast<const uint32_t*>(&y01),
+                         *reinterpret_cast<const uint32_t*>(&y23));
+      }
+    }
+    c0 = c1;
+  }
+}
 
 template <int NCOL>
-__global__ void __launch_bounds__(4 * NCOL, 1)
+__global__ void __launch_bounds__(4 * NCOL + (SpineSmem<NCOL>::kCounted ? 32 : 0), 1)
     gdn_prefill_spine_kernel(const __grid_constant__ PrefillParams p) {
   using S = SpineSmem<NCOL>;
   constexpr int kNS = kD / NCOL;  // slices per head
+  if (S::kCounted && int(blockIdx.x) >= p.n * p.Hv * kNS) {
+    const int chains = p.n * p.Hv * kNS;
+    spine_norm_ctas(p, int(blockIdx.x) - chains, int(gridDim.x) - chains);
+    return;
+  }
   constexpr int kIssuer = 64;     // warp 2, lane 0: issues the MMAs
   constexpr int kLoader = 96;     // warp 3, lane 0: issues the bulk copies
   // (neither is in an output warp, whose work trails the chain)
+  constexpr int kChain = 4 * NCOL;  // the chain's threads; a two-slice CTA has one more warp,
+                                    // which only turns progress into the device-wide count
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int slice = blockIdx.x % kNS, unit = blockIdx.x / kNS;
   // Units are handed out longest sequence first (ties: lower index first): CTAs start in
@@ -548,6 +713,9 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
   const int len = t_end - t_begin;
   if (len == 0) return;  // nothing to do: the state stays as it is
   const int nc = (len + kC - 1) / kC;
+  int32_t* cnt = p.counts + 2 * (size_t(seq) * p.Hv + h) + slice;
+  // chunks whose O rows this CTA has stored (set by kLoader after a chain barrier)
+  __shared__ int stored_s;
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -575,8 +743,34 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     mbar_init(bar_o, 1);
     mbar_init(ufull, 1);
     fence_mbar_init();
+    stored_s = 0;
   }
   if (warp == 0) tc::alloc(tslot, S::kTmemCols);
+  if (S::kCounted && tid >= kChain) {
+    // The counting warp: polls stored_s (acquire: the chain barrier before kLoader's
+    // release store ordered every output thread's stores before it) and publishes each
+    // new value behind a device-scope fence, off the chain's path.
+    __syncthreads();
+    int done = 0;
+    uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      int v;
+      asm volatile("ld.acquire.cta.shared.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(&stored_s))
+                   : "memory");
+      if (v != done) {
+        if (lane == 0) publish_count(cnt, v);
+        done = v;
+        t0 = globaltimer_ns();
+      }
+      if (v >= nc) break;  // all stored, or kCountStop
+      if (globaltimer_ns() - t0 > kWaitBudgetNs) {  // the chain reports its own stop
+        if (lane == 0) publish_count(cnt, kCountStop);
+        break;
+      }
+    }
+    __syncthreads();
+    return;
+  }
 
   const int q4 = warp & 3, cg = warp >> 2;
   const int row = 32 * q4 + lane;       // TMEM lane; the H row i of this thread
@@ -664,9 +858,13 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
   };
   auto sync_or_stop = [&]() -> bool {
     tc::fence_before_sync();
-    const bool stop = __syncthreads_or(bad) != 0;
+    const bool stop = S::kCounted ? named_sync_or(3, kChain, bad) : __syncthreads_or(bad) != 0;
     tc::fence_after_sync();
     return stop;
+  };
+  auto set_stored = [&](int v) {
+    asm volatile("st.release.cta.shared.s32 [%0], %1;" ::"r"(smem_u32(&stored_s)), "r"(v)
+                 : "memory");
   };
 
   bool aborted = false;
@@ -744,6 +942,8 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
     }
     fence_proxy_async_smem();
     if (sync_or_stop()) { aborted = true; break; }
+    // chunk c - 1's O rows were stored before that barrier
+    if (S::kCounted && tid == kLoader && c > 0) set_stored(c);
 
     // ---- MMA_b: K~^T Delta (the chain), then [P;*] Delta (the outputs)
     if (tid == kIssuer) {
@@ -856,6 +1056,10 @@ __global__ void __launch_bounds__(4 * NCOL, 1)
       *reinterpret_cast<float4*>(Hg + size_t(row) * kD + col0 + u) =
           make_float4(Hr[u], Hr[u + 1], Hr[u + 2], Hr[u + 3]);
   }
+  if constexpr (S::kCounted) {
+    named_sync(3, kChain);  // the last chunk's O rows are stored
+    if (tid == kLoader) set_stored(aborted ? kCountStop : nc);
+  }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::dealloc(tmem, S::kTmemCols);
@@ -867,7 +1071,40 @@ cudaError_t launch_spine(const PrefillParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(SpineSmem<NCOL>::kAlloc));
   if (e != cudaSuccess) return e;
-  kern<<<p.n * p.Hv * (kD / NCOL), 4 * NCOL, SpineSmem<NCOL>::kAlloc, stream>>>(p);
+  const int chains = p.n * p.Hv * (kD / NCOL);
+  if (!SpineSmem<NCOL>::kCounted) {
+    kern<<<chains, 4 * NCOL, SpineSmem<NCOL>::kAlloc, stream>>>(p);
+    return cudaGetLastError();
+  }
+  // Cooperative, so that every norm CTA's chains are resident: as many CTAs as fit at once.
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 4 * NCOL + 32,
+                                                    SpineSmem<NCOL>::kAlloc);
+  if (e != cudaSuccess) return e;
+  const int grid = per_sm * sm_count();
+  if (grid - chains < 2 * p.n * p.Hv) {
+    // fewer than two spare SMs per head (the norm CTAs would trail the chains): the chains
+    // alone, then the norm kernel
+    kern<<<chains, 4 * NCOL + 32, SpineSmem<NCOL>::kAlloc, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_gated_rmsnorm(p.o_half ? p.o_half : static_cast<const void*>(p.core_out),
+                                p.o_half != nullptr, p.z, p.z_stride, p.norm_w, p.norm_eps,
+                                p.total_tokens, p.Hv, kD, GDN_DTYPE_BF16, p.norm_gate, p.y,
+                                stream);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(4 * NCOL + 32);
+  cfg.dynamicSmemBytes = SpineSmem<NCOL>::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeCooperative;
+  attr.val.cooperative = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -890,19 +1127,15 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, float* o_work, cudaStream_
   // Column slices per (sequence, head): as many as one wave of CTAs holds, since the
   // spine's time is its chain of chunks, not its arithmetic.
   // A whole-row spine (128 columns) applies the gated norm itself; two column slices per
-  // head double the CTAs when one wave would otherwise leave SMs idle, and leave the norm
-  // to its own kernel.
+  // head double the chains when one wave would otherwise leave SMs idle, and leave the norm
+  // to the CTAs of the same launch on the SMs still free.
   const int units = p.n * p.Hv, sms = sm_count();
   if (units * 2 > sms) return launch_spine<128>(p, stream);
-  // Without an f32 core output to fill, O reaches the norm kernel as fp16 (2^-11 relative,
-  // far below the bf16 rounding of y), which halves that hand-off's bytes.
+  // Without an f32 core output to fill, O reaches the norm as fp16 (2^-11 relative, far
+  // below the bf16 rounding of y), which halves that hand-off's bytes.
   PrefillParams q = p;
   q.o_half = p.core_out ? nullptr : static_cast<void*>(o_work);
-  cudaError_t e = launch_spine<64>(q, stream);
-  if (e != cudaSuccess) return e;
-  return launch_gated_rmsnorm(q.o_half ? q.o_half : static_cast<const void*>(q.core_out),
-                              q.o_half != nullptr, p.z, p.z_stride, p.norm_w, p.norm_eps,
-                              p.total_tokens, p.Hv, kD, GDN_DTYPE_BF16, p.norm_gate, p.y, stream);
+  return launch_spine<64>(q, stream);
 }
 
 }  // namespace gdn

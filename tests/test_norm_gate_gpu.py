@@ -1,8 +1,8 @@
 """GPU parity of the sigmoid-gated norm (the gdn_norm_sigmoid models; layer_struct.rs, the
 gated_rms_norm_f32_strided_k field): gdn_dims.norm_gate = GDN_NORM_GATE_SIGMOID through
 every entry point that ends in the gated norm -- decode (norm warp), verify (per-token norm
-warps), the tensor-core prefill in both spine forms (fused norm with whole rows, and the
-column-sliced spine followed by the norm kernel), the token-sequential prefill -- and the
+warps), the tensor-core prefill in both spine forms (whole rows, and column slices with
+the norm in the launch's spare CTAs), the token-sequential prefill -- and the
 stand-alone gdn_gated_rmsnorm_sigmoid.  Same tolerances as the SiLU-gated tests."""
 import dataclasses
 
@@ -45,8 +45,8 @@ def test_verify_sigmoid_gate():
     check(w, r, [0, 11])
 
 
-@pytest.mark.parametrize("lens", [[100, 7, 129, 64, 1, 128],  # 192 (seq, head) units: fused norm
-                                  [300]])                      # 32 units: sliced spine + norm kernel
+@pytest.mark.parametrize("lens", [[100, 7, 129, 64, 1, 128],  # 192 (seq, head) units: whole rows
+                                  [300]])                      # 32 units: sliced spine
 def test_tensor_core_prefill_sigmoid_gate(lens):
     w = sigmoid_gated(wl.varlen_prefill(lens, seed=53))
     check_prefill(w, run_prefill(w))

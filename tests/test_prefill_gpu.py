@@ -114,10 +114,40 @@ def test_varlen_prefill_full_small():
 
 def test_prefill_without_core_output():
     """No f32 core output requested: two sequences take the column-sliced spine, which
-    hands O to the gated-norm kernel in fp16; y and the states still match."""
+    hands O to the norm in fp16; y and the states still match."""
     w = wl.varlen_prefill([300, 77], seed=18)
     assert tensor_core_path(w)
     check_prefill(w, run_prefill(w, with_core=False))
+
+
+@pytest.mark.parametrize("with_core", [True, False])
+def test_prefill_sliced_spine_empty_and_ragged(with_core):
+    """Column-sliced spine: an empty sequence (its chains leave at once) beside one with a
+    3-token last chunk, and a single-token sequence on its own (its norm in the spare CTAs
+    of the spine's launch)."""
+    for lens, seed in (([0, 131], 19), ([1], 20)):
+        w = wl.varlen_prefill(lens, seed=seed)
+        assert tensor_core_path(w) and w.n * w.shape.n_v_heads * 2 <= 152
+        r = run_prefill(w, with_core=with_core)
+        check_prefill(w, r)
+        if lens[0] == 0:
+            np.testing.assert_array_equal(r["h_pool"][0].cpu().numpy(), w.H0[0])
+
+
+@pytest.mark.parametrize("n,with_core", [(9, False), (9, True), (16, False)])
+def test_prefill_sliced_spine_norm_ctas(n, with_core):
+    """d = 128 with 4 value heads.  9 sequences: 36 (sequence, head) units whose two column
+    slices take 72 SMs; the 80 left run the norm, up to four 8-row parts of a chunk each,
+    over sequences of every length class (empty, one token, one chunk, ragged).  16
+    sequences leave fewer than two spare SMs per head, and the norm runs as its own kernel
+    after the chains."""
+    shape = wl.LayerShape(1, 4, 128, 128, 4, q_scale=128 ** -0.5)
+    rng = np.random.default_rng(21 + n)
+    lens = rng.integers(1, 160, size=n)
+    lens[:4] = [64, 0, 129, 1]
+    w = wl.varlen_prefill(lens, shape=shape, seed=21 + n)
+    assert tensor_core_path(w)
+    check_prefill(w, run_prefill(w, with_core=with_core))
 
 
 def test_varlen_prefill_full_f32_sequential():
