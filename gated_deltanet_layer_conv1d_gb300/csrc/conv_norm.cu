@@ -341,33 +341,46 @@ __global__ void gdn_gated_rmsnorm_kernel(const OT* __restrict__ o, const T* __re
                                          int64_t z_stride, const float* __restrict__ w,
                                          float eps, int T_, int Hv, T* __restrict__ y) {
   using A = Act<T>;
-  constexpr int kRows = 4;
+  constexpr int kRows = 8;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int j = lane * 4;
-  const bool live = j < D;
+  const bool live = lane * 4 < D;
+  const int j = live ? lane * 4 : 0;  // a lane past D reads (and discards) column 0
   const float4 w4 = live ? *reinterpret_cast<const float4*>(w + j) : make_float4(0.f, 0.f, 0.f, 0.f);
   const int rows = T_ * Hv;
   for (int r0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kRows; r0 < rows;
        r0 += warps * kRows) {
+    // a row past the end reads row 0: no branch between the loads, so all of them issue
+    // before the first use
     float4 ov[kRows], z4[kRows];
 #pragma unroll
     for (int k = 0; k < kRows; ++k) {
-      const int r = r0 + k, t = r / Hv, h = r - t * Hv;
-      ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z4[k] = ov[k];
-      if (live && r < rows) {
-        ov[k] = load_o4(o + size_t(r) * D + j);
-        z4[k] = A::load4(z + size_t(t) * z_stride + h * D + j);
+      const int r = r0 + k < rows ? r0 + k : 0, t = r / Hv, h = r - t * Hv;
+      ov[k] = load_o4(o + size_t(r) * D + j);
+      z4[k] = A::load4(z + size_t(t) * z_stride + h * D + j);
+    }
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      if (!live) {
+        ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z4[k] = ov[k];
       }
+    }
+    // the rows' sums side by side
+    float ss[kRows];
+#pragma unroll
+    for (int k = 0; k < kRows; ++k)
+      ss[k] = ov[k].x * ov[k].x + ov[k].y * ov[k].y + ov[k].z * ov[k].z + ov[k].w * ov[k].w;
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) ss[k] += __shfl_xor_sync(0xffffffffu, ss[k], m);
     }
 #pragma unroll
     for (int k = 0; k < kRows; ++k) {
       const int r = r0 + k, t = r / Hv, h = r - t * Hv;
-      const float ss =
-          warp_sum(ov[k].x * ov[k].x + ov[k].y * ov[k].y + ov[k].z * ov[k].z + ov[k].w * ov[k].w);
       if (live && r < rows) {
-        const float inv = rsqrtf(ss / float(D) + eps);
+        const float inv = rsqrtf(ss[k] / float(D) + eps);
         float4 yv;
         yv.x = ov[k].x * inv * w4.x * zgate_fast(z4[k].x, GATE);
         yv.y = ov[k].y * inv * w4.y * zgate_fast(z4[k].y, GATE);
