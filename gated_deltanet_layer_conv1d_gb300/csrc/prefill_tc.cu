@@ -1082,7 +1082,23 @@ cudaError_t launch_spine(const PrefillParams& p, cudaStream_t stream) {
                                                     SpineSmem<NCOL>::kAlloc);
   if (e != cudaSuccess) return e;
   const int grid = per_sm * sm_count();
-  if (grid - chains < 2 * p.n * p.Hv) {
+  if (grid - chains >= 2 * p.n * p.Hv) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(4 * NCOL + 32);
+    cfg.dynamicSmemBytes = SpineSmem<NCOL>::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeCooperative;
+    attr.val.cooperative = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaErrorCooperativeLaunchTooLarge) return e != cudaSuccess ? e : cudaGetLastError();
+    // fewer SMs than the device has are open to this context (an MPS limit, say)
+    (void)cudaGetLastError();
+  }
+  {
     // fewer than two spare SMs per head (the norm CTAs would trail the chains): the chains
     // alone, then the norm kernel
     kern<<<chains, 4 * NCOL + 32, SpineSmem<NCOL>::kAlloc, stream>>>(p);
@@ -1093,19 +1109,6 @@ cudaError_t launch_spine(const PrefillParams& p, cudaStream_t stream) {
                                 p.total_tokens, p.Hv, kD, GDN_DTYPE_BF16, p.norm_gate, p.y,
                                 stream);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(grid));
-  cfg.blockDim = dim3(4 * NCOL + 32);
-  cfg.dynamicSmemBytes = SpineSmem<NCOL>::kAlloc;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeCooperative;
-  attr.val.cooperative = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
 }
 
 }  // namespace

@@ -32,6 +32,10 @@
  *     kernel in the stream is still running.  A caller that rewrites those weights does so
  *     with a kernel or copy that is not the last work before the call (any kernel of its
  *     own does: it does not trigger early) -- in practice nothing changes for a caller.
+ *     The tensor-core prefill of few sequences (2 n H_v <= half the SMs) ends in one
+ *     cooperative launch that takes every SM for its length (the state chains and, beside
+ *     them, the gated norm); kernels on other streams share the GPU with it only before
+ *     and after.  Where the context may not use every SM, it runs as two plain launches.
  *   - Pointers marked "device" are CUDA device (or managed) memory; "host" is host memory.
  *   - Row strides are in ELEMENTS of the activation dtype.
  *   - Supported shapes: (d_k, d_v) in {(16, 16), (128, 128)}, d_conv = 4,
