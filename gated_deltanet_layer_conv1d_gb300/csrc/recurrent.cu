@@ -1320,7 +1320,15 @@ cudaError_t launch_rec(const RecParams& p, cudaStream_t stream) {
     if (per_sm > rec_min_blocks<KMAX, SH>()) per_sm = rec_min_blocks<KMAX, SH>();
   }
   const int cap = sm_count() * per_sm;
-  const int P = p.n_items < cap ? p.n_items : cap;
+  int P = p.n_items < cap ? p.n_items : cap;
+  if (KMAX == 1) {
+    // decode items all cost the same: the fewest CTAs that still need only as many rounds
+    // as a full grid, so the last round is (nearly) full too -- 2048 items on 152 SMs run
+    // as 147 CTAs x 14 rounds instead of 152 CTAs with 72 of them busy in the 14th
+    // (128-sequence decode 91.6 -> 90.2 us; fp16 pools, 2 CTAs per SM: 59.4 -> 59.1 us)
+    const int rounds = (p.n_items + P - 1) / P;
+    P = (p.n_items + rounds - 1) / rounds;
+  }
   return launch_pdl(kern, dim3(unsigned(P)), dim3(unsigned(rec_threads<NT, KMAX>())), smem, stream,
                     1u, p);
 }
