@@ -15,7 +15,8 @@
 // pool instead of table 0 and no intermediates.
 //
 // Design (HBM-bound: the state tile is read once, and written once per token kept):
-//   * persistent grid: one CTA per SM (two on fp16 decode pools); items are dealt to CTAs
+//   * persistent grid: one CTA per SM (two on fp16 decode pools; decode takes the fewest
+//     CTAs that need no more rounds, so its last round is full too); items are dealt to CTAs
 //     in a zig-zag over the item list (most tokens first), so ragged k balances;
 //   * threads: NT compute threads (16 warps for verify, 8 for decode); decode adds one
 //     producer warp and one norm warp;
