@@ -70,6 +70,17 @@ __device__ __forceinline__ float zgate(float z, int kind) { return (kind ? 1.f :
 __device__ __forceinline__ float zgate_fast(float z, int kind) {
   return __fdividef(kind ? 1.f : z, 1.f + __expf(-z));
 }
+// The same gate with one SFU operation instead of two, for results rounded to bf16:
+// sigmoid(z) = (1 + tanh(z / 2)) / 2 with the hardware tanh (tanh.approx: relative error
+// near 2^-11, so absolute below it), which leaves the sigmoid within about 2^-12 -- small
+// beside the 2^-9 relative rounding of a bf16 result of the row's typical size.  Not for
+// f32 outputs.
+__device__ __forceinline__ float zgate_bf16(float z, int kind) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
+  const float sg = fmaf(0.5f, t, 0.5f);
+  return kind ? sg : z * sg;
+}
 
 // 2^x with the hardware approximation (ex2.approx, relative error below 2^-22; subnormal
 // results flush to zero).

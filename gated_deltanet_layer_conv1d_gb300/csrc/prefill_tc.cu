@@ -652,11 +652,11 @@ __device__ void spine_norm_ctas(const PrefillParams& p, int k, int nr) {
         const float2 za = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zr[j].x));
         const float2 zb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zr[j].y));
         const __nv_bfloat162 y01 =
-            __floats2bfloat162_rn(o.x * inv * w4.x * zgate_fast(za.x, p.norm_gate),
-                                  o.y * inv * w4.y * zgate_fast(za.y, p.norm_gate));
+            __floats2bfloat162_rn(o.x * inv * w4.x * zgate_bf16(za.x, p.norm_gate),
+                                  o.y * inv * w4.y * zgate_bf16(za.y, p.norm_gate));
         const __nv_bfloat162 y23 =
-            __floats2bfloat162_rn(o.z * inv * w4.z * zgate_fast(zb.x, p.norm_gate),
-                                  o.w * inv * w4.w * zgate_fast(zb.y, p.norm_gate));
+            __floats2bfloat162_rn(o.z * inv * w4.z * zgate_bf16(zb.x, p.norm_gate),
+                                  o.w * inv * w4.w * zgate_bf16(zb.y, p.norm_gate));
         if (live[j])
           *reinterpret_cast<uint2*>(yg + orow[j] * kD + 4 * lane) =
               make_uint2(*reinterpret_cast<const uint32_t*>(&y01),
@@ -1027,8 +1027,8 @@ __global__ void __launch_bounds__(4 * NCOL + (SpineSmem<NCOL>::kCounted ? 32 : 0
               const float2 zf = __bfloat1622float2(z2[e]);
               const int u = 8 * k + 2 * e;
               const __nv_bfloat162 yy = __floats2bfloat162_rn(
-                  v[u] * inv * nw[u] * zgate_fast(zf.x, p.norm_gate),
-                  v[u + 1] * inv * nw[u + 1] * zgate_fast(zf.y, p.norm_gate));
+                  v[u] * inv * nw[u] * zgate_bf16(zf.x, p.norm_gate),
+                  v[u + 1] * inv * nw[u + 1] * zgate_bf16(zf.y, p.norm_gate));
               out[e] = *reinterpret_cast<const uint32_t*>(&yy);
             }
             *reinterpret_cast<uint4*>(yo + 8 * k) = make_uint4(out[0], out[1], out[2], out[3]);
