@@ -30,6 +30,8 @@
 
 namespace gdn {
 
+constexpr int kCountStride = 32;  // int32 words between the spine's progress counters
+
 struct PrefillLayout {
   static constexpr int kC = 64;                          // chunk length
   static constexpr size_t kTile = size_t(64) * 128 * 2;  // one fp16 [64][128] tile
@@ -76,12 +78,13 @@ struct PrefillLayout {
   size_t o_offset(int n, int total_tokens) const {
     return (slots(n, total_tokens) * slot_bytes() + 255) / 256 * 256;
   }
-  // byte offset of the two-slice spine's progress counters: int32 [n][Hv][2], after O
+  // byte offset of the two-slice spine's progress counters: int32 [n][Hv][2], each in a
+  // 128-byte line of its own (kCountStride words apart), after O
   size_t count_offset(int n, int total_tokens) const {
     return o_offset(n, total_tokens) + (size_t(total_tokens) * Hv * 128 * 4 + 255) / 256 * 256;
   }
   size_t total_bytes(int n, int total_tokens) const {
-    return count_offset(n, total_tokens) + size_t(n) * Hv * 2 * 4;
+    return count_offset(n, total_tokens) + size_t(n) * Hv * 2 * kCountStride * 4;
   }
 };
 

@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
   using S = PrepSmem;
   // the two-slice spine's progress counters start from zero on every call
   if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < 2 * p.n * p.Hv; i += blockDim.x) p.counts[i] = 0;
+    for (int i = threadIdx.x; i < 2 * p.n * p.Hv; i += blockDim.x) p.counts[i * kCountStride] = 0;
   const int cs = blockIdx.x / p.Hv, h = blockIdx.x % p.Hv, kh = h / p.G;
   // The sequence that owns chunk slot cs: the last s with base(s) <= cs.
   int seq = 0;
@@ -577,8 +577,8 @@ __device__ void spine_norm_ctas(const PrefillParams& p, int k, int nr) {
         for (int i = 0; i < nwu; ++i) {
           const int nc = (len_s[i] + kC - 1) / kC;
           if (nc <= c0) continue;
-          const int32_t* cnt = p.counts + 2 * uh_s[i];
-          const int v = min(load_count(cnt), load_count(cnt + 1));
+          const int32_t* cnt = p.counts + 2 * uh_s[i] * kCountStride;
+          const int v = min(load_count(cnt), load_count(cnt + kCountStride));
           if (v < nc) ready = min(ready, v);
         }
         if (ready > c0) break;
@@ -587,7 +587,7 @@ __device__ void spine_norm_ctas(const PrefillParams& p, int k, int nr) {
           ready = -1;
           break;
         }
-        __nanosleep(128);
+        __nanosleep(512);
       }
       __threadfence();
       upto_s = ready;
@@ -713,7 +713,7 @@ __global__ void __launch_bounds__(4 * NCOL + (SpineSmem<NCOL>::kCounted ? 32 : 0
   const int len = t_end - t_begin;
   if (len == 0) return;  // nothing to do: the state stays as it is
   const int nc = (len + kC - 1) / kC;
-  int32_t* cnt = p.counts + 2 * (size_t(seq) * p.Hv + h) + slice;
+  int32_t* cnt = p.counts + (2 * (size_t(seq) * p.Hv + h) + slice) * kCountStride;
   // chunks whose O rows this CTA has stored (set by kLoader after a chain barrier)
   __shared__ int stored_s;
 
