@@ -150,6 +150,28 @@ def test_prefill_sliced_spine_norm_ctas(n, with_core):
     check_prefill(w, run_prefill(w, with_core=with_core))
 
 
+def test_prefill_norm_ctas_bad_seqlens_sets_status():
+    """Tensor-core path with norm CTAs beside the chains (4 value heads, 2 sequences): a
+    decreasing cu_seqlens is reported on the status word, and the norm CTAs, which skip
+    what the chains skip, wait on nothing."""
+    shape = wl.LayerShape(1, 4, 128, 128, 4, q_scale=128 ** -0.5)
+    w = wl.varlen_prefill([9, 2], shape=shape, seed=25)
+    assert tensor_core_path(w)
+    d = torch.device("cuda")
+    dims = dev.dims_of(shape)
+    h_pool, conv_pool, slots = dev.states_to(w, d)
+    hsz = shape.n_v_heads * shape.d_k * shape.d_v * 4
+    hp = torch.tensor([h_pool.data_ptr() + i * hsz for i in range(2)], dtype=torch.int64, device=d)
+    cu = torch.from_numpy(np.array([0, 9, 7], np.int32)).to(d)  # decreasing: invalid
+    ws = torch.empty(gdn.gdn_prefill_workspace_bytes(dims, 2, 11, 9), dtype=torch.uint8, device=d)
+    y = torch.zeros((11, shape.n_v_heads * shape.d_v), dtype=torch.bfloat16, device=d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    gdn.gdn_prefill_chunked(dims, dev.weights_to(w, d), dev.tokens_to(w.tokens, torch.bfloat16, d),
+                            2, cu, 11, 9, hp, conv_pool, 2, slots, y, None, ws, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 18  # GDN_ERR_BAD_SEQLENS
+
+
 def test_varlen_prefill_full_f32_sequential():
     """d = 128 with f32 activations runs the token-sequential kernel (f32 class)."""
     rng = np.random.default_rng(15)
