@@ -172,6 +172,46 @@ def test_prefill_norm_ctas_bad_seqlens_sets_status():
     assert int(status.item()) == 18  # GDN_ERR_BAD_SEQLENS
 
 
+def test_prefill_norm_ctas_in_cuda_graph():
+    """The cooperative two-slice spine (one sequence, norm CTAs beside the chains) captured
+    in a CUDA graph and replayed gives y and the state bit for bit as an eager call does."""
+    w = wl.varlen_prefill([200], seed=27)
+    assert tensor_core_path(w)
+    d = torch.device("cuda")
+    sh = w.shape
+    dims = dev.dims_of(sh)
+    T = int(w.lens.sum())
+    cu = torch.from_numpy(w.cu_seqlens).to(d)
+    ws = torch.empty(gdn.gdn_prefill_workspace_bytes(dims, 1, T, T), dtype=torch.uint8, device=d)
+    weights = dev.weights_to(w, d)
+    tokens = dev.tokens_to(w.tokens, torch.bfloat16, d)
+    hsz = sh.n_v_heads * sh.d_k * sh.d_v * 4
+    outs = []
+    for graph in (False, True):
+        h_pool, conv_pool, slots = dev.states_to(w, d)
+        hp = torch.tensor([h_pool.data_ptr() + int(slots[0]) * hsz], dtype=torch.int64, device=d)
+        y = torch.empty((T, sh.n_v_heads * sh.d_v), dtype=torch.bfloat16, device=d)
+        status = torch.zeros(1, dtype=torch.int32, device=d)
+
+        def call(st):
+            gdn.gdn_prefill_chunked(dims, weights, tokens, 1, cu, T, T, hp, conv_pool, 1, slots,
+                                    y, None, ws, status, st)
+
+        if graph:
+            side = torch.cuda.Stream(d)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                call(side)
+            g.replay()
+        else:
+            call(torch.cuda.current_stream(d))
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        outs.append((y.clone(), h_pool[slots.long()].clone()))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
+
+
 def test_varlen_prefill_full_f32_sequential():
     """d = 128 with f32 activations runs the token-sequential kernel (f32 class)."""
     rng = np.random.default_rng(15)
